@@ -1,0 +1,177 @@
+/*
+ * kvsdecode.h -- C ABI of the GB300 (sm_103a) batched decode-step attention
+ * library: KV-cache scatter followed by split-K ("flash decoding") softmax
+ * attention under grouped-query attention.
+ *
+ * Source of the operations: realizar 0.8.5, src/cuda/executor/head_dim.rs,
+ * `flash_decoding_attention_into` (PAR-118) -- doc comment (layouts; the KV
+ * cache is cut into chunks processed in parallel, whose partial results are
+ * merged with softmax rescaling), "Step 1: Scatter K/V to caches", "Update
+ * cache lengths" (a sequence at position p attends rows 0..p), "Step 3:
+ * Compute max chunks needed" (ceil(seq_len / chunk)), "Step 4" (chunk
+ * kernel), "Step 5" (reduce kernel).  The device-resident position follows
+ * aprender-serve 0.70.2, src/gguf/cuda/forward_qwen35_cuda_graph.rs, module
+ * doc table (the K/V row is "scattered at *io.pos", read on the device).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are float32, C-contiguous, in DEVICE memory owned by the
+ *     caller; positions are int32 in device memory.  The library never
+ *     allocates, frees or synchronises; it does not keep pointers after a
+ *     call returns.
+ *   - Layouts (M sequences, H = num_heads query heads, Hkv = num_kv_heads,
+ *     G = H / Hkv, D = head_dim, Lmax = max_len):
+ *         q, out              [M][H][D]
+ *         k_rows, v_rows      [M][Hkv][D]          (this step's new rows)
+ *         k_cache, v_cache    [M][Hkv][Lmax][D]    (sequence stride Hkv*Lmax*D)
+ *         positions           [M]                  (int32)
+ *     Query head h reads kv head h / G (contiguous groups).  The softmax
+ *     scale is 1/sqrt(D).
+ *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream) and returns; kernels run asynchronously.
+ *     Ordering between calls is the stream's.  kvs_kv_scatter must be
+ *     ordered before kvs_flash_decode of the same layer: attention includes
+ *     row p, the row the scatter writes.
+ *   - Return value: KVS_OK, or a kvs_status code.  Argument errors are
+ *     detected on the host BEFORE anything is enqueued.  KVS_ERR_LAUNCH
+ *     carries a CUDA launch failure.
+ *   - d_status (nullable): a device int the caller zeroes.  Kernels record
+ *     the first device-detected error there (atomic compare-and-swap from
+ *     0): KVS_ERR_POSITION for a position outside [0, Lmax) (that sequence
+ *     is skipped; the scatter writes nothing for it and its attention
+ *     output rows are NaN), KVS_ERR_TIMEOUT if an internal pipeline wait
+ *     exceeded its bound (the kernel returns instead of hanging; outputs
+ *     of that call are undefined).
+ *   - Entry points are stateless and may be called from several host
+ *     threads on different streams.
+ */
+#ifndef KVSDECODE_H
+#define KVSDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvs_status {
+  KVS_OK = 0,
+  KVS_ERR_NULL = 1,        /* a required pointer is NULL */
+  KVS_ERR_DIMS = 2,        /* M < 0, H % Hkv != 0, sizes < 1, chunk_size < 0 */
+  KVS_ERR_UNSUPPORTED = 3, /* head_dim not 64 or 128, or H / Hkv > 8 */
+  KVS_ERR_ALIGN = 4,       /* a tensor pointer is not 16-byte aligned */
+  KVS_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required */
+  KVS_ERR_LAUNCH = 6,      /* CUDA reported a launch or device-query error */
+  KVS_ERR_POSITION = 7,    /* device: a position outside [0, max_len) */
+  KVS_ERR_TIMEOUT = 8      /* device: a bounded pipeline wait expired */
+} kvs_status;
+
+/* A cudaStream_t, passed as an opaque pointer so this header needs no CUDA
+ * include. */
+typedef void *kvs_stream_t;
+
+/*
+ * kvs_kv_scatter -- "Step 1: Scatter K/V to caches" of
+ * flash_decoding_attention_into, done for all M sequences, both K and V,
+ * in ONE launch (the pages launch it twice per sequence).
+ *
+ * For every sequence i with 0 <= p = positions[i] < max_len and every kv
+ * head g:  k_cache[i][g][p][:] = k_rows[i][g][:],  v_cache likewise.
+ * No other cache byte is touched; the copy is bit-exact.
+ *
+ *   k_rows, v_rows    in   [M][Hkv][D] float32, device, 16-byte aligned
+ *   positions         in   [M] int32, device
+ *   k_cache, v_cache  out  [M][Hkv][Lmax][D] float32, device, 16-byte aligned
+ *   M >= 0 (0: nothing enqueued), num_kv_heads >= 1, head_dim in {64, 128},
+ *   max_len >= 1.
+ * Errors: NULL, DIMS, UNSUPPORTED, ALIGN, LAUNCH on the host; POSITION via
+ * d_status.
+ */
+int kvs_kv_scatter(const float *k_rows, const float *v_rows,
+                   const int32_t *positions, float *k_cache, float *v_cache,
+                   int M, int num_kv_heads, int head_dim, int max_len,
+                   int *d_status, kvs_stream_t stream);
+
+/*
+ * kvs_choose_chunk_size -- the split-count rule used when a caller passes
+ * chunk_size = 0 (the pages fix one compile-time FLASH_DECODE_CHUNK_SIZE;
+ * here it depends on the shape and the SM count so that all SMs stay busy
+ * at small M and long contexts while partial traffic stays small).
+ * Returns a chunk size in rows (>= 1), or a negative kvs_status.
+ *   num_sms > 0: use that SM count; num_sms <= 0: query the current device.
+ */
+int kvs_choose_chunk_size(int M, int num_kv_heads, int head_dim, int max_len,
+                          int num_sms);
+
+/*
+ * kvs_flash_decode_workspace_bytes -- size of the scratch buffer that
+ * kvs_flash_decode needs for the chunk partials (running max, running sum
+ * and weighted-V accumulator of every chunk; the pages' flash_decode_partials
+ * buffer).  chunk_size = 0 resolves through kvs_choose_chunk_size on the
+ * current device.  Returns 0 on invalid arguments.
+ */
+size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads,
+                                        int head_dim, int max_len,
+                                        int chunk_size);
+
+/*
+ * kvs_flash_decode -- "Step 4" + "Step 5" of flash_decoding_attention_into:
+ * split-K decode attention over the scattered cache.
+ *
+ * For every sequence i (L = positions[i] + 1) and query head h (kv head
+ * g = h / G):  out[i][h][:] = softmax_j( q[i][h] . k_cache[i][g][j] / sqrt(D) )
+ * applied to v_cache[i][g][j][:], j = 0..L-1.  Rows j >= L are never read.
+ *
+ * The cache rows of every (sequence, kv head) are cut into chunks of
+ * chunk_size rows; each chunk yields (running max, running sum, weighted-V
+ * accumulator) for all G query heads of the group, reading each K/V row
+ * once; a second kernel merges the chunk partials with softmax rescaling.
+ *
+ *   q          in   [M][H][D] float32, device, 16-byte aligned
+ *   k_cache,
+ *   v_cache    in   [M][Hkv][Lmax][D] float32, device, 16-byte aligned
+ *   positions  in   [M] int32, device
+ *   out        out  [M][H][D] float32, device, 16-byte aligned
+ *   chunk_size      rows per chunk; 0 = kvs_choose_chunk_size
+ *   workspace       device scratch of >= kvs_flash_decode_workspace_bytes
+ *                   bytes, 256-byte aligned; contents need no initialisation
+ *                   and are overwritten; it must not be shared by calls
+ *                   that can overlap on the GPU.
+ * Errors: NULL, DIMS, UNSUPPORTED, ALIGN, WORKSPACE, LAUNCH on the host;
+ * POSITION, TIMEOUT via d_status.
+ */
+int kvs_flash_decode(const float *q, const float *k_cache,
+                     const float *v_cache, const int32_t *positions,
+                     float *out, int M, int num_heads, int num_kv_heads,
+                     int head_dim, int max_len, int chunk_size,
+                     void *workspace, size_t workspace_bytes, int *d_status,
+                     kvs_stream_t stream);
+
+/*
+ * The two halves of kvs_flash_decode, for callers that time or schedule the
+ * chunk and reduce kernels separately.  Called back to back on one stream
+ * with the same arguments they are exactly kvs_flash_decode.
+ *   kvs_flash_decode_partials: "Step 4" -- chunk partials into workspace.
+ *   kvs_flash_decode_reduce:   "Step 5" -- rescaled merge into out.
+ */
+int kvs_flash_decode_partials(const float *q, const float *k_cache,
+                              const float *v_cache, const int32_t *positions,
+                              int M, int num_heads, int num_kv_heads,
+                              int head_dim, int max_len, int chunk_size,
+                              void *workspace, size_t workspace_bytes,
+                              int *d_status, kvs_stream_t stream);
+
+int kvs_flash_decode_reduce(const int32_t *positions, float *out, int M,
+                            int num_heads, int num_kv_heads, int head_dim,
+                            int max_len, int chunk_size, void *workspace,
+                            size_t workspace_bytes, int *d_status,
+                            kvs_stream_t stream);
+
+/* Human-readable name of a kvs_status value (static string). */
+const char *kvs_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVSDECODE_H */

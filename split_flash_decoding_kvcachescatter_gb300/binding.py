@@ -1,0 +1,191 @@
+"""Thin Python binding of libkvsdecode.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls
+(include/kvsdecode.h).  It checks tensor dtype/device/contiguity, reads the
+sizes off the tensor shapes, passes raw device pointers and the current
+CUDA stream, and raises KvsError on a non-zero status.  All compute runs
+in the CUDA kernels of the library; there is no fallback of any kind: if
+the library is missing or fails to load, the functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvsdecode.so")
+
+KVS_OK = 0
+KVS_ERR_NULL = 1
+KVS_ERR_DIMS = 2
+KVS_ERR_UNSUPPORTED = 3
+KVS_ERR_ALIGN = 4
+KVS_ERR_WORKSPACE = 5
+KVS_ERR_LAUNCH = 6
+KVS_ERR_POSITION = 7
+KVS_ERR_TIMEOUT = 8
+
+# Every symbol include/kvsdecode.h declares.
+EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspace_bytes",
+           "kvs_flash_decode", "kvs_flash_decode_partials", "kvs_flash_decode_reduce",
+           "kvs_strerror")
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+
+class KvsError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {strerror(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m split_flash_decoding_kvcachescatter_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            L.kvs_kv_scatter.restype = _I
+            L.kvs_kv_scatter.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]
+            L.kvs_choose_chunk_size.restype = _I
+            L.kvs_choose_chunk_size.argtypes = [_I, _I, _I, _I, _I]
+            L.kvs_flash_decode_workspace_bytes.restype = _SZ
+            L.kvs_flash_decode_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
+            L.kvs_flash_decode.restype = _I
+            L.kvs_flash_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                           _P, _SZ, _P, _P]
+            L.kvs_flash_decode_partials.restype = _I
+            L.kvs_flash_decode_partials.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                                    _P, _SZ, _P, _P]
+            L.kvs_flash_decode_reduce.restype = _I
+            L.kvs_flash_decode_reduce.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
+                                                  _P, _P]
+            L.kvs_strerror.restype = ctypes.c_char_p
+            L.kvs_strerror.argtypes = [_I]
+            _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().kvs_strerror(int(status)).decode()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != KVS_OK:
+        raise KvsError(rc, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _f32(t: torch.Tensor, name: str, ndim: int) -> int:
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.dim() == ndim):
+        raise TypeError(f"{name}: need a contiguous float32 CUDA tensor with {ndim} dims, got "
+                        f"{tuple(t.shape)} {t.dtype} {t.device}")
+    return t.data_ptr()
+
+
+def _i32(t: torch.Tensor, name: str) -> int:
+    if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous() and t.dim() == 1):
+        raise TypeError(f"{name}: need a contiguous int32 CUDA vector")
+    return t.data_ptr()
+
+
+def _status_ptr(d_status) -> int:
+    if d_status is None:
+        return 0
+    if not (d_status.is_cuda and d_status.dtype == torch.int32):
+        raise TypeError("d_status: need an int32 CUDA tensor")
+    return d_status.data_ptr()
+
+
+def kvs_kv_scatter(k_rows, v_rows, positions, k_cache, v_cache, d_status=None, stream=None):
+    """Scatter k_rows/v_rows [M,Hkv,D] into caches [M,Hkv,Lmax,D] at positions [M]."""
+    M, Hkv, Lmax, D = k_cache.shape
+    if tuple(v_cache.shape) != (M, Hkv, Lmax, D) or tuple(k_rows.shape) != (M, Hkv, D) or \
+            tuple(v_rows.shape) != (M, Hkv, D) or positions.numel() != M:
+        raise ValueError("kvs_kv_scatter: inconsistent shapes")
+    rc = lib().kvs_kv_scatter(_f32(k_rows, "k_rows", 3), _f32(v_rows, "v_rows", 3),
+                              _i32(positions, "positions"), _f32(k_cache, "k_cache", 4),
+                              _f32(v_cache, "v_cache", 4), M, Hkv, D, Lmax,
+                              _status_ptr(d_status), _stream(stream))
+    _check(rc, "kvs_kv_scatter")
+
+
+def kvs_choose_chunk_size(M, num_kv_heads, head_dim, max_len, num_sms=0) -> int:
+    c = lib().kvs_choose_chunk_size(M, num_kv_heads, head_dim, max_len, num_sms)
+    if c <= 0:
+        raise KvsError(-c, "kvs_choose_chunk_size")
+    return c
+
+
+def kvs_flash_decode_workspace_bytes(M, num_heads, num_kv_heads, head_dim, max_len,
+                                     chunk_size) -> int:
+    return int(lib().kvs_flash_decode_workspace_bytes(M, num_heads, num_kv_heads, head_dim,
+                                                      max_len, chunk_size))
+
+
+def workspace(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size, device=None):
+    """A device byte buffer large enough for kvs_flash_decode (allocated by torch)."""
+    n = kvs_flash_decode_workspace_bytes(M, num_heads, num_kv_heads, head_dim, max_len,
+                                         chunk_size)
+    if n == 0 and M > 0:
+        raise KvsError(KVS_ERR_DIMS, "kvs_flash_decode_workspace_bytes")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def _attn_shapes(q, k_cache):
+    M, H, D = q.shape
+    M2, Hkv, Lmax, D2 = k_cache.shape
+    if M2 != M or D2 != D:
+        raise ValueError("q and k_cache disagree on M or head_dim")
+    return M, H, Hkv, D, Lmax
+
+
+def kvs_flash_decode(q, k_cache, v_cache, positions, out, chunk_size=0, workspace=None,
+                     d_status=None, stream=None):
+    """out[M,H,D] = split-K softmax attention of q over cache rows 0..positions[i]."""
+    M, H, Hkv, D, Lmax = _attn_shapes(q, k_cache)
+    if workspace is None:
+        raise ValueError("kvs_flash_decode: pass a workspace (see binding.workspace)")
+    rc = lib().kvs_flash_decode(_f32(q, "q", 3), _f32(k_cache, "k_cache", 4),
+                                _f32(v_cache, "v_cache", 4), _i32(positions, "positions"),
+                                _f32(out, "out", 3), M, H, Hkv, D, Lmax, int(chunk_size),
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _status_ptr(d_status), _stream(stream))
+    _check(rc, "kvs_flash_decode")
+
+
+def kvs_flash_decode_partials(q, k_cache, v_cache, positions, chunk_size, workspace,
+                              d_status=None, stream=None):
+    M, H, Hkv, D, Lmax = _attn_shapes(q, k_cache)
+    rc = lib().kvs_flash_decode_partials(
+        _f32(q, "q", 3), _f32(k_cache, "k_cache", 4), _f32(v_cache, "v_cache", 4),
+        _i32(positions, "positions"), M, H, Hkv, D, Lmax, int(chunk_size), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _status_ptr(d_status), _stream(stream))
+    _check(rc, "kvs_flash_decode_partials")
+
+
+def kvs_flash_decode_reduce(positions, out, num_kv_heads, max_len, chunk_size, workspace,
+                            d_status=None, stream=None):
+    M, H, D = out.shape
+    rc = lib().kvs_flash_decode_reduce(
+        _i32(positions, "positions"), _f32(out, "out", 3), M, H, num_kv_heads, D, max_len,
+        int(chunk_size), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _status_ptr(d_status), _stream(stream))
+    _check(rc, "kvs_flash_decode_reduce")

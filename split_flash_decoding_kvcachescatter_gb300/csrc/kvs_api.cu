@@ -1,0 +1,152 @@
+// kvs_api.cu -- the C ABI (include/kvsdecode.h): argument validation on the
+// host, the chunk-size rule, workspace sizing, and dispatch to the kernel
+// launchers.  Nothing here allocates, frees or synchronises.
+
+#include <cstdint>
+
+#include "kvs_launch.h"
+#include "kvsdecode.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool head_dim_supported(int D) { return D == 64 || D == 128; }
+
+// Shape checks shared by the attention entry points (no pointers).
+int check_attention_shape(int M, int H, int Hkv, int D, int max_len, int chunk) {
+  if (M < 0 || H < 1 || Hkv < 1 || max_len < 1 || chunk < 0) return KVS_ERR_DIMS;
+  if (H % Hkv != 0) return KVS_ERR_DIMS;
+  if (!head_dim_supported(D)) return KVS_ERR_UNSUPPORTED;
+  if (H / Hkv > 8) return KVS_ERR_UNSUPPORTED;
+  if ((int64_t)M * H > 0x7fffffffll) return KVS_ERR_DIMS;
+  return KVS_OK;
+}
+
+// chunk_size == 0 -> the library rule on the current device.
+int resolve_chunk(int M, int Hkv, int D, int max_len, int chunk) {
+  if (chunk > 0) return chunk;
+  return kvs_choose_chunk_size(M, Hkv, D, max_len, 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvs_strerror(int status) {
+  switch (status) {
+    case KVS_OK: return "ok";
+    case KVS_ERR_NULL: return "a required pointer is NULL";
+    case KVS_ERR_DIMS: return "invalid dimensions";
+    case KVS_ERR_UNSUPPORTED: return "unsupported head_dim or query-head group";
+    case KVS_ERR_ALIGN: return "pointer not aligned (16 bytes for tensors, 256 for workspace)";
+    case KVS_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVS_ERR_LAUNCH: return "CUDA launch or device query failed";
+    case KVS_ERR_POSITION: return "a position is outside [0, max_len)";
+    case KVS_ERR_TIMEOUT: return "a bounded device pipeline wait expired";
+    default: return "unknown kvs status";
+  }
+}
+
+int kvs_kv_scatter(const float *k_rows, const float *v_rows, const int32_t *positions,
+                   float *k_cache, float *v_cache, int M, int num_kv_heads, int head_dim,
+                   int max_len, int *d_status, kvs_stream_t stream) {
+  if (M < 0 || num_kv_heads < 1 || max_len < 1) return KVS_ERR_DIMS;
+  if (!head_dim_supported(head_dim)) return KVS_ERR_UNSUPPORTED;
+  if (M == 0) return KVS_OK;
+  if (!k_rows || !v_rows || !positions || !k_cache || !v_cache) return KVS_ERR_NULL;
+  if (!aligned(k_rows, 16) || !aligned(v_rows, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(positions, 4))
+    return KVS_ERR_ALIGN;
+  return kvs::launch_kv_scatter(k_rows, v_rows, positions, k_cache, v_cache, M, num_kv_heads,
+                                head_dim, max_len, d_status,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvs_choose_chunk_size(int M, int num_kv_heads, int head_dim, int max_len, int num_sms) {
+  if (M < 1 || num_kv_heads < 1 || max_len < 1) return -KVS_ERR_DIMS;
+  if (!head_dim_supported(head_dim)) return -KVS_ERR_UNSUPPORTED;
+  const int sms = num_sms > 0 ? num_sms : kvs::device_sm_count();
+  if (sms <= 0) return -KVS_ERR_LAUNCH;
+  // Persistent grid of 2 CTAs per SM.  With a full cache, aim for at least
+  // 16 chunks per CTA (static ranges then stay within ~6% of balanced) while
+  // keeping chunks >= 64 rows so partial traffic stays small.
+  const int64_t ctas = 2ll * sms;
+  const int64_t rows = (int64_t)M * num_kv_heads * max_len;
+  const int64_t target = rows / (16 * ctas);
+  int c = 64;
+  while (c < 1024 && 2ll * c <= target) c <<= 1;
+  return c;
+}
+
+size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads, int head_dim,
+                                        int max_len, int chunk_size) {
+  if (check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size) != KVS_OK)
+    return 0;
+  if (M == 0) return 0;
+  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
+  if (chunk <= 0) return 0;
+  return kvs::partial_layout(M, num_heads, head_dim, max_len, chunk).total_bytes;
+}
+
+int kvs_flash_decode_partials(const float *q, const float *k_cache, const float *v_cache,
+                              const int32_t *positions, int M, int num_heads,
+                              int num_kv_heads, int head_dim, int max_len, int chunk_size,
+                              void *workspace, size_t workspace_bytes, int *d_status,
+                              kvs_stream_t stream) {
+  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
+  if (rc != KVS_OK) return rc;
+  if (M == 0) return KVS_OK;
+  if (!q || !k_cache || !v_cache || !positions) return KVS_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(positions, 4))
+    return KVS_ERR_ALIGN;
+  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
+  if (chunk <= 0) return -chunk;
+  if (!workspace) return KVS_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KVS_ERR_ALIGN;
+  if (workspace_bytes < kvs::partial_layout(M, num_heads, head_dim, max_len, chunk).total_bytes)
+    return KVS_ERR_WORKSPACE;
+  return kvs::launch_fd_chunks(q, k_cache, v_cache, positions, M, num_heads, num_kv_heads,
+                               head_dim, max_len, chunk, workspace, d_status,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvs_flash_decode_reduce(const int32_t *positions, float *out, int M, int num_heads,
+                            int num_kv_heads, int head_dim, int max_len, int chunk_size,
+                            void *workspace, size_t workspace_bytes, int *d_status,
+                            kvs_stream_t stream) {
+  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
+  if (rc != KVS_OK) return rc;
+  if (M == 0) return KVS_OK;
+  if (!out || !positions) return KVS_ERR_NULL;
+  if (!aligned(out, 16) || !aligned(positions, 4)) return KVS_ERR_ALIGN;
+  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
+  if (chunk <= 0) return -chunk;
+  if (!workspace) return KVS_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KVS_ERR_ALIGN;
+  if (workspace_bytes < kvs::partial_layout(M, num_heads, head_dim, max_len, chunk).total_bytes)
+    return KVS_ERR_WORKSPACE;
+  return kvs::launch_fd_reduce(positions, out, M, num_heads, head_dim, max_len, chunk,
+                               workspace, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvs_flash_decode(const float *q, const float *k_cache, const float *v_cache,
+                     const int32_t *positions, float *out, int M, int num_heads,
+                     int num_kv_heads, int head_dim, int max_len, int chunk_size,
+                     void *workspace, size_t workspace_bytes, int *d_status,
+                     kvs_stream_t stream) {
+  // validate everything (out included) before the first launch
+  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
+  if (rc != KVS_OK) return rc;
+  if (M == 0) return KVS_OK;
+  if (!out) return KVS_ERR_NULL;
+  if (!aligned(out, 16)) return KVS_ERR_ALIGN;
+  rc = kvs_flash_decode_partials(q, k_cache, v_cache, positions, M, num_heads, num_kv_heads,
+                                 head_dim, max_len, chunk_size, workspace, workspace_bytes,
+                                 d_status, stream);
+  if (rc != KVS_OK) return rc;
+  return kvs_flash_decode_reduce(positions, out, M, num_heads, num_kv_heads, head_dim, max_len,
+                                 chunk_size, workspace, workspace_bytes, d_status, stream);
+}
+
+}  // extern "C"

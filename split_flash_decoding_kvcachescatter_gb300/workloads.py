@@ -173,3 +173,44 @@ def algorithmic_bytes(inp: DecodeInputs, w: Workload) -> dict:
     scat = 4 * w.M * w.num_kv_heads * w.head_dim * 4 + 4 * w.M
     return {"attention": attn, "scatter": scat, "step": attn + scat,
             "chunk_kernel": kv_bytes(inp, w) + w.M * w.num_heads * w.head_dim * 4}
+
+
+# Bit pattern used to poison cache rows that hold no live data (a NaN).
+POISON_BITS = -1  # 0xFFFFFFFF as int32
+
+
+def poisoned_cache(w: Workload, device):
+    """A [M, Hkv, Lmax, D] float32 device tensor whose every element is the
+    NaN with bits 0xFFFFFFFF, so reading any row that is not live shows up."""
+    import torch
+    t = torch.full((w.M, w.num_kv_heads, w.max_len, w.head_dim), POISON_BITS,
+                   dtype=torch.int32, device=device)
+    return t.view(torch.float32)
+
+
+def upload(inp: DecodeInputs, w: Workload, device, include_new_row: bool = False):
+    """Device tensors for one layer: q, k_rows, v_rows, positions and the two
+    caches holding rows 0..p_i-1 of every sequence (rows p_i.. poisoned).
+
+    With include_new_row the caches also hold row p_i, i.e. the state the
+    scatter must produce (used as the expected cache; built with plain
+    torch copies of the generator's arrays)."""
+    import torch
+    k_cache = poisoned_cache(w, device)
+    v_cache = poisoned_cache(w, device)
+    for i in range(w.M):
+        p = int(inp.positions[i])
+        if p < 0 or p >= w.max_len:
+            continue
+        n = p + 1 if include_new_row else p
+        if n > 0:
+            k_cache[i, :, :n, :].copy_(torch.from_numpy(np.ascontiguousarray(inp.k_seq[i][:, :n])))
+            v_cache[i, :, :n, :].copy_(torch.from_numpy(np.ascontiguousarray(inp.v_seq[i][:, :n])))
+    return {
+        "q": torch.from_numpy(inp.q).to(device),
+        "k_rows": torch.from_numpy(inp.k_rows).to(device),
+        "v_rows": torch.from_numpy(inp.v_rows).to(device),
+        "positions": torch.from_numpy(inp.positions.astype(np.int32)).to(device),
+        "k_cache": k_cache,
+        "v_cache": v_cache,
+    }

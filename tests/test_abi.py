@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/kvsdecode.h declares, and rejects bad
+arguments with the documented status before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from split_flash_decoding_kvcachescatter_gb300 import binding as B
+from split_flash_decoding_kvcachescatter_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvsdecode.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvs_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(B.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert isinstance(getattr(L, name), ctypes._CFuncPtr)
+
+
+def test_strerror_covers_all_codes(L):
+    for code in range(0, 9):
+        s = B.strerror(code)
+        assert s and "unknown" not in s
+    assert "unknown" in B.strerror(99)
+
+
+P = ctypes.c_void_p
+A16 = 1 << 20  # an aligned fake address; never dereferenced (validation fails first)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, None, None, None, None, -1, 2, 64, 16), B.KVS_ERR_DIMS),
+    ((None, None, None, None, None, 1, 0, 64, 16), B.KVS_ERR_DIMS),
+    ((None, None, None, None, None, 1, 2, 64, 0), B.KVS_ERR_DIMS),
+    ((None, None, None, None, None, 1, 2, 96, 16), B.KVS_ERR_UNSUPPORTED),
+    ((None, None, None, None, None, 1, 2, 64, 16), B.KVS_ERR_NULL),
+    ((A16, A16, A16, A16 + 4, A16, 1, 2, 64, 16), B.KVS_ERR_ALIGN),
+    ((A16, A16 + 8, A16, A16, A16, 1, 2, 64, 16), B.KVS_ERR_ALIGN),
+    ((A16, A16, A16 + 2, A16, A16, 1, 2, 64, 16), B.KVS_ERR_ALIGN),
+])
+def test_scatter_validation(L, args, code):
+    assert L.kvs_kv_scatter(*args, None, None) == code
+
+
+def test_scatter_empty_batch_ok(L):
+    assert L.kvs_kv_scatter(None, None, None, None, None, 0, 2, 64, 16, None, None) == 0
+
+
+def _fd(L, q=A16, k=A16, v=A16, pos=A16, out=A16, M=1, H=4, Hkv=2, D=64, Lmax=256, C=64,
+        ws=A16, wsb=1 << 30):
+    return L.kvs_flash_decode(q, k, v, pos, out, M, H, Hkv, D, Lmax, C, ws, wsb, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), B.KVS_ERR_DIMS),
+    (dict(H=0), B.KVS_ERR_DIMS),
+    (dict(H=6, Hkv=4), B.KVS_ERR_DIMS),
+    (dict(Lmax=0), B.KVS_ERR_DIMS),
+    (dict(C=-5), B.KVS_ERR_DIMS),
+    (dict(D=80), B.KVS_ERR_UNSUPPORTED),
+    (dict(D=256), B.KVS_ERR_UNSUPPORTED),
+    (dict(H=18, Hkv=2), B.KVS_ERR_UNSUPPORTED),
+    (dict(q=None), B.KVS_ERR_NULL),
+    (dict(k=None), B.KVS_ERR_NULL),
+    (dict(out=None), B.KVS_ERR_NULL),
+    (dict(pos=None), B.KVS_ERR_NULL),
+    (dict(q=A16 + 4), B.KVS_ERR_ALIGN),
+    (dict(v=A16 + 12), B.KVS_ERR_ALIGN),
+    (dict(out=A16 + 8), B.KVS_ERR_ALIGN),
+    (dict(ws=None), B.KVS_ERR_WORKSPACE),
+    (dict(ws=A16 + 16), B.KVS_ERR_ALIGN),
+    (dict(wsb=100), B.KVS_ERR_WORKSPACE),
+])
+def test_flash_decode_validation(L, kw, code):
+    assert _fd(L, **kw) == code
+
+
+def test_flash_decode_empty_batch_ok(L):
+    assert _fd(L, M=0, q=None, k=None, v=None, pos=None, out=None, ws=None, wsb=0) == 0
+
+
+def test_workspace_bytes_formula(L):
+    # acc [M][H][n][D] f32 + ml [M][H][n][2] f32, each rounded up to 256 bytes
+    for (M, H, Hkv, D, Lmax, C) in [(1, 4, 2, 64, 256, 64), (8, 32, 8, 128, 32768, 128),
+                                    (32, 40, 8, 128, 131072, 256), (3, 8, 2, 128, 1000, 7)]:
+        n = -(-Lmax // C)
+        acc = -(-(M * H * n * D * 4) // 256) * 256
+        ml = -(-(M * H * n * 2 * 4) // 256) * 256
+        assert B.kvs_flash_decode_workspace_bytes(M, H, Hkv, D, Lmax, C) == acc + ml
+    assert B.kvs_flash_decode_workspace_bytes(1, 6, 4, 64, 16, 8) == 0
+
+
+def test_chunk_rule_is_pow2_in_range(L):
+    for sms in (1, 76, 152, 160):
+        for (M, Hkv, D, Lmax) in [(1, 2, 64, 256), (32, 8, 128, 8192), (8, 8, 128, 32768),
+                                  (32, 8, 128, 131072), (1, 1, 128, 1 << 20)]:
+            c = B.kvs_choose_chunk_size(M, Hkv, D, Lmax, sms)
+            assert 64 <= c <= 1024 and (c & (c - 1)) == 0
+    # more SMs never asks for larger chunks
+    assert B.kvs_choose_chunk_size(32, 8, 128, 8192, 152) <= \
+        B.kvs_choose_chunk_size(32, 8, 128, 8192, 76)
+    with pytest.raises(B.KvsError):
+        B.kvs_choose_chunk_size(0, 8, 128, 8192, 152)

@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA path (through the C ABI) against the f64 CPU oracle.
+
+Bar: the scattered caches are bit-identical to the expected caches (every
+byte, untouched rows included); attention outputs are within max-abs 2e-5
+and max-rel 1e-4 (relative error taken where |oracle| >= 0.2) of the oracle.
+Inputs are the seeded synthetic workloads; rows past each position are
+poisoned with NaN so any read beyond row p shows up.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import gate
+from split_flash_decoding_kvcachescatter_gb300 import binding as B
+from split_flash_decoding_kvcachescatter_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from split_flash_decoding_kvcachescatter_gb300 import build
+    build.build()
+    B.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+def run_step(t, w, chunk, status=None, ws=None, poison_ws=True):
+    """Scatter + decode through the C ABI; returns out (device)."""
+    M, H, D = t["q"].shape
+    if ws is None:
+        ws = B.workspace(M, H, w.num_kv_heads, D, w.max_len, chunk, device=DEV)
+    if poison_ws:
+        ws.fill_(0xFF)
+    out = torch.full((M, H, D), float("nan"), device=DEV)
+    B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"], t["v_cache"],
+                     d_status=status)
+    B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
+                       chunk_size=chunk, workspace=ws, d_status=status)
+    return out
+
+
+def assert_cache_bit_exact(t, expected):
+    torch.cuda.synchronize()
+    for name in ("k_cache", "v_cache"):
+        same = torch.equal(t[name].view(torch.int32), expected[name].view(torch.int32))
+        assert same, f"{name} differs from the expected scatter result"
+
+
+def oracle_out(inp):
+    return oracle.decode_sequences(inp.q, inp.k_seq, inp.v_seq, inp.positions)
+
+
+def check_workload(w, chunks, layer=0, inp=None):
+    inp = inp if inp is not None else W.make_inputs(w, layer=layer)
+    t = W.upload(inp, w, DEV)
+    exp = W.upload(inp, w, DEV, include_new_row=True)
+    ref = oracle_out(inp)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    results = {}
+    for c in chunks:
+        out = run_step(t, w, c, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, B.strerror(int(status.item()))
+        results[c] = gate(out.cpu().numpy(), ref, where=f"{w.name} chunk={c}")
+    assert_cache_bit_exact(t, exp)
+    del t, exp
+    torch.cuda.empty_cache()
+    return results
+
+
+# ---------------------------------------------------------------- workloads
+def test_tiny_full_oracle_layout():
+    """tiny: also run the oracle's own scatter on the host cache layout."""
+    w = W.WORKLOADS["tiny"]
+    inp = W.make_inputs(w)
+    t = W.upload(inp, w, DEV)
+    host_k = t["k_cache"].cpu().numpy().copy()
+    host_v = t["v_cache"].cpu().numpy().copy()
+    assert oracle.kv_scatter(inp.k_rows, inp.v_rows, inp.positions, host_k, host_v) == 0
+    ref = oracle.decode(inp.q, host_k, host_v, inp.positions)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_step(t, w, w.chunk_size, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    gate(out.cpu().numpy(), ref, where="tiny")
+    assert np.array_equal(t["k_cache"].cpu().numpy().view(np.int32), host_k.view(np.int32))
+    assert np.array_equal(t["v_cache"].cpu().numpy().view(np.int32), host_v.view(np.int32))
+
+
+def test_small_model_all_24_layers():
+    w = W.WORKLOADS["small_model"]
+    pos = W.draw_positions(w)
+    for layer in range(w.layers):
+        inp = W.make_inputs(w, layer=layer, positions=pos)
+        check_workload(w, [w.chunk_size], inp=inp)
+
+
+@pytest.mark.slow
+def test_8b_batch_with_outliers():
+    w = W.WORKLOADS["8b_batch"]
+    check_workload(w, [0, 256])
+
+
+@pytest.mark.slow
+def test_long_context_chunk_sweep():
+    w = W.WORKLOADS["long_context"]
+    check_workload(w, list(w.chunk_sweep) + [0])
+
+
+@pytest.mark.slow
+def test_ragged_serving_mix():
+    w = W.WORKLOADS["ragged"]
+    check_workload(w, [w.chunk_size])
+
+
+# ---------------------------------------------------------------- shapes
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (6, 2), (8, 2), (10, 2), (12, 2), (14, 2),
+                                   (16, 2)])
+def test_group_sizes_and_head_dims(D, H, Hkv):
+    w = W.custom(M=5, num_heads=H, num_kv_heads=Hkv, head_dim=D, max_len=700, chunk_size=100,
+                 positions="uniform", seed=31 + H + D)
+    check_workload(w, [1 if H == 4 and Hkv == 4 else 37, 100, 128, 1000])
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 33, 64, 255, 256, 4096])
+def test_chunk_sizes_ragged_tail(chunk):
+    w = W.custom(M=3, num_heads=8, num_kv_heads=2, head_dim=128, max_len=1000,
+                 chunk_size=chunk, positions="uniform", seed=5)
+    check_workload(w, [chunk])
+
+
+# ---------------------------------------------------------------- edge cases
+def test_seq_len_one_returns_v_row_bitwise():
+    w = W.custom(M=6, num_heads=8, num_kv_heads=2, head_dim=128, max_len=64,
+                 positions="fixed", fixed_position=0, seed=3)
+    inp = W.make_inputs(w)
+    t = W.upload(inp, w, DEV)
+    out = run_step(t, w, 16).cpu().numpy()
+    G = w.group
+    for i in range(w.M):
+        for h in range(w.num_heads):
+            assert np.array_equal(out[i, h].view(np.int32), inp.v_rows[i, h // G].view(np.int32))
+
+
+def test_last_position_and_mixed_lengths():
+    w = W.custom(M=4, num_heads=32, num_kv_heads=8, head_dim=128, max_len=513,
+                 positions="uniform", seed=9)
+    pos = np.array([512, 0, 1, 300], np.int32)
+    inp = W.make_inputs(w, positions=pos)
+    check_workload(w, [64, 0], inp=inp)
+
+
+def test_out_of_range_positions_flag_and_skip():
+    w = W.custom(M=4, num_heads=8, num_kv_heads=2, head_dim=64, max_len=128, seed=11)
+    pos = np.array([5, 128, -1, 127], np.int32)
+    inp = W.make_inputs(w, positions=pos)
+    t = W.upload(inp, w, DEV)
+    exp = W.upload(inp, w, DEV, include_new_row=True)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_step(t, w, 32, status).cpu().numpy()
+    assert int(status.item()) == B.KVS_ERR_POSITION
+    assert np.all(np.isnan(out[1])) and np.all(np.isnan(out[2]))
+    good = [0, 3]
+    ref = oracle.decode_sequences(inp.q[good], [inp.k_seq[i] for i in good],
+                                  [inp.v_seq[i] for i in good], pos[good])
+    gate(out[good], ref, where="valid sequences beside invalid ones")
+    assert_cache_bit_exact(t, exp)
+
+
+def test_empty_batch_is_a_no_op():
+    L = B.lib()
+    assert L.kvs_kv_scatter(None, None, None, None, None, 0, 2, 64, 16, None, None) == 0
+    assert L.kvs_flash_decode(None, None, None, None, None, 0, 4, 2, 64, 16, 8, None, 0,
+                              None, None) == 0
+
+
+def test_repeatable_and_stream_ordered():
+    """Two calls give identical bits; a non-default stream works."""
+    w = W.custom(M=8, num_heads=32, num_kv_heads=8, head_dim=128, max_len=2000, seed=13)
+    inp = W.make_inputs(w)
+    t = W.upload(inp, w, DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        a = run_step(t, w, 0)
+        b = run_step(t, w, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    gate(a.cpu().numpy(), oracle_out(inp), where="side stream")
+
+
+def test_split_entry_points_equal_fused_entry():
+    w = W.custom(M=4, num_heads=16, num_kv_heads=4, head_dim=128, max_len=900, seed=17)
+    inp = W.make_inputs(w)
+    t = W.upload(inp, w, DEV)
+    a = run_step(t, w, 128)
+    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, 128, device=DEV)
+    b = torch.empty_like(a)
+    B.kvs_flash_decode_partials(t["q"], t["k_cache"], t["v_cache"], t["positions"], 128, ws)
+    B.kvs_flash_decode_reduce(t["positions"], b, w.num_kv_heads, w.max_len, 128, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_workspace_too_small_is_rejected_before_launch():
+    w = W.custom(M=2, num_heads=4, num_kv_heads=2, head_dim=64, max_len=256, seed=19)
+    inp = W.make_inputs(w)
+    t = W.upload(inp, w, DEV)
+    n = B.kvs_flash_decode_workspace_bytes(2, 4, 2, 64, 256, 64)
+    small = torch.empty(n - 256, dtype=torch.uint8, device=DEV)
+    out = torch.zeros_like(t["q"])
+    with pytest.raises(B.KvsError) as e:
+        B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
+                           chunk_size=64, workspace=small)
+    assert e.value.status == B.KVS_ERR_WORKSPACE
+    assert torch.count_nonzero(out).item() == 0
