@@ -1,0 +1,417 @@
+"""Benchmark of one decode step of the attention hot path on GB300.
+
+A step = kvs_kv_scatter (new K/V rows into the caches) + kvs_flash_decode
+(chunk kernel + reduce kernel) for one layer of a seeded synthetic workload,
+all through the C ABI.  Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--chunk C] [--impl kvs|reference]
+
+value      : algorithmic GB/s of the step (live KV bytes read + Q read + O
+             written + positions, plus the scatter's row bytes), inputs resident
+             in HBM, device time from CUDA events, max over ranks.
+e2e        : the same metric when every step also copies its inputs (q, new K/V
+             rows, positions) from pinned host memory and reads the output back.
+roofline   : the chunk kernel alone: its algorithmic bytes / its mean
+             event-timed duration, against the measured HBM copy bandwidth.
+cpu_baseline: the f64 CPU oracle on the host cores (rank 0, N=1 only).
+--impl reference times that oracle as the reference arm.
+Under torchrun every rank runs its own batch (weak scaling, no collective on
+the data path; a barrier and a max-reduction of the timings only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from split_flash_decoding_kvcachescatter_gb300 import workloads as W  # noqa: E402
+
+METRIC = "split-K decode attention: KV-cache HBM GB/s (% of GB300 peak) and µs/call"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+CHUNK_SOURCE = os.path.join(ROOT, "split_flash_decoding_kvcachescatter_gb300", "csrc",
+                            "flash_decode.cu")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def chunk_source_hash():
+    with open(CHUNK_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(workload, chunk):
+    """Per-launch DRAM bytes of the chunk kernel from a committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "fd_chunk_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    key = f"{workload}:{chunk}"
+    e = rec.get(key)
+    if not e or e.get("source_sha256_16") != chunk_source_hash():
+        return None
+    return int(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:  # timed region shorter than the sampling interval
+            inside = rows
+            window = "warmup + timed region"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3][5:9])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+def cpu_oracle_time(inp, w, repeats):
+    """Time the oracle over the whole workload `repeats` times on all cores."""
+    import oracle
+    threads = os.cpu_count() or 1
+    oracle.build()
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.decode_sequences(inp.q, inp.k_seq, inp.v_seq, inp.positions, threads=threads)
+    return time.perf_counter() - t0, threads
+
+
+def cpu_sample_plan(inp, w, budget_s=12.0):
+    """Repeats of the whole workload that fit in about budget_s of CPU time."""
+    macs = 2.0 * w.num_heads * w.head_dim * float(inp.seq_lens.sum())
+    est = macs / 1.0e9 / max(1, (os.cpu_count() or 1))  # ~1 GMAC/s per core
+    return max(1, min(20, int(budget_s / max(est, 1e-3))))
+
+
+def run_reference(args, w, inp, rank, world):
+    if rank != 0:
+        return
+    ab = W.algorithmic_bytes(inp, w)
+    reps = cpu_sample_plan(inp, w, budget_s=3.0)
+    per_step = []
+    threads = os.cpu_count() or 1
+    for s in range(args.warmup + args.steps):
+        dt, threads = cpu_oracle_time(inp, w, reps)
+        if s >= args.warmup:
+            per_step.append(dt / reps)
+    t = sum(per_step)
+    value = ab["step"] * len(per_step) / t / 1e9
+    sample = (f"whole {w.name} workload ({w.M} sequences x {w.num_heads} heads) per step, "
+              f"{reps} passes per step averaged, f64 C oracle on {threads} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(per_step),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "num_heads": w.num_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "max_len": w.max_len, "algorithmic_bytes_per_step": ab["step"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="8b_batch", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--chunk", type=int, default=None, help="override the chunk size")
+    ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank, world, local = dist_env()
+    w = W.WORKLOADS[args.config]
+    seed = w.seed + 7919 * rank  # each rank decodes its own batch
+    inp = W.make_inputs(w, seed=seed)
+
+    if args.impl == "reference":
+        return run_reference(args, w, inp, rank, world)
+
+    import torch
+    import torch.distributed as tdist
+
+    from split_flash_decoding_kvcachescatter_gb300 import binding as B
+    from split_flash_decoding_kvcachescatter_gb300 import build as kbuild
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        tdist.init_process_group("nccl", device_id=dev)
+    kbuild.build()
+    B.lib()
+
+    def barrier():
+        if world > 1:
+            tdist.barrier()
+
+    t = W.upload(inp, w, dev)
+    chunk = args.chunk if args.chunk is not None else w.chunk_size
+    resolved_chunk = chunk if chunk > 0 else B.kvs_choose_chunk_size(
+        w.M, w.num_kv_heads, w.head_dim, w.max_len)
+    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, resolved_chunk,
+                     device=dev)
+    out = torch.empty_like(t["q"])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ab = W.algorithmic_bytes(inp, w)
+    cache_bytes = 2 * w.cache_elems() * 4
+    flush = ab["step"] < 4 * L2_BYTES  # small working sets: scrub L2 between steps
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"], t["v_cache"],
+                         d_status=status)
+        if ev is not None:
+            ev[0].record(stream)
+        B.kvs_flash_decode_partials(t["q"], t["k_cache"], t["v_cache"], t["positions"],
+                                    resolved_chunk, ws, d_status=status)
+        if ev is not None:
+            ev[1].record(stream)
+        B.kvs_flash_decode_reduce(t["positions"], out, w.num_kv_heads, w.max_len,
+                                  resolved_chunk, ws, d_status=status)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        if flush:
+            scrub.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mids = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    for k in range(K):
+        if flush:
+            scrub.zero_()
+        starts[k].record(stream)
+        step(mids[k])
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall1 = time.time()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    chunk_ms = [a.elapsed_time(b) for a, b in mids]
+    scatter_ms = [s.elapsed_time(a) for s, (a, _) in zip(starts, mids)]
+    reduce_ms = [b.elapsed_time(e) for (_, b), e in zip(mids, ends)]
+    total_ms = sum(step_ms)
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status: {B.strerror(int(status.item()))}")
+
+    # ---- e2e: host buffers through the public API ----
+    Ke = args.e2e_steps or max(3, min(K, 500))
+    host = {k: t[k].cpu().pin_memory() for k in ("q", "k_rows", "v_rows", "positions")}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dev_in = {k: torch.empty_like(t[k]) for k in host}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        B.kvs_kv_scatter(dev_in["k_rows"], dev_in["v_rows"], dev_in["positions"], t["k_cache"],
+                         t["v_cache"], d_status=status)
+        B.kvs_flash_decode(dev_in["q"], t["k_cache"], t["v_cache"], dev_in["positions"], out,
+                           chunk_size=resolved_chunk, workspace=ws, d_status=status)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        if flush:
+            scrub.zero_()
+        e2e_step()
+        # the result must be on the host before the step counts as done
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if flush:  # take the scrub time back out
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(Ke):
+            scrub.zero_()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms -= s0.elapsed_time(s1) / Ke
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
+
+    # ---- reduce over ranks ----
+    times = torch.tensor([total_ms, e2e_ms, ab["step"] * K, ab["step"] * Ke], dtype=torch.float64,
+                         device=dev)
+    if world > 1:
+        mx = times.clone()
+        tdist.all_reduce(mx[:2], op=tdist.ReduceOp.MAX)
+        sm = times.clone()
+        tdist.all_reduce(sm[2:], op=tdist.ReduceOp.SUM)
+        total_ms_max, e2e_ms_max = float(mx[0]), float(mx[1])
+        bytes_all, bytes_e2e_all = float(sm[2]), float(sm[3])
+    else:
+        total_ms_max, e2e_ms_max = total_ms, e2e_ms
+        bytes_all, bytes_e2e_all = float(ab["step"] * K), float(ab["step"] * Ke)
+
+    if rank != 0:
+        if world > 1:
+            tdist.destroy_process_group()
+        return
+
+    value = bytes_all / (total_ms_max * 1e-3) / 1e9
+    e2e_value = bytes_e2e_all / (e2e_ms_max * Ke * 1e-3) / 1e9
+    chunk_mean = statistics.mean(chunk_ms)
+    achieved = ab["chunk_kernel"] / (chunk_mean * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    traffic = ncu_traffic(w.name, resolved_chunk)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        reps = cpu_sample_plan(inp, w)
+        dt, threads = cpu_oracle_time(inp, w, reps)
+        cpu = {"value": ab["step"] * reps / dt / 1e9, "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"whole {w.name} workload ({w.M} sequences x {w.num_heads} heads, "
+                         f"{int(inp.seq_lens.sum())} cached rows per kv head), {reps} passes, "
+                         f"f64 C oracle on {threads} host threads"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": w.name, "M": w.M, "num_heads": w.num_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "max_len": w.max_len,
+            "chunk_size": resolved_chunk,
+            "chunk_rule": "given" if chunk > 0 else "library rule (chunk_size=0)",
+            "live_kv_bytes": W.kv_bytes(inp, w),
+            "algorithmic_bytes_per_step": ab["step"],
+            "cache_bytes_allocated": cache_bytes,
+            "l2": ("L2 scrubbed (2x129 MB write) between timed steps, outside the events"
+                   if flush else "inputs larger than L2 (live KV bytes >> 129 MB)"),
+            "seed": seed, "parallelism": f"replicas x{world} (independent batches)",
+        },
+        "us_per_call": {"kv_scatter": 1e3 * statistics.mean(scatter_ms),
+                        "flash_decode": 1e3 * (statistics.mean(chunk_ms)
+                                               + statistics.mean(reduce_ms)),
+                        "chunk_kernel": 1e3 * chunk_mean,
+                        "reduce_kernel": 1e3 * statistics.mean(reduce_ms),
+                        "step_median": 1e3 * statistics.median(step_ms)},
+        "attention_gbs": ab["attention"] / ((statistics.mean(chunk_ms)
+                                             + statistics.mean(reduce_ms)) * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "fd_chunk_kernel", "peak_source": peak_kind,
+                     "bytes_per_launch": ab["chunk_kernel"]},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
