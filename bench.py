@@ -144,49 +144,83 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
-def cpu_oracle_time(inp, w, repeats):
-    """Time the oracle over the whole workload `repeats` times on all cores."""
-    import oracle
-    threads = os.cpu_count() or 1
-    oracle.build()
-    t0 = time.perf_counter()
-    for _ in range(repeats):
-        oracle.decode_sequences(inp.q, inp.k_seq, inp.v_seq, inp.positions, threads=threads)
-    return time.perf_counter() - t0, threads
+def _unit_bytes(inp, w, i):
+    """Algorithmic step bytes of sequence i, shared equally by its query heads."""
+    L = int(inp.positions[i]) + 1
+    seq = (2 * w.num_kv_heads * L * w.head_dim * 4 + 2 * w.num_heads * w.head_dim * 4 + 4
+           + 4 * w.num_kv_heads * w.head_dim * 4 + 4)
+    return seq / w.num_heads
 
 
-def cpu_sample_plan(inp, w, budget_s=12.0):
-    """Repeats of the whole workload that fit in about budget_s of CPU time."""
-    macs = 2.0 * w.num_heads * w.head_dim * float(inp.seq_lens.sum())
-    est = macs / 1.0e9 / max(1, (os.cpu_count() or 1))  # ~1 GMAC/s per core
-    return max(1, min(20, int(budget_s / max(est, 1e-3))))
+class CpuOracleRunner:
+    """Runs the f64 CPU oracle over (sequence, query head) units of the
+    workload, in rotation, on all host cores (the C call releases the GIL).
+    A sample is time-bounded: batches of units run until the budget is spent."""
+
+    def __init__(self, inp, w):
+        from concurrent.futures import ThreadPoolExecutor
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.inp, self.w = inp, w
+        self.threads = os.cpu_count() or 1
+        self.pool = ThreadPoolExecutor(max_workers=self.threads)
+        self.units = [(i, h) for i in range(w.M) for h in range(w.num_heads)]
+        self.next = 0
+        self.G = w.group
+
+    def _one(self, u):
+        i, h = u
+        L = int(self.inp.positions[i]) + 1
+        g = h // self.G
+        self.oracle.attend_row(self.inp.q[i, h], self.inp.k_seq[i][g, :L], self.inp.v_seq[i][g, :L])
+        return _unit_bytes(self.inp, self.w, i)
+
+    def sample(self, budget_s):
+        """(seconds, bytes, units) of one time-bounded sample."""
+        t0 = time.perf_counter()
+        done_bytes, n = 0.0, 0
+        batch = 2 * self.threads
+        while True:
+            us = [self.units[(self.next + k) % len(self.units)] for k in range(batch)]
+            self.next = (self.next + batch) % len(self.units)
+            done_bytes += sum(self.pool.map(self._one, us))
+            n += batch
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        return time.perf_counter() - t0, done_bytes, n
+
+    def describe(self, n_units, passes=None):
+        return (f"{n_units} (sequence, query head) units of the {self.w.name} workload in "
+                f"rotation ({len(self.units)} units = the whole batch), f64 C oracle on "
+                f"{self.threads} host threads")
 
 
 def run_reference(args, w, inp, rank, world):
     if rank != 0:
         return
     ab = W.algorithmic_bytes(inp, w)
-    reps = cpu_sample_plan(inp, w, budget_s=3.0)
-    per_step = []
-    threads = os.cpu_count() or 1
+    runner = CpuOracleRunner(inp, w)
+    budget = max(0.02, min(3.0, 150.0 / (args.steps + args.warmup)))
+    tot_t, tot_b, tot_n = 0.0, 0.0, 0
     for s in range(args.warmup + args.steps):
-        dt, threads = cpu_oracle_time(inp, w, reps)
+        dt, b, n = runner.sample(budget)
         if s >= args.warmup:
-            per_step.append(dt / reps)
-    t = sum(per_step)
-    value = ab["step"] * len(per_step) / t / 1e9
-    sample = (f"whole {w.name} workload ({w.M} sequences x {w.num_heads} heads) per step, "
-              f"{reps} passes per step averaged, f64 C oracle on {threads} host threads")
+            tot_t += dt
+            tot_b += b
+            tot_n += n
+    value = tot_b / tot_t / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(per_step),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "num_heads": w.num_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "max_len": w.max_len, "algorithmic_bytes_per_step": ab["step"]},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                   "max_len": w.max_len, "algorithmic_bytes_per_step": ab["step"],
+                   "step": f"a time-bounded sample of about {budget:.2f} s of oracle work"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": runner.threads,
+                         "kind": "oracle", "sample": runner.describe(tot_n)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -366,13 +400,11 @@ def main():
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        reps = cpu_sample_plan(inp, w)
-        dt, threads = cpu_oracle_time(inp, w, reps)
-        cpu = {"value": ab["step"] * reps / dt / 1e9, "unit": "GB/s", "cores": threads,
-               "kind": "oracle",
-               "sample": f"whole {w.name} workload ({w.M} sequences x {w.num_heads} heads, "
-                         f"{int(inp.seq_lens.sum())} cached rows per kv head), {reps} passes, "
-                         f"f64 C oracle on {threads} host threads"}
+        runner = CpuOracleRunner(inp, w)
+        runner.sample(0.5)  # warm the pool and the page cache
+        dt, b, n = runner.sample(10.0)
+        cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": runner.threads, "kind": "oracle",
+               "sample": runner.describe(n)}
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
