@@ -167,6 +167,48 @@ int kvs_flash_decode_reduce(const int32_t *positions, float *out, int M,
                             size_t workspace_bytes, int *d_status,
                             kvs_stream_t stream);
 
+/*
+ * kvs_flash_decode_static -- kvs_flash_decode for callers that cannot
+ * allocate device memory (no counterpart in the pages: they always hand the
+ * kernels a preallocated partials buffer).
+ *
+ * Who needs it: code that may not call cudaMalloc at the point where it runs
+ * attention -- a process under a fixed device-memory budget that forbids
+ * allocation after start-up, a plug-in host that lends streams and tensors
+ * but no allocator, or a runtime whose own allocator must not be re-entered
+ * from inside this call.  This entry point takes only inputs and outputs
+ * and allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine).
+ *
+ * Scratch: the chunk partials go to one buffer of KVS_STATIC_WORKSPACE_BYTES
+ * compiled into the library as a device array.  Every GPU on which the
+ * library's device code is loaded holds that buffer until the process
+ * exits.  Problems whose partials need more
+ * (kvs_flash_decode_workspace_bytes(...) > KVS_STATIC_WORKSPACE_BYTES)
+ * are rejected with KVS_ERR_WORKSPACE before anything is enqueued; use
+ * kvs_flash_decode with your own workspace for those.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the buffer's device address; make that first call before any stream
+ * capture on that device.
+ *
+ * Sharing: all calls on a device use the same buffer, which keeps whatever
+ * the last call left in it.  Nothing in it has to start at zero (each call
+ * writes every partial it later reads), but calls that can overlap on the
+ * GPU -- different streams without ordering between them, or different
+ * host threads -- race on the buffer and give wrong results.  Order such
+ * calls on one stream or with events.
+ *
+ * Arguments, layouts and the other errors: exactly as kvs_flash_decode.
+ */
+#define KVS_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+
+int kvs_flash_decode_static(const float *q, const float *k_cache,
+                            const float *v_cache, const int32_t *positions,
+                            float *out, int M, int num_heads, int num_kv_heads,
+                            int head_dim, int max_len, int chunk_size,
+                            int *d_status, kvs_stream_t stream);
+
 /* Human-readable name of a kvs_status value (static string). */
 const char *kvs_strerror(int status);
 

@@ -31,7 +31,10 @@ KVS_ERR_TIMEOUT = 8
 # Every symbol include/kvsdecode.h declares.
 EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspace_bytes",
            "kvs_flash_decode", "kvs_flash_decode_partials", "kvs_flash_decode_reduce",
-           "kvs_strerror")
+           "kvs_strerror", "kvs_flash_decode_static")
+
+# Size of the library's built-in scratch buffer used by kvs_flash_decode_static.
+KVS_STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +74,9 @@ def lib() -> ctypes.CDLL:
                                                     _P, _SZ, _P, _P]
             L.kvs_flash_decode_reduce.restype = _I
             L.kvs_flash_decode_reduce.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
+                                                  _P, _P]
+            L.kvs_flash_decode_static.restype = _I
+            L.kvs_flash_decode_static.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                   _P, _P]
             L.kvs_strerror.restype = ctypes.c_char_p
             L.kvs_strerror.argtypes = [_I]
@@ -189,3 +195,17 @@ def kvs_flash_decode_reduce(positions, out, num_kv_heads, max_len, chunk_size, w
         int(chunk_size), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _status_ptr(d_status), _stream(stream))
     _check(rc, "kvs_flash_decode_reduce")
+
+
+def kvs_flash_decode_static(q, k_cache, v_cache, positions, out, chunk_size=0, d_status=None,
+                            stream=None):
+    """kvs_flash_decode without a workspace argument: the partials go to the
+    library's built-in buffer (for callers that cannot allocate device memory;
+    calls that may overlap on the GPU must be ordered, see the C header)."""
+    M, H, Hkv, D, Lmax = _attn_shapes(q, k_cache)
+    rc = lib().kvs_flash_decode_static(_f32(q, "q", 3), _f32(k_cache, "k_cache", 4),
+                                       _f32(v_cache, "v_cache", 4),
+                                       _i32(positions, "positions"), _f32(out, "out", 3), M, H,
+                                       Hkv, D, Lmax, int(chunk_size), _status_ptr(d_status),
+                                       _stream(stream))
+    _check(rc, "kvs_flash_decode_static")
