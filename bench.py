@@ -53,6 +53,25 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(w, rank):
+    """Each rank decodes its own, independent batch (weak scaling)."""
+    return w.seed + 7919 * rank
+
+
+def reduce_over_ranks(step_ms, e2e_ms, bytes_timed, bytes_e2e, world, device):
+    """Max of the timings and sum of the bytes over all ranks (the only
+    communication of a multi-rank run; nothing on the data path)."""
+    if world <= 1:
+        return float(step_ms), float(e2e_ms), float(bytes_timed), float(bytes_e2e)
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=device)
+    b = torch.tensor([bytes_timed, bytes_e2e], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    tdist.all_reduce(b, op=tdist.ReduceOp.SUM)
+    return float(t[0]), float(t[1]), float(b[0]), float(b[1])
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -243,7 +262,7 @@ def main():
 
     rank, world, local = dist_env()
     w = W.WORKLOADS[args.config]
-    seed = w.seed + 7919 * rank  # each rank decodes its own batch
+    seed = rank_seed(w, rank)
     inp = W.make_inputs(w, seed=seed)
 
     if args.impl == "reference":
@@ -373,18 +392,8 @@ def main():
     clocks = sampler.summary(wall0, wall1)
 
     # ---- reduce over ranks ----
-    times = torch.tensor([total_ms, e2e_ms, ab["step"] * K, ab["step"] * Ke], dtype=torch.float64,
-                         device=dev)
-    if world > 1:
-        mx = times.clone()
-        tdist.all_reduce(mx[:2], op=tdist.ReduceOp.MAX)
-        sm = times.clone()
-        tdist.all_reduce(sm[2:], op=tdist.ReduceOp.SUM)
-        total_ms_max, e2e_ms_max = float(mx[0]), float(mx[1])
-        bytes_all, bytes_e2e_all = float(sm[2]), float(sm[3])
-    else:
-        total_ms_max, e2e_ms_max = total_ms, e2e_ms
-        bytes_all, bytes_e2e_all = float(ab["step"] * K), float(ab["step"] * Ke)
+    total_ms_max, e2e_ms_max, bytes_all, bytes_e2e_all = reduce_over_ranks(
+        total_ms, e2e_ms, ab["step"] * K, ab["step"] * Ke, world, dev)
 
     if rank != 0:
         if world > 1:
