@@ -93,11 +93,12 @@ int kvs_kv_scatter(const float *k_rows, const float *v_rows,
                    int *d_status, kvs_stream_t stream);
 
 /*
- * kvs_choose_chunk_size -- the split-count rule used when a caller passes
- * chunk_size = 0 (the pages fix one compile-time FLASH_DECODE_CHUNK_SIZE;
- * here it depends on the shape and the SM count so that all SMs stay busy
- * at small M and long contexts while partial traffic stays small).
- * Returns a chunk size in rows (>= 1), or a negative kvs_status.
+ * kvs_choose_chunk_size -- the chunk size used when a caller passes
+ * chunk_size = 0 (the pages fix one compile-time FLASH_DECODE_CHUNK_SIZE).
+ * Chunks are the scheduling atoms of the persistent chunk kernel, so the
+ * chunk size sets how evenly the live rows are shared among the SMs; the
+ * rule returns a power of two in [16, 64] that grows with the cache size
+ * per SM.  Returns a chunk size in rows (>= 1), or a negative kvs_status.
  *   num_sms > 0: use that SM count; num_sms <= 0: query the current device.
  */
 int kvs_choose_chunk_size(int M, int num_kv_heads, int head_dim, int max_len,
@@ -105,10 +106,12 @@ int kvs_choose_chunk_size(int M, int num_kv_heads, int head_dim, int max_len,
 
 /*
  * kvs_flash_decode_workspace_bytes -- size of the scratch buffer that
- * kvs_flash_decode needs for the chunk partials (running max, running sum
- * and weighted-V accumulator of every chunk; the pages' flash_decode_partials
- * buffer).  chunk_size = 0 resolves through kvs_choose_chunk_size on the
- * current device.  Returns 0 on invalid arguments.
+ * kvs_flash_decode needs: the softmax partials (running max, running sum and
+ * weighted-V accumulator; the pages' flash_decode_partials buffer), kept
+ * for each run of consecutive chunks one block of the chunk kernel handles,
+ * plus a small table of the blocks' ranges.  The size depends on M,
+ * num_heads, num_kv_heads and head_dim only (max_len and chunk_size are
+ * validated, not used).  Returns 0 on invalid arguments.
  */
 size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads,
                                         int head_dim, int max_len,
@@ -123,9 +126,12 @@ size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads,
  * applied to v_cache[i][g][j][:], j = 0..L-1.  Rows j >= L are never read.
  *
  * The cache rows of every (sequence, kv head) are cut into chunks of
- * chunk_size rows; each chunk yields (running max, running sum, weighted-V
- * accumulator) for all G query heads of the group, reading each K/V row
- * once; a second kernel merges the chunk partials with softmax rescaling.
+ * chunk_size rows, processed in parallel by a persistent grid; each chunk
+ * yields (running max, running sum, weighted-V accumulator) for all G query
+ * heads of the group, reading each K/V row once.  Consecutive chunks of one
+ * (sequence, kv head) that land on the same block are merged as they
+ * stream; a second kernel merges the remaining partials with softmax
+ * rescaling.
  *
  *   q          in   [M][H][D] float32, device, 16-byte aligned
  *   k_cache,
@@ -152,7 +158,8 @@ int kvs_flash_decode(const float *q, const float *k_cache,
  * chunk and reduce kernels separately.  Called back to back on one stream
  * with the same arguments they are exactly kvs_flash_decode.
  *   kvs_flash_decode_partials: "Step 4" -- chunk partials into workspace.
- *   kvs_flash_decode_reduce:   "Step 5" -- rescaled merge into out.
+ *   kvs_flash_decode_reduce:   "Step 5" -- rescaled merge into out
+ *                              (chunk_size is only validated here).
  */
 int kvs_flash_decode_partials(const float *q, const float *k_cache,
                               const float *v_cache, const int32_t *positions,

@@ -11,7 +11,9 @@
 // scattered at *io.pos) and one launch covers everything.
 //
 // Work: 2*M*Hkv*D floats read and written.  It is launch-latency bound; each
-// thread moves one float4 (coalesced 16-byte loads and stores).
+// thread moves one float4 (coalesced 16-byte loads and stores).  It is
+// launched with programmatic stream serialisation, so its launch overlaps the
+// tail of the previous kernel in the stream.
 
 #include "kvs_device.cuh"
 #include "kvs_launch.h"
@@ -24,6 +26,9 @@ __global__ void __launch_bounds__(256)
                       const int32_t *__restrict__ positions,
                       float4 *__restrict__ k_cache, float4 *__restrict__ v_cache,
                       int M, int Hkv, int D4, int max_len, int *d_status) {
+  // the caches may still be read by the preceding kernel in the stream
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int64_t per_cache = (int64_t)M * Hkv * D4;  // float4s per cache
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= 2 * per_cache) return;
@@ -52,12 +57,19 @@ int launch_kv_scatter(const float *k_rows, const float *v_rows,
   const int64_t total = 2ll * M * Hkv * D4;
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
-  kv_scatter_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-      reinterpret_cast<const float4 *>(k_rows),
-      reinterpret_cast<const float4 *>(v_rows), positions,
-      reinterpret_cast<float4 *>(k_cache), reinterpret_cast<float4 *>(v_cache),
-      M, Hkv, D4, max_len, d_status);
-  return cudaGetLastError() == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
+  static bool carveout_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && !carveout_set[dev]) {
+    // the same L1/shared split as the attention kernels that follow it
+    cudaFuncSetAttribute(kv_scatter_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    carveout_set[dev] = true;
+  }
+  const cudaError_t e = launch_pdl(
+      kv_scatter_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+      reinterpret_cast<const float4 *>(k_rows), reinterpret_cast<const float4 *>(v_rows),
+      positions, reinterpret_cast<float4 *>(k_cache), reinterpret_cast<float4 *>(v_cache), M,
+      Hkv, D4, max_len, d_status);
+  return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
 }  // namespace kvs

@@ -68,14 +68,16 @@ int kvs_choose_chunk_size(int M, int num_kv_heads, int head_dim, int max_len, in
   if (!head_dim_supported(head_dim)) return -KVS_ERR_UNSUPPORTED;
   const int sms = num_sms > 0 ? num_sms : kvs::device_sm_count();
   if (sms <= 0) return -KVS_ERR_LAUNCH;
-  // Persistent grid of 2 CTAs per SM.  With a full cache, aim for at least
-  // 16 chunks per CTA (static ranges then stay within ~6% of balanced) while
-  // keeping chunks >= 64 rows so partial traffic stays small.
-  const int64_t ctas = 2ll * sms;
-  const int64_t rows = (int64_t)M * num_kv_heads * max_len;
-  const int64_t target = rows / (16 * ctas);
-  int c = 64;
-  while (c < 1024 && 2ll * c <= target) c <<= 1;
+  // Chunks are the scheduling atoms of the persistent chunk kernel: a block's
+  // range starts and ends on chunk boundaries, so the chunk size is the
+  // granularity of the load balance (a block holds its 1/P share of the live
+  // rows to within one chunk).  Partials are kept per run of chunks, so small
+  // chunks cost no extra partial traffic.  Aim for about 1/128 of a block's
+  // share of a full cache, as a power of two in [16, 64].
+  const int64_t blocks = 2ll * sms;
+  const int64_t share = (int64_t)M * num_kv_heads * max_len / blocks;
+  int c = 16;
+  while (c < 64 && 2ll * c * 128 <= share) c <<= 1;
   return c;
 }
 
@@ -84,9 +86,9 @@ size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads, 
   if (check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size) != KVS_OK)
     return 0;
   if (M == 0) return 0;
-  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
-  if (chunk <= 0) return 0;
-  return kvs::partial_layout(M, num_heads, head_dim, max_len, chunk).total_bytes;
+  // The partials are kept per run of chunks (see kvs_launch.h), so the size
+  // depends on neither max_len nor the chunk size.
+  return kvs::ws_layout(M, num_kv_heads, num_heads / num_kv_heads, head_dim).total;
 }
 
 int kvs_flash_decode_partials(const float *q, const float *k_cache, const float *v_cache,
@@ -104,7 +106,7 @@ int kvs_flash_decode_partials(const float *q, const float *k_cache, const float 
   if (chunk <= 0) return -chunk;
   if (!workspace) return KVS_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KVS_ERR_ALIGN;
-  if (workspace_bytes < kvs::partial_layout(M, num_heads, head_dim, max_len, chunk).total_bytes)
+  if (workspace_bytes < kvs::ws_layout(M, num_kv_heads, num_heads / num_kv_heads, head_dim).total)
     return KVS_ERR_WORKSPACE;
   return kvs::launch_fd_chunks(q, k_cache, v_cache, positions, M, num_heads, num_kv_heads,
                                head_dim, max_len, chunk, workspace, d_status,
@@ -120,13 +122,11 @@ int kvs_flash_decode_reduce(const int32_t *positions, float *out, int M, int num
   if (M == 0) return KVS_OK;
   if (!out || !positions) return KVS_ERR_NULL;
   if (!aligned(out, 16) || !aligned(positions, 4)) return KVS_ERR_ALIGN;
-  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
-  if (chunk <= 0) return -chunk;
   if (!workspace) return KVS_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KVS_ERR_ALIGN;
-  if (workspace_bytes < kvs::partial_layout(M, num_heads, head_dim, max_len, chunk).total_bytes)
+  if (workspace_bytes < kvs::ws_layout(M, num_kv_heads, num_heads / num_kv_heads, head_dim).total)
     return KVS_ERR_WORKSPACE;
-  return kvs::launch_fd_reduce(positions, out, M, num_heads, head_dim, max_len, chunk,
+  return kvs::launch_fd_reduce(positions, out, M, num_heads, num_kv_heads, head_dim, max_len,
                                workspace, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
 

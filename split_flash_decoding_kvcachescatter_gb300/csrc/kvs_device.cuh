@@ -19,6 +19,17 @@ __device__ __forceinline__ void record_status(int *d_status, int code) {
   if (d_status != nullptr) atomicCAS(d_status, 0, code);
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its memory is visible (a no-op when the kernel
+// was launched without programmatic stream serialisation) ...
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// ... and let the next kernel in the stream start launching now.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

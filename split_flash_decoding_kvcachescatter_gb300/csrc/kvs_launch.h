@@ -2,48 +2,87 @@
 // and the kernel launchers.  Not installed; not part of the C ABI.
 #pragma once
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace kvs {
 
-// Workspace layout of the chunk partials, shared by the chunk and reduce
-// kernels.  For sequence i, query head h, chunk c (n_max = ceil(Lmax / C)):
-//   acc [((i*H + h)*n_max + c)*D + d]   weighted-V accumulator, float32
-//   ml  [((i*H + h)*n_max + c)*2 + 0]   running max of the scores (log2 units)
-//   ml  [((i*H + h)*n_max + c)*2 + 1]   running sum exp2(s - max)
-struct PartialLayout {
-  int64_t n_max;
-  size_t acc_bytes;  // offset of ml
-  size_t total_bytes;
-};
+// Upper bound on the chunk kernel's persistent grid (GB300: 152 SMs x 2).
+constexpr int kMaxChunkBlocks = 1024;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline PartialLayout partial_layout(int M, int H, int D, int max_len,
-                                    int chunk) {
-  PartialLayout p;
-  p.n_max = ((int64_t)max_len + chunk - 1) / chunk;
-  const size_t slots = (size_t)M * (size_t)H * (size_t)p.n_max;
-  p.acc_bytes = align_up(slots * (size_t)D * sizeof(float), 256);
-  p.total_bytes = p.acc_bytes + align_up(slots * 2 * sizeof(float), 256);
-  return p;
+// Workspace of kvs_flash_decode, shared by the chunk and reduce kernels.
+//   header  int num_blocks (the chunk kernel's grid size)
+//   table   int4 [kMaxChunkBlocks]: block b's first chunk (i, g, c) and
+//           whether the block has work (w); sorted by chunk.
+//   ml      float2 [slots][G]: (running max in log2 units, running sum)
+//   acc     float  [slots][G][D]: unnormalised weighted-V accumulator
+// A partial slot belongs to one run of consecutive chunks of one (i, g):
+//   slot i*Hkv + g          the run that starts at chunk 0 of (i, g)
+//   slot M*Hkv + b          the first run of block b, when it starts inside (i, g)
+// so slots = M*Hkv + kMaxChunkBlocks, independent of max_len and chunk size.
+struct WsLayout {
+  size_t off_table, off_ml, off_acc, total;
+  int64_t slots;
+};
+
+inline WsLayout ws_layout(int M, int Hkv, int G, int D) {
+  WsLayout l;
+  l.slots = (int64_t)M * Hkv + kMaxChunkBlocks;
+  l.off_table = 256;
+  l.off_ml = align_up(l.off_table + (size_t)kMaxChunkBlocks * 16, 256);
+  l.off_acc = align_up(l.off_ml + (size_t)l.slots * G * 8, 256);
+  l.total = align_up(l.off_acc + (size_t)l.slots * G * D * 4, 256);
+  return l;
 }
 
-int launch_kv_scatter(const float *k_rows, const float *v_rows,
-                      const int32_t *positions, float *k_cache, float *v_cache,
-                      int M, int Hkv, int D, int max_len, int *d_status,
-                      cudaStream_t stream);
+struct WsView {
+  int *num_blocks;
+  int4 *table;
+  float2 *ml;
+  float *acc;
+};
+
+inline WsView workspace_view(void *base, int M, int Hkv, int G, int D) {
+  const WsLayout l = ws_layout(M, Hkv, G, D);
+  unsigned char *p = static_cast<unsigned char *>(base);
+  return WsView{reinterpret_cast<int *>(p), reinterpret_cast<int4 *>(p + l.off_table),
+                reinterpret_cast<float2 *>(p + l.off_ml), reinterpret_cast<float *>(p + l.off_acc)};
+}
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// its predecessor in the stream finishes; every kernel of this library
+// executes griddepcontrol.wait before it touches global memory, so results
+// are those of plain stream order.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+int launch_kv_scatter(const float *k_rows, const float *v_rows, const int32_t *positions,
+                      float *k_cache, float *v_cache, int M, int Hkv, int D, int max_len,
+                      int *d_status, cudaStream_t stream);
 
 int launch_fd_chunks(const float *q, const float *k_cache, const float *v_cache,
-                     const int32_t *positions, int M, int H, int Hkv, int D,
-                     int max_len, int chunk, void *workspace, int *d_status,
-                     cudaStream_t stream);
+                     const int32_t *positions, int M, int H, int Hkv, int D, int max_len,
+                     int chunk, void *workspace, int *d_status, cudaStream_t stream);
 
-int launch_fd_reduce(const int32_t *positions, float *out, int M, int H, int D,
-                     int max_len, int chunk, const void *workspace,
-                     int *d_status, cudaStream_t stream);
+int launch_fd_reduce(const int32_t *positions, float *out, int M, int H, int Hkv, int D,
+                     int max_len, const void *workspace, int *d_status, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device); <= 0 on error.
 int device_sm_count();

@@ -99,13 +99,20 @@ def test_flash_decode_empty_batch_ok(L):
 
 
 def test_workspace_bytes_formula(L):
-    # acc [M][H][n][D] f32 + ml [M][H][n][2] f32, each rounded up to 256 bytes
+    # 256-byte header, a 1024-entry int4 block table, then per partial slot
+    # (M*Hkv + 1024 slots, G query heads each) a float2 (m, l) and D floats
+    # of accumulator; every section starts on a 256-byte boundary.
+    up = lambda x: -(-x // 256) * 256
     for (M, H, Hkv, D, Lmax, C) in [(1, 4, 2, 64, 256, 64), (8, 32, 8, 128, 32768, 128),
                                     (32, 40, 8, 128, 131072, 256), (3, 8, 2, 128, 1000, 7)]:
-        n = -(-Lmax // C)
-        acc = -(-(M * H * n * D * 4) // 256) * 256
-        ml = -(-(M * H * n * 2 * 4) // 256) * 256
-        assert B.kvs_flash_decode_workspace_bytes(M, H, Hkv, D, Lmax, C) == acc + ml
+        G = H // Hkv
+        slots = M * Hkv + 1024
+        off_ml = up(256 + 1024 * 16)
+        off_acc = up(off_ml + slots * G * 8)
+        assert B.kvs_flash_decode_workspace_bytes(M, H, Hkv, D, Lmax, C) == up(off_acc + slots * G * D * 4)
+        # independent of max_len and chunk size
+        assert B.kvs_flash_decode_workspace_bytes(M, H, Hkv, D, 7, 1) == \
+            B.kvs_flash_decode_workspace_bytes(M, H, Hkv, D, Lmax, C)
     assert B.kvs_flash_decode_workspace_bytes(1, 6, 4, 64, 16, 8) == 0
 
 
@@ -114,7 +121,7 @@ def test_chunk_rule_is_pow2_in_range(L):
         for (M, Hkv, D, Lmax) in [(1, 2, 64, 256), (32, 8, 128, 8192), (8, 8, 128, 32768),
                                   (32, 8, 128, 131072), (1, 1, 128, 1 << 20)]:
             c = B.kvs_choose_chunk_size(M, Hkv, D, Lmax, sms)
-            assert 64 <= c <= 1024 and (c & (c - 1)) == 0
+            assert 16 <= c <= 64 and (c & (c - 1)) == 0
     # more SMs never asks for larger chunks
     assert B.kvs_choose_chunk_size(32, 8, 128, 8192, 152) <= \
         B.kvs_choose_chunk_size(32, 8, 128, 8192, 76)

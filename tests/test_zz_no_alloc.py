@@ -63,10 +63,10 @@ def test_static_workspace_entry_matches_workspace_entry():
 def test_static_workspace_entry_rejects_problems_beyond_its_buffer():
     kbuild.build()
     L = B.lib()
-    # 32 sequences x 40 heads x 512 chunks x 130 floats needs ~341 MB of partials
-    need = B.kvs_flash_decode_workspace_bytes(32, 40, 8, 128, 131072, 256)
+    # 1024 sequences x 8 kv heads x 8 query heads per group: ~37 MB of partials
+    need = B.kvs_flash_decode_workspace_bytes(1024, 64, 8, 128, 4096, 64)
     assert need > B.KVS_STATIC_WORKSPACE_BYTES
     fake = 1 << 20  # never dereferenced: the size check comes first
-    rc = L.kvs_flash_decode_static(fake, fake, fake, fake, fake, 32, 40, 8, 128, 131072, 256,
+    rc = L.kvs_flash_decode_static(fake, fake, fake, fake, fake, 1024, 64, 8, 128, 4096, 64,
                                    None, None)
     assert rc == B.KVS_ERR_WORKSPACE
