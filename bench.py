@@ -1,8 +1,10 @@
 """Benchmark of one decode step of the attention hot path on GB300.
 
-A step = kvs_kv_scatter (new K/V rows into the caches) + kvs_flash_decode
-(chunk kernel + reduce kernel) for one layer of a seeded synthetic workload,
-all through the C ABI.  Prints ONE JSON line (rank 0).
+A step = one layer's decode step of a seeded synthetic workload through the C
+ABI: kvs_decode_step, i.e. the KV-cache scatter of the new rows, the split
+plan, the chunk partials and the rescaled merge, all in one kernel launch.
+The same step as kvs_kv_scatter + kvs_flash_decode (two launches) is timed
+beside it for the per-call breakdown.  Prints ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
                     [--chunk C] [--impl kvs|reference]
@@ -12,8 +14,9 @@ value      : algorithmic GB/s of the step (live KV bytes read + Q read + O
              in HBM, device time from CUDA events, max over ranks.
 e2e        : the same metric when every step also copies its inputs (q, new K/V
              rows, positions) from pinned host memory and reads the output back.
-roofline   : the chunk kernel alone: its algorithmic bytes / its mean
-             event-timed duration, against the measured HBM copy bandwidth.
+roofline   : the step kernel (the step's one launch): its algorithmic bytes /
+             its mean event-timed duration, against the measured HBM copy
+             bandwidth.
 cpu_baseline: the f64 CPU oracle on the host cores (rank 0, N=1 only).
 --impl reference times that oracle as the reference arm.
 Under torchrun every rank runs its own batch (weak scaling, no collective on
@@ -301,17 +304,20 @@ def main():
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
+    def step():
+        """The whole hot path in one launch: scatter, split plan, chunk
+        partials and the rescaled merge (kvs_decode_step)."""
+        B.kvs_decode_step(t["q"], t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
+                          t["v_cache"], out, chunk_size=resolved_chunk, workspace=ws,
+                          d_status=status)
+
+    def two_calls(mid):
+        """The same step as the two separate entry points, an event between."""
         B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"], t["v_cache"],
                          d_status=status)
-        if ev is not None:
-            ev[0].record(stream)
-        B.kvs_flash_decode_partials(t["q"], t["k_cache"], t["v_cache"], t["positions"],
-                                    resolved_chunk, ws, d_status=status)
-        if ev is not None:
-            ev[1].record(stream)
-        B.kvs_flash_decode_reduce(t["positions"], out, w.num_kv_heads, w.max_len,
-                                  resolved_chunk, ws, d_status=status)
+        mid.record(stream)
+        B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
+                           chunk_size=resolved_chunk, workspace=ws, d_status=status)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -340,23 +346,22 @@ def main():
     wall1 = time.time()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
-    # Region B (per-kernel breakdown, same steps): events between the kernels.
+    # Region B (breakdown): the step as kvs_kv_scatter + kvs_flash_decode,
+    # an event between the two launches.
     KB = min(K, 500)
     b_start = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
     b_end = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
-    mids = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(KB)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
     torch.cuda.synchronize()
     for k in range(KB):
         if flush:
             scrub.zero_()
         b_start[k].record(stream)
-        step(mids[k])
+        two_calls(mids[k])
         b_end[k].record(stream)
     torch.cuda.synchronize()
-    chunk_ms = [a.elapsed_time(b) for a, b in mids]
-    scatter_ms = [s.elapsed_time(a) for s, (a, _) in zip(b_start, mids)]
-    reduce_ms = [b.elapsed_time(e) for (_, b), e in zip(mids, b_end)]
+    scatter_ms = [s.elapsed_time(m) for s, m in zip(b_start, mids)]
+    decode_ms = [m.elapsed_time(e) for m, e in zip(mids, b_end)]
     if int(status.item()) != 0:
         raise SystemExit(f"device status: {B.strerror(int(status.item()))}")
 
@@ -371,10 +376,9 @@ def main():
     def e2e_step():
         for k in host:
             dev_in[k].copy_(host[k], non_blocking=True)
-        B.kvs_kv_scatter(dev_in["k_rows"], dev_in["v_rows"], dev_in["positions"], t["k_cache"],
-                         t["v_cache"], d_status=status)
-        B.kvs_flash_decode(dev_in["q"], t["k_cache"], t["v_cache"], dev_in["positions"], out,
-                           chunk_size=resolved_chunk, workspace=ws, d_status=status)
+        B.kvs_decode_step(dev_in["q"], dev_in["k_rows"], dev_in["v_rows"], dev_in["positions"],
+                          t["k_cache"], t["v_cache"], out, chunk_size=resolved_chunk,
+                          workspace=ws, d_status=status)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -416,8 +420,10 @@ def main():
 
     value = bytes_all / (total_ms_max * 1e-3) / 1e9
     e2e_value = bytes_e2e_all / (e2e_ms_max * Ke * 1e-3) / 1e9
-    chunk_mean = statistics.mean(chunk_ms)
-    achieved = ab["chunk_kernel"] / (chunk_mean * 1e-3) / 1e9
+    # The step is one launch of the step kernel, so the headline events time
+    # exactly that kernel: its algorithmic bytes are the step's.
+    step_mean_ms = total_ms / K
+    achieved = ab["step"] / (step_mean_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     traffic = ncu_traffic(w.name, resolved_chunk)
 
@@ -445,23 +451,19 @@ def main():
                    if flush else "inputs larger than L2 (live KV bytes >> 129 MB)"),
             "seed": seed, "parallelism": f"replicas x{world} (independent batches)",
         },
-        "us_per_call": {"step_mean": 1e3 * total_ms / K,
+        "us_per_call": {"decode_step": 1e3 * step_mean_ms,
+                        "decode_step_median": 1e3 * statistics.median(step_ms),
                         "kv_scatter": 1e3 * statistics.mean(scatter_ms),
-                        "flash_decode": 1e3 * (statistics.mean(chunk_ms)
-                                               + statistics.mean(reduce_ms)),
-                        "chunk_kernel": 1e3 * chunk_mean,
-                        "reduce_kernel": 1e3 * statistics.mean(reduce_ms),
-                        "step_median": 1e3 * statistics.median(step_ms),
+                        "flash_decode": 1e3 * statistics.mean(decode_ms),
                         "breakdown_steps": KB},
-        "attention_gbs": ab["attention"] / ((statistics.mean(chunk_ms)
-                                             + statistics.mean(reduce_ms)) * 1e-3) / 1e9,
+        "attention_gbs": ab["attention"] / (statistics.mean(decode_ms) * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "fd_chunk_kernel", "peak_source": peak_kind,
-                     "bytes_per_launch": ab["chunk_kernel"]},
+                     "kernel": "fd_step_kernel (kvs_decode_step)", "peak_source": peak_kind,
+                     "bytes_per_launch": ab["step"]},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
-        "gpu_launches": 3 * K,
+        "gpu_launches": K,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

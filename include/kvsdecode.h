@@ -118,8 +118,8 @@ size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads,
                                         int chunk_size);
 
 /*
- * kvs_flash_decode -- "Step 4" + "Step 5" of flash_decoding_attention_into:
- * split-K decode attention over the scattered cache.
+ * kvs_flash_decode -- "Step 3" to "Step 5" of flash_decoding_attention_into:
+ * split-K decode attention over the scattered cache, in one kernel launch.
  *
  * For every sequence i (L = positions[i] + 1) and query head h (kv head
  * g = h / G):  out[i][h][:] = softmax_j( q[i][h] . k_cache[i][g][j] / sqrt(D) )
@@ -129,9 +129,9 @@ size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads,
  * chunk_size rows, processed in parallel by a persistent grid; each chunk
  * yields (running max, running sum, weighted-V accumulator) for all G query
  * heads of the group, reading each K/V row once.  Consecutive chunks of one
- * (sequence, kv head) that land on the same block are merged as they
- * stream; a second kernel merges the remaining partials with softmax
- * rescaling.
+ * (sequence, kv head) handled by the same block merge as they stream; the
+ * block that completes a (sequence, kv head) merges its partials with
+ * softmax rescaling and writes the output.
  *
  *   q          in   [M][H][D] float32, device, 16-byte aligned
  *   k_cache,
@@ -154,25 +154,24 @@ int kvs_flash_decode(const float *q, const float *k_cache,
                      kvs_stream_t stream);
 
 /*
- * The two halves of kvs_flash_decode, for callers that time or schedule the
- * chunk and reduce kernels separately.  Called back to back on one stream
- * with the same arguments they are exactly kvs_flash_decode.
- *   kvs_flash_decode_partials: "Step 4" -- chunk partials into workspace.
- *   kvs_flash_decode_reduce:   "Step 5" -- rescaled merge into out
- *                              (chunk_size is only validated here).
+ * kvs_decode_step -- one whole decode step of the attention path: exactly
+ * kvs_kv_scatter(k_rows, v_rows, positions, k_cache, v_cache) followed by
+ * kvs_flash_decode(q, k_cache, v_cache, positions, out), in ONE kernel
+ * launch (the pages' flash_decoding_attention_into, Steps 1-5).  The
+ * attention reads row p of every sequence from k_rows / v_rows directly, so
+ * it does not wait for the cache write.
+ *
+ *   k_rows, v_rows    in   [M][Hkv][D] float32, device, 16-byte aligned
+ *   k_cache, v_cache  in/out [M][Hkv][Lmax][D]: row p of each sequence is
+ *                     written; rows 0..p-1 are read
+ *   other arguments, layouts and errors: as kvs_kv_scatter and
+ *   kvs_flash_decode (one workspace of kvs_flash_decode_workspace_bytes).
  */
-int kvs_flash_decode_partials(const float *q, const float *k_cache,
-                              const float *v_cache, const int32_t *positions,
-                              int M, int num_heads, int num_kv_heads,
-                              int head_dim, int max_len, int chunk_size,
-                              void *workspace, size_t workspace_bytes,
-                              int *d_status, kvs_stream_t stream);
-
-int kvs_flash_decode_reduce(const int32_t *positions, float *out, int M,
-                            int num_heads, int num_kv_heads, int head_dim,
-                            int max_len, int chunk_size, void *workspace,
-                            size_t workspace_bytes, int *d_status,
-                            kvs_stream_t stream);
+int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
+                    const int32_t *positions, float *k_cache, float *v_cache,
+                    float *out, int M, int num_heads, int num_kv_heads,
+                    int head_dim, int max_len, int chunk_size, void *workspace,
+                    size_t workspace_bytes, int *d_status, kvs_stream_t stream);
 
 /*
  * kvs_flash_decode_static -- kvs_flash_decode for callers that cannot

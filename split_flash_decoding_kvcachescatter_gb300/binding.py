@@ -30,8 +30,7 @@ KVS_ERR_TIMEOUT = 8
 
 # Every symbol include/kvsdecode.h declares.
 EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspace_bytes",
-           "kvs_flash_decode", "kvs_flash_decode_partials", "kvs_flash_decode_reduce",
-           "kvs_strerror", "kvs_flash_decode_static")
+           "kvs_flash_decode", "kvs_decode_step", "kvs_strerror", "kvs_flash_decode_static")
 
 # Size of the library's built-in scratch buffer used by kvs_flash_decode_static.
 KVS_STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024
@@ -69,12 +68,9 @@ def lib() -> ctypes.CDLL:
             L.kvs_flash_decode.restype = _I
             L.kvs_flash_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                            _P, _SZ, _P, _P]
-            L.kvs_flash_decode_partials.restype = _I
-            L.kvs_flash_decode_partials.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
-                                                    _P, _SZ, _P, _P]
-            L.kvs_flash_decode_reduce.restype = _I
-            L.kvs_flash_decode_reduce.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
-                                                  _P, _P]
+            L.kvs_decode_step.restype = _I
+            L.kvs_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                          _P, _SZ, _P, _P]
             L.kvs_flash_decode_static.restype = _I
             L.kvs_flash_decode_static.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                   _P, _P]
@@ -177,24 +173,22 @@ def kvs_flash_decode(q, k_cache, v_cache, positions, out, chunk_size=0, workspac
     _check(rc, "kvs_flash_decode")
 
 
-def kvs_flash_decode_partials(q, k_cache, v_cache, positions, chunk_size, workspace,
-                              d_status=None, stream=None):
+def kvs_decode_step(q, k_rows, v_rows, positions, k_cache, v_cache, out, chunk_size=0,
+                    workspace=None, d_status=None, stream=None):
+    """kvs_kv_scatter + kvs_flash_decode of one layer's decode step, in one launch."""
     M, H, Hkv, D, Lmax = _attn_shapes(q, k_cache)
-    rc = lib().kvs_flash_decode_partials(
-        _f32(q, "q", 3), _f32(k_cache, "k_cache", 4), _f32(v_cache, "v_cache", 4),
-        _i32(positions, "positions"), M, H, Hkv, D, Lmax, int(chunk_size), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _status_ptr(d_status), _stream(stream))
-    _check(rc, "kvs_flash_decode_partials")
-
-
-def kvs_flash_decode_reduce(positions, out, num_kv_heads, max_len, chunk_size, workspace,
-                            d_status=None, stream=None):
-    M, H, D = out.shape
-    rc = lib().kvs_flash_decode_reduce(
-        _i32(positions, "positions"), _f32(out, "out", 3), M, H, num_kv_heads, D, max_len,
-        int(chunk_size), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        _status_ptr(d_status), _stream(stream))
-    _check(rc, "kvs_flash_decode_reduce")
+    if workspace is None:
+        raise ValueError("kvs_decode_step: pass a workspace (see binding.workspace)")
+    if tuple(k_rows.shape) != (M, Hkv, D) or tuple(v_rows.shape) != (M, Hkv, D) or \
+            tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("kvs_decode_step: inconsistent shapes")
+    rc = lib().kvs_decode_step(_f32(q, "q", 3), _f32(k_rows, "k_rows", 3),
+                               _f32(v_rows, "v_rows", 3), _i32(positions, "positions"),
+                               _f32(k_cache, "k_cache", 4), _f32(v_cache, "v_cache", 4),
+                               _f32(out, "out", 3), M, H, Hkv, D, Lmax, int(chunk_size),
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _status_ptr(d_status), _stream(stream))
+    _check(rc, "kvs_decode_step")
 
 
 def kvs_flash_decode_static(q, k_cache, v_cache, positions, out, chunk_size=0, d_status=None,

@@ -1,36 +1,47 @@
-// flash_decode.cu -- split-K decode attention for sm_103a: the chunk kernel
-// (softmax partials over runs of cache chunks) and the reduce kernel (the
-// rescaled merge of the partials).
+// flash_decode.cu -- the decode-step attention kernel for sm_103a: split-K
+// flash decoding in ONE persistent kernel per call (split plan, chunk
+// partials, rescaled merge), optionally with the KV-cache scatter of the
+// same step folded in.
 //
 // Source: realizar 0.8.5, src/cuda/executor/head_dim.rs,
 // flash_decoding_attention_into (PAR-118): doc comment (split the KV cache
 // into chunks processed in parallel, then merge the partial results with
-// softmax rescaling), "Step 3: Compute max chunks needed" (a sequence of
-// length L has ceil(L / chunk) chunks), "Step 4" (chunk kernel, launched
-// there with one 32-thread block per (query head, sequence, chunk)), "Step
-// 5" (reduce kernel, one block per (query head, sequence)).
+// softmax rescaling), "Step 1: Scatter K/V to caches", "Step 3: Compute max
+// chunks needed" (a sequence of length L has ceil(L / chunk) chunks), "Step
+// 4" (chunk kernel, one 32-thread block per (query head, sequence, chunk))
+// and "Step 5" (reduce kernel, one block per (query head, sequence)).
 //
 // GB300 design (what differs from the pages):
 //  * Scheduling atom = chunk (sequence i, kv head g, chunk c) of `chunk`
 //    cache rows, ordered (i, g, c).  One chunk serves all G = H/Hkv query
 //    heads of its group, so every K/V byte leaves HBM once per call (the
 //    pages' per-query-head blocks read each row G times).
-//  * Persistent grid: #SMs x (CTAs per SM) blocks.  Block b takes the chunks
-//    whose first cache row falls in its 1/P share of all live rows
-//    (balanced by rows, so partial last chunks do not unbalance the SMs).
-//    Lengths, chunk counts and ranges are derived on the device from the
-//    device-resident positions.
-//  * A block merges consecutive chunks of the same (i, g) on the fly: its
-//    online-softmax state simply continues, so it writes ONE partial per run
-//    of chunks, not one per chunk.  A run that starts at chunk 0 owns partial
-//    slot i*Hkv + g; a run that starts inside (i, g) is the first run of its
-//    block b and owns slot M*Hkv + b.  Each block records its first chunk in a
-//    small table so the reduce can find the runs of any (i, g).
-//  * Warp-specialised block: one producer warp streams each run's K and V
-//    rows (contiguous ranges in the [Lmax][D] layout) and the group's q rows
-//    into a ring of shared-memory stages with 1-D bulk asynchronous copies
-//    (TMA, cp.async.bulk + mbarrier transaction counts); NW consumer warps
-//    compute.  Every wait is bounded in time.
+//  * Persistent grid of P blocks (#SMs x blocks per SM).  The live (i, g),
+//    in (i, g) order, are laid out in a "cost row" space where (i, g) takes
+//    L + cost rows (cost = the fixed price of a run, ~40 KB of K+V rows).
+//    That space is cut into P equal columns; block b takes the chunks that
+//    start in column b, so blocks get equal rows plus run overheads even when
+//    many sequences are short.  Lengths and columns are derived on the device
+//    from the device-resident positions.
+//  * A block merges consecutive chunks of one (i, g) on the fly (its
+//    online-softmax state just continues) and writes one partial per run:
+//    the run that starts at chunk 0 of (i, g) owns slot i*Hkv + g; a block's
+//    first run, when it starts inside (i, g), owns slot M*Hkv + b.
+//  * Merge without a second kernel: every run adds its row count to a
+//    per-(i, g) counter; the block whose run completes the L rows of (i, g)
+//    merges all of (i, g)'s runs (found from the same column arithmetic) and
+//    writes the output.  A (i, g) covered by a single run is written
+//    directly.  The counters carry the tag of the call that last used them,
+//    so the workspace needs no initialisation.
+//  * Scatter folded in (kvs_decode_step): blocks first write the step's new
+//    K/V rows into the caches; the attention reads row p of each sequence
+//    from the new-row input itself, so no block waits for another.
+//  * Warp-specialised block: the producer warp computes the block's range and
+//    one of its lanes streams each run's K and V rows (contiguous ranges of the
+//    [Lmax][D] layout) and the group's q rows into a ring of shared-memory
+//    stages with 1-D bulk asynchronous copies (TMA, cp.async.bulk + mbarrier
+//    transaction counts), writing a small descriptor per stage.  NW consumer
+//    warps follow the descriptors.  Every wait is bounded in time.
 //  * Consumer warp tile: RW rows x G heads.  Lanes split head_dim (one
 //    float4 per lane per row); q for the G heads lives in registers,
 //    pre-multiplied by log2(e)/sqrt(D) so the softmax runs in base 2.  The
@@ -38,17 +49,17 @@
 //    (each shuffle level halves the values a lane holds), leaving one score
 //    per lane.  Per tile and head: tile max -> running max, rescale factor,
 //    exp2 of the lane's own score, then P.V with float4 reads of V.
-//  * End of a run: the NW warps' (max, sum, acc) states merge in shared
-//    memory into the run's partial: acc (unnormalised), m, l.
-//  * Kernels are launched with programmatic stream serialisation: each one
-//    waits (griddepcontrol.wait) before touching global memory, so the
-//    launch of the next kernel overlaps the tail of the previous one.
+//  * Launched with programmatic stream serialisation: it waits
+//    (griddepcontrol.wait) before touching global memory, so its launch
+//    overlaps the tail of the previous kernel in the stream.
 //
 // Partial semantics (per query head, run R of rows):
 //   m = max_{j in R} s_j,  l = sum exp2(s_j - m),  acc = sum exp2(s_j - m) v_j,
 //   s_j = log2(e) q.k_j / sqrt(D).
-// Reduce: M* = max m,  out = sum 2^(m - M*) acc / sum 2^(m - M*) l.
+// Merge: M* = max m,  out = sum 2^(m - M*) acc / sum 2^(m - M*) l.
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <mutex>
 
@@ -70,8 +81,32 @@ __host__ __device__ constexpr int ilog2(int x) {
   return l;
 }
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
+
+// Stage descriptor written by the producer, read by the consumers.
+constexpr int kRunStart = 1;  // first stage of a run: the stage also holds q
+constexpr int kRunEnd = 2;    // last stage of a run: merge, write the partial
+constexpr int kNoMore = 4;    // no stage: the block is done
+struct StageDesc {
+  int flags;
+  int nrows;     // rows in this stage
+  int ig;        // i * Hkv + g
+  int run_rows;  // rows of the whole run
+  int L;         // length of sequence i
+  int pad;
+  long long slot;  // partial slot of the run
+  long long S;     // first row of (i, g) in the (i, g, row) order
+};
+
+// Fixed price of one run, in bytes of K+V rows: it sets the `cost` rows that
+// each (i, g) adds to the balanced split (40 rows at D = 128, 80 at D = 64).
+constexpr int kRunCostBytes = 40960;
+
+// Scratch of the (i, g) merge (aliases the warp-state merge area).
+constexpr int kMergeWindow = 32;  // runs weighted per pass
+constexpr int kMergeScratchBytes = kMergeWindow * 4 + kMergeWindow * 8 * 4 + 8 * 4 * 2 + 16;
 
 // Compile-time geometry of one (head_dim, group) instantiation.
 template <int D_, int G_>
@@ -99,17 +134,20 @@ struct Geo {
   static constexpr int OFF_P = OFF_SCORE + SCORE_BYTES;
   static constexpr int P_BYTES = NW * RW * GP * 4;
   static constexpr int OFF_MACC = round_up(OFF_P + P_BYTES, 128);
-  static constexpr int MACC_BYTES = NW * G * D * 4;
-  static constexpr int OFF_MM = OFF_MACC + MACC_BYTES;
+  static constexpr int MACC_BYTES = cmax(NW * G * D * 4, kMergeScratchBytes);
+  static constexpr int OFF_MM = OFF_MACC + round_up(MACC_BYTES, 16);
   static constexpr int OFF_ML = OFF_MM + round_up(NW * G * 4, 16);
   static constexpr int OFF_MLL = OFF_ML + round_up(NW * G * 4, 16);
-  static constexpr int OFF_BAR = round_up(OFF_MLL + NW * 32 * 4, 16);
-  static constexpr int OFF_INFO = OFF_BAR + (2 * S + 1) * 8;  // 4 x int64
-  static constexpr int OFF_FLAG = OFF_INFO + 32;              // abort, no_abort
+  static constexpr int OFF_DESC = round_up(OFF_MLL + NW * 32 * 4, 16);
+  static constexpr int OFF_BAR = OFF_DESC + S * (int)sizeof(StageDesc);
+  static constexpr int OFF_INFO = OFF_BAR + (2 * S + 1) * 8;  // R, U (int64)
+  static constexpr int OFF_FLAG = OFF_INFO + 32;              // abort, no_abort, last
   static constexpr int SMEM_BYTES = round_up(OFF_FLAG + 16, 128);
   static_assert(G >= 1 && G <= LPR, "group larger than lanes per row");
   static_assert(RP * G <= LPR, "slots exceed lanes");
   static_assert(RW * G <= 32 * RPI, "tile too large");
+  // two blocks per SM: 228 KB of shared memory less 1 KB reserved per block
+  static_assert(SMEM_BYTES <= (228 * 1024) / 2 - 1024, "two blocks per SM must fit");
 };
 
 // Length attended by sequence i (0 for an out-of-range position).
@@ -120,18 +158,25 @@ __device__ __forceinline__ int seq_len_at(const int32_t *positions, int i, int m
 
 // ---------------------------------------------------------------------------
 // Split plan on the device (warp-cooperative; every lane returns the result)
+//
+// Work is balanced in a "cost row" space: (i, g) occupies L + cost rows --
+// `cost` rows that stand for the fixed price of a run (its start, the merge
+// of the warp states, the partial or output write) followed by its L cache
+// rows; chunk c of (i, g) starts at cost row V + cost + c*chunk, where V is
+// the first cost row of (i, g).  The live (i, g) follow each other in
+// (i, g) order.  Sequences with L = 0 occupy nothing.
 // ---------------------------------------------------------------------------
 struct SplitTotals {
-  long long rows;   // sum_i Hkv * L_i   (live (kv head, row) pairs)
+  long long rows;   // sum_i Hkv * (L_i + cost) over live sequences
   long long units;  // sum_i Hkv * ceil(L_i / chunk)
 };
 
 __device__ SplitTotals warp_split_totals(const int32_t *positions, int M, int Hkv, int max_len,
-                                         int chunk, int lane) {
+                                         int chunk, int cost, int lane) {
   long long rows = 0, units = 0;
   for (int i = lane; i < M; i += 32) {
     const int L = seq_len_at(positions, i, max_len);
-    rows += (long long)Hkv * L;
+    if (L > 0) rows += (long long)Hkv * (L + cost);
     units += (long long)Hkv * ((L + chunk - 1) / chunk);
   }
 #pragma unroll
@@ -142,17 +187,31 @@ __device__ SplitTotals warp_split_totals(const int32_t *positions, int M, int Hk
   return {rows, units};
 }
 
-// Global index of the first chunk whose first row is at or after row t of
-// the (i, g, row)-ordered row space; `total_units` if t is past the end.
+// First cost row of sequence i (warp-cooperative).
+__device__ long long warp_seq_row0(int i, const int32_t *positions, int Hkv, int max_len,
+                                   int cost, int lane) {
+  long long r = 0;
+  for (int j = lane; j < i; j += 32) {
+    const int L = seq_len_at(positions, j, max_len);
+    if (L > 0) r += (long long)Hkv * (L + cost);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
+}
+
+// Global index of the first chunk that starts at or after cost row t;
+// `total_units` if t is past the end.
 __device__ long long warp_first_unit_at_row(long long t, const int32_t *positions, int M,
-                                            int Hkv, int max_len, int chunk,
+                                            int Hkv, int max_len, int chunk, int cost,
                                             long long total_units, int lane) {
   long long row_base = 0, unit_base = 0;
   for (int i0 = 0; i0 < M; i0 += 32) {
     const int i = i0 + lane;
     const int L = (i < M) ? seq_len_at(positions, i, max_len) : 0;
     const int n = (L + chunk - 1) / chunk;
-    const long long rows = (long long)Hkv * L, units = (long long)Hkv * n;
+    const long long rows = (L > 0) ? (long long)Hkv * (L + cost) : 0;
+    const long long units = (long long)Hkv * n;
     long long rinc = rows, uinc = units;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -169,9 +228,10 @@ __device__ long long warp_first_unit_at_row(long long t, const int32_t *position
     long long u = 0;
     if (hit) {
       const long long off = t - rexcl;
-      const long long g = off / L;
-      const long long r = off - g * L;
-      u = uexcl + g * n + (r + chunk - 1) / chunk;  // == next (i, g)'s first chunk when c == n
+      const long long span = (long long)L + cost;
+      const long long g = off / span;
+      const long long r = off - g * span - cost;  // offset from chunk 0's start
+      u = uexcl + g * n + (r <= 0 ? 0 : (r + chunk - 1) / chunk);  // c == n: next (i, g)
     }
     const unsigned ballot = __ballot_sync(0xffffffffu, hit);
     if (ballot) return __shfl_sync(0xffffffffu, u, __ffs(ballot) - 1);
@@ -214,6 +274,61 @@ __device__ int3 warp_unit_to_igc(long long u, const int32_t *positions, int M, i
   return make_int3(M, 0, 0);
 }
 
+// ---------------------------------------------------------------------------
+// Columns: block b owns the chunks that start in cost rows [R*b/P, R*(b+1)/P).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ long long column_start_row(long long R, int P, int b) {
+  return R * b / P;
+}
+
+// Column holding cost row r (0 <= r < R): the largest b with R*b/P <= r.
+__device__ __forceinline__ int column_of_row(long long r, long long R, int P) {
+  const long long c = (r * P + P - 1) / R;
+  return (int)(c < P - 1 ? c : P - 1);
+}
+
+// Counters tagged with the call that last used them: the value is
+// (tag << 32 | count).  A value left by another call (another tag, or
+// whatever the workspace held) counts as zero: the first adder of this call
+// replaces it with (tag, amount).  Each returns the count before the add.
+// Bounded: after 2^20 failed attempts they record KVS_ERR_TIMEOUT and return
+// 0xffffffff.  `v` is what an atomicAdd(ctr, amount) returned.
+__device__ unsigned resolve_tagged_add(unsigned long long *ctr, unsigned long long v,
+                                       unsigned amount, unsigned tag, int *d_status) {
+  for (int attempt = 0; attempt < (1 << 20); ++attempt) {
+    if ((unsigned)(v >> 32) == tag) return (unsigned)v;
+    const unsigned long long cur = v + amount;
+    const unsigned long long mine = ((unsigned long long)tag << 32) | amount;
+    const unsigned long long prev = atomicCAS(ctr, cur, mine);
+    if (prev == cur) return 0u;
+    if ((unsigned)(prev >> 32) == tag)
+      v = atomicAdd(ctr, (unsigned long long)amount);
+    else
+      v = prev - amount;
+  }
+  record_status(d_status, KVS_ERR_TIMEOUT);
+  return 0xffffffffu;
+}
+
+__device__ __forceinline__ unsigned tagged_add(unsigned long long *ctr, unsigned amount,
+                                               unsigned tag, int *d_status) {
+  return resolve_tagged_add(ctr, atomicAdd(ctr, (unsigned long long)amount), amount, tag,
+                            d_status);
+}
+
+// max for floats in shared memory (order-independent, so deterministic)
+__device__ __forceinline__ void smem_max_float(float *addr, float v) {
+  if (v >= 0.f)
+    atomicMax(reinterpret_cast<int *>(addr), __float_as_int(v));
+  else
+    atomicMin(reinterpret_cast<unsigned *>(addr), __float_as_uint(v));
+}
+
+
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
 // A run: consecutive chunks of one (i, g) inside a block's range.
 struct Run {
   int i, g, c;  // first chunk of the run
@@ -235,7 +350,7 @@ __device__ __forceinline__ Run make_run(int i, int g, int c, long long remaining
 
 // The run after `r` (called only while chunks remain): next kv head of the
 // sequence, else the next sequence that has rows.  Never reads past M-1; if
-// the list ended (it cannot when the range came from the same positions) the
+// the list ended (it cannot when the piece came from the same positions) the
 // run is empty (units = 0), which ends the loops.
 __device__ __forceinline__ Run next_run(const Run &r, long long remaining,
                                         const int32_t *positions, int M, int Hkv,
@@ -276,54 +391,182 @@ __device__ __forceinline__ float butterfly_sum(float (&v)[NS], int li) {
 }
 
 // ---------------------------------------------------------------------------
-// Chunk kernel
+// Merge of all runs of one (i, g), by the NW consumer warps of the block
+// whose run completed (i, g).  Runs: the one at chunk 0 (slot i*Hkv + g) and,
+// for every chunk cc > 0 at which a block's range starts, that block's first
+// run (slot M*Hkv + block; of several blocks starting at the same chunk only
+// the last has work).  Candidate blocks come in row order, so the runs do
+// too and the sums are taken in a fixed order.
+// ---------------------------------------------------------------------------
+template <int D, int G, int NW>
+__device__ void merge_runs(const WsView &ws, float *out, int i, int g, int M, int Hkv,
+                           long long S, int L, long long R, int P, int chunk, int cost,
+                           unsigned char *scratch) {
+  constexpr int LPR = D / 4;
+  constexpr int NT = NW * 32;
+  constexpr int NE = (G * LPR + NT - 1) / NT;
+  int *s_list = reinterpret_cast<int *>(scratch);  // [kMergeWindow]
+  float(*s_w)[8] = reinterpret_cast<float(*)[8]>(scratch + kMergeWindow * 4);
+  float *s_mx = reinterpret_cast<float *>(scratch + kMergeWindow * 4 + kMergeWindow * 32);
+  float *s_l = s_mx + 8;
+  int *s_n = reinterpret_cast<int *>(s_l + 8);
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int H = Hkv * G;
+  const int n = (L + chunk - 1) / chunk;
+  const long long c0 = S + cost;  // cost row where chunk 0 of (i, g) starts
+  // candidate blocks: those whose range may start at a chunk cc in (0, n)
+  const int b_lo = (L >= 2) ? column_of_row(c0 + 1, R, P) : 0;
+  const int b_hi = (L >= 2) ? column_of_row(c0 + L - 1, R, P) : -1;
+  const int ncand = b_hi - b_lo + 1;
+  auto cand_chunk = [&](int j) -> int {  // chunk where block b_lo + j starts, or -1
+    const long long r = column_start_row(R, P, b_lo + j) - c0;
+    if (r <= 0 || r >= L) return -1;
+    const int cc = (int)((r + chunk - 1) / chunk);
+    return cc < n ? cc : -1;
+  };
+  auto run_slot = [&](int j) -> int {  // j = -1: the chunk-0 run; else -1 if not a run
+    if (j < 0) return i * Hkv + g;
+    const int cc = cand_chunk(j);
+    if (cc < 0) return -1;
+    if (j + 1 < ncand && cand_chunk(j + 1) == cc) return -1;  // an empty block; the next starts here
+    return M * Hkv + b_lo + j;
+  };
+  if (t < G) {
+    s_mx[t] = neg_inf();
+    s_l[t] = 0.f;
+  }
+  consumer_sync(NT);
+  // pass 1: the maximum over the runs, per query head
+  for (int j = t - 1; j < ncand; j += NT) {
+    const int sl = run_slot(j);
+    if (sl < 0) continue;
+#pragma unroll
+    for (int h = 0; h < G; ++h) smem_max_float(&s_mx[h], __ldcg(&ws.ml[(size_t)sl * G + h]).x);
+  }
+  consumer_sync(NT);
+  // pass 2: rescaled sums over windows of runs, in row order
+  const float4 *acc4 = reinterpret_cast<const float4 *>(ws.acc);
+  float4 a[NE];
+#pragma unroll
+  for (int q = 0; q < NE; ++q) a[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = -1; base < ncand; base += kMergeWindow) {
+    if (t < 32) {
+      const int j = base + t;
+      const int sl = (j < ncand) ? run_slot(j) : -1;
+      const unsigned ballot = __ballot_sync(0xffffffffu, sl >= 0);
+      if (sl >= 0) s_list[__popc(ballot & ((1u << lane) - 1u))] = sl;
+      if (lane == 0) *s_n = __popc(ballot);
+    }
+    consumer_sync(NT);
+    const int nb = *s_n;
+    for (int e = t; e < nb * G; e += NT) {
+      const int r = e / G;
+      const int h = e - r * G;
+      s_w[r][h] = exp2f(__ldcg(&ws.ml[(size_t)s_list[r] * G + h]).x - s_mx[h]);
+    }
+    consumer_sync(NT);
+    if (t < G) {
+      float l = s_l[t];
+      for (int r = 0; r < nb; ++r) l = fmaf(s_w[r][t], __ldcg(&ws.ml[(size_t)s_list[r] * G + t]).y, l);
+      s_l[t] = l;
+    }
+#pragma unroll
+    for (int q = 0; q < NE; ++q) {
+      const int e = t + q * NT;
+      if (e < G * LPR) {
+        const int h = e / LPR;
+        const int d4 = e - h * LPR;
+#pragma unroll 4
+        for (int r = 0; r < nb; ++r) {
+          const float w = s_w[r][h];
+          const float4 b = __ldcg(&acc4[((size_t)s_list[r] * G + h) * LPR + d4]);
+          a[q].x = fmaf(w, b.x, a[q].x);
+          a[q].y = fmaf(w, b.y, a[q].y);
+          a[q].z = fmaf(w, b.z, a[q].z);
+          a[q].w = fmaf(w, b.w, a[q].w);
+        }
+      }
+    }
+    consumer_sync(NT);
+  }
+  float4 *o4 = reinterpret_cast<float4 *>(out) + ((size_t)i * H + (size_t)g * G) * LPR;
+#pragma unroll
+  for (int q = 0; q < NE; ++q) {
+    const int e = t + q * NT;
+    if (e < G * LPR) {
+      const float inv = 1.f / s_l[e / LPR];
+      o4[e] = make_float4(a[q].x * inv, a[q].y * inv, a[q].z * inv, a[q].w * inv);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The step kernel (k_rows == nullptr: attention only; else scatter + attention)
 // ---------------------------------------------------------------------------
 template <int D, int G>
 __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
-    fd_chunk_kernel(const float *__restrict__ q, const float *__restrict__ k_cache,
-                    const float *__restrict__ v_cache,
-                    const int32_t *__restrict__ positions, WsView ws, int M, int Hkv,
-                    int max_len, int chunk, float qscale, int *d_status) {
+    fd_step_kernel(const float *__restrict__ q, float *k_cache, float *v_cache,
+                   const int32_t *__restrict__ positions, const float *__restrict__ k_rows,
+                   const float *__restrict__ v_rows, float *__restrict__ out, WsView ws, int M,
+                   int Hkv, int max_len, int chunk, float qscale, unsigned tag, int *d_status) {
   using C = Geo<D, G>;
+  constexpr int kCost = kRunCostBytes / (8 * D);  // cost rows per (i, g)
   extern __shared__ __align__(128) unsigned char smem[];
+  StageDesc *desc = reinterpret_cast<StageDesc *>(smem + C::OFF_DESC);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *empty = full + C::S;
-  uint64_t *mbar = empty + C::S;
-  long long *info = reinterpret_cast<long long *>(smem + C::OFF_INFO);  // u0, u1, i, g|c
+  uint64_t *mbar = empty + C::S;  // consumer warps: end-of-run steps
+  long long *info = reinterpret_cast<long long *>(smem + C::OFF_INFO);  // R, U
   volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
   volatile int *no_abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG + 4);
+  volatile int *s_last = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int H = Hkv * G;
+  const int P = gridDim.x;
+  const bool scatter = (k_rows != nullptr);
 
   // Everything below reads inputs a previous kernel may have written, and
-  // writes the workspace a previous reduce may still read.
+  // writes the caches, the workspace and the output a previous kernel may
+  // still read.
   grid_dependency_wait();
 
-  // ---- split plan: this block's chunk range (warp 0), barrier init --------
+  // ---- sequences with a position outside [0, max_len): NaN rows, status ----
+  for (int i = blockIdx.x; i < M; i += P) {
+    if (seq_len_at(positions, i, max_len) == 0) {
+      const float nan = __int_as_float(0x7fc00000);
+      float4 *o4 = reinterpret_cast<float4 *>(out) + (size_t)i * H * (D / 4);
+      for (int e = threadIdx.x; e < H * (D / 4); e += C::THREADS)
+        o4[e] = make_float4(nan, nan, nan, nan);
+      if (threadIdx.x == 0) record_status(d_status, KVS_ERR_POSITION);
+    }
+  }
+  // ---- Step 1, scatter: this block's share of the new rows (float4 each) ----
+  if (scatter) {
+    constexpr int D4 = D / 4;
+    const long long per_cache = (long long)M * Hkv * D4;
+    for (long long e = (long long)blockIdx.x * C::THREADS + threadIdx.x; e < 2 * per_cache;
+         e += (long long)P * C::THREADS) {
+      const bool is_v = e >= per_cache;
+      const long long f = is_v ? e - per_cache : e;
+      const long long ig = f / D4;
+      const int p = __ldg(positions + ig / Hkv);
+      if (p < 0 || p >= max_len) continue;
+      const size_t dst = ((size_t)ig * max_len + p) * D4 + (f - ig * D4);
+      if (is_v)
+        reinterpret_cast<float4 *>(v_cache)[dst] = __ldg(reinterpret_cast<const float4 *>(v_rows) + f);
+      else
+        reinterpret_cast<float4 *>(k_cache)[dst] = __ldg(reinterpret_cast<const float4 *>(k_rows) + f);
+    }
+  }
+
   if (warp == 0) {
-    const SplitTotals tot = warp_split_totals(positions, M, Hkv, max_len, chunk, lane);
-    const long long P = gridDim.x;
-    const long long b = blockIdx.x;
-    const long long t0 = tot.rows * b / P;
-    const long long t1 = tot.rows * (b + 1) / P;
-    const long long u0 = warp_first_unit_at_row(t0, positions, M, Hkv, max_len, chunk,
-                                                tot.units, lane);
-    const long long u1 = (b + 1 == P) ? tot.units
-                                      : warp_first_unit_at_row(t1, positions, M, Hkv, max_len,
-                                                               chunk, tot.units, lane);
-    const int3 igc = (u0 < tot.units)
-                         ? warp_unit_to_igc(u0, positions, M, Hkv, max_len, chunk, lane)
-                         : make_int3(M, 0, 0);
+    const SplitTotals tot = warp_split_totals(positions, M, Hkv, max_len, chunk, kCost, lane);
     if (lane == 0) {
-      info[0] = u0;
-      info[1] = u1;
-      info[2] = igc.x;
-      info[3] = ((long long)igc.y << 32) | (unsigned)igc.z;
-      // run table entry: this block's first chunk; w = 1 if it has work
-      ws.table[b] = make_int4(igc.x, igc.y, igc.z, u0 < u1 ? 1 : 0);
-      if (b == 0) *ws.num_blocks = (int)P;
+      info[0] = tot.rows;
+      info[1] = tot.units;
       for (int s = 0; s < C::S; ++s) {
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], C::NW);
@@ -331,58 +574,112 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       mbar_init(mbar, C::NW);
       *abort = 0;
       *no_abort = 0;
+      *s_last = 0;
       fence_mbar_init();
     }
   }
   __syncthreads();
   allow_dependent_launch();
-  const long long u0 = info[0], u1 = info[1];
-  if (u0 >= u1) return;
-  const int start_i = (int)info[2];
-  const int start_g = (int)(info[3] >> 32);
-  const int start_c = (int)(info[3] & 0xffffffff);
+  const long long R = info[0], U = info[1];
+  if (R == 0) return;
 
   if (warp == C::NW) {
-    // ===================== producer warp: one lane issues copies ==========
-    if (lane != 0) return;
+    // ===================== producer warp =================================
+    // The whole warp computes this block's range (the split-plan searches are
+    // warp-cooperative); lane 0 issues the copies and writes descriptors.
     const uint64_t pol_stream = policy_evict_first();
     uint32_t k = 0;
-    bool ok = true;
-    long long remaining = u1 - u0;
-    Run run = make_run(start_i, start_g, start_c, remaining, positions, max_len, chunk);
-    while (ok && remaining > 0 && run.units > 0) {
-      const int r0 = run.c * chunk;
-      const int r1 = (int)min((long long)(run.c + run.units) * chunk, (long long)run.L);
-      const size_t head_base = ((size_t)run.i * Hkv + run.g) * (size_t)max_len;
-      for (int rs = r0, st = 0; rs < r1; rs += C::T, ++st, ++k) {
+    int ok = 1;
+    const int b = blockIdx.x;
+    const long long ub = warp_first_unit_at_row(column_start_row(R, P, b), positions, M, Hkv,
+                                                max_len, chunk, kCost, U, lane);
+    const long long ue = (b + 1 == P) ? U
+                                      : warp_first_unit_at_row(column_start_row(R, P, b + 1),
+                                                               positions, M, Hkv, max_len, chunk,
+                                                               kCost, U, lane);
+    if (ub < ue) {
+      const int3 igc = warp_unit_to_igc(ub, positions, M, Hkv, max_len, chunk, lane);
+      long long seq_row0 = warp_seq_row0(igc.x, positions, Hkv, max_len, kCost, lane);
+      const long long block_slot = (long long)M * Hkv + b;
+      long long remaining = ue - ub;
+      Run run = make_run(igc.x, igc.y, igc.z, remaining, positions, max_len, chunk);
+      int run_seq = run.i;
+      while (ok && remaining > 0 && run.units > 0) {
+        if (run.i != run_seq) {  // moved to a later sequence: advance its first row
+          for (int j = run_seq; j < run.i; ++j) {
+            const int Lj = seq_len_at(positions, j, max_len);
+            if (Lj > 0) seq_row0 += (long long)Hkv * (Lj + kCost);
+          }
+          run_seq = run.i;
+        }
+        const long long slot = (run.c == 0) ? (long long)run.i * Hkv + run.g : block_slot;
+        const int r0 = run.c * chunk;
+        const int r1 = (int)min((long long)(run.c + run.units) * chunk, (long long)run.L);
+        const size_t head_base = ((size_t)run.i * Hkv + run.g) * (size_t)max_len;
+        const size_t row_src = ((size_t)run.i * Hkv + run.g) * D;  // new row of (i, g)
+        for (int rs = r0, st = 0; rs < r1 && ok; rs += C::T, ++st, ++k) {
+          if (lane == 0) {
+            const uint32_t s = k % C::S;
+            const uint32_t use = k / C::S;
+            if (!mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
+              ok = 0;
+            } else {
+              const int nrows = min(C::T, r1 - rs);
+              StageDesc &dd = desc[s];
+              dd.flags = (st == 0 ? kRunStart : 0) | (rs + C::T >= r1 ? kRunEnd : 0);
+              dd.nrows = nrows;
+              dd.ig = run.i * Hkv + run.g;
+              dd.run_rows = r1 - r0;
+              dd.L = run.L;
+              dd.slot = slot;
+              dd.S = seq_row0 + (long long)run.g * (run.L + kCost);
+              const uint32_t kv_bytes = (uint32_t)nrows * D * 4;
+              const uint32_t bytes = 2 * kv_bytes + (st == 0 ? (uint32_t)C::Q_BYTES : 0u);
+              unsigned char *stage = smem + s * C::STAGE_BYTES;
+              mbar_arrive_expect_tx(&full[s], bytes);
+              const size_t row0 = (head_base + rs) * D;
+              // with the scatter folded in, row L-1 (position p) comes from the new rows
+              const bool tail = scatter && (rs + nrows == run.L);
+              const uint32_t cache_bytes = tail ? kv_bytes - D * 4 : kv_bytes;
+              if (cache_bytes > 0) {
+                bulk_g2s_hint(stage, k_cache + row0, cache_bytes, &full[s], pol_stream);
+                bulk_g2s_hint(stage + C::KV_BYTES, v_cache + row0, cache_bytes, &full[s], pol_stream);
+              }
+              if (tail) {
+                bulk_g2s(stage + cache_bytes, k_rows + row_src, D * 4, &full[s]);
+                bulk_g2s(stage + C::KV_BYTES + cache_bytes, v_rows + row_src, D * 4, &full[s]);
+              }
+              if (st == 0)
+                bulk_g2s(stage + 2 * C::KV_BYTES,
+                         q + ((size_t)run.i * H + (size_t)run.g * G) * D, C::Q_BYTES, &full[s]);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        remaining -= run.units;
+        if (ok && remaining > 0)
+          run = next_run(run, remaining, positions, M, Hkv, max_len, chunk);
+      }
+    }
+    if (lane == 0) {
+      if (ok) {  // tell the consumers there is nothing more
         const uint32_t s = k % C::S;
         const uint32_t use = k / C::S;
-        if (!mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
-          ok = false;
-          break;
+        if (mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
+          desc[s].flags = kNoMore;
+          desc[s].nrows = 0;
+          mbar_arrive(&full[s]);
+        } else {
+          ok = 0;
         }
-        const int nrows = min(C::T, r1 - rs);
-        const uint32_t kv_bytes = (uint32_t)nrows * D * 4;
-        const uint32_t bytes = 2 * kv_bytes + (st == 0 ? (uint32_t)C::Q_BYTES : 0u);
-        unsigned char *stage = smem + s * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        const size_t row0 = (head_base + rs) * D;
-        bulk_g2s_hint(stage, k_cache + row0, kv_bytes, &full[s], pol_stream);
-        bulk_g2s_hint(stage + C::KV_BYTES, v_cache + row0, kv_bytes, &full[s], pol_stream);
-        if (st == 0)
-          bulk_g2s(stage + 2 * C::KV_BYTES,
-                   q + ((size_t)run.i * H + (size_t)run.g * G) * D, C::Q_BYTES, &full[s]);
       }
-      remaining -= run.units;
-      if (ok && remaining > 0)
-        run = next_run(run, remaining, positions, M, Hkv, max_len, chunk);
-    }
-    if (!ok) {
-      *abort = 1;
-      record_status(d_status, KVS_ERR_TIMEOUT);
-      // let every copy already issued land before the block can exit
-      for (uint32_t j = (k > (uint32_t)C::S ? k - C::S : 0u); j < k; ++j)
-        mbar_wait(&full[j % C::S], (j / C::S) & 1u, no_abort);
+      if (!ok) {
+        *abort = 1;
+        record_status(d_status, KVS_ERR_TIMEOUT);
+        // let every copy already issued land before the block can exit
+        for (uint32_t j = (k > (uint32_t)C::S ? k - C::S : 0u); j < k; ++j)
+          mbar_wait(&full[j % C::S], (j / C::S) & 1u, no_abort);
+      }
     }
     return;
   }
@@ -416,128 +713,136 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   float l_lane = 0.f;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
+    qv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
     acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
     m_run[h] = neg_inf();
   }
 
-  uint32_t k = 0;
   uint32_t mphase = 0;
-  long long remaining = u1 - u0;
-  Run run = make_run(start_i, start_g, start_c, remaining, positions, max_len, chunk);
-  while (remaining > 0 && run.units > 0) {
-    const int r0 = run.c * chunk;
-    const int r1 = (int)min((long long)(run.c + run.units) * chunk, (long long)run.L);
-    for (int rs = r0, st = 0; rs < r1; rs += C::T, ++st, ++k) {
-      const uint32_t s = k % C::S;
-      const uint32_t use = k / C::S;
-      if (!mbar_wait(&full[s], use & 1u, abort)) {
-        *abort = 1;
-        record_status(d_status, KVS_ERR_TIMEOUT);
-        return;
+  auto consumers_barrier = [&]() -> bool {  // bounded; every consumer warp arrives once
+    __syncwarp();
+    if (lane == 0) mbar_arrive(mbar);
+    if (!mbar_wait(mbar, mphase, abort)) {
+      *abort = 1;
+      record_status(d_status, KVS_ERR_TIMEOUT);
+      return false;
+    }
+    mphase ^= 1u;
+    return true;
+  };
+
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t s = k % C::S;
+    const uint32_t use = k / C::S;
+    if (!mbar_wait(&full[s], use & 1u, abort)) {
+      *abort = 1;
+      record_status(d_status, KVS_ERR_TIMEOUT);
+      return;
+    }
+    const StageDesc dsc = desc[s];
+    if (dsc.flags & kNoMore) break;
+    const unsigned char *stage = smem + s * C::STAGE_BYTES;
+    const float4 *sK = reinterpret_cast<const float4 *>(stage);
+    const float4 *sV = reinterpret_cast<const float4 *>(stage + C::KV_BYTES);
+    if (dsc.flags & kRunStart) {
+      const float4 *sQ = reinterpret_cast<const float4 *>(stage + 2 * C::KV_BYTES);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float4 t = sQ[h * C::LPR + li];
+        qv[h] = make_float4(t.x * qscale, t.y * qscale, t.z * qscale, t.w * qscale);
       }
-      const unsigned char *stage = smem + s * C::STAGE_BYTES;
-      const float4 *sK = reinterpret_cast<const float4 *>(stage);
-      const float4 *sV = reinterpret_cast<const float4 *>(stage + C::KV_BYTES);
-      if (st == 0) {
-        const float4 *sQ = reinterpret_cast<const float4 *>(stage + 2 * C::KV_BYTES);
+    }
+    const int my_valid = min(max(dsc.nrows - w * C::RW, 0), C::RW);
+    if (my_valid > 0) {
+      const int tile0 = w * C::RW;
+      // ---- scores: partial dot products, then the butterfly ----
+      float part[C::NSLOT];
+#pragma unroll
+      for (int j = 0; j < C::NSLOT; ++j) part[j] = 0.f;
+#pragma unroll
+      for (int r = 0; r < C::RP; ++r) {
+        const int row = tile0 + r * C::RPI + gi;
+        const float4 kv = sK[row * C::LPR + li];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float4 t = sQ[h * C::LPR + li];
-          qv[h] = make_float4(t.x * qscale, t.y * qscale, t.z * qscale, t.w * qscale);
+          float d = qv[h].x * kv.x;
+          d = fmaf(qv[h].y, kv.y, d);
+          d = fmaf(qv[h].z, kv.z, d);
+          d = fmaf(qv[h].w, kv.w, d);
+          part[r * G + h] = d;
         }
       }
-      const int nrows = min(C::T, r1 - rs);
-      const int my_valid = min(max(nrows - w * C::RW, 0), C::RW);
-      if (my_valid > 0) {
-        const int tile0 = w * C::RW;
-        // ---- scores: partial dot products, then the butterfly ----
-        float part[C::NSLOT];
+      const float sc = butterfly_sum<C::NSLOT, C::LOG2NS, C::LPR>(part, li);
+      const bool valid = slot_used && slot_row < my_valid;
+      const float s_val = valid ? sc : neg_inf();
+      if (owner) sS[slot_h * C::RWP + slot_row] = s_val;
+      __syncwarp();
+      // ---- running max and rescale factors (all lanes, all heads) ----
+      float alpha[G];
+      float m_new[G];
 #pragma unroll
-        for (int j = 0; j < C::NSLOT; ++j) part[j] = 0.f;
+      for (int h = 0; h < G; ++h) {
+        const float4 *row4 = reinterpret_cast<const float4 *>(sS + h * C::RWP);
+        float tmax = neg_inf();
 #pragma unroll
-        for (int r = 0; r < C::RP; ++r) {
-          const int row = tile0 + r * C::RPI + gi;
-          const float4 kv = sK[row * C::LPR + li];
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float d = qv[h].x * kv.x;
-            d = fmaf(qv[h].y, kv.y, d);
-            d = fmaf(qv[h].z, kv.z, d);
-            d = fmaf(qv[h].w, kv.w, d);
-            part[r * G + h] = d;
-          }
+        for (int j = 0; j < C::RWP / 4; ++j) {
+          const float4 t = row4[j];
+          tmax = fmaxf(tmax, fmaxf(fmaxf(t.x, t.y), fmaxf(t.z, t.w)));
         }
-        const float sc = butterfly_sum<C::NSLOT, C::LOG2NS, C::LPR>(part, li);
-        const bool valid = slot_used && slot_row < my_valid;
-        const float s_val = valid ? sc : neg_inf();
-        if (owner) sS[slot_h * C::RWP + slot_row] = s_val;
-        __syncwarp();
-        // ---- running max and rescale factors (all lanes, all heads) ----
-        float alpha[G];
-        float m_new[G];
+        m_new[h] = fmaxf(m_run[h], tmax);
+        alpha[h] = (m_new[h] == m_run[h]) ? 1.f : exp2f(m_run[h] - m_new[h]);
+      }
+      // ---- own-slot probability ----
+      float mh = m_new[0];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 *row4 = reinterpret_cast<const float4 *>(sS + h * C::RWP);
-          float tmax = neg_inf();
+      for (int h = 1; h < G; ++h) mh = (slot_h == h) ? m_new[h] : mh;
+      float ah = alpha[0];
 #pragma unroll
-          for (int j = 0; j < C::RWP / 4; ++j) {
-            const float4 t = row4[j];
-            tmax = fmaxf(tmax, fmaxf(fmaxf(t.x, t.y), fmaxf(t.z, t.w)));
-          }
-          m_new[h] = fmaxf(m_run[h], tmax);
-          alpha[h] = (m_new[h] == m_run[h]) ? 1.f : exp2f(m_run[h] - m_new[h]);
-        }
-        // ---- own-slot probability ----
-        float mh = m_new[0];
+      for (int h = 1; h < G; ++h) ah = (slot_h == h) ? alpha[h] : ah;
+      const float p = valid ? exp2f(s_val - mh) : 0.f;
+      if (owner) {
+        sP[slot_row * C::GP + slot_h] = p;
+        l_lane = l_lane * ah + p;
+      }
 #pragma unroll
-        for (int h = 1; h < G; ++h) mh = (slot_h == h) ? m_new[h] : mh;
-        float ah = alpha[0];
-#pragma unroll
-        for (int h = 1; h < G; ++h) ah = (slot_h == h) ? alpha[h] : ah;
-        const float p = valid ? exp2f(s_val - mh) : 0.f;
-        if (owner) {
-          sP[slot_row * C::GP + slot_h] = p;
-          l_lane = l_lane * ah + p;
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          m_run[h] = m_new[h];
-          acc[h].x *= alpha[h];
-          acc[h].y *= alpha[h];
-          acc[h].z *= alpha[h];
-          acc[h].w *= alpha[h];
-        }
-        __syncwarp();
-        // ---- P.V ----
-#pragma unroll
-        for (int r = 0; r < C::RP; ++r) {
-          const int trow = r * C::RPI + gi;
-          if (trow < my_valid) {
-            const float4 vv = sV[(tile0 + trow) * C::LPR + li];
-            float pr[C::GP];
-#pragma unroll
-            for (int j = 0; j < C::GP / 4; ++j) {
-              const float4 t = reinterpret_cast<const float4 *>(sP + trow * C::GP)[j];
-              pr[4 * j + 0] = t.x;
-              pr[4 * j + 1] = t.y;
-              pr[4 * j + 2] = t.z;
-              pr[4 * j + 3] = t.w;
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              acc[h].x = fmaf(pr[h], vv.x, acc[h].x);
-              acc[h].y = fmaf(pr[h], vv.y, acc[h].y);
-              acc[h].z = fmaf(pr[h], vv.z, acc[h].z);
-              acc[h].w = fmaf(pr[h], vv.w, acc[h].w);
-            }
-          }
-        }
+      for (int h = 0; h < G; ++h) {
+        m_run[h] = m_new[h];
+        acc[h].x *= alpha[h];
+        acc[h].y *= alpha[h];
+        acc[h].z *= alpha[h];
+        acc[h].w *= alpha[h];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      // ---- P.V ----
+#pragma unroll
+      for (int r = 0; r < C::RP; ++r) {
+        const int trow = r * C::RPI + gi;
+        if (trow < my_valid) {
+          const float4 vv = sV[(tile0 + trow) * C::LPR + li];
+          float pr[C::GP];
+#pragma unroll
+          for (int j = 0; j < C::GP / 4; ++j) {
+            const float4 t = reinterpret_cast<const float4 *>(sP + trow * C::GP)[j];
+            pr[4 * j + 0] = t.x;
+            pr[4 * j + 1] = t.y;
+            pr[4 * j + 2] = t.z;
+            pr[4 * j + 3] = t.w;
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            acc[h].x = fmaf(pr[h], vv.x, acc[h].x);
+            acc[h].y = fmaf(pr[h], vv.y, acc[h].y);
+            acc[h].z = fmaf(pr[h], vv.z, acc[h].z);
+            acc[h].w = fmaf(pr[h], vv.w, acc[h].w);
+          }
+        }
+      }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (!(dsc.flags & kRunEnd)) continue;
 
-    // ---- end of run: merge the NW warp states into the run's partial ----
+    // ---- end of run: merge the NW warp states --------------------------------
     if (C::RPI > 1) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -567,50 +872,55 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       }
       sL[w * G + lane] = lsum;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(mbar);
-    if (!mbar_wait(mbar, mphase, abort)) {
-      *abort = 1;
-      record_status(d_status, KVS_ERR_TIMEOUT);
-      return;
-    }
-    mphase ^= 1u;
-    {
-      // slot of this run: (i, g) if it starts at chunk 0, else this block's
-      const long long slot_id = (run.c == 0) ? (long long)run.i * Hkv + run.g
-                                             : (long long)M * Hkv + blockIdx.x;
-      const int t = threadIdx.x;  // 0 .. NW*32-1
-      for (int e = t; run.L > 0 && e < G * C::LPR; e += C::NW * 32) {
-        const int h = e / C::LPR;
-        const int d4 = e - h * C::LPR;
-        float mx = neg_inf();
+    if (!consumers_barrier()) return;
+    // A run that covers all of (i, g) is the answer; any other run is a
+    // partial for the (i, g) merge.
+    const bool whole = (dsc.run_rows == dsc.L);
+    const int i_seq = dsc.ig / Hkv;
+    const int g_kv = dsc.ig - i_seq * Hkv;
+    for (int e = threadIdx.x; e < G * C::LPR; e += C::NW * 32) {
+      const int h = e / C::LPR;
+      const int d4 = e - h * C::LPR;
+      float mx = neg_inf();
 #pragma unroll
-        for (int w2 = 0; w2 < C::NW; ++w2) mx = fmaxf(mx, sM[w2 * G + h]);
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        float lsum = 0.f;
+      for (int w2 = 0; w2 < C::NW; ++w2) mx = fmaxf(mx, sM[w2 * G + h]);
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lsum = 0.f;
 #pragma unroll
-        for (int w2 = 0; w2 < C::NW; ++w2) {
-          const float mw = sM[w2 * G + h];
-          const float sc = (mw == neg_inf()) ? 0.f : exp2f(mw - mx);
-          const float4 b = sAcc[(w2 * G + h) * C::LPR + d4];
-          a.x = fmaf(sc, b.x, a.x);
-          a.y = fmaf(sc, b.y, a.y);
-          a.z = fmaf(sc, b.z, a.z);
-          a.w = fmaf(sc, b.w, a.w);
-          lsum = fmaf(sc, sL[w2 * G + h], lsum);
-        }
-        const size_t sl = (size_t)slot_id * G + h;
-        reinterpret_cast<float4 *>(ws.acc)[sl * C::LPR + d4] = a;
-        if (d4 == 0) ws.ml[sl] = make_float2(mx, lsum);
+      for (int w2 = 0; w2 < C::NW; ++w2) {
+        const float mw = sM[w2 * G + h];
+        const float sc = (mw == neg_inf()) ? 0.f : exp2f(mw - mx);
+        const float4 b = sAcc[(w2 * G + h) * C::LPR + d4];
+        a.x = fmaf(sc, b.x, a.x);
+        a.y = fmaf(sc, b.y, a.y);
+        a.z = fmaf(sc, b.z, a.z);
+        a.w = fmaf(sc, b.w, a.w);
+        lsum = fmaf(sc, sL[w2 * G + h], lsum);
+      }
+      if (whole) {
+        const float inv = 1.f / lsum;
+        reinterpret_cast<float4 *>(out)[((size_t)i_seq * H + (size_t)g_kv * G + h) * C::LPR + d4] =
+            make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+      } else {
+        const size_t sl = (size_t)dsc.slot * G + h;
+        __stcg(&reinterpret_cast<float4 *>(ws.acc)[sl * C::LPR + d4], a);
+        if (d4 == 0) __stcg(&ws.ml[sl], make_float2(mx, lsum));
       }
     }
-    if (lane == 0) mbar_arrive(mbar);
-    if (!mbar_wait(mbar, mphase, abort)) {
-      *abort = 1;
-      record_status(d_status, KVS_ERR_TIMEOUT);
-      return;
+    if (!whole) __threadfence();  // partials visible GPU-wide before the count
+    if (!consumers_barrier()) return;
+    if (!whole) {
+      if (threadIdx.x == 0) {
+        const unsigned before = tagged_add(ws.done + dsc.ig, (unsigned)dsc.run_rows, tag, d_status);
+        *s_last = (before != 0xffffffffu && before + (unsigned)dsc.run_rows == (unsigned)dsc.L);
+      }
+      if (!consumers_barrier()) return;
+      if (*s_last) {  // every run of (i, g) is in: merge them
+        __threadfence();
+        merge_runs<D, G, C::NW>(ws, out, i_seq, g_kv, M, Hkv, dsc.S, dsc.L, R, P, chunk, kCost,
+                                smem + C::OFF_MACC);
+      }
     }
-    mphase ^= 1u;
     // reset the running state for the next run
     l_lane = 0.f;
 #pragma unroll
@@ -618,139 +928,6 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
       m_run[h] = neg_inf();
     }
-    remaining -= run.units;
-    if (remaining > 0) run = next_run(run, remaining, positions, M, Hkv, max_len, chunk);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Reduce kernel: one 128-thread block per (sequence, query head).
-// ---------------------------------------------------------------------------
-// (i, g, c) < (e.x, e.y, e.z) lexicographically
-__device__ __forceinline__ bool igc_before(int i, int g, int c, int4 e) {
-  return i < e.x || (i == e.x && (g < e.y || (g == e.y && c < e.z)));
-}
-
-template <int D>
-__global__ void __launch_bounds__(128)
-    fd_reduce_kernel(const int32_t *__restrict__ positions, WsView ws, float *__restrict__ out,
-                     int M, int Hkv, int G, int max_len, int P, int *d_status) {
-  constexpr int LPR = D / 4;
-  constexpr int NP = 128 / LPR;  // run phases
-  grid_dependency_wait();
-  allow_dependent_launch();
-  const int H = Hkv * G;
-  const int ih = blockIdx.x;
-  const int i = ih / H;
-  const int h = ih - i * H;
-  const int g = h / G;
-  const int hh = h - g * G;
-  const int t = threadIdx.x;
-  const int cp = t / LPR;
-  const int d4 = t % LPR;
-  const float4 *acc4 = reinterpret_cast<const float4 *>(ws.acc);
-  __shared__ int4 s_tab[kMaxChunkBlocks];
-  __shared__ int s_first, s_count;
-  __shared__ float s_m[NP], s_l[NP];
-  __shared__ float4 s_acc[NP][LPR];
-
-  // Everything that does not depend on the block table is loaded at once:
-  // the position, the chunk-0 run's partial and the table itself.
-  const size_t slot0 = ((size_t)i * Hkv + g) * G + hh;
-  const int L = seq_len_at(positions, i, max_len);
-  float2 ml0 = make_float2(0.f, 0.f);
-  float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (cp == 0) {
-    ml0 = ws.ml[slot0];
-    acc0 = acc4[slot0 * LPR + d4];
-  }
-  for (int b = t; b < P; b += 128) s_tab[b] = ws.table[b];
-
-  float4 *o4 = reinterpret_cast<float4 *>(out) + (size_t)ih * LPR;
-  if (L == 0) {
-    const float nan = __int_as_float(0x7fc00000);
-    if (t < LPR) o4[t] = make_float4(nan, nan, nan, nan);
-    if (t == 0 && h == 0) record_status(d_status, KVS_ERR_POSITION);
-    return;
-  }
-  __syncthreads();
-  // Runs of (i, g): the run at chunk 0 (slot i*Hkv + g) and the first run of
-  // every block whose range starts inside (i, g) (slot M*Hkv + b).  The table
-  // is sorted by chunk: find the first entry after (i, g, 0).
-  if (t == 0) {
-    int lo = 0, hi = P;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (igc_before(i, g, 0, s_tab[mid])) hi = mid;
-      else lo = mid + 1;
-    }
-    int cnt = 0;
-    while (lo + cnt < P && s_tab[lo + cnt].x == i && s_tab[lo + cnt].y == g) ++cnt;
-    s_first = lo;
-    s_count = cnt;
-  }
-  __syncthreads();
-  const int first = s_first;
-  const int nruns = 1 + s_count;  // run 0 is the chunk-0 run
-
-  // Each phase cp merges runs cp, cp + NP, ... online (running max and
-  // rescaling), then the NP phase states are merged.
-  float m = neg_inf(), l = 0.f;
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (cp == 0) {
-    m = ml0.x;
-    l = ml0.y;
-    a = acc0;
-  }
-  for (int r = (cp == 0 ? NP : cp); r < nruns; r += NP) {
-    if (s_tab[first + r - 1].w == 0) continue;  // a block without work
-    const size_t sl = ((size_t)M * Hkv + first + r - 1) * G + hh;
-    const float2 ml = ws.ml[sl];
-    const float4 b = acc4[sl * LPR + d4];
-    const float mn = fmaxf(m, ml.x);
-    const float wa = (m == neg_inf()) ? 0.f : exp2f(m - mn);
-    const float wb = exp2f(ml.x - mn);
-    a.x = fmaf(wb, b.x, wa * a.x);
-    a.y = fmaf(wb, b.y, wa * a.y);
-    a.z = fmaf(wb, b.z, wa * a.z);
-    a.w = fmaf(wb, b.w, wa * a.w);
-    l = fmaf(wb, ml.y, wa * l);
-    m = mn;
-  }
-  if (nruns <= NP) {
-    // at most one run per phase: phases >= nruns hold nothing
-    if (nruns == 1) {
-      if (cp == 0) {
-        const float inv = 1.f / l;
-        o4[d4] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-      }
-      return;
-    }
-  }
-  if (d4 == 0) {
-    s_m[cp] = m;
-    s_l[cp] = l;
-  }
-  s_acc[cp][d4] = a;
-  __syncthreads();
-  if (cp == 0) {
-    float mx = s_m[0];
-#pragma unroll
-    for (int j = 1; j < NP; ++j) mx = fmaxf(mx, s_m[j]);
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lt = 0.f;
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-      const float w = (s_m[j] == neg_inf()) ? 0.f : exp2f(s_m[j] - mx);
-      const float4 b = s_acc[j][d4];
-      r.x = fmaf(w, b.x, r.x);
-      r.y = fmaf(w, b.y, r.y);
-      r.z = fmaf(w, b.z, r.z);
-      r.w = fmaf(w, b.w, r.w);
-      lt = fmaf(w, s_l[j], lt);
-    }
-    const float inv = 1.f / lt;
-    o4[d4] = make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
   }
 }
 
@@ -759,21 +936,21 @@ __global__ void __launch_bounds__(128)
 // ---------------------------------------------------------------------------
 constexpr int kMaxDevices = 64;
 
-struct ChunkLaunchInfo {
+struct StepLaunchInfo {
   int blocks_per_sm = 0;
   bool configured = false;
 };
 
-// Blocks per SM of one chunk-kernel instantiation on the current device
+// Blocks per SM of one step-kernel instantiation on device `dev`
 // (configures the kernel's shared-memory attributes on first use).
 template <int D, int G>
-int chunk_blocks_per_sm(int dev) {
+int step_blocks_per_sm(int dev) {
   using C = Geo<D, G>;
-  static ChunkLaunchInfo info[kMaxDevices];
+  static StepLaunchInfo info[kMaxDevices];
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   if (!info[dev].configured) {
-    auto kern = fd_chunk_kernel<D, G>;
+    auto kern = fd_step_kernel<D, G>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return -1;
@@ -793,57 +970,53 @@ int chunk_blocks_per_sm(int dev) {
 // stream for the launch and pipeline fill to pay off.
 constexpr long long kMinRowsPerBlock = 32;
 
-template <int D, int G>
-int chunk_grid(int M, int Hkv, int max_len) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
-  const int bps = chunk_blocks_per_sm<D, G>(dev);
-  const int sms = device_sm_count();
-  if (bps <= 0 || sms <= 0) return -1;
-  const long long rows_max = (long long)M * Hkv * max_len;
-  const long long by_rows = std::max(1ll, (rows_max + kMinRowsPerBlock - 1) / kMinRowsPerBlock);
-  return (int)std::min<long long>({(long long)sms * bps, (long long)kMaxChunkBlocks, by_rows});
+// Tag of one launch for the workspace counters: distinct for consecutive
+// launches of this process (a 32-bit counter started at a time-derived
+// value, never 0), so a counter left by an earlier call, or whatever a fresh
+// workspace holds, is recognised as stale.
+unsigned next_call_tag() {
+  static std::atomic<unsigned> counter{
+      (unsigned)(std::chrono::steady_clock::now().time_since_epoch().count() * 2654435761ull)};
+  unsigned t;
+  do {
+    t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  } while (t == 0u);
+  return t;
 }
 
 template <int D, int G>
-int launch_chunks_impl(const float *q, const float *k_cache, const float *v_cache,
-                       const int32_t *positions, int M, int Hkv, int max_len, int chunk,
-                       void *workspace, int *d_status, cudaStream_t stream) {
+int launch_step_impl(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+                     const float *k_rows, const float *v_rows, float *out, int M, int Hkv,
+                     int max_len, int chunk, void *workspace, int *d_status, cudaStream_t stream) {
   using C = Geo<D, G>;
-  const int grid = chunk_grid<D, G>(M, Hkv, max_len);
-  if (grid <= 0) return KVS_ERR_LAUNCH;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVS_ERR_LAUNCH;
+  const int bps = step_blocks_per_sm<D, G>(dev);
+  const int sms = device_sm_count();
+  if (bps <= 0 || sms <= 0) return KVS_ERR_LAUNCH;
+  const long long rows_max = (long long)M * Hkv * max_len;
+  const long long by_rows = std::max(1ll, (rows_max + kMinRowsPerBlock - 1) / kMinRowsPerBlock);
+  const int grid =
+      (int)std::min<long long>({(long long)sms * bps, (long long)kMaxChunkBlocks, by_rows});
   const WsView ws = workspace_view(workspace, M, Hkv, G, D);
   const float qscale = (float)(1.4426950408889634074 / std::sqrt((double)D));
-  const cudaError_t e = launch_pdl(fd_chunk_kernel<D, G>, dim3(grid), dim3(C::THREADS),
-                                   C::SMEM_BYTES, stream, q, k_cache, v_cache, positions, ws, M,
-                                   Hkv, max_len, chunk, qscale, d_status);
+  const cudaError_t e = launch_pdl(fd_step_kernel<D, G>, dim3(grid), dim3(C::THREADS),
+                                   C::SMEM_BYTES, stream, q, k_cache, v_cache, positions, k_rows,
+                                   v_rows, out, ws, M, Hkv, max_len, chunk, qscale,
+                                   next_call_tag(), d_status);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
 template <int D>
-int grid_for_group(int G, int M, int Hkv, int max_len) {
+int dispatch_group(int G, const float *q, float *k_cache, float *v_cache,
+                   const int32_t *positions, const float *k_rows, const float *v_rows,
+                   float *out, int M, int Hkv, int max_len, int chunk, void *workspace,
+                   int *d_status, cudaStream_t stream) {
   switch (G) {
-    case 1: return chunk_grid<D, 1>(M, Hkv, max_len);
-    case 2: return chunk_grid<D, 2>(M, Hkv, max_len);
-    case 3: return chunk_grid<D, 3>(M, Hkv, max_len);
-    case 4: return chunk_grid<D, 4>(M, Hkv, max_len);
-    case 5: return chunk_grid<D, 5>(M, Hkv, max_len);
-    case 6: return chunk_grid<D, 6>(M, Hkv, max_len);
-    case 7: return chunk_grid<D, 7>(M, Hkv, max_len);
-    case 8: return chunk_grid<D, 8>(M, Hkv, max_len);
-    default: return -1;
-  }
-}
-
-template <int D>
-int dispatch_group(int G, const float *q, const float *k_cache, const float *v_cache,
-                   const int32_t *positions, int M, int Hkv, int max_len, int chunk,
-                   void *workspace, int *d_status, cudaStream_t stream) {
-  switch (G) {
-#define KVS_CASE(g)                                                                      \
-  case g:                                                                                \
-    return launch_chunks_impl<D, g>(q, k_cache, v_cache, positions, M, Hkv, max_len,    \
-                                    chunk, workspace, d_status, stream);
+#define KVS_CASE(g)                                                                           \
+  case g:                                                                                     \
+    return launch_step_impl<D, g>(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv, \
+                                  max_len, chunk, workspace, d_status, stream);
     KVS_CASE(1)
     KVS_CASE(2)
     KVS_CASE(3)
@@ -872,47 +1045,18 @@ int device_sm_count() {
   return cache[dev];
 }
 
-int launch_fd_chunks(const float *q, const float *k_cache, const float *v_cache,
-                     const int32_t *positions, int M, int H, int Hkv, int D, int max_len,
-                     int chunk, void *workspace, int *d_status, cudaStream_t stream) {
+int launch_fd_step(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+                   const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
+                   int D, int max_len, int chunk, void *workspace, int *d_status,
+                   cudaStream_t stream) {
   const int G = H / Hkv;
   if (D == 128)
-    return dispatch_group<128>(G, q, k_cache, v_cache, positions, M, Hkv, max_len, chunk,
-                               workspace, d_status, stream);
+    return dispatch_group<128>(G, q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv,
+                               max_len, chunk, workspace, d_status, stream);
   if (D == 64)
-    return dispatch_group<64>(G, q, k_cache, v_cache, positions, M, Hkv, max_len, chunk,
-                              workspace, d_status, stream);
+    return dispatch_group<64>(G, q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv,
+                              max_len, chunk, workspace, d_status, stream);
   return KVS_ERR_UNSUPPORTED;
-}
-
-int launch_fd_reduce(const int32_t *positions, float *out, int M, int H, int Hkv, int D,
-                     int max_len, const void *workspace, int *d_status, cudaStream_t stream) {
-  const int G = H / Hkv;
-  const WsView ws = workspace_view(const_cast<void *>(workspace), M, Hkv, G, D);
-  const unsigned blocks = (unsigned)((int64_t)M * H);
-  // the chunk kernel's grid size: the number of valid block-table entries
-  const int P = (D == 128) ? grid_for_group<128>(G, M, Hkv, max_len)
-                           : grid_for_group<64>(G, M, Hkv, max_len);
-  if (P <= 0) return KVS_ERR_LAUNCH;
-  static bool carveout_set[kMaxDevices] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices && !carveout_set[dev]) {
-    // the same L1/shared split as the chunk kernel, so SMs need no
-    // reconfiguration between the two launches
-    cudaFuncSetAttribute(fd_reduce_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(fd_reduce_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    carveout_set[dev] = true;
-  }
-  cudaError_t e;
-  if (D == 128)
-    e = launch_pdl(fd_reduce_kernel<128>, dim3(blocks), dim3(128), 0, stream, positions, ws, out,
-                   M, Hkv, G, max_len, P, d_status);
-  else if (D == 64)
-    e = launch_pdl(fd_reduce_kernel<64>, dim3(blocks), dim3(128), 0, stream, positions, ws, out,
-                   M, Hkv, G, max_len, P, d_status);
-  else
-    return KVS_ERR_UNSUPPORTED;
-  return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
 }  // namespace kvs

@@ -91,43 +91,20 @@ size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads, 
   return kvs::ws_layout(M, num_kv_heads, num_heads / num_kv_heads, head_dim).total;
 }
 
-int kvs_flash_decode_partials(const float *q, const float *k_cache, const float *v_cache,
-                              const int32_t *positions, int M, int num_heads,
-                              int num_kv_heads, int head_dim, int max_len, int chunk_size,
-                              void *workspace, size_t workspace_bytes, int *d_status,
-                              kvs_stream_t stream) {
-  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
-  if (rc != KVS_OK) return rc;
-  if (M == 0) return KVS_OK;
-  if (!q || !k_cache || !v_cache || !positions) return KVS_ERR_NULL;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(positions, 4))
+// Pointer and workspace checks shared by the attention entry points.
+static int check_attention_buffers(const float *q, const float *k_cache, const float *v_cache,
+                                   const int32_t *positions, const float *out, int M,
+                                   int num_heads, int num_kv_heads, int head_dim,
+                                   const void *workspace, size_t workspace_bytes) {
+  if (!q || !k_cache || !v_cache || !positions || !out) return KVS_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(positions, 4))
     return KVS_ERR_ALIGN;
-  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
-  if (chunk <= 0) return -chunk;
   if (!workspace) return KVS_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KVS_ERR_ALIGN;
   if (workspace_bytes < kvs::ws_layout(M, num_kv_heads, num_heads / num_kv_heads, head_dim).total)
     return KVS_ERR_WORKSPACE;
-  return kvs::launch_fd_chunks(q, k_cache, v_cache, positions, M, num_heads, num_kv_heads,
-                               head_dim, max_len, chunk, workspace, d_status,
-                               reinterpret_cast<cudaStream_t>(stream));
-}
-
-int kvs_flash_decode_reduce(const int32_t *positions, float *out, int M, int num_heads,
-                            int num_kv_heads, int head_dim, int max_len, int chunk_size,
-                            void *workspace, size_t workspace_bytes, int *d_status,
-                            kvs_stream_t stream) {
-  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
-  if (rc != KVS_OK) return rc;
-  if (M == 0) return KVS_OK;
-  if (!out || !positions) return KVS_ERR_NULL;
-  if (!aligned(out, 16) || !aligned(positions, 4)) return KVS_ERR_ALIGN;
-  if (!workspace) return KVS_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return KVS_ERR_ALIGN;
-  if (workspace_bytes < kvs::ws_layout(M, num_kv_heads, num_heads / num_kv_heads, head_dim).total)
-    return KVS_ERR_WORKSPACE;
-  return kvs::launch_fd_reduce(positions, out, M, num_heads, num_kv_heads, head_dim, max_len,
-                               workspace, d_status, reinterpret_cast<cudaStream_t>(stream));
+  return KVS_OK;
 }
 
 int kvs_flash_decode(const float *q, const float *k_cache, const float *v_cache,
@@ -135,18 +112,39 @@ int kvs_flash_decode(const float *q, const float *k_cache, const float *v_cache,
                      int num_kv_heads, int head_dim, int max_len, int chunk_size,
                      void *workspace, size_t workspace_bytes, int *d_status,
                      kvs_stream_t stream) {
-  // validate everything (out included) before the first launch
   int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
   if (rc != KVS_OK) return rc;
   if (M == 0) return KVS_OK;
-  if (!out) return KVS_ERR_NULL;
-  if (!aligned(out, 16)) return KVS_ERR_ALIGN;
-  rc = kvs_flash_decode_partials(q, k_cache, v_cache, positions, M, num_heads, num_kv_heads,
-                                 head_dim, max_len, chunk_size, workspace, workspace_bytes,
-                                 d_status, stream);
+  rc = check_attention_buffers(q, k_cache, v_cache, positions, out, M, num_heads, num_kv_heads,
+                               head_dim, workspace, workspace_bytes);
   if (rc != KVS_OK) return rc;
-  return kvs_flash_decode_reduce(positions, out, M, num_heads, num_kv_heads, head_dim, max_len,
-                                 chunk_size, workspace, workspace_bytes, d_status, stream);
+  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
+  if (chunk <= 0) return -chunk;
+  // the caches are only read when no new rows are passed
+  return kvs::launch_fd_step(q, const_cast<float *>(k_cache), const_cast<float *>(v_cache),
+                             positions, nullptr, nullptr, out, M, num_heads, num_kv_heads,
+                             head_dim, max_len, chunk, workspace, d_status,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
+                    const int32_t *positions, float *k_cache, float *v_cache, float *out, int M,
+                    int num_heads, int num_kv_heads, int head_dim, int max_len, int chunk_size,
+                    void *workspace, size_t workspace_bytes, int *d_status,
+                    kvs_stream_t stream) {
+  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
+  if (rc != KVS_OK) return rc;
+  if (M == 0) return KVS_OK;
+  if (!k_rows || !v_rows) return KVS_ERR_NULL;
+  if (!aligned(k_rows, 16) || !aligned(v_rows, 16)) return KVS_ERR_ALIGN;
+  rc = check_attention_buffers(q, k_cache, v_cache, positions, out, M, num_heads, num_kv_heads,
+                               head_dim, workspace, workspace_bytes);
+  if (rc != KVS_OK) return rc;
+  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
+  if (chunk <= 0) return -chunk;
+  return kvs::launch_fd_step(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, num_heads,
+                             num_kv_heads, head_dim, max_len, chunk, workspace, d_status,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -9,39 +9,39 @@
 
 namespace kvs {
 
-// Upper bound on the chunk kernel's persistent grid (GB300: 152 SMs x 2).
+// Upper bound on the step kernel's persistent grid (GB300: 152 SMs x 2).
 constexpr int kMaxChunkBlocks = 1024;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace of kvs_flash_decode, shared by the chunk and reduce kernels.
-//   header  int num_blocks (the chunk kernel's grid size)
-//   table   int4 [kMaxChunkBlocks]: block b's first chunk (i, g, c) and
-//           whether the block has work (w); sorted by chunk.
+// Workspace of kvs_flash_decode / kvs_decode_step.
+//   header  256 bytes, reserved
+//   done    u64 [M*Hkv]: rows of (i, g) whose partial is written (counters
+//           carry the tag of the call that last used them, so the buffer
+//           needs no initialisation)
 //   ml      float2 [slots][G]: (running max in log2 units, running sum)
 //   acc     float  [slots][G][D]: unnormalised weighted-V accumulator
 // A partial slot belongs to one run of consecutive chunks of one (i, g):
 //   slot i*Hkv + g          the run that starts at chunk 0 of (i, g)
-//   slot M*Hkv + b          the first run of block b, when it starts inside (i, g)
+//   slot M*Hkv + b          block b's first run, when it starts inside (i, g)
 // so slots = M*Hkv + kMaxChunkBlocks, independent of max_len and chunk size.
 struct WsLayout {
-  size_t off_table, off_ml, off_acc, total;
+  size_t off_done, off_ml, off_acc, total;
   int64_t slots;
 };
 
 inline WsLayout ws_layout(int M, int Hkv, int G, int D) {
   WsLayout l;
   l.slots = (int64_t)M * Hkv + kMaxChunkBlocks;
-  l.off_table = 256;
-  l.off_ml = align_up(l.off_table + (size_t)kMaxChunkBlocks * 16, 256);
+  l.off_done = 256;
+  l.off_ml = align_up(l.off_done + (size_t)M * Hkv * 8, 256);
   l.off_acc = align_up(l.off_ml + (size_t)l.slots * G * 8, 256);
   l.total = align_up(l.off_acc + (size_t)l.slots * G * D * 4, 256);
   return l;
 }
 
 struct WsView {
-  int *num_blocks;
-  int4 *table;
+  unsigned long long *done;
   float2 *ml;
   float *acc;
 };
@@ -49,7 +49,7 @@ struct WsView {
 inline WsView workspace_view(void *base, int M, int Hkv, int G, int D) {
   const WsLayout l = ws_layout(M, Hkv, G, D);
   unsigned char *p = static_cast<unsigned char *>(base);
-  return WsView{reinterpret_cast<int *>(p), reinterpret_cast<int4 *>(p + l.off_table),
+  return WsView{reinterpret_cast<unsigned long long *>(p + l.off_done),
                 reinterpret_cast<float2 *>(p + l.off_ml), reinterpret_cast<float *>(p + l.off_acc)};
 }
 
@@ -77,12 +77,12 @@ int launch_kv_scatter(const float *k_rows, const float *v_rows, const int32_t *p
                       float *k_cache, float *v_cache, int M, int Hkv, int D, int max_len,
                       int *d_status, cudaStream_t stream);
 
-int launch_fd_chunks(const float *q, const float *k_cache, const float *v_cache,
-                     const int32_t *positions, int M, int H, int Hkv, int D, int max_len,
-                     int chunk, void *workspace, int *d_status, cudaStream_t stream);
-
-int launch_fd_reduce(const int32_t *positions, float *out, int M, int H, int Hkv, int D,
-                     int max_len, const void *workspace, int *d_status, cudaStream_t stream);
+// One launch of the step kernel: split-K attention over the caches; with
+// k_rows/v_rows non-null the scatter of those rows is done in the same launch.
+int launch_fd_step(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+                   const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
+                   int D, int max_len, int chunk, void *workspace, int *d_status,
+                   cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device); <= 0 on error.
 int device_sm_count();

@@ -94,20 +94,43 @@ def test_flash_decode_validation(L, kw, code):
     assert _fd(L, **kw) == code
 
 
+def _ds(L, q=A16, kr=A16, vr=A16, pos=A16, k=A16, v=A16, out=A16, M=1, H=4, Hkv=2, D=64,
+        Lmax=256, C=64, ws=A16, wsb=1 << 30):
+    return L.kvs_decode_step(q, kr, vr, pos, k, v, out, M, H, Hkv, D, Lmax, C, ws, wsb, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), B.KVS_ERR_DIMS),
+    (dict(H=6, Hkv=4), B.KVS_ERR_DIMS),
+    (dict(D=96), B.KVS_ERR_UNSUPPORTED),
+    (dict(kr=None), B.KVS_ERR_NULL),
+    (dict(vr=None), B.KVS_ERR_NULL),
+    (dict(k=None), B.KVS_ERR_NULL),
+    (dict(out=None), B.KVS_ERR_NULL),
+    (dict(kr=A16 + 4), B.KVS_ERR_ALIGN),
+    (dict(v=A16 + 8), B.KVS_ERR_ALIGN),
+    (dict(ws=None), B.KVS_ERR_WORKSPACE),
+    (dict(wsb=64), B.KVS_ERR_WORKSPACE),
+])
+def test_decode_step_validation(L, kw, code):
+    assert _ds(L, **kw) == code
+
+
 def test_flash_decode_empty_batch_ok(L):
     assert _fd(L, M=0, q=None, k=None, v=None, pos=None, out=None, ws=None, wsb=0) == 0
 
 
 def test_workspace_bytes_formula(L):
-    # 256-byte header, a 1024-entry int4 block table, then per partial slot
-    # (M*Hkv + 1024 slots, G query heads each) a float2 (m, l) and D floats
-    # of accumulator; every section starts on a 256-byte boundary.
+    # 256-byte header, one 8-byte completion counter per (sequence, kv head),
+    # then per partial slot (M*Hkv + 1024 slots, G query heads each) a float2
+    # (m, l) and D floats of accumulator; each section starts on a 256-byte
+    # boundary.
     up = lambda x: -(-x // 256) * 256
     for (M, H, Hkv, D, Lmax, C) in [(1, 4, 2, 64, 256, 64), (8, 32, 8, 128, 32768, 128),
                                     (32, 40, 8, 128, 131072, 256), (3, 8, 2, 128, 1000, 7)]:
         G = H // Hkv
         slots = M * Hkv + 1024
-        off_ml = up(256 + 1024 * 16)
+        off_ml = up(256 + M * Hkv * 8)
         off_acc = up(off_ml + slots * G * 8)
         assert B.kvs_flash_decode_workspace_bytes(M, H, Hkv, D, Lmax, C) == up(off_acc + slots * G * D * 4)
         # independent of max_len and chunk size

@@ -30,18 +30,25 @@ def _built():
     torch.cuda.synchronize()
 
 
-def run_step(t, w, chunk, status=None, ws=None, poison_ws=True):
-    """Scatter + decode through the C ABI; returns out (device)."""
+def run_step(t, w, chunk, status=None, ws=None, poison_ws=True, fused=False):
+    """One decode step through the C ABI; returns out (device).
+
+    fused=False: kvs_kv_scatter then kvs_flash_decode (two launches);
+    fused=True:  kvs_decode_step (one launch)."""
     M, H, D = t["q"].shape
     if ws is None:
         ws = B.workspace(M, H, w.num_kv_heads, D, w.max_len, chunk, device=DEV)
     if poison_ws:
         ws.fill_(0xFF)
     out = torch.full((M, H, D), float("nan"), device=DEV)
-    B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"], t["v_cache"],
-                     d_status=status)
-    B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
-                       chunk_size=chunk, workspace=ws, d_status=status)
+    if fused:
+        B.kvs_decode_step(t["q"], t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
+                          t["v_cache"], out, chunk_size=chunk, workspace=ws, d_status=status)
+    else:
+        B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"], t["v_cache"],
+                         d_status=status)
+        B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
+                           chunk_size=chunk, workspace=ws, d_status=status)
     return out
 
 
@@ -57,19 +64,24 @@ def oracle_out(inp):
 
 
 def check_workload(w, chunks, layer=0, inp=None):
+    """Both entry paths (two launches, and the fused step) against the oracle,
+    for every chunk size, plus the bit-exact caches."""
     inp = inp if inp is not None else W.make_inputs(w, layer=layer)
-    t = W.upload(inp, w, DEV)
     exp = W.upload(inp, w, DEV, include_new_row=True)
     ref = oracle_out(inp)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     results = {}
-    for c in chunks:
-        out = run_step(t, w, c, status)
-        torch.cuda.synchronize()
-        assert int(status.item()) == 0, B.strerror(int(status.item()))
-        results[c] = gate(out.cpu().numpy(), ref, where=f"{w.name} chunk={c}")
-    assert_cache_bit_exact(t, exp)
-    del t, exp
+    for fused in (False, True):
+        t = W.upload(inp, w, DEV)
+        for c in chunks:
+            out = run_step(t, w, c, status, fused=fused)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0, B.strerror(int(status.item()))
+            results[(fused, c)] = gate(out.cpu().numpy(), ref,
+                                       where=f"{w.name} chunk={c} fused={fused}")
+        assert_cache_bit_exact(t, exp)
+        del t
+    del exp
     torch.cuda.empty_cache()
     return results
 
@@ -196,17 +208,51 @@ def test_repeatable_and_stream_ordered():
     gate(a.cpu().numpy(), oracle_out(inp), where="side stream")
 
 
-def test_split_entry_points_equal_fused_entry():
-    w = W.custom(M=4, num_heads=16, num_kv_heads=4, head_dim=128, max_len=900, seed=17)
+def test_fused_step_equals_scatter_then_decode_bitwise():
+    """kvs_decode_step = kvs_kv_scatter + kvs_flash_decode, bit for bit."""
+    w = W.custom(M=6, num_heads=40, num_kv_heads=8, head_dim=128, max_len=1500, seed=17)
     inp = W.make_inputs(w)
-    t = W.upload(inp, w, DEV)
-    a = run_step(t, w, 128)
-    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, 128, device=DEV)
-    b = torch.empty_like(a)
-    B.kvs_flash_decode_partials(t["q"], t["k_cache"], t["v_cache"], t["positions"], 128, ws)
-    B.kvs_flash_decode_reduce(t["positions"], b, w.num_kv_heads, w.max_len, 128, ws)
+    t1 = W.upload(inp, w, DEV)
+    t2 = W.upload(inp, w, DEV)
+    a = run_step(t1, w, 64)
+    b = run_step(t2, w, 64, fused=True)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    for name in ("k_cache", "v_cache"):
+        assert torch.equal(t1[name].view(torch.int32), t2[name].view(torch.int32))
+
+
+def test_fused_step_bad_position_flags_and_skips():
+    w = W.custom(M=3, num_heads=8, num_kv_heads=2, head_dim=128, max_len=64, seed=23)
+    pos = np.array([10, 64, 63], np.int32)
+    inp = W.make_inputs(w, positions=pos)
+    t = W.upload(inp, w, DEV)
+    exp = W.upload(inp, w, DEV, include_new_row=True)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_step(t, w, 16, status, fused=True).cpu().numpy()
+    assert int(status.item()) == B.KVS_ERR_POSITION
+    assert np.all(np.isnan(out[1]))
+    good = [0, 2]
+    ref = oracle.decode_sequences(inp.q[good], [inp.k_seq[i] for i in good],
+                                  [inp.v_seq[i] for i in good], pos[good])
+    gate(out[good], ref, where="fused step beside an invalid position")
+    assert_cache_bit_exact(t, exp)
+
+
+def test_workspace_reuse_across_shapes_and_calls():
+    """One workspace, garbage-filled, reused by calls of different shapes: the
+    tagged counters must never take a stale value as this call's."""
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=DEV)
+    ws.fill_(0x5A)
+    for seed, (M, H, Hkv, L) in enumerate([(4, 32, 8, 3000), (2, 8, 2, 700), (4, 32, 8, 3000)]):
+        w = W.custom(M=M, num_heads=H, num_kv_heads=Hkv, head_dim=128, max_len=L, seed=50 + seed)
+        inp = W.make_inputs(w)
+        t = W.upload(inp, w, DEV)
+        for fused in (False, True, True):
+            t = W.upload(inp, w, DEV)
+            out = run_step(t, w, 32, ws=ws, poison_ws=False, fused=fused)
+            torch.cuda.synchronize()
+            gate(out.cpu().numpy(), oracle_out(inp), where=f"reuse {seed} fused={fused}")
 
 
 def test_workspace_too_small_is_rejected_before_launch():
