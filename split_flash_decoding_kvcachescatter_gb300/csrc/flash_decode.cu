@@ -106,6 +106,7 @@ constexpr int kRunCostBytes = 40960;
 
 // Scratch of the (i, g) merge (aliases the warp-state merge area).
 constexpr int kMergeWindow = 32;  // runs weighted per pass
+constexpr int kFastRuns = 16;     // runs merged with one load of their (m, l)
 constexpr int kMergeScratchBytes = kMergeWindow * 4 + kMergeWindow * 8 * 4 + 8 * 4 * 2 + 16;
 
 // Compile-time geometry of one (head_dim, group) instantiation.
@@ -432,6 +433,59 @@ __device__ void merge_runs(const WsView &ws, float *out, int i, int g, int M, in
     if (j + 1 < ncand && cand_chunk(j + 1) == cc) return -1;  // an empty block; the next starts here
     return M * Hkv + b_lo + j;
   };
+  // Fast path, the usual case: at most kFastRuns runs, all candidates in one
+  // window.  Every partial is loaded at once into registers, then merged.
+  if (ncand < kMergeWindow) {
+    if (t < 32) {
+      const int j = t - 1;
+      const int sl = (j < ncand) ? run_slot(j) : -1;
+      const unsigned ballot = __ballot_sync(0xffffffffu, sl >= 0);
+      if (sl >= 0) s_list[__popc(ballot & ((1u << lane) - 1u))] = sl;
+      if (lane == 0) *s_n = __popc(ballot);
+    }
+    consumer_sync(NT);
+    const int nb = *s_n;
+    if (nb <= kFastRuns) {
+      // (m, l) of every run and head, loaded once into shared memory
+      float2(*s_ml)[8] = reinterpret_cast<float2(*)[8]>(s_w);  // [kFastRuns][8]
+      for (int e = t; e < nb * G; e += NT) {
+        const int r = e / G;
+        const int h = e - r * G;
+        s_ml[r][h] = __ldcg(&ws.ml[(size_t)s_list[r] * G + h]);
+      }
+      consumer_sync(NT);
+      const float4 *acc4 = reinterpret_cast<const float4 *>(ws.acc);
+      float4 *o4 = reinterpret_cast<float4 *>(out) + ((size_t)i * H + (size_t)g * G) * LPR;
+#pragma unroll
+      for (int q = 0; q < NE; ++q) {
+        const int e = t + q * NT;
+        if (e < G * LPR) {
+          const int h = e / LPR;
+          const int d4 = e - h * LPR;
+          float mx = neg_inf();
+          for (int r = 0; r < nb; ++r) mx = fmaxf(mx, s_ml[r][h].x);
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+          float l = 0.f;
+#pragma unroll 4
+          for (int r = 0; r < nb; ++r) {
+            const float2 ml = s_ml[r][h];
+            const float w = exp2f(ml.x - mx);
+            const float4 bb = __ldcg(&acc4[((size_t)s_list[r] * G + h) * LPR + d4]);
+            a.x = fmaf(w, bb.x, a.x);
+            a.y = fmaf(w, bb.y, a.y);
+            a.z = fmaf(w, bb.z, a.z);
+            a.w = fmaf(w, bb.w, a.w);
+            l = fmaf(w, ml.y, l);
+          }
+          const float inv = 1.f / l;
+          o4[e] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+        }
+      }
+      consumer_sync(NT);  // the scratch is read by every thread before it is reused
+      return;
+    }
+  }
+
   if (t < G) {
     s_mx[t] = neg_inf();
     s_l[t] = 0.f;
