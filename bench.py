@@ -91,9 +91,9 @@ def chunk_source_hash():
 
 
 def ncu_traffic(workload, chunk):
-    """Per-launch DRAM bytes of the chunk kernel from a committed ncu summary,
+    """Per-launch DRAM bytes of the step kernel from a committed ncu summary,
     if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "fd_chunk_traffic.json")
+    path = os.path.join(ROOT, "profiles", "fd_step_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
