@@ -259,6 +259,8 @@ def main():
     ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--graph", action="store_true",
+                    help="launch the whole (multi-layer) step as one captured CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -290,34 +292,59 @@ def main():
         if world > 1:
             tdist.barrier()
 
-    t = W.upload(inp, w, dev)
+    nl = w.layers  # a step covers every layer of the workload (24 for small_model)
+    inps = [inp] + [W.make_inputs(w, layer=l, seed=seed, positions=inp.positions)
+                    for l in range(1, nl)]
+    ts = [W.upload(x, w, dev) for x in inps]
     chunk = args.chunk if args.chunk is not None else w.chunk_size
     resolved_chunk = chunk if chunk > 0 else B.kvs_choose_chunk_size(
         w.M, w.num_kv_heads, w.head_dim, w.max_len)
     ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, resolved_chunk,
                      device=dev)
-    out = torch.empty_like(t["q"])
+    outs = [torch.empty_like(t["q"]) for t in ts]
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ab = W.algorithmic_bytes(inp, w)
-    cache_bytes = 2 * w.cache_elems() * 4
+    ab1 = W.algorithmic_bytes(inp, w)  # one layer; every layer has the same positions
+    ab = {k: v * nl for k, v in ab1.items()}
+    cache_bytes = 2 * w.cache_elems() * 4 * nl
     flush = ab["step"] < 4 * L2_BYTES  # small working sets: scrub L2 between steps
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     stream = torch.cuda.current_stream()
 
-    def step():
-        """The whole hot path in one launch: scatter, split plan, chunk
+    def eager_step():
+        """The whole hot path, one launch per layer: scatter, split plan, chunk
         partials and the rescaled merge (kvs_decode_step)."""
-        B.kvs_decode_step(t["q"], t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
-                          t["v_cache"], out, chunk_size=resolved_chunk, workspace=ws,
-                          d_status=status)
+        for t, out in zip(ts, outs):
+            B.kvs_decode_step(t["q"], t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
+                              t["v_cache"], out, chunk_size=resolved_chunk, workspace=ws,
+                              d_status=status)
+
+    graph = None
+    if args.graph:
+        eager_step()  # configure the kernels outside the capture
+        torch.cuda.synchronize()
+        graph = B.kvs_step_graph_create(
+            [t["q"] for t in ts], [t["k_rows"] for t in ts], [t["v_rows"] for t in ts],
+            ts[0]["positions"], [t["k_cache"] for t in ts], [t["v_cache"] for t in ts], outs,
+            chunk_size=resolved_chunk, workspace=ws, d_status=status)
+        for t in ts[1:]:  # the graph reads the positions of layer 0 for every layer
+            t["positions"] = ts[0]["positions"]
+
+    def step():
+        if graph is not None:
+            graph.launch(stream)
+        else:
+            eager_step()
 
     def two_calls(mid):
-        """The same step as the two separate entry points, an event between."""
-        B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"], t["v_cache"],
-                         d_status=status)
+        """The same step as the two separate entry points (all layers' scatters,
+        an event, then all layers' attention)."""
+        for t in ts:
+            B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
+                             t["v_cache"], d_status=status)
         mid.record(stream)
-        B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
-                           chunk_size=resolved_chunk, workspace=ws, d_status=status)
+        for t, out in zip(ts, outs):
+            B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
+                               chunk_size=resolved_chunk, workspace=ws, d_status=status)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -367,19 +394,26 @@ def main():
 
     # ---- e2e: host buffers through the public API ----
     Ke = args.e2e_steps or max(3, min(K, 500))
-    host = {k: t[k].cpu().pin_memory() for k in ("q", "k_rows", "v_rows", "positions")}
-    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dev_in = {k: torch.empty_like(t[k]) for k in host}
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = host_out.numel() * host_out.element_size()
+    names = ("q", "k_rows", "v_rows")
+    host = [{k: t[k].cpu().pin_memory() for k in names} for t in ts]
+    host_pos = ts[0]["positions"].cpu().pin_memory()
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    dev_in = [{k: torch.empty_like(t[k]) for k in names} for t in ts]
+    dev_pos = torch.empty_like(ts[0]["positions"])
+    h2d = sum(v.numel() * v.element_size() for h in host for v in h.values()) + \
+        host_pos.numel() * host_pos.element_size()
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
 
     def e2e_step():
-        for k in host:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        B.kvs_decode_step(dev_in["q"], dev_in["k_rows"], dev_in["v_rows"], dev_in["positions"],
-                          t["k_cache"], t["v_cache"], out, chunk_size=resolved_chunk,
-                          workspace=ws, d_status=status)
-        host_out.copy_(out, non_blocking=True)
+        dev_pos.copy_(host_pos, non_blocking=True)
+        for l, t in enumerate(ts):
+            for k in names:
+                dev_in[l][k].copy_(host[l][k], non_blocking=True)
+            B.kvs_decode_step(dev_in[l]["q"], dev_in[l]["k_rows"], dev_in[l]["v_rows"], dev_pos,
+                              t["k_cache"], t["v_cache"], outs[l], chunk_size=resolved_chunk,
+                              workspace=ws, d_status=status)
+        for l in range(nl):
+            host_out[l].copy_(outs[l], non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -420,8 +454,9 @@ def main():
 
     value = bytes_all / (total_ms_max * 1e-3) / 1e9
     e2e_value = bytes_e2e_all / (e2e_ms_max * Ke * 1e-3) / 1e9
-    # The step is one launch of the step kernel, so the headline events time
-    # exactly that kernel: its algorithmic bytes are the step's.
+    # A step is one launch of the step kernel per layer and nothing else, so
+    # the headline events time exactly those launches: bytes per launch over
+    # the mean launch time is the step's bytes over the step's time.
     step_mean_ms = total_ms / K
     achieved = ab["step"] / (step_mean_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -444,7 +479,9 @@ def main():
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "max_len": w.max_len,
             "chunk_size": resolved_chunk,
             "chunk_rule": "given" if chunk > 0 else "library rule (chunk_size=0)",
-            "live_kv_bytes": W.kv_bytes(inp, w),
+            "layers": nl, "launch": ("one CUDA graph for all layers" if graph is not None
+                                     else f"{nl} kvs_decode_step launch(es)"),
+            "live_kv_bytes": W.kv_bytes(inp, w) * nl,
             "algorithmic_bytes_per_step": ab["step"],
             "cache_bytes_allocated": cache_bytes,
             "l2": ("L2 scrubbed (2x129 MB write) between timed steps, outside the events"
@@ -460,10 +497,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "fd_step_kernel (kvs_decode_step)", "peak_source": peak_kind,
-                     "bytes_per_launch": ab["step"]},
+                     "bytes_per_launch": ab1["step"]},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
-        "gpu_launches": K,
+        "gpu_launches": K * nl,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

@@ -174,6 +174,44 @@ int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
                     size_t workspace_bytes, int *d_status, kvs_stream_t stream);
 
 /*
+ * CUDA graph of a whole multi-layer decode step (the pages' graphed decode:
+ * realizar 0.8.5 batched_forward.rs / reduces.rs capture and replay, and
+ * aprender-serve 0.70.2 forward_qwen35_cuda_graph.rs, module doc: one graph
+ * launch replays every layer; per-token inputs live at fixed device
+ * addresses that the host rewrites before each replay).
+ *
+ * kvs_step_graph_create captures, on `stream` (not the legacy default
+ * stream; it must not be capturing already), one kvs_decode_step per layer
+ * l = 0..layers-1 with q[l], k_rows[l], v_rows[l], k_cache[l], v_cache[l],
+ * out[l] (host arrays of `layers` device pointers) and the shared
+ * `positions`, `workspace` (one buffer serves all layers: the layers run in
+ * order) and `d_status`.  Capture uses the thread-local mode and is always
+ * ended; on any error nothing is kept and the status is returned (the
+ * caller can stay on the eager path).  Every pointer is frozen into the
+ * graph: update the buffers' contents, never their addresses, between
+ * launches.  The graph and its executable are CUDA objects owned by the
+ * handle; the library allocates no device memory.
+ *
+ * kvs_step_graph_launch enqueues the whole step on `stream`.
+ * kvs_step_graph_destroy releases the handle (NULL is a no-op).
+ */
+typedef struct kvs_step_graph kvs_step_graph;
+
+int kvs_step_graph_create(int layers, const float *const *q,
+                          const float *const *k_rows,
+                          const float *const *v_rows, const int32_t *positions,
+                          float *const *k_cache, float *const *v_cache,
+                          float *const *out, int M, int num_heads,
+                          int num_kv_heads, int head_dim, int max_len,
+                          int chunk_size, void *workspace,
+                          size_t workspace_bytes, int *d_status,
+                          kvs_stream_t stream, kvs_step_graph **graph);
+
+int kvs_step_graph_launch(kvs_step_graph *graph, kvs_stream_t stream);
+
+int kvs_step_graph_destroy(kvs_step_graph *graph);
+
+/*
  * kvs_flash_decode_static -- kvs_flash_decode for callers that cannot
  * allocate device memory (no counterpart in the pages: they always hand the
  * kernels a preallocated partials buffer).

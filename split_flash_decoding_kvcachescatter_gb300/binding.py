@@ -30,7 +30,8 @@ KVS_ERR_TIMEOUT = 8
 
 # Every symbol include/kvsdecode.h declares.
 EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspace_bytes",
-           "kvs_flash_decode", "kvs_decode_step", "kvs_strerror", "kvs_flash_decode_static")
+           "kvs_flash_decode", "kvs_decode_step", "kvs_strerror", "kvs_flash_decode_static",
+           "kvs_step_graph_create", "kvs_step_graph_launch", "kvs_step_graph_destroy")
 
 # Size of the library's built-in scratch buffer used by kvs_flash_decode_static.
 KVS_STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024
@@ -74,6 +75,13 @@ def lib() -> ctypes.CDLL:
             L.kvs_flash_decode_static.restype = _I
             L.kvs_flash_decode_static.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                   _P, _P]
+            L.kvs_step_graph_create.restype = _I
+            L.kvs_step_graph_create.argtypes = [_I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                                _I, _I, _P, _SZ, _P, _P, _P]
+            L.kvs_step_graph_launch.restype = _I
+            L.kvs_step_graph_launch.argtypes = [_P, _P]
+            L.kvs_step_graph_destroy.restype = _I
+            L.kvs_step_graph_destroy.argtypes = [_P]
             L.kvs_strerror.restype = ctypes.c_char_p
             L.kvs_strerror.argtypes = [_I]
             _lib = L
@@ -203,3 +211,49 @@ def kvs_flash_decode_static(q, k_cache, v_cache, positions, out, chunk_size=0, d
                                        Hkv, D, Lmax, int(chunk_size), _status_ptr(d_status),
                                        _stream(stream))
     _check(rc, "kvs_flash_decode_static")
+
+
+class StepGraph:
+    """Handle of kvs_step_graph_create: a whole multi-layer decode step as one
+    CUDA graph over fixed buffers (update their contents, not their
+    addresses, between launches)."""
+
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep  # the captured tensors must outlive the graph
+
+    def launch(self, stream=None):
+        _check(lib().kvs_step_graph_launch(self._h, _stream(stream)), "kvs_step_graph_launch")
+
+    def destroy(self):
+        if self._h:
+            lib().kvs_step_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def kvs_step_graph_create(q, k_rows, v_rows, positions, k_cache, v_cache, out, chunk_size=0,
+                          workspace=None, d_status=None, stream=None):
+    """Capture one kvs_decode_step per layer (lists of per-layer tensors)."""
+    layers = len(q)
+    if not (len(k_rows) == len(v_rows) == len(k_cache) == len(v_cache) == len(out) == layers):
+        raise ValueError("kvs_step_graph_create: one tensor per layer in every list")
+    if workspace is None:
+        raise ValueError("kvs_step_graph_create: pass a workspace")
+    M, H, Hkv, D, Lmax = _attn_shapes(q[0], k_cache[0])
+    arr = lambda ts, name, nd: (ctypes.c_void_p * layers)(*[_f32(t, name, nd) for t in ts])
+    s = torch.cuda.Stream() if stream is None else stream
+    handle = ctypes.c_void_p()
+    rc = lib().kvs_step_graph_create(
+        layers, arr(q, "q", 3), arr(k_rows, "k_rows", 3), arr(v_rows, "v_rows", 3),
+        _i32(positions, "positions"), arr(k_cache, "k_cache", 4), arr(v_cache, "v_cache", 4),
+        arr(out, "out", 3), M, H, Hkv, D, Lmax, int(chunk_size), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _status_ptr(d_status), _stream(s),
+        ctypes.byref(handle))
+    _check(rc, "kvs_step_graph_create")
+    return StepGraph(handle, (q, k_rows, v_rows, positions, k_cache, v_cache, out, workspace))

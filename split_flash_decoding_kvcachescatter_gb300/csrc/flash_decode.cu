@@ -32,7 +32,8 @@
 //    merges all of (i, g)'s runs (found from the same column arithmetic) and
 //    writes the output.  A (i, g) covered by a single run is written
 //    directly.  The counters carry the tag of the call that last used them,
-//    so the workspace needs no initialisation.
+//    so the workspace needs no initialisation, and the merging block resets
+//    its counter, so replaying a captured graph (same tag) is safe too.
 //  * Scatter folded in (kvs_decode_step): blocks first write the step's new
 //    K/V rows into the caches; the attention reads row p of each sequence
 //    from the new-row input itself, so no block waits for another.
@@ -966,7 +967,12 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     if (!whole) {
       if (threadIdx.x == 0) {
         const unsigned before = tagged_add(ws.done + dsc.ig, (unsigned)dsc.run_rows, tag, d_status);
-        *s_last = (before != 0xffffffffu && before + (unsigned)dsc.run_rows == (unsigned)dsc.L);
+        const bool last = (before != 0xffffffffu && before + (unsigned)dsc.run_rows == (unsigned)dsc.L);
+        // Every run of (i, g) has counted: reset the counter (tag 0 is never
+        // a call's tag), so a later launch with the same tag -- a replayed
+        // CUDA graph freezes the tag argument -- starts from zero too.
+        if (last) ws.done[dsc.ig] = 0ull;
+        *s_last = last;
       }
       if (!consumers_barrier()) return;
       if (*s_last) {  // every run of (i, g) is in: merge them
@@ -1097,6 +1103,28 @@ int device_sm_count() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+int prepare_step_kernel(int H, int Hkv, int D) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVS_ERR_LAUNCH;
+  if (Hkv < 1 || H % Hkv != 0) return KVS_ERR_DIMS;
+  const int G = H / Hkv;
+  int bps = -1;
+  switch (D * 16 + G) {
+#define KVS_PREP(d, g)                          \
+  case d * 16 + g:                              \
+    bps = step_blocks_per_sm<d, g>(dev);        \
+    break;
+    KVS_PREP(64, 1) KVS_PREP(64, 2) KVS_PREP(64, 3) KVS_PREP(64, 4)
+    KVS_PREP(64, 5) KVS_PREP(64, 6) KVS_PREP(64, 7) KVS_PREP(64, 8)
+    KVS_PREP(128, 1) KVS_PREP(128, 2) KVS_PREP(128, 3) KVS_PREP(128, 4)
+    KVS_PREP(128, 5) KVS_PREP(128, 6) KVS_PREP(128, 7) KVS_PREP(128, 8)
+#undef KVS_PREP
+    default:
+      return KVS_ERR_UNSUPPORTED;
+  }
+  return (bps > 0 && device_sm_count() > 0) ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
 int launch_fd_step(const float *q, float *k_cache, float *v_cache, const int32_t *positions,

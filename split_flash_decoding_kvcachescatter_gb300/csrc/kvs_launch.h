@@ -84,6 +84,10 @@ int launch_fd_step(const float *q, float *k_cache, float *v_cache, const int32_t
                    int D, int max_len, int chunk, void *workspace, int *d_status,
                    cudaStream_t stream);
 
+// Sets the step kernel's attributes for (H / Hkv, D) on the current device
+// (done on first use anyway; a stream capture calls it beforehand).
+int prepare_step_kernel(int H, int Hkv, int D);
+
 // Number of SMs of the current device (cached per device); <= 0 on error.
 int device_sm_count();
 

@@ -150,3 +150,20 @@ def test_chunk_rule_is_pow2_in_range(L):
         B.kvs_choose_chunk_size(32, 8, 128, 8192, 76)
     with pytest.raises(B.KvsError):
         B.kvs_choose_chunk_size(0, 8, 128, 8192, 152)
+
+
+def test_step_graph_host_checks(L):
+    h = ctypes.c_void_p()
+    args = [None] * 7
+    # no output handle
+    assert L.kvs_step_graph_create(1, *args, 1, 4, 2, 64, 16, 0, None, 0, None, A16, None) == \
+        B.KVS_ERR_NULL
+    # zero layers, negative chunk, legacy default stream: rejected before any CUDA call
+    assert L.kvs_step_graph_create(0, *args, 1, 4, 2, 64, 16, 0, None, 0, None, A16,
+                                   ctypes.byref(h)) == B.KVS_ERR_DIMS
+    assert L.kvs_step_graph_create(1, *args, 1, 4, 2, 64, 16, -1, None, 0, None, A16,
+                                   ctypes.byref(h)) == B.KVS_ERR_DIMS
+    assert L.kvs_step_graph_create(1, *args, 1, 4, 2, 64, 16, 0, None, 0, None, None,
+                                   ctypes.byref(h)) == B.KVS_ERR_NULL
+    assert L.kvs_step_graph_destroy(None) == 0
+    assert L.kvs_step_graph_launch(None, None) == B.KVS_ERR_NULL

@@ -267,3 +267,75 @@ def test_workspace_too_small_is_rejected_before_launch():
                            chunk_size=64, workspace=small)
     assert e.value.status == B.KVS_ERR_WORKSPACE
     assert torch.count_nonzero(out).item() == 0
+
+
+def test_graph_replay_with_new_inputs():
+    """A captured CUDA graph freezes every kernel argument; replays with new
+    inputs copied into the captured buffers must still match the oracle."""
+    w = W.custom(M=8, num_heads=32, num_kv_heads=8, head_dim=128, max_len=3000, seed=61)
+    inp_a = W.make_inputs(w, seed=61)
+    inp_b = W.make_inputs(w, seed=62)
+    t = W.upload(inp_a, w, DEV)
+    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, 0, device=DEV)
+    ws.fill_(0x33)
+    out = torch.empty_like(t["q"])
+
+    def step():
+        B.kvs_decode_step(t["q"], t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
+                          t["v_cache"], out, chunk_size=0, workspace=ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # first call on the device configures the kernel outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for inp in (inp_a, inp_b, inp_a):
+        fresh = W.upload(inp, w, DEV)
+        for name in fresh:
+            t[name].copy_(fresh[name])
+        g.replay()
+        torch.cuda.synchronize()
+        gate(out.cpu().numpy(), oracle_out(inp), where="graph replay")
+
+
+def test_step_graph_multi_layer():
+    """kvs_step_graph_create: L layers' decode steps in one graph launch, then
+    relaunched after new inputs are copied into the same buffers."""
+    layers = 4
+    w = W.custom(M=4, num_heads=14, num_kv_heads=2, head_dim=64, max_len=900, chunk_size=64,
+                 seed=70)
+    pos = W.draw_positions(w)
+    ins = [W.make_inputs(w, layer=l, positions=pos) for l in range(layers)]
+    ts = [W.upload(x, w, DEV) for x in ins]
+    exps = [W.upload(x, w, DEV, include_new_row=True) for x in ins]
+    outs = [torch.full_like(t["q"], float("nan")) for t in ts]
+    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, 64, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.Stream()
+    g = B.kvs_step_graph_create([t["q"] for t in ts], [t["k_rows"] for t in ts],
+                                [t["v_rows"] for t in ts], ts[0]["positions"],
+                                [t["k_cache"] for t in ts], [t["v_cache"] for t in ts], outs,
+                                chunk_size=64, workspace=ws, d_status=status, stream=stream)
+    g.launch(stream)
+    stream.synchronize()
+    assert int(status.item()) == 0
+    for l in range(layers):
+        gate(outs[l].cpu().numpy(), oracle_out(ins[l]), where=f"graph layer {l}")
+        assert_cache_bit_exact(ts[l], exps[l])
+    # a second token: new q and rows, next positions, same buffers
+    pos2 = np.minimum(pos + 1, w.max_len - 1).astype(np.int32)
+    ins2 = [W.make_inputs(w, layer=l, positions=pos2, seed=71) for l in range(layers)]
+    for l in range(layers):
+        fresh = W.upload(ins2[l], w, DEV)
+        for name in ("q", "k_rows", "v_rows", "k_cache", "v_cache"):
+            ts[l][name].copy_(fresh[name])
+    ts[0]["positions"].copy_(torch.from_numpy(pos2).to(DEV))
+    g.launch(stream)
+    stream.synchronize()
+    for l in range(layers):
+        gate(outs[l].cpu().numpy(), oracle_out(ins2[l]), where=f"graph relaunch layer {l}")
+    g.destroy()
