@@ -83,6 +83,7 @@ __host__ __device__ constexpr int ilog2(int x) {
 }
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 __host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
@@ -106,9 +107,14 @@ struct StageDesc {
 constexpr int kRunCostBytes = 40960;
 
 // Scratch of the (i, g) merge (aliases the warp-state merge area).
-constexpr int kMergeWindow = 32;  // runs weighted per pass
-constexpr int kFastRuns = 16;     // runs merged with one load of their (m, l)
-constexpr int kMergeScratchBytes = kMergeWindow * 4 + kMergeWindow * 8 * 4 + 8 * 4 * 2 + 16;
+constexpr int kMergeWindow = 32;  // candidate blocks examined per pass
+// Partial loads a merging thread keeps in flight: 8, or 4 for groups of more
+// than 5 heads, whose chunk loop leaves fewer registers free.
+__host__ __device__ constexpr int merge_batch(int G) { return G <= 5 ? 8 : 4; }
+constexpr int kMergeScratchBytes = kMergeWindow * 4 + 16;
+
+// Shared memory budget of the stage ring (two blocks per SM).
+constexpr int kRingBytes = 96 * 1024;
 
 // Compile-time geometry of one (head_dim, group) instantiation.
 template <int D_, int G_>
@@ -117,7 +123,6 @@ struct Geo {
   static constexpr int G = G_;
   static constexpr int NW = 4;                    // consumer warps
   static constexpr int THREADS = (NW + 1) * 32;   // + one producer warp
-  static constexpr int S = 3;                     // pipeline stages
   static constexpr int LPR = D / 4;               // lanes per row (float4 each)
   static constexpr int RPI = 32 / LPR;            // rows per warp instruction
   static constexpr int RP = (LPR / G) < 8 ? (LPR / G) : 8;  // rows per lane group
@@ -131,6 +136,10 @@ struct Geo {
   static constexpr int KV_BYTES = T * D * 4;      // one of K or V per stage
   static constexpr int Q_BYTES = G * D * 4;
   static constexpr int STAGE_BYTES = round_up(2 * KV_BYTES + Q_BYTES, 128);
+  // pipeline stages: as many as fit in kRingBytes, at least 3 and at most 8
+  // (small stages -- head_dim 64 with a large group -- get a deeper ring, so
+  // that one block alone still keeps tens of KB of K/V in flight)
+  static constexpr int S = cmin(8, cmax(3, kRingBytes / STAGE_BYTES));
   static constexpr int OFF_SCORE = S * STAGE_BYTES;
   static constexpr int SCORE_BYTES = NW * G * RWP * 4;
   static constexpr int OFF_P = OFF_SCORE + SCORE_BYTES;
@@ -318,15 +327,6 @@ __device__ __forceinline__ unsigned tagged_add(unsigned long long *ctr, unsigned
                             d_status);
 }
 
-// max for floats in shared memory (order-independent, so deterministic)
-__device__ __forceinline__ void smem_max_float(float *addr, float v) {
-  if (v >= 0.f)
-    atomicMax(reinterpret_cast<int *>(addr), __float_as_int(v));
-  else
-    atomicMin(reinterpret_cast<unsigned *>(addr), __float_as_uint(v));
-}
-
-
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
@@ -399,19 +399,22 @@ __device__ __forceinline__ float butterfly_sum(float (&v)[NS], int li) {
 // run (slot M*Hkv + block; of several blocks starting at the same chunk only
 // the last has work).  Candidate blocks come in row order, so the runs do
 // too and the sums are taken in a fixed order.
+//
+// One pass with a running maximum, as in the chunk loop itself: each thread
+// owns (query head, float4 column) outputs and takes the runs in batches of
+// MB, issuing all of a batch's loads -- (m, l) and accumulator -- before it
+// uses any, so a batch costs one L2 round trip.
 // ---------------------------------------------------------------------------
 template <int D, int G, int NW>
-__device__ void merge_runs(const WsView &ws, float *out, int i, int g, int M, int Hkv,
+__device__ __noinline__ void merge_runs(const WsView &ws, float *out, int i, int g, int M, int Hkv,
                            long long S, int L, long long R, int P, int chunk, int cost,
                            unsigned char *scratch) {
   constexpr int LPR = D / 4;
   constexpr int NT = NW * 32;
   constexpr int NE = (G * LPR + NT - 1) / NT;
+  constexpr int MB = merge_batch(G) / NE;  // NE * MB loads in flight per thread
   int *s_list = reinterpret_cast<int *>(scratch);  // [kMergeWindow]
-  float(*s_w)[8] = reinterpret_cast<float(*)[8]>(scratch + kMergeWindow * 4);
-  float *s_mx = reinterpret_cast<float *>(scratch + kMergeWindow * 4 + kMergeWindow * 32);
-  float *s_l = s_mx + 8;
-  int *s_n = reinterpret_cast<int *>(s_l + 8);
+  int *s_n = s_list + kMergeWindow;
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int H = Hkv * G;
@@ -434,79 +437,18 @@ __device__ void merge_runs(const WsView &ws, float *out, int i, int g, int M, in
     if (j + 1 < ncand && cand_chunk(j + 1) == cc) return -1;  // an empty block; the next starts here
     return M * Hkv + b_lo + j;
   };
-  // Fast path, the usual case: at most kFastRuns runs, all candidates in one
-  // window.  Every partial is loaded at once into registers, then merged.
-  if (ncand < kMergeWindow) {
-    if (t < 32) {
-      const int j = t - 1;
-      const int sl = (j < ncand) ? run_slot(j) : -1;
-      const unsigned ballot = __ballot_sync(0xffffffffu, sl >= 0);
-      if (sl >= 0) s_list[__popc(ballot & ((1u << lane) - 1u))] = sl;
-      if (lane == 0) *s_n = __popc(ballot);
-    }
-    consumer_sync(NT);
-    const int nb = *s_n;
-    if (nb <= kFastRuns) {
-      // (m, l) of every run and head, loaded once into shared memory
-      float2(*s_ml)[8] = reinterpret_cast<float2(*)[8]>(s_w);  // [kFastRuns][8]
-      for (int e = t; e < nb * G; e += NT) {
-        const int r = e / G;
-        const int h = e - r * G;
-        s_ml[r][h] = __ldcg(&ws.ml[(size_t)s_list[r] * G + h]);
-      }
-      consumer_sync(NT);
-      const float4 *acc4 = reinterpret_cast<const float4 *>(ws.acc);
-      float4 *o4 = reinterpret_cast<float4 *>(out) + ((size_t)i * H + (size_t)g * G) * LPR;
-#pragma unroll
-      for (int q = 0; q < NE; ++q) {
-        const int e = t + q * NT;
-        if (e < G * LPR) {
-          const int h = e / LPR;
-          const int d4 = e - h * LPR;
-          float mx = neg_inf();
-          for (int r = 0; r < nb; ++r) mx = fmaxf(mx, s_ml[r][h].x);
-          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-          float l = 0.f;
-#pragma unroll 4
-          for (int r = 0; r < nb; ++r) {
-            const float2 ml = s_ml[r][h];
-            const float w = exp2f(ml.x - mx);
-            const float4 bb = __ldcg(&acc4[((size_t)s_list[r] * G + h) * LPR + d4]);
-            a.x = fmaf(w, bb.x, a.x);
-            a.y = fmaf(w, bb.y, a.y);
-            a.z = fmaf(w, bb.z, a.z);
-            a.w = fmaf(w, bb.w, a.w);
-            l = fmaf(w, ml.y, l);
-          }
-          const float inv = 1.f / l;
-          o4[e] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-        }
-      }
-      consumer_sync(NT);  // the scratch is read by every thread before it is reused
-      return;
-    }
-  }
 
-  if (t < G) {
-    s_mx[t] = neg_inf();
-    s_l[t] = 0.f;
-  }
-  consumer_sync(NT);
-  // pass 1: the maximum over the runs, per query head
-  for (int j = t - 1; j < ncand; j += NT) {
-    const int sl = run_slot(j);
-    if (sl < 0) continue;
-#pragma unroll
-    for (int h = 0; h < G; ++h) smem_max_float(&s_mx[h], __ldcg(&ws.ml[(size_t)sl * G + h]).x);
-  }
-  consumer_sync(NT);
-  // pass 2: rescaled sums over windows of runs, in row order
   const float4 *acc4 = reinterpret_cast<const float4 *>(ws.acc);
   float4 a[NE];
+  float mq[NE], lq[NE];
 #pragma unroll
-  for (int q = 0; q < NE; ++q) a[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q = 0; q < NE; ++q) {
+    a[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    mq[q] = neg_inf();
+    lq[q] = 0.f;
+  }
   for (int base = -1; base < ncand; base += kMergeWindow) {
-    if (t < 32) {
+    if (t < 32) {  // this window's runs, compacted in order
       const int j = base + t;
       const int sl = (j < ncand) ? run_slot(j) : -1;
       const unsigned ballot = __ballot_sync(0xffffffffu, sl >= 0);
@@ -515,42 +457,57 @@ __device__ void merge_runs(const WsView &ws, float *out, int i, int g, int M, in
     }
     consumer_sync(NT);
     const int nb = *s_n;
-    for (int e = t; e < nb * G; e += NT) {
-      const int r = e / G;
-      const int h = e - r * G;
-      s_w[r][h] = exp2f(__ldcg(&ws.ml[(size_t)s_list[r] * G + h]).x - s_mx[h]);
-    }
-    consumer_sync(NT);
-    if (t < G) {
-      float l = s_l[t];
-      for (int r = 0; r < nb; ++r) l = fmaf(s_w[r][t], __ldcg(&ws.ml[(size_t)s_list[r] * G + t]).y, l);
-      s_l[t] = l;
-    }
+    for (int r0 = 0; r0 < nb; r0 += MB) {
+      const int nr = min(MB, nb - r0);
+      float2 ml[NE][MB];
+      float4 bb[NE][MB];
 #pragma unroll
-    for (int q = 0; q < NE; ++q) {
-      const int e = t + q * NT;
-      if (e < G * LPR) {
+      for (int q = 0; q < NE; ++q) {
+        const int e = min(t + q * NT, G * LPR - 1);  // a spare thread re-reads a valid slot
         const int h = e / LPR;
         const int d4 = e - h * LPR;
-#pragma unroll 4
-        for (int r = 0; r < nb; ++r) {
-          const float w = s_w[r][h];
-          const float4 b = __ldcg(&acc4[((size_t)s_list[r] * G + h) * LPR + d4]);
-          a[q].x = fmaf(w, b.x, a[q].x);
-          a[q].y = fmaf(w, b.y, a[q].y);
-          a[q].z = fmaf(w, b.z, a[q].z);
-          a[q].w = fmaf(w, b.w, a[q].w);
+#pragma unroll
+        for (int j = 0; j < MB; ++j) {
+          if (j < nr) {
+            const size_t sl = (size_t)s_list[r0 + j] * G + h;
+            ml[q][j] = __ldcg(&ws.ml[sl]);
+            bb[q][j] = __ldcg(&acc4[sl * LPR + d4]);
+          }
         }
       }
+#pragma unroll
+      for (int q = 0; q < NE; ++q) {
+        float mb = mq[q];
+#pragma unroll
+        for (int j = 0; j < MB; ++j)
+          if (j < nr) mb = fmaxf(mb, ml[q][j].x);
+        const float sc = (mq[q] == neg_inf()) ? 0.f : exp2f(mq[q] - mb);
+        float4 acc = make_float4(a[q].x * sc, a[q].y * sc, a[q].z * sc, a[q].w * sc);
+        float l = lq[q] * sc;
+#pragma unroll
+        for (int j = 0; j < MB; ++j) {
+          if (j < nr) {
+            const float w = exp2f(ml[q][j].x - mb);
+            acc.x = fmaf(w, bb[q][j].x, acc.x);
+            acc.y = fmaf(w, bb[q][j].y, acc.y);
+            acc.z = fmaf(w, bb[q][j].z, acc.z);
+            acc.w = fmaf(w, bb[q][j].w, acc.w);
+            l = fmaf(w, ml[q][j].y, l);
+          }
+        }
+        a[q] = acc;
+        lq[q] = l;
+        mq[q] = mb;
+      }
     }
-    consumer_sync(NT);
+    consumer_sync(NT);  // every thread has read the list before it is rewritten
   }
   float4 *o4 = reinterpret_cast<float4 *>(out) + ((size_t)i * H + (size_t)g * G) * LPR;
 #pragma unroll
   for (int q = 0; q < NE; ++q) {
     const int e = t + q * NT;
     if (e < G * LPR) {
-      const float inv = 1.f / s_l[e / LPR];
+      const float inv = 1.f / lq[q];
       o4[e] = make_float4(a[q].x * inv, a[q].y * inv, a[q].z * inv, a[q].w * inv);
     }
   }
