@@ -125,13 +125,20 @@ size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads,
  * g = h / G):  out[i][h][:] = softmax_j( q[i][h] . k_cache[i][g][j] / sqrt(D) )
  * applied to v_cache[i][g][j][:], j = 0..L-1.  Rows j >= L are never read.
  *
- * The cache rows of every (sequence, kv head) are cut into chunks of
- * chunk_size rows, processed in parallel by a persistent grid; each chunk
- * yields (running max, running sum, weighted-V accumulator) for all G query
- * heads of the group, reading each K/V row once.  Consecutive chunks of one
- * (sequence, kv head) handled by the same block merge as they stream; the
- * block that completes a (sequence, kv head) merges its partials with
- * softmax rescaling and writes the output.
+ Two schedules compute this (see kvs_set_schedule); both read each K/V
+ * row once for all G query heads of its group, and both return the same
+ * attention up to float rounding:
+ *  - persistent: the cache rows of every (sequence, kv head) are cut into
+ *    chunks of chunk_size rows, processed in parallel by a persistent grid;
+ *    each chunk yields (running max, running sum, weighted-V accumulator).
+ *    Consecutive chunks of one (sequence, kv head) handled by the same
+ *    block merge as they stream; the block that completes a (sequence, kv
+ *    head) merges its partials with softmax rescaling through the
+ *    workspace and writes the output.
+ *  - cluster (small steps): one thread-block cluster of up to 16 blocks per
+ *    (sequence, kv head); block r takes rows [L*r/CS, L*(r+1)/CS) and the
+ *    partials are merged with the same rescaling in distributed shared
+ *    memory.  chunk_size and the workspace are validated but not used.
  *
  *   q          in   [M][H][D] float32, device, 16-byte aligned
  *   k_cache,
@@ -252,6 +259,45 @@ int kvs_flash_decode_static(const float *q, const float *k_cache,
                             float *out, int M, int num_heads, int num_kv_heads,
                             int head_dim, int max_len, int chunk_size,
                             int *d_status, kvs_stream_t stream);
+
+/*
+ * Kernel schedule of kvs_flash_decode, kvs_decode_step (and so of the
+ * graphs and the static entry point), process-wide:
+ *   KVS_SCHEDULE_AUTO        the cluster kernel when M * num_kv_heads <=
+ *                            65535 and M * num_kv_heads * max_len *
+ *                            head_dim * 8 bytes (the K/V bytes of a full
+ *                            cache) is at most 64 MiB -- steps that are
+ *                            bound by latency, not bandwidth -- else the
+ *                            persistent kernel (the default);
+ *   KVS_SCHEDULE_PERSISTENT  always the persistent kernel;
+ *   KVS_SCHEDULE_CLUSTER     the cluster kernel whenever M * num_kv_heads
+ *                            <= 65535.
+ * kvs_set_schedule returns the previous schedule, or -KVS_ERR_DIMS for an
+ * unknown value (nothing changes).  The schedule is read when a call is
+ * made (a captured graph keeps the kernel chosen at capture).
+ */
+typedef enum kvs_schedule {
+  KVS_SCHEDULE_AUTO = 0,
+  KVS_SCHEDULE_PERSISTENT = 1,
+  KVS_SCHEDULE_CLUSTER = 2
+} kvs_schedule;
+
+int kvs_set_schedule(int schedule);
+int kvs_get_schedule(void);
+
+/* The kernel a call with these sizes would run under the schedule in force:
+ * KVS_SCHEDULE_PERSISTENT or KVS_SCHEDULE_CLUSTER, or a negative kvs_status
+ * (DIMS, UNSUPPORTED). */
+int kvs_schedule_for(int M, int num_kv_heads, int head_dim, int max_len);
+
+/*
+ * kvs_prepare -- sets up, on the current device, both attention kernels
+ * for (num_heads, num_kv_heads, head_dim): shared-memory attributes and the
+ * largest cluster size the device can co-schedule.  Every entry point does
+ * this on first use; call it first when the first attention call will be
+ * made under stream capture.  Errors: DIMS, UNSUPPORTED, LAUNCH.
+ */
+int kvs_prepare(int num_heads, int num_kv_heads, int head_dim);
 
 /* Human-readable name of a kvs_status value (static string). */
 const char *kvs_strerror(int status);

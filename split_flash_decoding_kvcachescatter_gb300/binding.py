@@ -31,7 +31,13 @@ KVS_ERR_TIMEOUT = 8
 # Every symbol include/kvsdecode.h declares.
 EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspace_bytes",
            "kvs_flash_decode", "kvs_decode_step", "kvs_strerror", "kvs_flash_decode_static",
-           "kvs_step_graph_create", "kvs_step_graph_launch", "kvs_step_graph_destroy")
+           "kvs_step_graph_create", "kvs_step_graph_launch", "kvs_step_graph_destroy",
+           "kvs_set_schedule", "kvs_get_schedule", "kvs_schedule_for", "kvs_prepare")
+
+# kvs_schedule values (kernel schedule of the attention entry points)
+KVS_SCHEDULE_AUTO = 0
+KVS_SCHEDULE_PERSISTENT = 1
+KVS_SCHEDULE_CLUSTER = 2
 
 # Size of the library's built-in scratch buffer used by kvs_flash_decode_static.
 KVS_STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024
@@ -82,6 +88,14 @@ def lib() -> ctypes.CDLL:
             L.kvs_step_graph_launch.argtypes = [_P, _P]
             L.kvs_step_graph_destroy.restype = _I
             L.kvs_step_graph_destroy.argtypes = [_P]
+            L.kvs_set_schedule.restype = _I
+            L.kvs_set_schedule.argtypes = [_I]
+            L.kvs_get_schedule.restype = _I
+            L.kvs_get_schedule.argtypes = []
+            L.kvs_schedule_for.restype = _I
+            L.kvs_schedule_for.argtypes = [_I, _I, _I, _I]
+            L.kvs_prepare.restype = _I
+            L.kvs_prepare.argtypes = [_I, _I, _I]
             L.kvs_strerror.restype = ctypes.c_char_p
             L.kvs_strerror.argtypes = [_I]
             _lib = L
@@ -135,6 +149,31 @@ def kvs_kv_scatter(k_rows, v_rows, positions, k_cache, v_cache, d_status=None, s
                               _f32(v_cache, "v_cache", 4), M, Hkv, D, Lmax,
                               _status_ptr(d_status), _stream(stream))
     _check(rc, "kvs_kv_scatter")
+
+
+def kvs_set_schedule(schedule: int) -> int:
+    """Set the process-wide kernel schedule (KVS_SCHEDULE_*); returns the previous one."""
+    prev = lib().kvs_set_schedule(int(schedule))
+    if prev < 0:
+        raise KvsError(-prev, "kvs_set_schedule")
+    return prev
+
+
+def kvs_get_schedule() -> int:
+    return int(lib().kvs_get_schedule())
+
+
+def kvs_schedule_for(M, num_kv_heads, head_dim, max_len) -> int:
+    """KVS_SCHEDULE_PERSISTENT or KVS_SCHEDULE_CLUSTER: the kernel such a call would run."""
+    r = lib().kvs_schedule_for(M, num_kv_heads, head_dim, max_len)
+    if r < 0:
+        raise KvsError(-r, "kvs_schedule_for")
+    return r
+
+
+def kvs_prepare(num_heads, num_kv_heads, head_dim) -> None:
+    """Set up both attention kernels for this shape on the current device."""
+    _check(lib().kvs_prepare(num_heads, num_kv_heads, head_dim), "kvs_prepare")
 
 
 def kvs_choose_chunk_size(M, num_kv_heads, head_dim, max_len, num_sms=0) -> int:

@@ -1,0 +1,438 @@
+// fd_cluster.cu -- the decode-step attention for small steps: one thread-block
+// cluster per (sequence, kv head), the split-K partials merged through
+// distributed shared memory.
+//
+// Source: realizar 0.8.5, src/cuda/executor/head_dim.rs,
+// flash_decoding_attention_into (PAR-118): doc comment (split the KV cache
+// into chunks processed in parallel, then merge the partial results with
+// softmax rescaling), "Step 1: Scatter K/V to caches" and "Step 4" / "Step 5"
+// (chunk and reduce kernels).
+//
+// Why a second kernel: when a step moves only a few MB (a small model, short
+// caches) the persistent kernel is bound by latency, not bandwidth, and most
+// of that latency is its global-memory merge protocol -- partial stores, a
+// fence, a counter atomic, then the merging block's loads, each a round trip
+// through L2.  Here the CS blocks that share one (i, g) form a cluster:
+//  * block r of the cluster streams rows [L*r/CS, L*(r+1)/CS) of (i, g)
+//    with the same warp-specialised pipeline and consumer tile as the
+//    persistent kernel (bulk async copies into a ring of stages);
+//  * each block leaves its partial (m, l, acc for the G heads) in its own
+//    shared memory, the cluster synchronises once, and block 0 reads the
+//    CS partials over distributed shared memory, merges them and writes the
+//    output; a second cluster barrier keeps every block's shared memory
+//    alive until block 0 has read it.
+// No workspace, no atomics, no global round trip between the partials and
+// the merge.  The fused scatter works as in the persistent kernel: the last
+// block of the cluster writes the new rows and reads row p from them.
+//
+// Every thread of every block reaches both cluster barriers on every path
+// (the only early exit, an invalid position, is taken by the whole cluster
+// before the first barrier), and every mbarrier wait is bounded in time, so
+// a lost copy ends in KVS_ERR_TIMEOUT, never in a hang.
+
+#include <cmath>
+#include <mutex>
+
+#include "fd_tile.cuh"
+#include "kvs_device.cuh"
+#include "kvs_launch.h"
+
+namespace kvs {
+
+namespace {
+
+constexpr int kMaxClusterDevices = 64;
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Address of the same shared-memory location in cluster block `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
+    fd_cluster_kernel(const float *__restrict__ q, float *k_cache, float *v_cache,
+                      const int32_t *__restrict__ positions, const float *__restrict__ k_rows,
+                      const float *__restrict__ v_rows, float *__restrict__ out, int Hkv,
+                      int max_len, float qscale, int *d_status) {
+  using C = Geo<D, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  StageDesc *desc = reinterpret_cast<StageDesc *>(smem + C::OFF_DESC);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *empty = full + C::S;
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
+  volatile int *no_abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG + 4);
+  // this block's partial, published to the cluster: acc aliases warp 0's
+  // accumulator slot, (m, l) the lane-sum area (both free after publish())
+  float4 *part_acc = reinterpret_cast<float4 *>(smem + C::OFF_MACC);  // [G][D/4]
+  float2 *part_ml = reinterpret_cast<float2 *>(smem + C::OFF_MLL);    // [G]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // grid (CS, M*Hkv), clusters of (CS, 1, 1): one cluster per (i, g)
+  const uint32_t rank = cluster_rank();
+  const int ncl = (int)gridDim.x;
+  const int ig = blockIdx.y;
+  const int i = ig / Hkv;
+  const int g = ig - i * Hkv;
+  const int H = Hkv * G;
+  const bool scatter = (k_rows != nullptr);
+
+  grid_dependency_wait();
+  const int p = __ldg(positions + i);
+  if (p < 0 || p >= max_len) {  // the whole cluster leaves here, before any cluster barrier
+    if (rank == 0) {
+      const float nan = __int_as_float(0x7fc00000);
+      float4 *o4 = reinterpret_cast<float4 *>(out) + ((size_t)i * H + (size_t)g * G) * (D / 4);
+      for (int e = threadIdx.x; e < G * (D / 4); e += C::THREADS)
+        o4[e] = make_float4(nan, nan, nan, nan);
+      if (threadIdx.x == 0) record_status(d_status, KVS_ERR_POSITION);
+    }
+    return;
+  }
+  const int L = p + 1;
+  const int r0 = (int)((long long)L * rank / ncl);
+  const int r1 = (int)((long long)L * (rank + 1) / ncl);
+
+  // ---- Step 1, scatter: the block holding row p writes the new rows ----
+  if (scatter && rank == (uint32_t)(ncl - 1)) {
+    constexpr int D4 = D / 4;
+    const size_t dst = (((size_t)i * Hkv + g) * max_len + p) * D4;
+    const size_t src = ((size_t)i * Hkv + g) * D4;
+    for (int e = threadIdx.x; e < 2 * D4; e += C::THREADS) {
+      if (e < D4)
+        reinterpret_cast<float4 *>(k_cache)[dst + e] =
+            __ldg(reinterpret_cast<const float4 *>(k_rows) + src + e);
+      else
+        reinterpret_cast<float4 *>(v_cache)[dst + e - D4] =
+            __ldg(reinterpret_cast<const float4 *>(v_rows) + src + e - D4);
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::NW);
+    }
+    *abort = 0;
+    *no_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  allow_dependent_launch();
+
+  if (warp == C::NW) {
+    // ===================== producer warp (lane 0 issues) ====================
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first();
+      uint32_t k = 0;
+      int ok = 1;
+      const size_t head_base = ((size_t)i * Hkv + g) * (size_t)max_len;
+      const size_t row_src = ((size_t)i * Hkv + g) * D;  // new row of (i, g)
+      for (int rs = r0; rs < r1 && ok; rs += C::T, ++k) {
+        const uint32_t s = k % C::S;
+        const uint32_t use = k / C::S;
+        if (!mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
+          ok = 0;
+          break;
+        }
+        const int nrows = min(C::T, r1 - rs);
+        StageDesc &dd = desc[s];
+        dd.flags = (rs == r0 ? kRunStart : 0) | (rs + C::T >= r1 ? kRunEnd : 0);
+        dd.nrows = nrows;
+        const uint32_t kv_bytes = (uint32_t)nrows * D * 4;
+        const uint32_t bytes = 2 * kv_bytes + (rs == r0 ? (uint32_t)C::Q_BYTES : 0u);
+        unsigned char *stage = smem + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        const size_t row0 = (head_base + rs) * D;
+        // with the scatter folded in, row L-1 (position p) comes from the new rows
+        const bool tail = scatter && (rs + nrows == L);
+        const uint32_t cache_bytes = tail ? kv_bytes - D * 4 : kv_bytes;
+        if (cache_bytes > 0) {
+          bulk_g2s_hint(stage, k_cache + row0, cache_bytes, &full[s], pol_stream);
+          bulk_g2s_hint(stage + C::KV_BYTES, v_cache + row0, cache_bytes, &full[s], pol_stream);
+        }
+        if (tail) {
+          bulk_g2s(stage + cache_bytes, k_rows + row_src, D * 4, &full[s]);
+          bulk_g2s(stage + C::KV_BYTES + cache_bytes, v_rows + row_src, D * 4, &full[s]);
+        }
+        if (rs == r0)
+          bulk_g2s(stage + 2 * C::KV_BYTES, q + ((size_t)i * H + (size_t)g * G) * D, C::Q_BYTES,
+                   &full[s]);
+      }
+      if (ok) {  // tell the consumers there is nothing more
+        const uint32_t s = k % C::S;
+        const uint32_t use = k / C::S;
+        if (mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
+          desc[s].flags = kNoMore;
+          desc[s].nrows = 0;
+          mbar_arrive(&full[s]);
+        } else {
+          ok = 0;
+        }
+      }
+      if (!ok) {
+        *abort = 1;
+        record_status(d_status, KVS_ERR_TIMEOUT);
+        // let every copy already issued land before the block goes on
+        for (uint32_t j = (k > (uint32_t)C::S ? k - C::S : 0u); j < k; ++j)
+          mbar_wait(&full[j % C::S], (j / C::S) & 1u, no_abort);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ===================== consumer warps ===================================
+    const TileLane<D, G> tl = tile_lane<D, G>(smem, warp, lane);
+    float4 qv[G];
+    float4 acc[G];
+    float m_run[G];
+    float l_lane;
+#pragma unroll
+    for (int h = 0; h < G; ++h) qv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    tile_reset<G>(acc, m_run, l_lane);
+    for (uint32_t k = 0;; ++k) {
+      const uint32_t s = k % C::S;
+      const uint32_t use = k / C::S;
+      if (!mbar_wait(&full[s], use & 1u, abort)) {
+        *abort = 1;
+        record_status(d_status, KVS_ERR_TIMEOUT);
+        break;
+      }
+      const StageDesc dsc = desc[s];
+      if (dsc.flags & kNoMore) break;
+      const unsigned char *stage = smem + s * C::STAGE_BYTES;
+      if (dsc.flags & kRunStart) tile_load_q<D, G>(tl, stage, qscale, qv);
+      tile_consume<D, G>(tl, stage, dsc.nrows, qv, acc, m_run, l_lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // A block with no rows publishes m = -inf, l = 0, acc = 0.
+    tile_publish<D, G>(tl, acc, m_run, l_lane);
+    consumer_sync(C::NW * 32);
+    for (int e = threadIdx.x; e < G * C::LPR; e += C::NW * 32) {
+      float4 a;
+      float mx, lsum;
+      merged_warp_states<D, G>(smem, e, a, mx, lsum);
+      part_acc[e] = a;  // only this thread reads or writes element e here
+      if (e % C::LPR == 0) part_ml[e / C::LPR] = make_float2(mx, lsum);
+    }
+  }
+
+  cluster_sync_all();  // every block's partial is in its shared memory
+  if (rank == 0 && warp < C::NW) {
+    constexpr int kMaxCS = 16;
+    for (int e = threadIdx.x; e < G * C::LPR; e += C::NW * 32) {
+      const int h = e / C::LPR;
+      float2 ml[kMaxCS];
+      float mx = neg_inf();
+#pragma unroll
+      for (int rr = 0; rr < kMaxCS; ++rr) {
+        if (rr < ncl) {
+          ml[rr] = ld_dsmem_f2(dsmem_addr(part_ml + h, rr));
+          mx = fmaxf(mx, ml[rr].x);
+        }
+      }
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      float l = 0.f;
+#pragma unroll
+      for (int rr = 0; rr < kMaxCS; ++rr) {
+        if (rr < ncl) {
+          const float w = (ml[rr].x == neg_inf()) ? 0.f : exp2f(ml[rr].x - mx);
+          const float4 b = ld_dsmem_f4(dsmem_addr(part_acc + e, rr));
+          a.x = fmaf(w, b.x, a.x);
+          a.y = fmaf(w, b.y, a.y);
+          a.z = fmaf(w, b.z, a.z);
+          a.w = fmaf(w, b.w, a.w);
+          l = fmaf(w, ml[rr].y, l);
+        }
+      }
+      const float inv = 1.f / l;
+      reinterpret_cast<float4 *>(out)[((size_t)i * H + (size_t)g * G) * C::LPR + e] =
+          make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+    }
+  }
+  cluster_sync_all();  // block 0 has read every partial: shared memory may go
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+// Target rows per block: a block's slice should be a few stages, so that the
+// cluster's blocks finish together soon after their first copies land.
+constexpr int kClusterRowsPerBlock = 32;
+
+struct ClusterInfo {
+  int max_size = 0;
+  bool configured = false;
+};
+
+// Largest cluster size (a power of two <= 16) that this instantiation can be
+// launched with on device `dev`; configures its attributes on first use.
+template <int D, int G>
+int cluster_max_size(int dev) {
+  using C = Geo<D, G>;
+  static ClusterInfo info[kMaxClusterDevices];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!info[dev].configured) {
+    auto kern = fd_cluster_kernel<D, G>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return -1;
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    int cs = 16;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      cs = 8;
+    }
+    for (; cs >= 1; cs >>= 1) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cs, 1, 1);
+      cfg.blockDim = dim3(C::THREADS, 1, 1);
+      cfg.dynamicSmemBytes = C::SMEM_BYTES;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cs;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) break;
+      cudaGetLastError();
+    }
+    if (cs < 1) return -1;
+    info[dev].max_size = cs;
+    info[dev].configured = true;
+  }
+  return info[dev].max_size;
+}
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxClusterDevices) return -1;
+  return dev;
+}
+
+template <int D, int G>
+int launch_cluster_impl(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+                        const float *k_rows, const float *v_rows, float *out, int M, int Hkv,
+                        int max_len, int *d_status, cudaStream_t stream) {
+  using C = Geo<D, G>;
+  const int dev = current_device();
+  if (dev < 0) return KVS_ERR_LAUNCH;
+  const int cs_max = cluster_max_size<D, G>(dev);
+  if (cs_max <= 0) return KVS_ERR_LAUNCH;
+  const long long pairs = (long long)M * Hkv;
+  if (pairs > kMaxClusterPairs) return KVS_ERR_UNSUPPORTED;
+  int cs = 1;
+  while (cs < cs_max && (long long)cs * kClusterRowsPerBlock < max_len) cs <<= 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, (unsigned)pairs, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const float qscale = (float)(1.4426950408889634074 / std::sqrt((double)D));
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fd_cluster_kernel<D, G>, q, k_cache, v_cache,
+                                           positions, k_rows, v_rows, out, Hkv, max_len, qscale,
+                                           d_status);
+  return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
+}
+
+template <int D>
+int cluster_dispatch(int G, const float *q, float *k_cache, float *v_cache,
+                     const int32_t *positions, const float *k_rows, const float *v_rows,
+                     float *out, int M, int Hkv, int max_len, int *d_status,
+                     cudaStream_t stream) {
+  switch (G) {
+#define KVS_CASE(g)                                                                            \
+  case g:                                                                                      \
+    return launch_cluster_impl<D, g>(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, \
+                                     Hkv, max_len, d_status, stream);
+    KVS_CASE(1)
+    KVS_CASE(2)
+    KVS_CASE(3)
+    KVS_CASE(4)
+    KVS_CASE(5)
+    KVS_CASE(6)
+    KVS_CASE(7)
+    KVS_CASE(8)
+#undef KVS_CASE
+    default:
+      return KVS_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+int prepare_cluster_kernel(int H, int Hkv, int D) {
+  const int dev = current_device();
+  if (dev < 0) return KVS_ERR_LAUNCH;
+  if (Hkv < 1 || H % Hkv != 0) return KVS_ERR_DIMS;
+  const int G = H / Hkv;
+  int cs = -1;
+  switch (D * 16 + G) {
+#define KVS_PREP(d, g)                     \
+  case d * 16 + g:                         \
+    cs = cluster_max_size<d, g>(dev);      \
+    break;
+    KVS_PREP(64, 1) KVS_PREP(64, 2) KVS_PREP(64, 3) KVS_PREP(64, 4)
+    KVS_PREP(64, 5) KVS_PREP(64, 6) KVS_PREP(64, 7) KVS_PREP(64, 8)
+    KVS_PREP(128, 1) KVS_PREP(128, 2) KVS_PREP(128, 3) KVS_PREP(128, 4)
+    KVS_PREP(128, 5) KVS_PREP(128, 6) KVS_PREP(128, 7) KVS_PREP(128, 8)
+#undef KVS_PREP
+    default:
+      return KVS_ERR_UNSUPPORTED;
+  }
+  return cs > 0 ? KVS_OK : KVS_ERR_LAUNCH;
+}
+
+int launch_fd_cluster(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+                      const float *k_rows, const float *v_rows, float *out, int M, int H,
+                      int Hkv, int D, int max_len, int *d_status, cudaStream_t stream) {
+  const int G = H / Hkv;
+  if (D == 128)
+    return cluster_dispatch<128>(G, q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv,
+                                 max_len, d_status, stream);
+  if (D == 64)
+    return cluster_dispatch<64>(G, q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv,
+                                max_len, d_status, stream);
+  return KVS_ERR_UNSUPPORTED;
+}
+
+}  // namespace kvs

@@ -66,100 +66,15 @@
 
 #include "kvs_device.cuh"
 #include "kvs_launch.h"
+#include "fd_tile.cuh"
 
 namespace kvs {
 
 namespace {
 
-__host__ __device__ constexpr int pow2ceil(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
-}
-__host__ __device__ constexpr int ilog2(int x) {
-  int l = 0;
-  while ((1 << l) < x) ++l;
-  return l;
-}
-__host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
-__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
-__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
-
-__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
-
-// Stage descriptor written by the producer, read by the consumers.
-constexpr int kRunStart = 1;  // first stage of a run: the stage also holds q
-constexpr int kRunEnd = 2;    // last stage of a run: merge, write the partial
-constexpr int kNoMore = 4;    // no stage: the block is done
-struct StageDesc {
-  int flags;
-  int nrows;     // rows in this stage
-  int ig;        // i * Hkv + g
-  int run_rows;  // rows of the whole run
-  int L;         // length of sequence i
-  int pad;
-  long long slot;  // partial slot of the run
-  long long S;     // first row of (i, g) in the (i, g, row) order
-};
-
 // Fixed price of one run, in bytes of K+V rows: it sets the `cost` rows that
 // each (i, g) adds to the balanced split (40 rows at D = 128, 80 at D = 64).
 constexpr int kRunCostBytes = 40960;
-
-// Scratch of the (i, g) merge (aliases the warp-state merge area).
-constexpr int kMergeWindow = 32;  // candidate blocks examined per pass
-// Partial loads a merging thread keeps in flight: 8, or 4 for groups of more
-// than 5 heads, whose chunk loop leaves fewer registers free.
-__host__ __device__ constexpr int merge_batch(int G) { return G <= 5 ? 8 : 4; }
-constexpr int kMergeScratchBytes = kMergeWindow * 4 + 16;
-
-// Shared memory budget of the stage ring (two blocks per SM).
-constexpr int kRingBytes = 96 * 1024;
-
-// Compile-time geometry of one (head_dim, group) instantiation.
-template <int D_, int G_>
-struct Geo {
-  static constexpr int D = D_;
-  static constexpr int G = G_;
-  static constexpr int NW = 4;                    // consumer warps
-  static constexpr int THREADS = (NW + 1) * 32;   // + one producer warp
-  static constexpr int LPR = D / 4;               // lanes per row (float4 each)
-  static constexpr int RPI = 32 / LPR;            // rows per warp instruction
-  static constexpr int RP = (LPR / G) < 8 ? (LPR / G) : 8;  // rows per lane group
-  static constexpr int NSLOT = pow2ceil(RP * G);  // butterfly slots (<= LPR)
-  static constexpr int LOG2NS = ilog2(NSLOT);
-  static constexpr int SPAN = LPR / NSLOT;        // lanes sharing one slot
-  static constexpr int RW = RPI * RP;             // rows per warp tile
-  static constexpr int T = NW * RW;               // rows per stage
-  static constexpr int RWP = round_up(RW, 4);     // padded score row length
-  static constexpr int GP = round_up(G, 4);       // padded p row length
-  static constexpr int KV_BYTES = T * D * 4;      // one of K or V per stage
-  static constexpr int Q_BYTES = G * D * 4;
-  static constexpr int STAGE_BYTES = round_up(2 * KV_BYTES + Q_BYTES, 128);
-  // pipeline stages: as many as fit in kRingBytes, at least 3 and at most 8
-  // (small stages -- head_dim 64 with a large group -- get a deeper ring, so
-  // that one block alone still keeps tens of KB of K/V in flight)
-  static constexpr int S = cmin(8, cmax(3, kRingBytes / STAGE_BYTES));
-  static constexpr int OFF_SCORE = S * STAGE_BYTES;
-  static constexpr int SCORE_BYTES = NW * G * RWP * 4;
-  static constexpr int OFF_P = OFF_SCORE + SCORE_BYTES;
-  static constexpr int P_BYTES = NW * RW * GP * 4;
-  static constexpr int OFF_MACC = round_up(OFF_P + P_BYTES, 128);
-  static constexpr int MACC_BYTES = cmax(NW * G * D * 4, kMergeScratchBytes);
-  static constexpr int OFF_MM = OFF_MACC + round_up(MACC_BYTES, 16);
-  static constexpr int OFF_ML = OFF_MM + round_up(NW * G * 4, 16);
-  static constexpr int OFF_MLL = OFF_ML + round_up(NW * G * 4, 16);
-  static constexpr int OFF_DESC = round_up(OFF_MLL + NW * 32 * 4, 16);
-  static constexpr int OFF_BAR = OFF_DESC + S * (int)sizeof(StageDesc);
-  static constexpr int OFF_INFO = OFF_BAR + (2 * S + 1) * 8;  // R, U (int64)
-  static constexpr int OFF_FLAG = OFF_INFO + 32;              // abort, no_abort, last
-  static constexpr int SMEM_BYTES = round_up(OFF_FLAG + 16, 128);
-  static_assert(G >= 1 && G <= LPR, "group larger than lanes per row");
-  static_assert(RP * G <= LPR, "slots exceed lanes");
-  static_assert(RW * G <= 32 * RPI, "tile too large");
-  // two blocks per SM: 228 KB of shared memory less 1 KB reserved per block
-  static_assert(SMEM_BYTES <= (228 * 1024) / 2 - 1024, "two blocks per SM must fit");
-};
 
 // Length attended by sequence i (0 for an out-of-range position).
 __device__ __forceinline__ int seq_len_at(const int32_t *positions, int i, int max_len) {
@@ -327,9 +242,6 @@ __device__ __forceinline__ unsigned tagged_add(unsigned long long *ctr, unsigned
                             d_status);
 }
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
 
 // A run: consecutive chunks of one (i, g) inside a block's range.
 struct Run {
@@ -366,30 +278,6 @@ __device__ __forceinline__ Run next_run(const Run &r, long long remaining,
   e.units = 0;
   e.L = 0;
   return e;
-}
-
-// Transposing butterfly: lane li (within a group of LPR lanes) holds v[NS]
-// partial sums; afterwards it returns the full sum (over the LPR lanes) of
-// slot li / (LPR / NS).
-template <int NS, int LOG2NS, int LPR>
-__device__ __forceinline__ float butterfly_sum(float (&v)[NS], int li) {
-#pragma unroll
-  for (int k = 0; k < LOG2NS; ++k) {
-    const int half = NS >> (k + 1);
-    const int dist = LPR >> (k + 1);
-    const bool upper = (li & dist) != 0;
-#pragma unroll
-    for (int j = 0; j < half; ++j) {
-      const float send = upper ? v[j] : v[j + half];
-      const float keep = upper ? v[j + half] : v[j];
-      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, dist);
-    }
-  }
-  float r = v[0];
-#pragma unroll
-  for (int dist = LPR / NS / 2; dist >= 1; dist >>= 1)
-    r += __shfl_xor_sync(0xffffffffu, r, dist);
-  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -697,38 +585,14 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   }
 
   // ========================= consumer warps ================================
-  const int w = warp;
-  const int gi = lane / C::LPR;  // row group within the warp instruction
-  const int li = lane % C::LPR;  // float4 column
-  float *sS = reinterpret_cast<float *>(smem + C::OFF_SCORE) + w * G * C::RWP;  // [G][RWP]
-  float *sP = reinterpret_cast<float *>(smem + C::OFF_P) + w * C::RW * C::GP;   // [RW][GP]
-  float4 *sAcc = reinterpret_cast<float4 *>(smem + C::OFF_MACC);               // [NW][G][D/4]
-  float *sM = reinterpret_cast<float *>(smem + C::OFF_MM);                     // [NW][G]
-  float *sL = reinterpret_cast<float *>(smem + C::OFF_ML);                     // [NW][G]
-  float *sLl = reinterpret_cast<float *>(smem + C::OFF_MLL);                   // [NW][32]
-
-  for (int e = lane; e < G * C::RWP; e += 32) sS[e] = neg_inf();
-  for (int e = lane; e < C::RW * C::GP; e += 32) sP[e] = 0.f;
-  __syncwarp();
-
-  // this lane's score slot
-  const int slot = li / C::SPAN;
-  const bool slot_used = slot < C::RP * G;
-  const bool owner = slot_used && (li % C::SPAN) == 0;
-  const int slot_r = slot / G;
-  const int slot_h = slot - slot_r * G;
-  const int slot_row = slot_r * C::RPI + gi;  // row within the warp tile
-
+  const TileLane<D, G> tl = tile_lane<D, G>(smem, warp, lane);
   float4 qv[G];
   float4 acc[G];
   float m_run[G];
-  float l_lane = 0.f;
+  float l_lane;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    qv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-    acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-    m_run[h] = neg_inf();
-  }
+  for (int h = 0; h < G; ++h) qv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+  tile_reset<G>(acc, m_run, l_lane);
 
   uint32_t mphase = 0;
   auto consumers_barrier = [&]() -> bool {  // bounded; every consumer warp arrives once
@@ -754,136 +618,14 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     const StageDesc dsc = desc[s];
     if (dsc.flags & kNoMore) break;
     const unsigned char *stage = smem + s * C::STAGE_BYTES;
-    const float4 *sK = reinterpret_cast<const float4 *>(stage);
-    const float4 *sV = reinterpret_cast<const float4 *>(stage + C::KV_BYTES);
-    if (dsc.flags & kRunStart) {
-      const float4 *sQ = reinterpret_cast<const float4 *>(stage + 2 * C::KV_BYTES);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float4 t = sQ[h * C::LPR + li];
-        qv[h] = make_float4(t.x * qscale, t.y * qscale, t.z * qscale, t.w * qscale);
-      }
-    }
-    const int my_valid = min(max(dsc.nrows - w * C::RW, 0), C::RW);
-    if (my_valid > 0) {
-      const int tile0 = w * C::RW;
-      // ---- scores: partial dot products, then the butterfly ----
-      float part[C::NSLOT];
-#pragma unroll
-      for (int j = 0; j < C::NSLOT; ++j) part[j] = 0.f;
-#pragma unroll
-      for (int r = 0; r < C::RP; ++r) {
-        const int row = tile0 + r * C::RPI + gi;
-        const float4 kv = sK[row * C::LPR + li];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float d = qv[h].x * kv.x;
-          d = fmaf(qv[h].y, kv.y, d);
-          d = fmaf(qv[h].z, kv.z, d);
-          d = fmaf(qv[h].w, kv.w, d);
-          part[r * G + h] = d;
-        }
-      }
-      const float sc = butterfly_sum<C::NSLOT, C::LOG2NS, C::LPR>(part, li);
-      const bool valid = slot_used && slot_row < my_valid;
-      const float s_val = valid ? sc : neg_inf();
-      if (owner) sS[slot_h * C::RWP + slot_row] = s_val;
-      __syncwarp();
-      // ---- running max and rescale factors (all lanes, all heads) ----
-      float alpha[G];
-      float m_new[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float4 *row4 = reinterpret_cast<const float4 *>(sS + h * C::RWP);
-        float tmax = neg_inf();
-#pragma unroll
-        for (int j = 0; j < C::RWP / 4; ++j) {
-          const float4 t = row4[j];
-          tmax = fmaxf(tmax, fmaxf(fmaxf(t.x, t.y), fmaxf(t.z, t.w)));
-        }
-        m_new[h] = fmaxf(m_run[h], tmax);
-        alpha[h] = (m_new[h] == m_run[h]) ? 1.f : exp2f(m_run[h] - m_new[h]);
-      }
-      // ---- own-slot probability ----
-      float mh = m_new[0];
-#pragma unroll
-      for (int h = 1; h < G; ++h) mh = (slot_h == h) ? m_new[h] : mh;
-      float ah = alpha[0];
-#pragma unroll
-      for (int h = 1; h < G; ++h) ah = (slot_h == h) ? alpha[h] : ah;
-      const float p = valid ? exp2f(s_val - mh) : 0.f;
-      if (owner) {
-        sP[slot_row * C::GP + slot_h] = p;
-        l_lane = l_lane * ah + p;
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        m_run[h] = m_new[h];
-        acc[h].x *= alpha[h];
-        acc[h].y *= alpha[h];
-        acc[h].z *= alpha[h];
-        acc[h].w *= alpha[h];
-      }
-      __syncwarp();
-      // ---- P.V ----
-#pragma unroll
-      for (int r = 0; r < C::RP; ++r) {
-        const int trow = r * C::RPI + gi;
-        if (trow < my_valid) {
-          const float4 vv = sV[(tile0 + trow) * C::LPR + li];
-          float pr[C::GP];
-#pragma unroll
-          for (int j = 0; j < C::GP / 4; ++j) {
-            const float4 t = reinterpret_cast<const float4 *>(sP + trow * C::GP)[j];
-            pr[4 * j + 0] = t.x;
-            pr[4 * j + 1] = t.y;
-            pr[4 * j + 2] = t.z;
-            pr[4 * j + 3] = t.w;
-          }
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            acc[h].x = fmaf(pr[h], vv.x, acc[h].x);
-            acc[h].y = fmaf(pr[h], vv.y, acc[h].y);
-            acc[h].z = fmaf(pr[h], vv.z, acc[h].z);
-            acc[h].w = fmaf(pr[h], vv.w, acc[h].w);
-          }
-        }
-      }
-    }
+    if (dsc.flags & kRunStart) tile_load_q<D, G>(tl, stage, qscale, qv);
+    tile_consume<D, G>(tl, stage, dsc.nrows, qv, acc, m_run, l_lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     if (!(dsc.flags & kRunEnd)) continue;
 
     // ---- end of run: merge the NW warp states --------------------------------
-    if (C::RPI > 1) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int o = C::LPR; o < 32; o <<= 1) {
-          acc[h].x += __shfl_xor_sync(0xffffffffu, acc[h].x, o);
-          acc[h].y += __shfl_xor_sync(0xffffffffu, acc[h].y, o);
-          acc[h].z += __shfl_xor_sync(0xffffffffu, acc[h].z, o);
-          acc[h].w += __shfl_xor_sync(0xffffffffu, acc[h].w, o);
-        }
-      }
-    }
-    if (gi == 0) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) sAcc[(w * G + h) * C::LPR + li] = acc[h];
-    }
-    sLl[w * 32 + lane] = owner ? l_lane : 0.f;
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      if (lane == h) sM[w * G + h] = m_run[h];
-    __syncwarp();
-    if (lane < G) {
-      float lsum = 0.f;
-      for (int l2 = 0; l2 < 32; ++l2) {
-        const int s2 = (l2 % C::LPR) / C::SPAN;
-        if (s2 < C::RP * G && (s2 % G) == lane) lsum += sLl[w * 32 + l2];
-      }
-      sL[w * G + lane] = lsum;
-    }
+    tile_publish<D, G>(tl, acc, m_run, l_lane);
     if (!consumers_barrier()) return;
     // A run that covers all of (i, g) is the answer; any other run is a
     // partial for the (i, g) merge.
@@ -893,22 +635,9 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     for (int e = threadIdx.x; e < G * C::LPR; e += C::NW * 32) {
       const int h = e / C::LPR;
       const int d4 = e - h * C::LPR;
-      float mx = neg_inf();
-#pragma unroll
-      for (int w2 = 0; w2 < C::NW; ++w2) mx = fmaxf(mx, sM[w2 * G + h]);
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      float lsum = 0.f;
-#pragma unroll
-      for (int w2 = 0; w2 < C::NW; ++w2) {
-        const float mw = sM[w2 * G + h];
-        const float sc = (mw == neg_inf()) ? 0.f : exp2f(mw - mx);
-        const float4 b = sAcc[(w2 * G + h) * C::LPR + d4];
-        a.x = fmaf(sc, b.x, a.x);
-        a.y = fmaf(sc, b.y, a.y);
-        a.z = fmaf(sc, b.z, a.z);
-        a.w = fmaf(sc, b.w, a.w);
-        lsum = fmaf(sc, sL[w2 * G + h], lsum);
-      }
+      float4 a;
+      float mx, lsum;
+      merged_warp_states<D, G>(smem, e, a, mx, lsum);
       if (whole) {
         const float inv = 1.f / lsum;
         reinterpret_cast<float4 *>(out)[((size_t)i_seq * H + (size_t)g_kv * G + h) * C::LPR + d4] =
@@ -938,13 +667,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
                                 smem + C::OFF_MACC);
       }
     }
-    // reset the running state for the next run
-    l_lane = 0.f;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-      m_run[h] = neg_inf();
-    }
+    tile_reset<G>(acc, m_run, l_lane);  // the next run starts from nothing
   }
 }
 

@@ -2,6 +2,7 @@
 // host, the chunk-size rule, workspace sizing, and dispatch to the kernel
 // launchers.  Nothing here allocates, frees or synchronises.
 
+#include <atomic>
 #include <cstdint>
 
 #include "kvs_launch.h"
@@ -21,6 +22,37 @@ int check_attention_shape(int M, int H, int Hkv, int D, int max_len, int chunk) 
   if (H / Hkv > 8) return KVS_ERR_UNSUPPORTED;
   if ((int64_t)M * H > 0x7fffffffll) return KVS_ERR_DIMS;
   return KVS_OK;
+}
+
+// Kernel schedule (kvs_set_schedule); process-wide.
+std::atomic<int> g_schedule{KVS_SCHEDULE_AUTO};
+
+// Upper bound of the K/V bytes of one step below which the automatic
+// schedule takes the cluster kernel: such steps are bound by latency, and
+// the cluster kernel's merge costs no global-memory round trips.
+constexpr long long kClusterAutoBytes = 64ll << 20;
+
+bool use_cluster(int M, int Hkv, int D, int max_len) {
+  const long long pairs = (long long)M * Hkv;
+  if (pairs > kvs::kMaxClusterPairs) return false;
+  switch (g_schedule.load(std::memory_order_relaxed)) {
+    case KVS_SCHEDULE_PERSISTENT: return false;
+    case KVS_SCHEDULE_CLUSTER: return true;
+    default: return pairs * max_len * D * 8 <= kClusterAutoBytes;
+  }
+}
+
+// The attention launch of kvs_flash_decode (k_rows == nullptr) and
+// kvs_decode_step, on the schedule in force.
+int launch_attention(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+                     const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
+                     int D, int max_len, int chunk, void *workspace, int *d_status,
+                     cudaStream_t stream) {
+  if (use_cluster(M, Hkv, D, max_len))
+    return kvs::launch_fd_cluster(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, H, Hkv,
+                                  D, max_len, d_status, stream);
+  return kvs::launch_fd_step(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, H, Hkv, D,
+                             max_len, chunk, workspace, d_status, stream);
 }
 
 // chunk_size == 0 -> the library rule on the current device.
@@ -121,10 +153,10 @@ int kvs_flash_decode(const float *q, const float *k_cache, const float *v_cache,
   const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
   if (chunk <= 0) return -chunk;
   // the caches are only read when no new rows are passed
-  return kvs::launch_fd_step(q, const_cast<float *>(k_cache), const_cast<float *>(v_cache),
-                             positions, nullptr, nullptr, out, M, num_heads, num_kv_heads,
-                             head_dim, max_len, chunk, workspace, d_status,
-                             reinterpret_cast<cudaStream_t>(stream));
+  return launch_attention(q, const_cast<float *>(k_cache), const_cast<float *>(v_cache),
+                          positions, nullptr, nullptr, out, M, num_heads, num_kv_heads, head_dim,
+                          max_len, chunk, workspace, d_status,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
@@ -142,9 +174,34 @@ int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
   if (rc != KVS_OK) return rc;
   const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
   if (chunk <= 0) return -chunk;
-  return kvs::launch_fd_step(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, num_heads,
-                             num_kv_heads, head_dim, max_len, chunk, workspace, d_status,
-                             reinterpret_cast<cudaStream_t>(stream));
+  return launch_attention(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, num_heads,
+                          num_kv_heads, head_dim, max_len, chunk, workspace, d_status,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvs_set_schedule(int schedule) {
+  if (schedule != KVS_SCHEDULE_AUTO && schedule != KVS_SCHEDULE_PERSISTENT &&
+      schedule != KVS_SCHEDULE_CLUSTER)
+    return -KVS_ERR_DIMS;
+  return g_schedule.exchange(schedule);
+}
+
+int kvs_get_schedule(void) { return g_schedule.load(); }
+
+int kvs_schedule_for(int M, int num_kv_heads, int head_dim, int max_len) {
+  if (M < 1 || num_kv_heads < 1 || max_len < 1) return -KVS_ERR_DIMS;
+  if (!head_dim_supported(head_dim)) return -KVS_ERR_UNSUPPORTED;
+  return use_cluster(M, num_kv_heads, head_dim, max_len) ? KVS_SCHEDULE_CLUSTER
+                                                         : KVS_SCHEDULE_PERSISTENT;
+}
+
+int kvs_prepare(int num_heads, int num_kv_heads, int head_dim) {
+  if (num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0) return KVS_ERR_DIMS;
+  if (!head_dim_supported(head_dim)) return KVS_ERR_UNSUPPORTED;
+  if (num_heads / num_kv_heads > 8) return KVS_ERR_UNSUPPORTED;
+  const int rc = kvs::prepare_step_kernel(num_heads, num_kv_heads, head_dim);
+  if (rc != KVS_OK) return rc;
+  return kvs::prepare_cluster_kernel(num_heads, num_kv_heads, head_dim);
 }
 
 }  // extern "C"

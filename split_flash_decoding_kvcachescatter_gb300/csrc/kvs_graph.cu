@@ -45,7 +45,7 @@ int kvs_step_graph_create(int layers, const float *const *q, const float *const 
   const int chunk = chunk_size > 0 ? chunk_size
                                    : kvs_choose_chunk_size(M, num_kv_heads, head_dim, max_len, 0);
   if (chunk <= 0) return -chunk;
-  int rc = kvs::prepare_step_kernel(num_heads, num_kv_heads, head_dim);
+  int rc = kvs_prepare(num_heads, num_kv_heads, head_dim);
   if (rc != KVS_OK) return rc;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

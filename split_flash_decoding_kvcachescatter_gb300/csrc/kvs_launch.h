@@ -84,6 +84,17 @@ int launch_fd_step(const float *q, float *k_cache, float *v_cache, const int32_t
                    int D, int max_len, int chunk, void *workspace, int *d_status,
                    cudaStream_t stream);
 
+// One launch of the cluster kernel (one thread-block cluster per (sequence,
+// kv head), partials merged in distributed shared memory; no workspace).
+// Requires M * Hkv <= kMaxClusterPairs.
+constexpr long long kMaxClusterPairs = 65535;
+int launch_fd_cluster(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+                      const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
+                      int D, int max_len, int *d_status, cudaStream_t stream);
+
+// Sets the cluster kernel's attributes for (H / Hkv, D) on the current device.
+int prepare_cluster_kernel(int H, int Hkv, int D);
+
 // Sets the step kernel's attributes for (H / Hkv, D) on the current device
 // (done on first use anyway; a stream capture calls it beforehand).
 int prepare_step_kernel(int H, int Hkv, int D);

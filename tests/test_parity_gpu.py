@@ -30,6 +30,17 @@ def _built():
     torch.cuda.synchronize()
 
 
+@pytest.fixture(autouse=True, params=[B.KVS_SCHEDULE_PERSISTENT, B.KVS_SCHEDULE_CLUSTER],
+                ids=["persistent", "cluster"])
+def schedule(request, _built):
+    """Every test here runs on both kernels: the persistent split-K kernel
+    (partials merged through the workspace) and the cluster kernel (partials
+    merged in distributed shared memory)."""
+    prev = B.kvs_set_schedule(request.param)
+    yield request.param
+    B.kvs_set_schedule(prev)
+
+
 def run_step(t, w, chunk, status=None, ws=None, poison_ws=True, fused=False):
     """One decode step through the C ABI; returns out (device).
 
@@ -339,3 +350,48 @@ def test_step_graph_multi_layer():
     for l in range(layers):
         gate(outs[l].cpu().numpy(), oracle_out(ins2[l]), where=f"graph relaunch layer {l}")
     g.destroy()
+
+
+# ---------------------------------------------------------------- schedules
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("max_len", [1, 2, 31, 32, 33, 100, 513, 1200])
+def test_cache_lengths_across_cluster_sizes(schedule, D, max_len):
+    """Cache lengths that give every cluster size from 1 to 16 (and slices
+    of 0, 1 or a few rows per block), with the first and last positions."""
+    w = W.custom(M=4, num_heads=8, num_kv_heads=2, head_dim=D, max_len=max_len,
+                 positions="uniform", seed=71 + max_len + D)
+    assert B.kvs_schedule_for(w.M, w.num_kv_heads, D, max_len) == schedule
+    pos = np.array([max_len - 1, 0, (max_len - 1) // 2, max(0, max_len - 2)], np.int32)
+    inp = W.make_inputs(w, positions=pos)
+    check_workload(w, [16], inp=inp)
+
+
+def test_many_pairs_fall_back_to_the_persistent_kernel(schedule):
+    """M * Hkv above one grid dimension (65535 clusters) takes the persistent
+    kernel under every schedule; with one row per sequence the output is the
+    V row itself, bit for bit."""
+    w = W.custom(M=8193, num_heads=16, num_kv_heads=8, head_dim=64, max_len=1,
+                 positions="fixed", fixed_position=0, seed=17)
+    assert B.kvs_schedule_for(w.M, w.num_kv_heads, 64, 1) == B.KVS_SCHEDULE_PERSISTENT
+    inp = W.make_inputs(w)
+    t = W.upload(inp, w, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_step(t, w, 16, status, fused=True).cpu().numpy()
+    assert int(status.item()) == 0
+    G = w.group
+    for h in range(w.num_heads):
+        assert np.array_equal(out[:, h].view(np.int32), inp.v_rows[:, h // G].view(np.int32))
+
+
+def test_auto_schedule_picks_by_size():
+    prev = B.kvs_set_schedule(B.KVS_SCHEDULE_AUTO)
+    try:
+        tiny, small = W.WORKLOADS["tiny"], W.WORKLOADS["small_model"]
+        big = W.WORKLOADS["8b_batch"]
+        for w, want in ((tiny, B.KVS_SCHEDULE_CLUSTER), (small, B.KVS_SCHEDULE_CLUSTER),
+                        (big, B.KVS_SCHEDULE_PERSISTENT)):
+            assert B.kvs_schedule_for(w.M, w.num_kv_heads, w.head_dim, w.max_len) == want
+        check_workload(tiny, [tiny.chunk_size])
+    finally:
+        B.kvs_set_schedule(prev)
+
