@@ -45,8 +45,14 @@ from split_flash_decoding_kvcachescatter_gb300 import workloads as W  # noqa: E4
 METRIC = "split-K decode attention: KV-cache HBM GB/s (% of GB300 peak) and µs/call"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
-CHUNK_SOURCE = os.path.join(ROOT, "split_flash_decoding_kvcachescatter_gb300", "csrc",
-                            "flash_decode.cu")
+CSRC = os.path.join(ROOT, "split_flash_decoding_kvcachescatter_gb300", "csrc")
+# Sources of each attention kernel (a recorded ncu capture is used only
+# while these are unchanged).
+KERNEL_SOURCES = {
+    "persistent": ("flash_decode.cu", "fd_tile.cuh", "kvs_device.cuh"),
+    "cluster": ("fd_cluster.cu", "fd_tile.cuh", "kvs_device.cuh"),
+}
+KERNEL_NAMES = {"persistent": "fd_step_kernel", "cluster": "fd_cluster_kernel"}
 
 
 def dist_env():
@@ -85,23 +91,26 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def chunk_source_hash():
-    with open(CHUNK_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_source_hash(kernel):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, chunk):
-    """Per-launch DRAM bytes of the step kernel from a committed ncu summary,
-    if it was taken on the current kernel source; else None."""
+def ncu_traffic(kernel, workload, chunk):
+    """Per-launch DRAM bytes of the attention kernel from a committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "fd_step_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
         return None
-    key = f"{workload}:{chunk}"
+    key = f"{workload}:{chunk}" if kernel == "persistent" else f"{workload}:{kernel}"
     e = rec.get(key)
-    if not e or e.get("source_sha256_16") != chunk_source_hash():
+    if not e or e.get("source_sha256_16") != kernel_source_hash(kernel):
         return None
     return int(e["dram_bytes_per_launch"])
 
@@ -261,6 +270,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--graph", action="store_true",
                     help="launch the whole (multi-layer) step as one captured CUDA graph")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "persistent", "cluster"],
+                    help="attention kernel (kvs_set_schedule)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -287,6 +298,11 @@ def main():
         tdist.init_process_group("nccl", device_id=dev)
     kbuild.build()
     B.lib()
+    B.kvs_set_schedule({"auto": B.KVS_SCHEDULE_AUTO, "persistent": B.KVS_SCHEDULE_PERSISTENT,
+                        "cluster": B.KVS_SCHEDULE_CLUSTER}[args.schedule])
+    kernel = ("cluster" if B.kvs_schedule_for(w.M, w.num_heads, w.num_kv_heads, w.head_dim,
+                                               w.max_len) == B.KVS_SCHEDULE_CLUSTER
+              else "persistent")
 
     def barrier():
         if world > 1:
@@ -460,7 +476,7 @@ def main():
     step_mean_ms = total_ms / K
     achieved = ab["step"] / (step_mean_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    traffic = ncu_traffic(w.name, resolved_chunk)
+    traffic = ncu_traffic(kernel, w.name, resolved_chunk)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -479,6 +495,7 @@ def main():
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "max_len": w.max_len,
             "chunk_size": resolved_chunk,
             "chunk_rule": "given" if chunk > 0 else "library rule (chunk_size=0)",
+            "schedule": args.schedule, "kernel": KERNEL_NAMES[kernel],
             "layers": nl, "launch": ("one CUDA graph for all layers" if graph is not None
                                      else f"{nl} kvs_decode_step launch(es)"),
             "live_kv_bytes": W.kv_bytes(inp, w) * nl,
@@ -496,7 +513,8 @@ def main():
         "attention_gbs": ab["attention"] / (statistics.mean(decode_ms) * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "fd_step_kernel (kvs_decode_step)", "peak_source": peak_kind,
+                     "kernel": f"{KERNEL_NAMES[kernel]} (kvs_decode_step)",
+                     "peak_source": peak_kind,
                      "bytes_per_launch": ab1["step"]},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},

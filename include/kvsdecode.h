@@ -263,12 +263,14 @@ int kvs_flash_decode_static(const float *q, const float *k_cache,
 /*
  * Kernel schedule of kvs_flash_decode, kvs_decode_step (and so of the
  * graphs and the static entry point), process-wide:
- *   KVS_SCHEDULE_AUTO        the cluster kernel when M * num_kv_heads <=
- *                            65535 and M * num_kv_heads * max_len *
- *                            head_dim * 8 bytes (the K/V bytes of a full
- *                            cache) is at most 64 MiB -- steps that are
- *                            bound by latency, not bandwidth -- else the
- *                            persistent kernel (the default);
+ *   KVS_SCHEDULE_AUTO        (the default) the cluster kernel for steps
+ *                            bound by latency rather than bandwidth: the
+ *                            K/V bytes of full caches (M * num_kv_heads *
+ *                            max_len * head_dim * 8) at most 64 MiB, every
+ *                            cluster of the launch resident at once on the
+ *                            current device, and each block's slice of a
+ *                            full cache at most 512 KiB; else the
+ *                            persistent kernel;
  *   KVS_SCHEDULE_PERSISTENT  always the persistent kernel;
  *   KVS_SCHEDULE_CLUSTER     the cluster kernel whenever M * num_kv_heads
  *                            <= 65535.
@@ -285,10 +287,12 @@ typedef enum kvs_schedule {
 int kvs_set_schedule(int schedule);
 int kvs_get_schedule(void);
 
-/* The kernel a call with these sizes would run under the schedule in force:
- * KVS_SCHEDULE_PERSISTENT or KVS_SCHEDULE_CLUSTER, or a negative kvs_status
- * (DIMS, UNSUPPORTED). */
-int kvs_schedule_for(int M, int num_kv_heads, int head_dim, int max_len);
+/* The kernel a call with these sizes would run on the current device under
+ * the schedule in force: KVS_SCHEDULE_PERSISTENT or KVS_SCHEDULE_CLUSTER, or
+ * a negative kvs_status (DIMS, UNSUPPORTED).  Without a usable device the
+ * automatic schedule answers KVS_SCHEDULE_PERSISTENT. */
+int kvs_schedule_for(int M, int num_heads, int num_kv_heads, int head_dim,
+                     int max_len);
 
 /*
  * kvs_prepare -- sets up, on the current device, both attention kernels

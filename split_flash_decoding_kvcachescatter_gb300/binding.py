@@ -93,7 +93,7 @@ def lib() -> ctypes.CDLL:
             L.kvs_get_schedule.restype = _I
             L.kvs_get_schedule.argtypes = []
             L.kvs_schedule_for.restype = _I
-            L.kvs_schedule_for.argtypes = [_I, _I, _I, _I]
+            L.kvs_schedule_for.argtypes = [_I, _I, _I, _I, _I]
             L.kvs_prepare.restype = _I
             L.kvs_prepare.argtypes = [_I, _I, _I]
             L.kvs_strerror.restype = ctypes.c_char_p
@@ -163,9 +163,9 @@ def kvs_get_schedule() -> int:
     return int(lib().kvs_get_schedule())
 
 
-def kvs_schedule_for(M, num_kv_heads, head_dim, max_len) -> int:
+def kvs_schedule_for(M, num_heads, num_kv_heads, head_dim, max_len) -> int:
     """KVS_SCHEDULE_PERSISTENT or KVS_SCHEDULE_CLUSTER: the kernel such a call would run."""
-    r = lib().kvs_schedule_for(M, num_kv_heads, head_dim, max_len)
+    r = lib().kvs_schedule_for(M, num_heads, num_kv_heads, head_dim, max_len)
     if r < 0:
         raise KvsError(-r, "kvs_schedule_for")
     return r

@@ -43,6 +43,12 @@ namespace {
 
 constexpr int kMaxClusterDevices = 64;
 
+// Block geometry: that of the persistent kernel (4 consumer warps, two
+// blocks per SM).  Measured on GB300, 8 consumer warps at one block per SM
+// made small steps slower (fewer clusters resident at once).
+template <int D, int G>
+using ClusterGeo = Geo<D, G, 4, 2>;
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
@@ -75,12 +81,12 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
+__global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::MINB)
     fd_cluster_kernel(const float *__restrict__ q, float *k_cache, float *v_cache,
                       const int32_t *__restrict__ positions, const float *__restrict__ k_rows,
                       const float *__restrict__ v_rows, float *__restrict__ out, int Hkv,
                       int max_len, float qscale, int *d_status) {
-  using C = Geo<D, G>;
+  using C = ClusterGeo<D, G>;
   extern __shared__ __align__(128) unsigned char smem[];
   StageDesc *desc = reinterpret_cast<StageDesc *>(smem + C::OFF_DESC);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     __syncwarp();
   } else {
     // ===================== consumer warps ===================================
-    const TileLane<D, G> tl = tile_lane<D, G>(smem, warp, lane);
+    const TileLane<C> tl = tile_lane<C>(smem, warp, lane);
     float4 qv[G];
     float4 acc[G];
     float m_run[G];
@@ -226,18 +232,18 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       const StageDesc dsc = desc[s];
       if (dsc.flags & kNoMore) break;
       const unsigned char *stage = smem + s * C::STAGE_BYTES;
-      if (dsc.flags & kRunStart) tile_load_q<D, G>(tl, stage, qscale, qv);
-      tile_consume<D, G>(tl, stage, dsc.nrows, qv, acc, m_run, l_lane);
+      if (dsc.flags & kRunStart) tile_load_q<C>(tl, stage, qscale, qv);
+      tile_consume<C>(tl, stage, dsc.nrows, qv, acc, m_run, l_lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
     // A block with no rows publishes m = -inf, l = 0, acc = 0.
-    tile_publish<D, G>(tl, acc, m_run, l_lane);
+    tile_publish<C>(tl, acc, m_run, l_lane);
     consumer_sync(C::NW * 32);
     for (int e = threadIdx.x; e < G * C::LPR; e += C::NW * 32) {
       float4 a;
       float mx, lsum;
-      merged_warp_states<D, G>(smem, e, a, mx, lsum);
+      merged_warp_states<C>(smem, e, a, mx, lsum);
       part_acc[e] = a;  // only this thread reads or writes element e here
       if (e % C::LPR == 0) part_ml[e / C::LPR] = make_float2(mx, lsum);
     }
@@ -286,32 +292,46 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
 // cluster's blocks finish together soon after their first copies land.
 constexpr int kClusterRowsPerBlock = 32;
 
+constexpr int kClusterSizes = 5;  // 1, 2, 4, 8, 16
+
 struct ClusterInfo {
   int max_size = 0;
+  int active[kClusterSizes] = {0};  // clusters of size 2^k resident at once
   bool configured = false;
 };
 
-// Largest cluster size (a power of two <= 16) that this instantiation can be
-// launched with on device `dev`; configures its attributes on first use.
+// Cluster size for a cache of max_len rows, given the largest launchable.
+inline int cluster_size_for(int max_len, int cs_max) {
+  int cs = 1;
+  while (cs < cs_max && (long long)cs * kClusterRowsPerBlock < max_len) cs <<= 1;
+  return cs;
+}
+
+// Configures this instantiation on device `dev` on first use and returns its
+// record: the largest cluster size (a power of two <= 16) it can be launched
+// with, and how many clusters of each size the device keeps resident.
 template <int D, int G>
-int cluster_max_size(int dev) {
-  using C = Geo<D, G>;
+const ClusterInfo *cluster_info(int dev) {
+  using C = ClusterGeo<D, G>;
   static ClusterInfo info[kMaxClusterDevices];
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   if (!info[dev].configured) {
     auto kern = fd_cluster_kernel<D, G>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
-      return -1;
+        cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
     cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    int cs = 16;
+    int top = 16;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
         cudaSuccess) {
       cudaGetLastError();
-      cs = 8;
+      top = 8;
     }
-    for (; cs >= 1; cs >>= 1) {
+    ClusterInfo rec;
+    for (int k = 0, cs = 1; cs <= top; ++k, cs <<= 1) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(cs, 1, 1);
       cfg.blockDim = dim3(C::THREADS, 1, 1);
@@ -324,14 +344,19 @@ int cluster_max_size(int dev) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) break;
-      cudaGetLastError();
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      if (n <= 0) break;
+      rec.active[k] = n;
+      rec.max_size = cs;
     }
-    if (cs < 1) return -1;
-    info[dev].max_size = cs;
-    info[dev].configured = true;
+    if (rec.max_size < 1) return nullptr;
+    rec.configured = true;
+    info[dev] = rec;
   }
-  return info[dev].max_size;
+  return &info[dev];
 }
 
 int current_device() {
@@ -344,15 +369,14 @@ template <int D, int G>
 int launch_cluster_impl(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
                         const float *k_rows, const float *v_rows, float *out, int M, int Hkv,
                         int max_len, int *d_status, cudaStream_t stream) {
-  using C = Geo<D, G>;
+  using C = ClusterGeo<D, G>;
   const int dev = current_device();
   if (dev < 0) return KVS_ERR_LAUNCH;
-  const int cs_max = cluster_max_size<D, G>(dev);
-  if (cs_max <= 0) return KVS_ERR_LAUNCH;
+  const ClusterInfo *ci = cluster_info<D, G>(dev);
+  if (!ci) return KVS_ERR_LAUNCH;
   const long long pairs = (long long)M * Hkv;
   if (pairs > kMaxClusterPairs) return KVS_ERR_UNSUPPORTED;
-  int cs = 1;
-  while (cs < cs_max && (long long)cs * kClusterRowsPerBlock < max_len) cs <<= 1;
+  const int cs = cluster_size_for(max_len, ci->max_size);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, (unsigned)pairs, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
@@ -405,11 +429,11 @@ int prepare_cluster_kernel(int H, int Hkv, int D) {
   if (dev < 0) return KVS_ERR_LAUNCH;
   if (Hkv < 1 || H % Hkv != 0) return KVS_ERR_DIMS;
   const int G = H / Hkv;
-  int cs = -1;
+  const ClusterInfo *ci = nullptr;
   switch (D * 16 + G) {
 #define KVS_PREP(d, g)                     \
   case d * 16 + g:                         \
-    cs = cluster_max_size<d, g>(dev);      \
+    ci = cluster_info<d, g>(dev);          \
     break;
     KVS_PREP(64, 1) KVS_PREP(64, 2) KVS_PREP(64, 3) KVS_PREP(64, 4)
     KVS_PREP(64, 5) KVS_PREP(64, 6) KVS_PREP(64, 7) KVS_PREP(64, 8)
@@ -419,7 +443,41 @@ int prepare_cluster_kernel(int H, int Hkv, int D) {
     default:
       return KVS_ERR_UNSUPPORTED;
   }
-  return cs > 0 ? KVS_OK : KVS_ERR_LAUNCH;
+  return ci ? KVS_OK : KVS_ERR_LAUNCH;
+}
+
+// Whether the automatic schedule should take the cluster kernel: every
+// cluster of the launch resident at once (one wave), and each block's slice
+// of a full cache at most kClusterAutoSliceBytes.  Measured on GB300: the
+// cluster kernel wins on a few (sequence, kv head) pairs with short slices
+// (a small model's 8 pairs: 12 us against 18 us a layer), and loses once
+// its clusters need a second wave.
+int cluster_auto_ok(int M, int H, int Hkv, int D, int max_len) {
+  constexpr long long kClusterAutoSliceBytes = 512ll << 10;
+  const int dev = current_device();
+  if (dev < 0 || Hkv < 1 || H % Hkv != 0) return 0;
+  const int G = H / Hkv;
+  const ClusterInfo *ci = nullptr;
+  switch (D * 16 + G) {
+#define KVS_INFO(d, g)                     \
+  case d * 16 + g:                         \
+    ci = cluster_info<d, g>(dev);          \
+    break;
+    KVS_INFO(64, 1) KVS_INFO(64, 2) KVS_INFO(64, 3) KVS_INFO(64, 4)
+    KVS_INFO(64, 5) KVS_INFO(64, 6) KVS_INFO(64, 7) KVS_INFO(64, 8)
+    KVS_INFO(128, 1) KVS_INFO(128, 2) KVS_INFO(128, 3) KVS_INFO(128, 4)
+    KVS_INFO(128, 5) KVS_INFO(128, 6) KVS_INFO(128, 7) KVS_INFO(128, 8)
+#undef KVS_INFO
+    default:
+      return 0;
+  }
+  if (!ci) return 0;
+  const int cs = cluster_size_for(max_len, ci->max_size);
+  int k = 0;
+  while ((1 << k) < cs) ++k;
+  const long long pairs = (long long)M * Hkv;
+  const long long slice_bytes = ((long long)max_len + cs - 1) / cs * D * 8;
+  return pairs <= ci->active[k] && slice_bytes <= kClusterAutoSliceBytes;
 }
 
 int launch_fd_cluster(const float *q, float *k_cache, float *v_cache, const int32_t *positions,

@@ -60,11 +60,12 @@ constexpr int kMergeScratchBytes = kMergeWindow * 4 + 16;
 constexpr int kRingBytes = 96 * 1024;
 
 // Compile-time geometry of one (head_dim, group) instantiation.
-template <int D_, int G_>
+template <int D_, int G_, int NW_ = 4, int MINB_ = 2>
 struct Geo {
   static constexpr int D = D_;
   static constexpr int G = G_;
-  static constexpr int NW = 4;                    // consumer warps
+  static constexpr int NW = NW_;                  // consumer warps
+  static constexpr int MINB = MINB_;              // blocks per SM the budget is for
   static constexpr int THREADS = (NW + 1) * 32;   // + one producer warp
   static constexpr int LPR = D / 4;               // lanes per row (float4 each)
   static constexpr int RPI = 32 / LPR;            // rows per warp instruction
@@ -100,8 +101,8 @@ struct Geo {
   static_assert(G >= 1 && G <= LPR, "group larger than lanes per row");
   static_assert(RP * G <= LPR, "slots exceed lanes");
   static_assert(RW * G <= 32 * RPI, "tile too large");
-  // two blocks per SM: 228 KB of shared memory less 1 KB reserved per block
-  static_assert(SMEM_BYTES <= (228 * 1024) / 2 - 1024, "two blocks per SM must fit");
+  // MINB blocks per SM: 228 KB of shared memory less 1 KB reserved per block
+  static_assert(SMEM_BYTES <= (228 * 1024) / MINB - 1024, "MINB blocks per SM must fit");
 };
 
 // ---------------------------------------------------------------------------
@@ -145,7 +146,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // forms RP*G partial dot products; the transposing butterfly leaves lane
 // li with the full score of slot li / SPAN (row slot_row, head slot_h).
 // ---------------------------------------------------------------------------
-template <int D, int G>
+template <class C>
 struct TileLane {
   int w, lane, gi, li;
   int slot_h, slot_row;
@@ -159,10 +160,10 @@ struct TileLane {
 };
 
 // The lane's view; also clears this warp's score and probability tiles.
-template <int D, int G>
-__device__ __forceinline__ TileLane<D, G> tile_lane(unsigned char *smem, int warp, int lane) {
-  using C = Geo<D, G>;
-  TileLane<D, G> t;
+template <class C>
+__device__ __forceinline__ TileLane<C> tile_lane(unsigned char *smem, int warp, int lane) {
+  constexpr int G = C::G;
+  TileLane<C> t;
   t.w = warp;
   t.lane = lane;
   t.gi = lane / C::LPR;
@@ -197,10 +198,10 @@ __device__ __forceinline__ void tile_reset(float4 (&acc)[G], float (&m_run)[G], 
 }
 
 // q rows of the group (a run's first stage), pre-scaled by log2(e)/sqrt(D).
-template <int D, int G>
-__device__ __forceinline__ void tile_load_q(const TileLane<D, G> &t, const unsigned char *stage,
-                                            float qscale, float4 (&qv)[G]) {
-  using C = Geo<D, G>;
+template <class C>
+__device__ __forceinline__ void tile_load_q(const TileLane<C> &t, const unsigned char *stage,
+                                            float qscale, float4 (&qv)[C::G]) {
+  constexpr int G = C::G;
   const float4 *sQ = reinterpret_cast<const float4 *>(stage + 2 * C::KV_BYTES);
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -211,11 +212,12 @@ __device__ __forceinline__ void tile_load_q(const TileLane<D, G> &t, const unsig
 
 // Folds the stage's nrows K/V rows (this warp's tile of them) into the
 // running state.
-template <int D, int G>
-__device__ __forceinline__ void tile_consume(const TileLane<D, G> &t, const unsigned char *stage,
-                                             int nrows, const float4 (&qv)[G], float4 (&acc)[G],
-                                             float (&m_run)[G], float &l_lane) {
-  using C = Geo<D, G>;
+template <class C>
+__device__ __forceinline__ void tile_consume(const TileLane<C> &t, const unsigned char *stage,
+                                             int nrows, const float4 (&qv)[C::G],
+                                             float4 (&acc)[C::G], float (&m_run)[C::G],
+                                             float &l_lane) {
+  constexpr int G = C::G;
   const float4 *sK = reinterpret_cast<const float4 *>(stage);
   const float4 *sV = reinterpret_cast<const float4 *>(stage + C::KV_BYTES);
   const int my_valid = min(max(nrows - t.w * C::RW, 0), C::RW);
@@ -307,10 +309,10 @@ __device__ __forceinline__ void tile_consume(const TileLane<D, G> &t, const unsi
 
 // End of a run: this warp's (m, l, acc) into shared memory.  The block's
 // consumer warps must then synchronise before merged_warp_states() reads them.
-template <int D, int G>
-__device__ __forceinline__ void tile_publish(const TileLane<D, G> &t, float4 (&acc)[G],
-                                             const float (&m_run)[G], float l_lane) {
-  using C = Geo<D, G>;
+template <class C>
+__device__ __forceinline__ void tile_publish(const TileLane<C> &t, float4 (&acc)[C::G],
+                                             const float (&m_run)[C::G], float l_lane) {
+  constexpr int G = C::G;
   if (C::RPI > 1) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -344,10 +346,10 @@ __device__ __forceinline__ void tile_publish(const TileLane<D, G> &t, float4 (&a
 
 // The run's (m, l, acc) of head h = e / (D/4), float4 column d4 = e % (D/4),
 // merged over the NW published warp states (m = -inf when the run has no row).
-template <int D, int G>
+template <class C>
 __device__ __forceinline__ void merged_warp_states(const unsigned char *smem, int e, float4 &a,
                                                    float &mx, float &lsum) {
-  using C = Geo<D, G>;
+  constexpr int G = C::G;
   const float4 *sAcc = reinterpret_cast<const float4 *>(smem + C::OFF_MACC);
   const float *sM = reinterpret_cast<const float *>(smem + C::OFF_MM);
   const float *sL = reinterpret_cast<const float *>(smem + C::OFF_ML);

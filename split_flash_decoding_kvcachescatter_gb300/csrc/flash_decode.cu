@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   }
 
   // ========================= consumer warps ================================
-  const TileLane<D, G> tl = tile_lane<D, G>(smem, warp, lane);
+  const TileLane<C> tl = tile_lane<C>(smem, warp, lane);
   float4 qv[G];
   float4 acc[G];
   float m_run[G];
@@ -618,14 +618,14 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     const StageDesc dsc = desc[s];
     if (dsc.flags & kNoMore) break;
     const unsigned char *stage = smem + s * C::STAGE_BYTES;
-    if (dsc.flags & kRunStart) tile_load_q<D, G>(tl, stage, qscale, qv);
-    tile_consume<D, G>(tl, stage, dsc.nrows, qv, acc, m_run, l_lane);
+    if (dsc.flags & kRunStart) tile_load_q<C>(tl, stage, qscale, qv);
+    tile_consume<C>(tl, stage, dsc.nrows, qv, acc, m_run, l_lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     if (!(dsc.flags & kRunEnd)) continue;
 
     // ---- end of run: merge the NW warp states --------------------------------
-    tile_publish<D, G>(tl, acc, m_run, l_lane);
+    tile_publish<C>(tl, acc, m_run, l_lane);
     if (!consumers_barrier()) return;
     // A run that covers all of (i, g) is the answer; any other run is a
     // partial for the (i, g) merge.
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       const int d4 = e - h * C::LPR;
       float4 a;
       float mx, lsum;
-      merged_warp_states<D, G>(smem, e, a, mx, lsum);
+      merged_warp_states<C>(smem, e, a, mx, lsum);
       if (whole) {
         const float inv = 1.f / lsum;
         reinterpret_cast<float4 *>(out)[((size_t)i_seq * H + (size_t)g_kv * G + h) * C::LPR + d4] =

@@ -27,18 +27,20 @@ int check_attention_shape(int M, int H, int Hkv, int D, int max_len, int chunk) 
 // Kernel schedule (kvs_set_schedule); process-wide.
 std::atomic<int> g_schedule{KVS_SCHEDULE_AUTO};
 
-// Upper bound of the K/V bytes of one step below which the automatic
-// schedule takes the cluster kernel: such steps are bound by latency, and
-// the cluster kernel's merge costs no global-memory round trips.
+// Upper bound of the K/V bytes of one step above which the automatic
+// schedule never considers the cluster kernel (checked before any device
+// query).
 constexpr long long kClusterAutoBytes = 64ll << 20;
 
-bool use_cluster(int M, int Hkv, int D, int max_len) {
+bool use_cluster(int M, int H, int Hkv, int D, int max_len) {
   const long long pairs = (long long)M * Hkv;
   if (pairs > kvs::kMaxClusterPairs) return false;
   switch (g_schedule.load(std::memory_order_relaxed)) {
     case KVS_SCHEDULE_PERSISTENT: return false;
     case KVS_SCHEDULE_CLUSTER: return true;
-    default: return pairs * max_len * D * 8 <= kClusterAutoBytes;
+    default:
+      if (pairs * max_len * D * 8 > kClusterAutoBytes) return false;
+      return kvs::cluster_auto_ok(M, H, Hkv, D, max_len) != 0;
   }
 }
 
@@ -48,7 +50,7 @@ int launch_attention(const float *q, float *k_cache, float *v_cache, const int32
                      const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
                      int D, int max_len, int chunk, void *workspace, int *d_status,
                      cudaStream_t stream) {
-  if (use_cluster(M, Hkv, D, max_len))
+  if (use_cluster(M, H, Hkv, D, max_len))
     return kvs::launch_fd_cluster(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, H, Hkv,
                                   D, max_len, d_status, stream);
   return kvs::launch_fd_step(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, H, Hkv, D,
@@ -188,11 +190,12 @@ int kvs_set_schedule(int schedule) {
 
 int kvs_get_schedule(void) { return g_schedule.load(); }
 
-int kvs_schedule_for(int M, int num_kv_heads, int head_dim, int max_len) {
-  if (M < 1 || num_kv_heads < 1 || max_len < 1) return -KVS_ERR_DIMS;
-  if (!head_dim_supported(head_dim)) return -KVS_ERR_UNSUPPORTED;
-  return use_cluster(M, num_kv_heads, head_dim, max_len) ? KVS_SCHEDULE_CLUSTER
-                                                         : KVS_SCHEDULE_PERSISTENT;
+int kvs_schedule_for(int M, int num_heads, int num_kv_heads, int head_dim, int max_len) {
+  const int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, 0);
+  if (rc != KVS_OK) return -rc;
+  if (M < 1) return -KVS_ERR_DIMS;
+  return use_cluster(M, num_heads, num_kv_heads, head_dim, max_len) ? KVS_SCHEDULE_CLUSTER
+                                                                    : KVS_SCHEDULE_PERSISTENT;
 }
 
 int kvs_prepare(int num_heads, int num_kv_heads, int head_dim) {

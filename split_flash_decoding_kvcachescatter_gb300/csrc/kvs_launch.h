@@ -95,6 +95,10 @@ int launch_fd_cluster(const float *q, float *k_cache, float *v_cache, const int3
 // Sets the cluster kernel's attributes for (H / Hkv, D) on the current device.
 int prepare_cluster_kernel(int H, int Hkv, int D);
 
+// 1 if the automatic schedule should run this shape on the cluster kernel
+// (current device; configures the kernel on first use), else 0.
+int cluster_auto_ok(int M, int H, int Hkv, int D, int max_len);
+
 // Sets the step kernel's attributes for (H / Hkv, D) on the current device
 // (done on first use anyway; a stream capture calls it beforehand).
 int prepare_step_kernel(int H, int Hkv, int D);

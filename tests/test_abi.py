@@ -173,28 +173,27 @@ def test_schedule_set_get_and_rule(L):
     prev = B.kvs_set_schedule(B.KVS_SCHEDULE_AUTO)
     try:
         assert B.kvs_get_schedule() == B.KVS_SCHEDULE_AUTO
-        # automatic rule: the cluster kernel while a full cache is <= 64 MiB
-        # of K/V and M * Hkv fits one grid dimension
-        assert B.kvs_schedule_for(4, 2, 64, 2048) == B.KVS_SCHEDULE_CLUSTER  # 8 MiB
-        assert B.kvs_schedule_for(1, 2, 64, 256) == B.KVS_SCHEDULE_CLUSTER
-        assert B.kvs_schedule_for(32, 8, 128, 8192) == B.KVS_SCHEDULE_PERSISTENT  # 2 GiB
-        assert B.kvs_schedule_for(4, 8, 128, 1024) == B.KVS_SCHEDULE_CLUSTER  # 32 MiB
-        assert B.kvs_schedule_for(8, 8, 128, 1024) == B.KVS_SCHEDULE_CLUSTER  # 64 MiB
-        assert B.kvs_schedule_for(8, 8, 128, 1025) == B.KVS_SCHEDULE_PERSISTENT
-        assert B.kvs_schedule_for(65536, 1, 64, 1) == B.KVS_SCHEDULE_PERSISTENT  # pairs
+        # automatic rule, the part decided before any device query: full
+        # caches above 64 MiB of K/V, or more pairs than a grid dimension,
+        # always take the persistent kernel
+        assert B.kvs_schedule_for(32, 32, 8, 128, 8192) == B.KVS_SCHEDULE_PERSISTENT  # 2 GiB
+        assert B.kvs_schedule_for(8, 32, 8, 128, 1025) == B.KVS_SCHEDULE_PERSISTENT
+        assert B.kvs_schedule_for(65536, 1, 1, 64, 1) == B.KVS_SCHEDULE_PERSISTENT
         assert B.kvs_set_schedule(B.KVS_SCHEDULE_PERSISTENT) == B.KVS_SCHEDULE_AUTO
-        assert B.kvs_schedule_for(1, 2, 64, 256) == B.KVS_SCHEDULE_PERSISTENT
+        assert B.kvs_schedule_for(1, 4, 2, 64, 256) == B.KVS_SCHEDULE_PERSISTENT
         assert B.kvs_set_schedule(B.KVS_SCHEDULE_CLUSTER) == B.KVS_SCHEDULE_PERSISTENT
-        assert B.kvs_schedule_for(32, 8, 128, 8192) == B.KVS_SCHEDULE_CLUSTER
-        assert B.kvs_schedule_for(65535, 1, 64, 1) == B.KVS_SCHEDULE_CLUSTER
-        assert B.kvs_schedule_for(65536, 1, 64, 1) == B.KVS_SCHEDULE_PERSISTENT
+        assert B.kvs_schedule_for(32, 32, 8, 128, 8192) == B.KVS_SCHEDULE_CLUSTER
+        assert B.kvs_schedule_for(65535, 1, 1, 64, 1) == B.KVS_SCHEDULE_CLUSTER
+        assert B.kvs_schedule_for(65536, 1, 1, 64, 1) == B.KVS_SCHEDULE_PERSISTENT
         with pytest.raises(B.KvsError):
             B.kvs_set_schedule(7)
         assert B.kvs_get_schedule() == B.KVS_SCHEDULE_CLUSTER  # unchanged by a bad value
         with pytest.raises(B.KvsError):
-            B.kvs_schedule_for(1, 2, 96, 16)
+            B.kvs_schedule_for(1, 4, 2, 96, 16)
         with pytest.raises(B.KvsError):
-            B.kvs_schedule_for(0, 2, 64, 16)
+            B.kvs_schedule_for(0, 4, 2, 64, 16)
+        with pytest.raises(B.KvsError):
+            B.kvs_schedule_for(1, 4, 3, 64, 16)
     finally:
         B.kvs_set_schedule(prev)
 

@@ -360,7 +360,7 @@ def test_cache_lengths_across_cluster_sizes(schedule, D, max_len):
     of 0, 1 or a few rows per block), with the first and last positions."""
     w = W.custom(M=4, num_heads=8, num_kv_heads=2, head_dim=D, max_len=max_len,
                  positions="uniform", seed=71 + max_len + D)
-    assert B.kvs_schedule_for(w.M, w.num_kv_heads, D, max_len) == schedule
+    assert B.kvs_schedule_for(w.M, w.num_heads, w.num_kv_heads, D, max_len) == schedule
     pos = np.array([max_len - 1, 0, (max_len - 1) // 2, max(0, max_len - 2)], np.int32)
     inp = W.make_inputs(w, positions=pos)
     check_workload(w, [16], inp=inp)
@@ -372,7 +372,8 @@ def test_many_pairs_fall_back_to_the_persistent_kernel(schedule):
     V row itself, bit for bit."""
     w = W.custom(M=8193, num_heads=16, num_kv_heads=8, head_dim=64, max_len=1,
                  positions="fixed", fixed_position=0, seed=17)
-    assert B.kvs_schedule_for(w.M, w.num_kv_heads, 64, 1) == B.KVS_SCHEDULE_PERSISTENT
+    assert B.kvs_schedule_for(w.M, w.num_heads, w.num_kv_heads, 64, 1) == \
+        B.KVS_SCHEDULE_PERSISTENT
     inp = W.make_inputs(w)
     t = W.upload(inp, w, DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -388,9 +389,12 @@ def test_auto_schedule_picks_by_size():
     try:
         tiny, small = W.WORKLOADS["tiny"], W.WORKLOADS["small_model"]
         big = W.WORKLOADS["8b_batch"]
+        # 32 (sequence, kv head) pairs need more clusters than stay resident
+        many = W.custom(M=4, num_heads=32, num_kv_heads=8, head_dim=128, max_len=2048)
         for w, want in ((tiny, B.KVS_SCHEDULE_CLUSTER), (small, B.KVS_SCHEDULE_CLUSTER),
-                        (big, B.KVS_SCHEDULE_PERSISTENT)):
-            assert B.kvs_schedule_for(w.M, w.num_kv_heads, w.head_dim, w.max_len) == want
+                        (big, B.KVS_SCHEDULE_PERSISTENT), (many, B.KVS_SCHEDULE_PERSISTENT)):
+            got = B.kvs_schedule_for(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len)
+            assert got == want, w.name
         check_workload(tiny, [tiny.chunk_size])
     finally:
         B.kvs_set_schedule(prev)
