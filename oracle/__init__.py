@@ -197,3 +197,47 @@ def decode_sequences(q, k_seq, v_seq, positions, threads=None):
         with ThreadPoolExecutor(max_workers=n) as ex:
             list(ex.map(one, range(M)))
     return out
+
+
+def decode_step_slots(q, k_rows, v_rows, positions, slots, done, k_pool, v_pool, out):
+    """One decode step over a pool of cache slots with finished sequences.
+
+    Follows realizar 0.8.5, src/cuda/executor/head_dim.rs,
+    ``flash_decoding_attention_into``: "Step 2: Build pointer arrays" (each
+    sequence's K/V cache is found through a per-sequence pointer; here an
+    index into the pool k_pool/v_pool [num_slots][Hkv][Lmax][D]) and the
+    PMAT-076 note in the same step (a finished sequence gets seq_len 0, so
+    the attention kernels skip it).  Step 1 scatters every sequence before
+    any attention runs, finished or not.
+
+    In place: k_pool, v_pool (scatter) and out [M][H][D] (attention).
+      slots[i]  pool slot of sequence i (None: slot i)
+      done[i]   nonzero: finished -- the scatter still happens, the
+                attention does not, and out[i] keeps its contents (None: none)
+    A sequence whose position is outside [0, Lmax) or whose slot is outside
+    [0, num_slots) is not scattered; unless finished its out rows become NaN.
+    Returns the indices of such sequences.
+    """
+    M, H, D = q.shape
+    S, Hkv, Lmax, D2 = k_pool.shape
+    assert D2 == D and v_pool.shape == k_pool.shape and out.shape == (M, H, D)
+    slots = np.arange(M, dtype=np.int64) if slots is None else np.asarray(slots, np.int64)
+    done = np.zeros(M, bool) if done is None else (np.asarray(done) != 0)
+    positions = np.asarray(positions, np.int64)
+    bad = [i for i in range(M)
+           if not (0 <= positions[i] < Lmax) or not (0 <= slots[i] < S)]
+    # Step 1: the new rows of every sequence, at its position in its slot
+    for i in range(M):
+        if i in bad:
+            continue
+        k_pool[slots[i], :, positions[i], :] = k_rows[i]
+        v_pool[slots[i], :, positions[i], :] = v_rows[i]
+    # Steps 3-5: attention of every sequence that is not finished
+    for i in range(M):
+        if done[i]:
+            continue
+        if i in bad:
+            out[i] = np.nan
+            continue
+        out[i] = attend_seq(q[i], k_pool[slots[i]], v_pool[slots[i]], int(positions[i]) + 1)
+    return bad

@@ -321,3 +321,103 @@ def test_scatter_skips_out_of_range_positions():
     assert oracle.kv_scatter(kr, vr, pos, Kc, Vc) == 2
     assert np.array_equal(Kc[:2], Kc0[:2]) and np.array_equal(Vc[:2], Vc0[:2])
     assert np.array_equal(Kc[2, :, 5], kr[2]) and np.array_equal(Vc[2, :, 5], vr[2])
+
+
+# ---------------------------------------------------------------- pool slots and finished sequences
+def _slot_case(M=5, S=8, Hkv=2, G=2, D=16, Lmax=12, seed=41):
+    rng = np.random.default_rng(seed)
+    H = Hkv * G
+    q = rng.standard_normal((M, H, D)).astype(np.float32)
+    k_rows = rng.standard_normal((M, Hkv, D)).astype(np.float32)
+    v_rows = rng.standard_normal((M, Hkv, D)).astype(np.float32)
+    k_pool = rng.standard_normal((S, Hkv, Lmax, D)).astype(np.float32)
+    v_pool = rng.standard_normal((S, Hkv, Lmax, D)).astype(np.float32)
+    pos = rng.integers(0, Lmax, M).astype(np.int32)
+    slots = rng.permutation(S)[:M].astype(np.int32)
+    return q, k_rows, v_rows, pos, slots, k_pool, v_pool
+
+
+def test_slots_identity_reduces_to_scatter_then_decode():
+    """slot i for sequence i and nothing finished is the plain step (pinned above)."""
+    q, kr, vr, pos, _, kp, vp = _slot_case(S=5)
+    kc, vc = kp.copy(), vp.copy()
+    assert oracle.kv_scatter(kr, vr, pos, kc, vc) == 0
+    want = oracle.decode(q, kc, vc, pos)
+    out = np.zeros_like(q)
+    assert oracle.decode_step_slots(q, kr, vr, pos, None, None, kp, vp, out) == []
+    assert np.array_equal(out, want)
+    assert np.array_equal(kp, kc) and np.array_equal(vp, vc)
+
+
+def test_slots_follow_the_sequence_not_its_index():
+    """Relabelling the pool (pool'[perm[s]] = pool[s], slot'_i = perm[slot_i])
+    changes neither the outputs nor what each sequence's slot holds."""
+    q, kr, vr, pos, slots, kp, vp = _slot_case()
+    out1 = np.zeros_like(q)
+    kp1, vp1 = kp.copy(), vp.copy()
+    oracle.decode_step_slots(q, kr, vr, pos, slots, None, kp1, vp1, out1)
+    perm = np.random.default_rng(3).permutation(kp.shape[0])
+    kp2, vp2 = np.empty_like(kp), np.empty_like(vp)
+    kp2[perm], vp2[perm] = kp, vp
+    out2 = np.zeros_like(q)
+    oracle.decode_step_slots(q, kr, vr, pos, perm[slots].astype(np.int32), None, kp2, vp2, out2)
+    assert np.array_equal(out1, out2)
+    assert np.array_equal(kp2[perm], kp1) and np.array_equal(vp2[perm], vp1)
+    # and each sequence attends its own slot's rows: a slot-i-for-i answer differs
+    out3 = np.zeros_like(q)
+    oracle.decode_step_slots(q, kr, vr, pos, None, None, kp.copy(), vp.copy(), out3)
+    assert not np.array_equal(out1, out3)
+
+
+def test_slot_scatter_writes_only_the_position_rows_of_each_slot():
+    q, kr, vr, pos, slots, kp, vp = _slot_case()
+    want_k, want_v = kp.copy(), vp.copy()
+    want_k[slots, :, pos, :] = kr
+    want_v[slots, :, pos, :] = vr
+    oracle.decode_step_slots(q, kr, vr, pos, slots, None, kp, vp, np.zeros_like(q))
+    assert np.array_equal(kp, want_k) and np.array_equal(vp, want_v)
+
+
+def test_finished_sequences_keep_their_output_and_still_scatter():
+    q, kr, vr, pos, slots, kp, vp = _slot_case()
+    done = np.array([0, 1, 0, 1, 0], np.uint8)
+    before = np.random.default_rng(9).standard_normal(q.shape).astype(np.float32)
+    out = before.copy()
+    kp0, vp0 = kp.copy(), vp.copy()
+    oracle.decode_step_slots(q, kr, vr, pos, slots, done, kp, vp, out)
+    for i in range(len(done)):
+        if done[i]:
+            assert np.array_equal(out[i], before[i])
+        else:
+            assert not np.array_equal(out[i], before[i])
+        assert np.array_equal(kp[slots[i], :, pos[i]], kr[i])  # scattered either way
+    # the live sequences equal a run without the finished ones
+    live = np.flatnonzero(done == 0)
+    out_live = np.zeros((len(live),) + q.shape[1:], np.float32)
+    oracle.decode_step_slots(q[live], kr[live], vr[live], pos[live], slots[live], None,
+                             kp0, vp0, out_live)
+    assert np.array_equal(out[live], out_live)
+
+
+def test_bad_slot_or_position_is_skipped_and_nan():
+    q, kr, vr, pos, slots, kp, vp = _slot_case()
+    slots = slots.copy()
+    pos = pos.copy()
+    slots[1] = kp.shape[0]      # one past the pool
+    slots[2] = -1
+    pos[3] = kp.shape[2]        # one past Lmax
+    done = np.array([0, 0, 1, 0, 0], np.uint8)
+    kp0, vp0 = kp.copy(), vp.copy()
+    out = np.zeros_like(q)
+    bad = oracle.decode_step_slots(q, kr, vr, pos, slots, done, kp, vp, out)
+    assert bad == [1, 2, 3]
+    assert np.all(np.isnan(out[1])) and np.all(np.isnan(out[3]))
+    assert np.array_equal(out[2], np.zeros_like(out[2]))  # finished: untouched
+    for i in (0, 4):
+        assert np.all(np.isfinite(out[i]))
+    touched = {(int(slots[i]), int(pos[i])) for i in (0, 4)}
+    for s in range(kp.shape[0]):
+        for r in range(kp.shape[2]):
+            same = np.array_equal(kp[s, :, r], kp0[s, :, r]) and \
+                np.array_equal(vp[s, :, r], vp0[s, :, r])
+            assert same == ((s, r) not in touched)
