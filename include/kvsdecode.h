@@ -63,7 +63,8 @@ typedef enum kvs_status {
   KVS_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required */
   KVS_ERR_LAUNCH = 6,      /* CUDA reported a launch or device-query error */
   KVS_ERR_POSITION = 7,    /* device: a position outside [0, max_len) */
-  KVS_ERR_TIMEOUT = 8      /* device: a bounded pipeline wait expired */
+  KVS_ERR_TIMEOUT = 8,     /* device: a bounded pipeline wait expired */
+  KVS_ERR_SLOT = 9         /* device: a cache slot outside [0, num_slots) */
 } kvs_status;
 
 /* A cudaStream_t, passed as an opaque pointer so this header needs no CUDA
@@ -179,6 +180,43 @@ int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
                     float *out, int M, int num_heads, int num_kv_heads,
                     int head_dim, int max_len, int chunk_size, void *workspace,
                     size_t workspace_bytes, int *d_status, kvs_stream_t stream);
+
+/*
+ * kvs_decode_step_slots -- kvs_decode_step for a serving batch whose
+ * sequences live in arbitrary slots of a cache pool, some of them finished
+ * (the pages' "Step 2: Build pointer arrays": a per-sequence cache pointer
+ * for non-contiguous slots and mid-batch joins, and PMAT-076: a finished
+ * slot gets seq_len 0 so the attention kernels skip it).
+ *
+ *   k_pool, v_pool  in/out [num_slots][Hkv][Lmax][D] float32, device,
+ *                   16-byte aligned: the cache pool
+ *   slots           in  [M] int32, device, or NULL (sequence i uses slot i;
+ *                   then num_slots >= M): the pool slot of each sequence.
+ *                   Slots are indices, so the kernels can check them: one
+ *                   outside [0, num_slots) is KVS_ERR_SLOT via d_status, and
+ *                   that sequence is neither scattered nor attended (its out
+ *                   rows are NaN unless it is finished).  Two sequences must
+ *                   not share a slot (they would race).
+ *   done            in  [M] uint8, device, or NULL (none finished): nonzero
+ *                   marks a finished sequence.  As on the pages, its new
+ *                   row is still scattered, but no attention runs for it and
+ *                   its out rows are left exactly as they were.
+ *   k_rows, v_rows  in  [M][Hkv][D], or both NULL: attention only, no scatter
+ *   q, out, positions, chunk_size, workspace, d_status, stream: as
+ *   kvs_decode_step (one workspace of kvs_flash_decode_workspace_bytes for
+ *   M sequences; the pool size does not change it).
+ * Errors: DIMS (also num_slots < 1, or slots NULL with num_slots < M), NULL
+ * (one of k_rows / v_rows NULL), ALIGN, UNSUPPORTED, WORKSPACE, LAUNCH on the
+ * host; POSITION, SLOT, TIMEOUT via d_status.
+ */
+int kvs_decode_step_slots(const float *q, const float *k_rows,
+                          const float *v_rows, const int32_t *positions,
+                          const int32_t *slots, const uint8_t *done,
+                          float *k_pool, float *v_pool, int num_slots,
+                          float *out, int M, int num_heads, int num_kv_heads,
+                          int head_dim, int max_len, int chunk_size,
+                          void *workspace, size_t workspace_bytes,
+                          int *d_status, kvs_stream_t stream);
 
 /*
  * CUDA graph of a whole multi-layer decode step (the pages' graphed decode:

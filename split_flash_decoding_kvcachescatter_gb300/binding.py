@@ -27,12 +27,14 @@ KVS_ERR_WORKSPACE = 5
 KVS_ERR_LAUNCH = 6
 KVS_ERR_POSITION = 7
 KVS_ERR_TIMEOUT = 8
+KVS_ERR_SLOT = 9
 
 # Every symbol include/kvsdecode.h declares.
 EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspace_bytes",
            "kvs_flash_decode", "kvs_decode_step", "kvs_strerror", "kvs_flash_decode_static",
            "kvs_step_graph_create", "kvs_step_graph_launch", "kvs_step_graph_destroy",
-           "kvs_set_schedule", "kvs_get_schedule", "kvs_schedule_for", "kvs_prepare")
+           "kvs_set_schedule", "kvs_get_schedule", "kvs_schedule_for", "kvs_prepare",
+           "kvs_decode_step_slots")
 
 # kvs_schedule values (kernel schedule of the attention entry points)
 KVS_SCHEDULE_AUTO = 0
@@ -88,6 +90,9 @@ def lib() -> ctypes.CDLL:
             L.kvs_step_graph_launch.argtypes = [_P, _P]
             L.kvs_step_graph_destroy.restype = _I
             L.kvs_step_graph_destroy.argtypes = [_P]
+            L.kvs_decode_step_slots.restype = _I
+            L.kvs_decode_step_slots.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I,
+                                                _I, _I, _I, _I, _P, _SZ, _P, _P]
             L.kvs_set_schedule.restype = _I
             L.kvs_set_schedule.argtypes = [_I]
             L.kvs_get_schedule.restype = _I
@@ -236,6 +241,43 @@ def kvs_decode_step(q, k_rows, v_rows, positions, k_cache, v_cache, out, chunk_s
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                _status_ptr(d_status), _stream(stream))
     _check(rc, "kvs_decode_step")
+
+
+def kvs_decode_step_slots(q, k_rows, v_rows, positions, slots, done, k_pool, v_pool, out,
+                          chunk_size=0, workspace=None, d_status=None, stream=None):
+    """Decode step over a cache pool [S, Hkv, Lmax, D]: sequence i uses slot
+    slots[i] (int32 [M], or None for slot i); done (uint8 [M] or None) marks
+    finished sequences, which are scattered but not attended (their out rows
+    are left as they are).  k_rows and v_rows both None: attention only."""
+    M, H, D = q.shape
+    S, Hkv, Lmax, D2 = k_pool.shape
+    if D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != (M, H, D):
+        raise ValueError("kvs_decode_step_slots: inconsistent shapes")
+    if workspace is None:
+        raise ValueError("kvs_decode_step_slots: pass a workspace (see binding.workspace)")
+    if (k_rows is None) != (v_rows is None):
+        raise ValueError("kvs_decode_step_slots: pass both k_rows and v_rows, or neither")
+    kr = 0 if k_rows is None else _f32(k_rows, "k_rows", 3)
+    vr = 0 if v_rows is None else _f32(v_rows, "v_rows", 3)
+    if k_rows is not None and (tuple(k_rows.shape) != (M, Hkv, D) or
+                               tuple(v_rows.shape) != (M, Hkv, D)):
+        raise ValueError("kvs_decode_step_slots: k_rows / v_rows must be [M, Hkv, D]")
+    sl = 0 if slots is None else _i32(slots, "slots")
+    if slots is not None and slots.numel() != M:
+        raise ValueError("kvs_decode_step_slots: slots must have M entries")
+    dn = 0
+    if done is not None:
+        if not (done.is_cuda and done.dtype == torch.uint8 and done.is_contiguous() and
+                done.numel() == M):
+            raise TypeError("done: need a contiguous uint8 CUDA vector of M entries")
+        dn = done.data_ptr()
+    rc = lib().kvs_decode_step_slots(_f32(q, "q", 3), kr, vr, _i32(positions, "positions"), sl,
+                                     dn, _f32(k_pool, "k_pool", 4), _f32(v_pool, "v_pool", 4), S,
+                                     _f32(out, "out", 3), M, H, Hkv, D, Lmax, int(chunk_size),
+                                     workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(),
+                                     _status_ptr(d_status), _stream(stream))
+    _check(rc, "kvs_decode_step_slots")
 
 
 def kvs_flash_decode_static(q, k_cache, v_cache, positions, out, chunk_size=0, d_status=None,

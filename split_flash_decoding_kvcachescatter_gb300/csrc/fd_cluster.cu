@@ -82,10 +82,9 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 
 template <int D, int G>
 __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::MINB)
-    fd_cluster_kernel(const float *__restrict__ q, float *k_cache, float *v_cache,
-                      const int32_t *__restrict__ positions, const float *__restrict__ k_rows,
-                      const float *__restrict__ v_rows, float *__restrict__ out, int Hkv,
-                      int max_len, float qscale, int *d_status) {
+    fd_cluster_kernel(const float *__restrict__ q, float *k_cache, float *v_cache, SeqMap sm,
+                      const float *__restrict__ k_rows, const float *__restrict__ v_rows,
+                      float *__restrict__ out, int Hkv, float qscale, int *d_status) {
   using C = ClusterGeo<D, G>;
   extern __shared__ __align__(128) unsigned char smem[];
   StageDesc *desc = reinterpret_cast<StageDesc *>(smem + C::OFF_DESC);
@@ -110,25 +109,14 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   const bool scatter = (k_rows != nullptr);
 
   grid_dependency_wait();
-  const int p = __ldg(positions + i);
-  if (p < 0 || p >= max_len) {  // the whole cluster leaves here, before any cluster barrier
-    if (rank == 0) {
-      const float nan = __int_as_float(0x7fc00000);
-      float4 *o4 = reinterpret_cast<float4 *>(out) + ((size_t)i * H + (size_t)g * G) * (D / 4);
-      for (int e = threadIdx.x; e < G * (D / 4); e += C::THREADS)
-        o4[e] = make_float4(nan, nan, nan, nan);
-      if (threadIdx.x == 0) record_status(d_status, KVS_ERR_POSITION);
-    }
-    return;
-  }
-  const int L = p + 1;
-  const int r0 = (int)((long long)L * rank / ncl);
-  const int r1 = (int)((long long)L * (rank + 1) / ncl);
-
-  // ---- Step 1, scatter: the block holding row p writes the new rows ----
-  if (scatter && rank == (uint32_t)(ncl - 1)) {
+  const int err = sm.error(i);
+  const bool finished = sm.finished(i);
+  const int p = __ldg(sm.pos + i);
+  // ---- Step 1, scatter: the block holding row p writes the new rows (a
+  //      finished sequence too; none for a bad position or slot) ----
+  if (scatter && err == KVS_OK && rank == (uint32_t)(ncl - 1)) {
     constexpr int D4 = D / 4;
-    const size_t dst = (((size_t)i * Hkv + g) * max_len + p) * D4;
+    const size_t dst = sm.row_index(i, g, p) * D4;
     const size_t src = ((size_t)i * Hkv + g) * D4;
     for (int e = threadIdx.x; e < 2 * D4; e += C::THREADS) {
       if (e < D4)
@@ -139,6 +127,21 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
             __ldg(reinterpret_cast<const float4 *>(v_rows) + src + e - D4);
     }
   }
+  if (err != KVS_OK || finished) {  // the whole cluster leaves here, before any cluster barrier
+    if (err != KVS_OK && rank == 0) {
+      if (!finished) {  // a finished sequence's output is left as it is
+        const float nan = __int_as_float(0x7fc00000);
+        float4 *o4 = reinterpret_cast<float4 *>(out) + ((size_t)i * H + (size_t)g * G) * (D / 4);
+        for (int e = threadIdx.x; e < G * (D / 4); e += C::THREADS)
+          o4[e] = make_float4(nan, nan, nan, nan);
+      }
+      if (threadIdx.x == 0) record_status(d_status, err);
+    }
+    return;
+  }
+  const int L = p + 1;
+  const int r0 = (int)((long long)L * rank / ncl);
+  const int r1 = (int)((long long)L * (rank + 1) / ncl);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::S; ++s) {
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       const uint64_t pol_stream = policy_evict_first();
       uint32_t k = 0;
       int ok = 1;
-      const size_t head_base = ((size_t)i * Hkv + g) * (size_t)max_len;
+      const size_t head_base = sm.row_index(i, g, 0);
       const size_t row_src = ((size_t)i * Hkv + g) * D;  // new row of (i, g)
       for (int rs = r0; rs < r1 && ok; rs += C::T, ++k) {
         const uint32_t s = k % C::S;
@@ -366,9 +369,10 @@ int current_device() {
 }
 
 template <int D, int G>
-int launch_cluster_impl(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+int launch_cluster_impl(const float *q, float *k_cache, float *v_cache, const SeqArgs &seqs,
                         const float *k_rows, const float *v_rows, float *out, int M, int Hkv,
-                        int max_len, int *d_status, cudaStream_t stream) {
+                        int *d_status, cudaStream_t stream) {
+  const int max_len = seqs.max_len;
   using C = ClusterGeo<D, G>;
   const int dev = current_device();
   if (dev < 0) return KVS_ERR_LAUNCH;
@@ -392,22 +396,21 @@ int launch_cluster_impl(const float *q, float *k_cache, float *v_cache, const in
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const float qscale = (float)(1.4426950408889634074 / std::sqrt((double)D));
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fd_cluster_kernel<D, G>, q, k_cache, v_cache,
-                                           positions, k_rows, v_rows, out, Hkv, max_len, qscale,
-                                           d_status);
+  const SeqMap sm{seqs.positions, seqs.slots, seqs.done, max_len, seqs.num_slots, Hkv};
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fd_cluster_kernel<D, G>, q, k_cache, v_cache, sm,
+                                           k_rows, v_rows, out, Hkv, qscale, d_status);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
 template <int D>
 int cluster_dispatch(int G, const float *q, float *k_cache, float *v_cache,
-                     const int32_t *positions, const float *k_rows, const float *v_rows,
-                     float *out, int M, int Hkv, int max_len, int *d_status,
-                     cudaStream_t stream) {
+                     const SeqArgs &seqs, const float *k_rows, const float *v_rows,
+                     float *out, int M, int Hkv, int *d_status, cudaStream_t stream) {
   switch (G) {
 #define KVS_CASE(g)                                                                            \
   case g:                                                                                      \
-    return launch_cluster_impl<D, g>(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, \
-                                     Hkv, max_len, d_status, stream);
+    return launch_cluster_impl<D, g>(q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, Hkv, \
+                                     d_status, stream);
     KVS_CASE(1)
     KVS_CASE(2)
     KVS_CASE(3)
@@ -480,16 +483,16 @@ int cluster_auto_ok(int M, int H, int Hkv, int D, int max_len) {
   return pairs <= ci->active[k] && slice_bytes <= kClusterAutoSliceBytes;
 }
 
-int launch_fd_cluster(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+int launch_fd_cluster(const float *q, float *k_cache, float *v_cache, const SeqArgs &seqs,
                       const float *k_rows, const float *v_rows, float *out, int M, int H,
-                      int Hkv, int D, int max_len, int *d_status, cudaStream_t stream) {
+                      int Hkv, int D, int *d_status, cudaStream_t stream) {
   const int G = H / Hkv;
   if (D == 128)
-    return cluster_dispatch<128>(G, q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv,
-                                 max_len, d_status, stream);
+    return cluster_dispatch<128>(G, q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, Hkv,
+                                 d_status, stream);
   if (D == 64)
-    return cluster_dispatch<64>(G, q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv,
-                                max_len, d_status, stream);
+    return cluster_dispatch<64>(G, q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, Hkv,
+                                d_status, stream);
   return KVS_ERR_UNSUPPORTED;
 }
 

@@ -14,6 +14,7 @@
 #include <cstdint>
 
 #include "kvs_device.cuh"
+#include "kvsdecode.h"
 
 namespace kvs {
 namespace {
@@ -133,6 +134,50 @@ __device__ __forceinline__ float butterfly_sum(float (&v)[NS], int li) {
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
+
+// ---------------------------------------------------------------------------
+// Where each sequence's cache lives and how many rows it attends.
+//   pos[i]   position of sequence i: it attends rows 0..pos[i]
+//   slot[i]  its slot in the cache pool [num_slots][Hkv][max_len][D]
+//            (null: slot i)
+//   done[i]  nonzero: finished -- scattered, but not attended (null: none)
+// ---------------------------------------------------------------------------
+struct SeqMap {
+  const int32_t *pos;
+  const int32_t *slot;
+  const uint8_t *done;
+  int max_len;
+  int num_slots;
+  int Hkv;
+
+  __device__ __forceinline__ int slot_of(int i) const { return slot ? __ldg(slot + i) : i; }
+  __device__ __forceinline__ bool finished(int i) const { return done && __ldg(done + i) != 0; }
+  // KVS_OK, or why sequence i can be neither scattered nor attended
+  __device__ __forceinline__ int error(int i) const {
+    const int p = __ldg(pos + i);
+    if (p < 0 || p >= max_len) return KVS_ERR_POSITION;
+    if (slot) {
+      const int s = __ldg(slot + i);
+      if (s < 0 || s >= num_slots) return KVS_ERR_SLOT;
+    }
+    return KVS_OK;
+  }
+  // rows attended by sequence i (0: finished, or a bad position or slot)
+  __device__ __forceinline__ int len(int i) const {
+    if (finished(i)) return 0;
+    const int p = __ldg(pos + i);
+    if (p < 0 || p >= max_len) return 0;
+    if (slot) {
+      const int s = __ldg(slot + i);
+      if (s < 0 || s >= num_slots) return 0;
+    }
+    return p + 1;
+  }
+  // index of row r of kv head g of sequence i's cache, in rows of D floats
+  __device__ __forceinline__ size_t row_index(int i, int g, int r) const {
+    return ((size_t)slot_of(i) * Hkv + g) * (size_t)max_len + r;
+  }
+};
 
 // ---------------------------------------------------------------------------
 // One consumer warp's view of the stage ring (TileLane) and its running

@@ -76,11 +76,6 @@ namespace {
 // each (i, g) adds to the balanced split (40 rows at D = 128, 80 at D = 64).
 constexpr int kRunCostBytes = 40960;
 
-// Length attended by sequence i (0 for an out-of-range position).
-__device__ __forceinline__ int seq_len_at(const int32_t *positions, int i, int max_len) {
-  const int p = __ldg(positions + i);
-  return (p >= 0 && p < max_len) ? p + 1 : 0;
-}
 
 // ---------------------------------------------------------------------------
 // Split plan on the device (warp-cooperative; every lane returns the result)
@@ -97,11 +92,11 @@ struct SplitTotals {
   long long units;  // sum_i Hkv * ceil(L_i / chunk)
 };
 
-__device__ SplitTotals warp_split_totals(const int32_t *positions, int M, int Hkv, int max_len,
-                                         int chunk, int cost, int lane) {
+__device__ SplitTotals warp_split_totals(const SeqMap &sm, int M, int Hkv, int chunk, int cost,
+                                         int lane) {
   long long rows = 0, units = 0;
   for (int i = lane; i < M; i += 32) {
-    const int L = seq_len_at(positions, i, max_len);
+    const int L = sm.len(i);
     if (L > 0) rows += (long long)Hkv * (L + cost);
     units += (long long)Hkv * ((L + chunk - 1) / chunk);
   }
@@ -114,11 +109,10 @@ __device__ SplitTotals warp_split_totals(const int32_t *positions, int M, int Hk
 }
 
 // First cost row of sequence i (warp-cooperative).
-__device__ long long warp_seq_row0(int i, const int32_t *positions, int Hkv, int max_len,
-                                   int cost, int lane) {
+__device__ long long warp_seq_row0(int i, const SeqMap &sm, int Hkv, int cost, int lane) {
   long long r = 0;
   for (int j = lane; j < i; j += 32) {
-    const int L = seq_len_at(positions, j, max_len);
+    const int L = sm.len(j);
     if (L > 0) r += (long long)Hkv * (L + cost);
   }
 #pragma unroll
@@ -128,13 +122,13 @@ __device__ long long warp_seq_row0(int i, const int32_t *positions, int Hkv, int
 
 // Global index of the first chunk that starts at or after cost row t;
 // `total_units` if t is past the end.
-__device__ long long warp_first_unit_at_row(long long t, const int32_t *positions, int M,
-                                            int Hkv, int max_len, int chunk, int cost,
-                                            long long total_units, int lane) {
+__device__ long long warp_first_unit_at_row(long long t, const SeqMap &sm, int M, int Hkv,
+                                            int chunk, int cost, long long total_units,
+                                            int lane) {
   long long row_base = 0, unit_base = 0;
   for (int i0 = 0; i0 < M; i0 += 32) {
     const int i = i0 + lane;
-    const int L = (i < M) ? seq_len_at(positions, i, max_len) : 0;
+    const int L = (i < M) ? sm.len(i) : 0;
     const int n = (L + chunk - 1) / chunk;
     const long long rows = (L > 0) ? (long long)Hkv * (L + cost) : 0;
     const long long units = (long long)Hkv * n;
@@ -168,12 +162,12 @@ __device__ long long warp_first_unit_at_row(long long t, const int32_t *position
 }
 
 // (i, g, c) of global chunk index u (< total units).
-__device__ int3 warp_unit_to_igc(long long u, const int32_t *positions, int M, int Hkv,
-                                 int max_len, int chunk, int lane) {
+__device__ int3 warp_unit_to_igc(long long u, const SeqMap &sm, int M, int Hkv, int chunk,
+                                 int lane) {
   long long unit_base = 0;
   for (int i0 = 0; i0 < M; i0 += 32) {
     const int i = i0 + lane;
-    const int L = (i < M) ? seq_len_at(positions, i, max_len) : 0;
+    const int L = (i < M) ? sm.len(i) : 0;
     const int n = (L + chunk - 1) / chunk;
     const long long units = (long long)Hkv * n;
     long long uinc = units;
@@ -251,12 +245,12 @@ struct Run {
 };
 
 __device__ __forceinline__ Run make_run(int i, int g, int c, long long remaining,
-                                        const int32_t *positions, int max_len, int chunk) {
+                                        const SeqMap &sm, int chunk) {
   Run r;
   r.i = i;
   r.g = g;
   r.c = c;
-  r.L = seq_len_at(positions, i, max_len);
+  r.L = sm.len(i);
   r.n = (r.L + chunk - 1) / chunk;
   r.units = (int)min((long long)(r.n - c), remaining);
   return r;
@@ -266,13 +260,12 @@ __device__ __forceinline__ Run make_run(int i, int g, int c, long long remaining
 // sequence, else the next sequence that has rows.  Never reads past M-1; if
 // the list ended (it cannot when the piece came from the same positions) the
 // run is empty (units = 0), which ends the loops.
-__device__ __forceinline__ Run next_run(const Run &r, long long remaining,
-                                        const int32_t *positions, int M, int Hkv,
-                                        int max_len, int chunk) {
-  if (r.g + 1 < Hkv) return make_run(r.i, r.g + 1, 0, remaining, positions, max_len, chunk);
+__device__ __forceinline__ Run next_run(const Run &r, long long remaining, const SeqMap &sm,
+                                        int M, int Hkv, int chunk) {
+  if (r.g + 1 < Hkv) return make_run(r.i, r.g + 1, 0, remaining, sm, chunk);
   for (int i = r.i + 1; i < M; ++i) {
-    if (seq_len_at(positions, i, max_len) > 0)
-      return make_run(i, 0, 0, remaining, positions, max_len, chunk);
+    if (sm.len(i) > 0)
+      return make_run(i, 0, 0, remaining, sm, chunk);
   }
   Run e = r;
   e.units = 0;
@@ -406,10 +399,10 @@ __device__ __noinline__ void merge_runs(const WsView &ws, float *out, int i, int
 // ---------------------------------------------------------------------------
 template <int D, int G>
 __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
-    fd_step_kernel(const float *__restrict__ q, float *k_cache, float *v_cache,
-                   const int32_t *__restrict__ positions, const float *__restrict__ k_rows,
-                   const float *__restrict__ v_rows, float *__restrict__ out, WsView ws, int M,
-                   int Hkv, int max_len, int chunk, float qscale, unsigned tag, int *d_status) {
+    fd_step_kernel(const float *__restrict__ q, float *k_cache, float *v_cache, SeqMap sm,
+                   const float *__restrict__ k_rows, const float *__restrict__ v_rows,
+                   float *__restrict__ out, WsView ws, int M, int Hkv, int chunk, float qscale,
+                   unsigned tag, int *d_status) {
   using C = Geo<D, G>;
   constexpr int kCost = kRunCostBytes / (8 * D);  // cost rows per (i, g)
   extern __shared__ __align__(128) unsigned char smem[];
@@ -433,14 +426,18 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   // still read.
   grid_dependency_wait();
 
-  // ---- sequences with a position outside [0, max_len): NaN rows, status ----
+  // ---- sequences with a bad position or slot: status, and NaN rows unless
+  //      finished (a finished sequence's output is left as it is) ----
   for (int i = blockIdx.x; i < M; i += P) {
-    if (seq_len_at(positions, i, max_len) == 0) {
-      const float nan = __int_as_float(0x7fc00000);
-      float4 *o4 = reinterpret_cast<float4 *>(out) + (size_t)i * H * (D / 4);
-      for (int e = threadIdx.x; e < H * (D / 4); e += C::THREADS)
-        o4[e] = make_float4(nan, nan, nan, nan);
-      if (threadIdx.x == 0) record_status(d_status, KVS_ERR_POSITION);
+    const int err = sm.error(i);
+    if (err != KVS_OK) {
+      if (!sm.finished(i)) {
+        const float nan = __int_as_float(0x7fc00000);
+        float4 *o4 = reinterpret_cast<float4 *>(out) + (size_t)i * H * (D / 4);
+        for (int e = threadIdx.x; e < H * (D / 4); e += C::THREADS)
+          o4[e] = make_float4(nan, nan, nan, nan);
+      }
+      if (threadIdx.x == 0) record_status(d_status, err);
     }
   }
   // ---- Step 1, scatter: this block's share of the new rows (float4 each) ----
@@ -452,9 +449,10 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       const bool is_v = e >= per_cache;
       const long long f = is_v ? e - per_cache : e;
       const long long ig = f / D4;
-      const int p = __ldg(positions + ig / Hkv);
-      if (p < 0 || p >= max_len) continue;
-      const size_t dst = ((size_t)ig * max_len + p) * D4 + (f - ig * D4);
+      const int i = (int)(ig / Hkv);
+      if (sm.error(i) != KVS_OK) continue;
+      const int p = __ldg(sm.pos + i);
+      const size_t dst = sm.row_index(i, (int)(ig - (long long)i * Hkv), p) * D4 + (f - ig * D4);
       if (is_v)
         reinterpret_cast<float4 *>(v_cache)[dst] = __ldg(reinterpret_cast<const float4 *>(v_rows) + f);
       else
@@ -463,7 +461,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   }
 
   if (warp == 0) {
-    const SplitTotals tot = warp_split_totals(positions, M, Hkv, max_len, chunk, kCost, lane);
+    const SplitTotals tot = warp_split_totals(sm, M, Hkv, chunk, kCost, lane);
     if (lane == 0) {
       info[0] = tot.rows;
       info[1] = tot.units;
@@ -491,23 +489,22 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     uint32_t k = 0;
     int ok = 1;
     const int b = blockIdx.x;
-    const long long ub = warp_first_unit_at_row(column_start_row(R, P, b), positions, M, Hkv,
-                                                max_len, chunk, kCost, U, lane);
+    const long long ub =
+        warp_first_unit_at_row(column_start_row(R, P, b), sm, M, Hkv, chunk, kCost, U, lane);
     const long long ue = (b + 1 == P) ? U
                                       : warp_first_unit_at_row(column_start_row(R, P, b + 1),
-                                                               positions, M, Hkv, max_len, chunk,
-                                                               kCost, U, lane);
+                                                               sm, M, Hkv, chunk, kCost, U, lane);
     if (ub < ue) {
-      const int3 igc = warp_unit_to_igc(ub, positions, M, Hkv, max_len, chunk, lane);
-      long long seq_row0 = warp_seq_row0(igc.x, positions, Hkv, max_len, kCost, lane);
+      const int3 igc = warp_unit_to_igc(ub, sm, M, Hkv, chunk, lane);
+      long long seq_row0 = warp_seq_row0(igc.x, sm, Hkv, kCost, lane);
       const long long block_slot = (long long)M * Hkv + b;
       long long remaining = ue - ub;
-      Run run = make_run(igc.x, igc.y, igc.z, remaining, positions, max_len, chunk);
+      Run run = make_run(igc.x, igc.y, igc.z, remaining, sm, chunk);
       int run_seq = run.i;
       while (ok && remaining > 0 && run.units > 0) {
         if (run.i != run_seq) {  // moved to a later sequence: advance its first row
           for (int j = run_seq; j < run.i; ++j) {
-            const int Lj = seq_len_at(positions, j, max_len);
+            const int Lj = sm.len(j);
             if (Lj > 0) seq_row0 += (long long)Hkv * (Lj + kCost);
           }
           run_seq = run.i;
@@ -515,7 +512,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
         const long long slot = (run.c == 0) ? (long long)run.i * Hkv + run.g : block_slot;
         const int r0 = run.c * chunk;
         const int r1 = (int)min((long long)(run.c + run.units) * chunk, (long long)run.L);
-        const size_t head_base = ((size_t)run.i * Hkv + run.g) * (size_t)max_len;
+        const size_t head_base = sm.row_index(run.i, run.g, 0);
         const size_t row_src = ((size_t)run.i * Hkv + run.g) * D;  // new row of (i, g)
         for (int rs = r0, st = 0; rs < r1 && ok; rs += C::T, ++st, ++k) {
           if (lane == 0) {
@@ -558,7 +555,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
         }
         remaining -= run.units;
         if (ok && remaining > 0)
-          run = next_run(run, remaining, positions, M, Hkv, max_len, chunk);
+          run = next_run(run, remaining, sm, M, Hkv, chunk);
       }
     }
     if (lane == 0) {
@@ -725,9 +722,10 @@ unsigned next_call_tag() {
 }
 
 template <int D, int G>
-int launch_step_impl(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+int launch_step_impl(const float *q, float *k_cache, float *v_cache, const SeqArgs &seqs,
                      const float *k_rows, const float *v_rows, float *out, int M, int Hkv,
-                     int max_len, int chunk, void *workspace, int *d_status, cudaStream_t stream) {
+                     int chunk, void *workspace, int *d_status, cudaStream_t stream) {
+  const int max_len = seqs.max_len;
   using C = Geo<D, G>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVS_ERR_LAUNCH;
@@ -741,22 +739,24 @@ int launch_step_impl(const float *q, float *k_cache, float *v_cache, const int32
   const WsView ws = workspace_view(workspace, M, Hkv, G, D);
   const float qscale = (float)(1.4426950408889634074 / std::sqrt((double)D));
   const cudaError_t e = launch_pdl(fd_step_kernel<D, G>, dim3(grid), dim3(C::THREADS),
-                                   C::SMEM_BYTES, stream, q, k_cache, v_cache, positions, k_rows,
-                                   v_rows, out, ws, M, Hkv, max_len, chunk, qscale,
-                                   next_call_tag(), d_status);
+                                   C::SMEM_BYTES, stream, q, k_cache, v_cache,
+                                   SeqMap{seqs.positions, seqs.slots, seqs.done, max_len,
+                                          seqs.num_slots, Hkv},
+                                   k_rows, v_rows, out, ws, M, Hkv, chunk, qscale, next_call_tag(),
+                                   d_status);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
 template <int D>
 int dispatch_group(int G, const float *q, float *k_cache, float *v_cache,
-                   const int32_t *positions, const float *k_rows, const float *v_rows,
-                   float *out, int M, int Hkv, int max_len, int chunk, void *workspace,
+                   const SeqArgs &seqs, const float *k_rows, const float *v_rows,
+                   float *out, int M, int Hkv, int chunk, void *workspace,
                    int *d_status, cudaStream_t stream) {
   switch (G) {
 #define KVS_CASE(g)                                                                           \
   case g:                                                                                     \
-    return launch_step_impl<D, g>(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv, \
-                                  max_len, chunk, workspace, d_status, stream);
+    return launch_step_impl<D, g>(q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, Hkv, chunk, \
+                                  workspace, d_status, stream);
     KVS_CASE(1)
     KVS_CASE(2)
     KVS_CASE(3)
@@ -807,17 +807,16 @@ int prepare_step_kernel(int H, int Hkv, int D) {
   return (bps > 0 && device_sm_count() > 0) ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
-int launch_fd_step(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+int launch_fd_step(const float *q, float *k_cache, float *v_cache, const SeqArgs &seqs,
                    const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
-                   int D, int max_len, int chunk, void *workspace, int *d_status,
-                   cudaStream_t stream) {
+                   int D, int chunk, void *workspace, int *d_status, cudaStream_t stream) {
   const int G = H / Hkv;
   if (D == 128)
-    return dispatch_group<128>(G, q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv,
-                               max_len, chunk, workspace, d_status, stream);
+    return dispatch_group<128>(G, q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, Hkv, chunk,
+                               workspace, d_status, stream);
   if (D == 64)
-    return dispatch_group<64>(G, q, k_cache, v_cache, positions, k_rows, v_rows, out, M, Hkv,
-                              max_len, chunk, workspace, d_status, stream);
+    return dispatch_group<64>(G, q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, Hkv, chunk,
+                              workspace, d_status, stream);
   return KVS_ERR_UNSUPPORTED;
 }
 

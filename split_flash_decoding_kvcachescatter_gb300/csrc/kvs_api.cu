@@ -46,15 +46,14 @@ bool use_cluster(int M, int H, int Hkv, int D, int max_len) {
 
 // The attention launch of kvs_flash_decode (k_rows == nullptr) and
 // kvs_decode_step, on the schedule in force.
-int launch_attention(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+int launch_attention(const float *q, float *k_cache, float *v_cache, const kvs::SeqArgs &seqs,
                      const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
-                     int D, int max_len, int chunk, void *workspace, int *d_status,
-                     cudaStream_t stream) {
-  if (use_cluster(M, H, Hkv, D, max_len))
-    return kvs::launch_fd_cluster(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, H, Hkv,
-                                  D, max_len, d_status, stream);
-  return kvs::launch_fd_step(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, H, Hkv, D,
-                             max_len, chunk, workspace, d_status, stream);
+                     int D, int chunk, void *workspace, int *d_status, cudaStream_t stream) {
+  if (use_cluster(M, H, Hkv, D, seqs.max_len))
+    return kvs::launch_fd_cluster(q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, H, Hkv, D,
+                                  d_status, stream);
+  return kvs::launch_fd_step(q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, H, Hkv, D, chunk,
+                             workspace, d_status, stream);
 }
 
 // chunk_size == 0 -> the library rule on the current device.
@@ -78,6 +77,7 @@ const char *kvs_strerror(int status) {
     case KVS_ERR_LAUNCH: return "CUDA launch or device query failed";
     case KVS_ERR_POSITION: return "a position is outside [0, max_len)";
     case KVS_ERR_TIMEOUT: return "a bounded device pipeline wait expired";
+    case KVS_ERR_SLOT: return "a cache slot is outside [0, num_slots)";
     default: return "unknown kvs status";
   }
 }
@@ -155,10 +155,10 @@ int kvs_flash_decode(const float *q, const float *k_cache, const float *v_cache,
   const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
   if (chunk <= 0) return -chunk;
   // the caches are only read when no new rows are passed
-  return launch_attention(q, const_cast<float *>(k_cache), const_cast<float *>(v_cache),
-                          positions, nullptr, nullptr, out, M, num_heads, num_kv_heads, head_dim,
-                          max_len, chunk, workspace, d_status,
-                          reinterpret_cast<cudaStream_t>(stream));
+  const kvs::SeqArgs seqs{positions, nullptr, nullptr, max_len, M};
+  return launch_attention(q, const_cast<float *>(k_cache), const_cast<float *>(v_cache), seqs,
+                          nullptr, nullptr, out, M, num_heads, num_kv_heads, head_dim, chunk,
+                          workspace, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
@@ -176,8 +176,33 @@ int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
   if (rc != KVS_OK) return rc;
   const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
   if (chunk <= 0) return -chunk;
-  return launch_attention(q, k_cache, v_cache, positions, k_rows, v_rows, out, M, num_heads,
-                          num_kv_heads, head_dim, max_len, chunk, workspace, d_status,
+  const kvs::SeqArgs seqs{positions, nullptr, nullptr, max_len, M};
+  return launch_attention(q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, num_heads,
+                          num_kv_heads, head_dim, chunk, workspace, d_status,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvs_decode_step_slots(const float *q, const float *k_rows, const float *v_rows,
+                          const int32_t *positions, const int32_t *slots, const uint8_t *done,
+                          float *k_pool, float *v_pool, int num_slots, float *out, int M,
+                          int num_heads, int num_kv_heads, int head_dim, int max_len,
+                          int chunk_size, void *workspace, size_t workspace_bytes,
+                          int *d_status, kvs_stream_t stream) {
+  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
+  if (rc != KVS_OK) return rc;
+  if (num_slots < 1 || (!slots && num_slots < M)) return KVS_ERR_DIMS;
+  if (M == 0) return KVS_OK;
+  if ((k_rows == nullptr) != (v_rows == nullptr)) return KVS_ERR_NULL;
+  if (k_rows && (!aligned(k_rows, 16) || !aligned(v_rows, 16))) return KVS_ERR_ALIGN;
+  if (slots && !aligned(slots, 4)) return KVS_ERR_ALIGN;
+  rc = check_attention_buffers(q, k_pool, v_pool, positions, out, M, num_heads, num_kv_heads,
+                               head_dim, workspace, workspace_bytes);
+  if (rc != KVS_OK) return rc;
+  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
+  if (chunk <= 0) return -chunk;
+  const kvs::SeqArgs seqs{positions, slots, done, max_len, num_slots};
+  return launch_attention(q, k_pool, v_pool, seqs, k_rows, v_rows, out, M, num_heads,
+                          num_kv_heads, head_dim, chunk, workspace, d_status,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -73,24 +73,34 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// The sequences of one call: positions, and optionally a cache slot per
+// sequence (slots == nullptr: slot i, num_slots == M) and a finished flag
+// per sequence (done == nullptr: none).  All device pointers.
+struct SeqArgs {
+  const int32_t *positions;
+  const int32_t *slots;
+  const uint8_t *done;
+  int max_len;
+  int num_slots;
+};
+
 int launch_kv_scatter(const float *k_rows, const float *v_rows, const int32_t *positions,
                       float *k_cache, float *v_cache, int M, int Hkv, int D, int max_len,
                       int *d_status, cudaStream_t stream);
 
 // One launch of the step kernel: split-K attention over the caches; with
 // k_rows/v_rows non-null the scatter of those rows is done in the same launch.
-int launch_fd_step(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+int launch_fd_step(const float *q, float *k_cache, float *v_cache, const SeqArgs &seqs,
                    const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
-                   int D, int max_len, int chunk, void *workspace, int *d_status,
-                   cudaStream_t stream);
+                   int D, int chunk, void *workspace, int *d_status, cudaStream_t stream);
 
 // One launch of the cluster kernel (one thread-block cluster per (sequence,
 // kv head), partials merged in distributed shared memory; no workspace).
 // Requires M * Hkv <= kMaxClusterPairs.
 constexpr long long kMaxClusterPairs = 65535;
-int launch_fd_cluster(const float *q, float *k_cache, float *v_cache, const int32_t *positions,
+int launch_fd_cluster(const float *q, float *k_cache, float *v_cache, const SeqArgs &seqs,
                       const float *k_rows, const float *v_rows, float *out, int M, int H, int Hkv,
-                      int D, int max_len, int *d_status, cudaStream_t stream);
+                      int D, int *d_status, cudaStream_t stream);
 
 // Sets the cluster kernel's attributes for (H / Hkv, D) on the current device.
 int prepare_cluster_kernel(int H, int Hkv, int D);

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_strerror_covers_all_codes(L):
-    for code in range(0, 9):
+    for code in range(0, 10):
         s = B.strerror(code)
         assert s and "unknown" not in s
     assert "unknown" in B.strerror(99)
@@ -203,3 +203,34 @@ def test_prepare_validates_before_touching_cuda(L):
     assert L.kvs_prepare(0, 1, 64) == B.KVS_ERR_DIMS
     assert L.kvs_prepare(4, 2, 96) == B.KVS_ERR_UNSUPPORTED
     assert L.kvs_prepare(18, 2, 64) == B.KVS_ERR_UNSUPPORTED
+
+
+def _dss(L, q=A16, kr=A16, vr=A16, pos=A16, slots=A16, done=A16, k=A16, v=A16, S=4, out=A16,
+         M=2, H=4, Hkv=2, D=64, Lmax=16, C=8, ws=A16, wsb=1 << 30):
+    return L.kvs_decode_step_slots(q, kr, vr, pos, slots, done, k, v, S, out, M, H, Hkv, D, Lmax,
+                                   C, ws, wsb, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), B.KVS_ERR_DIMS),
+    (dict(S=0), B.KVS_ERR_DIMS),
+    (dict(slots=None, S=1), B.KVS_ERR_DIMS),       # slot i needs num_slots >= M
+    (dict(H=6, Hkv=4), B.KVS_ERR_DIMS),
+    (dict(D=96), B.KVS_ERR_UNSUPPORTED),
+    (dict(kr=None), B.KVS_ERR_NULL),               # one of the new-row inputs alone
+    (dict(vr=None), B.KVS_ERR_NULL),
+    (dict(q=None), B.KVS_ERR_NULL),
+    (dict(k=None), B.KVS_ERR_NULL),
+    (dict(kr=A16 + 4), B.KVS_ERR_ALIGN),
+    (dict(slots=A16 + 2), B.KVS_ERR_ALIGN),
+    (dict(k=A16 + 8), B.KVS_ERR_ALIGN),
+    (dict(ws=None), B.KVS_ERR_WORKSPACE),
+    (dict(wsb=64), B.KVS_ERR_WORKSPACE),
+])
+def test_decode_step_slots_validation(L, kw, code):
+    assert _dss(L, **kw) == code
+
+
+def test_decode_step_slots_empty_batch_ok(L):
+    assert _dss(L, M=0, q=None, kr=None, vr=None, pos=None, slots=None, done=None, k=None,
+                v=None, out=None, ws=None, wsb=0) == 0

@@ -399,3 +399,112 @@ def test_auto_schedule_picks_by_size():
     finally:
         B.kvs_set_schedule(prev)
 
+
+
+# ---------------------------------------------------------------- pool slots, finished sequences
+def _pool_case(w, S, seed, slots=None, done=None):
+    """Device pool [S][Hkv][Lmax][D] holding sequence i's live rows in slot
+    slots[i] (other slots poisoned), plus the matching numpy arrays."""
+    inp = W.make_inputs(w)
+    t = W.upload(inp, w, DEV)
+    rng = np.random.default_rng(seed)
+    if slots is None:
+        slots = rng.permutation(S)[:w.M].astype(np.int32)
+    if done is None:
+        done = np.zeros(w.M, np.uint8)
+    pool_k = W.poisoned_cache(W.custom(M=S, num_heads=w.num_heads, num_kv_heads=w.num_kv_heads,
+                                       head_dim=w.head_dim, max_len=w.max_len), DEV)
+    pool_v = pool_k.clone()
+    ok = [i for i in range(w.M) if 0 <= slots[i] < S]
+    idx = torch.tensor([int(slots[i]) for i in ok], dtype=torch.long, device=DEV)
+    src = torch.tensor(ok, dtype=torch.long, device=DEV)
+    pool_k[idx] = t["k_cache"][src]
+    pool_v[idx] = t["v_cache"][src]
+    return inp, t, slots, done, pool_k, pool_v
+
+
+def _oracle_pool_step(inp, slots, done, pool_k, pool_v, out_before):
+    kp, vp = pool_k.cpu().numpy().copy(), pool_v.cpu().numpy().copy()
+    out = out_before.copy()
+    bad = oracle.decode_step_slots(inp.q, inp.k_rows, inp.v_rows, inp.positions, slots, done,
+                                   kp, vp, out)
+    return out, kp, vp, bad
+
+
+@pytest.mark.parametrize("D,H,Hkv", [(64, 14, 2), (128, 32, 8), (128, 40, 8)])
+def test_pool_slots_and_finished_sequences(schedule, D, H, Hkv):
+    w = W.custom(M=6, num_heads=H, num_kv_heads=Hkv, head_dim=D, max_len=300,
+                 positions="uniform", seed=101 + D + H)
+    S = 9
+    done = np.array([0, 1, 0, 0, 1, 0], np.uint8)
+    inp, t, slots, done, pk, pv = _pool_case(w, S, seed=5, done=done)
+    before = np.random.default_rng(7).standard_normal((w.M, H, D)).astype(np.float32)
+    ref, kp_ref, vp_ref, bad = _oracle_pool_step(inp, slots, done, pk, pv, before)
+    assert bad == []
+    out = torch.from_numpy(before).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = B.workspace(w.M, H, Hkv, D, w.max_len, 32, device=DEV).fill_(0xFF)
+    B.kvs_decode_step_slots(t["q"], t["k_rows"], t["v_rows"], t["positions"],
+                            torch.from_numpy(slots).to(DEV), torch.from_numpy(done).to(DEV),
+                            pk, pv, out, chunk_size=32, workspace=ws, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.cpu().numpy()
+    live = np.flatnonzero(done == 0)
+    fin = np.flatnonzero(done != 0)
+    gate(got[live], ref[live], where=f"pool slots D={D} G={H // Hkv}")
+    assert np.array_equal(got[fin].view(np.int32), before[fin].view(np.int32))
+    assert np.array_equal(pk.cpu().numpy().view(np.int32), kp_ref.view(np.int32))
+    assert np.array_equal(pv.cpu().numpy().view(np.int32), vp_ref.view(np.int32))
+    # attention only (no new rows) over the scattered pool gives the same bits
+    out2 = torch.from_numpy(before).to(DEV)
+    B.kvs_decode_step_slots(t["q"], None, None, t["positions"], torch.from_numpy(slots).to(DEV),
+                            torch.from_numpy(done).to(DEV), pk, pv, out2, chunk_size=32,
+                            workspace=ws, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(out2.cpu().numpy().view(np.int32), got.view(np.int32))
+    assert np.array_equal(pk.cpu().numpy().view(np.int32), kp_ref.view(np.int32))
+
+
+def test_pool_identity_slots_equal_decode_step(schedule):
+    """slots None and done None is kvs_decode_step, bit for bit."""
+    w = W.custom(M=4, num_heads=8, num_kv_heads=2, head_dim=128, max_len=777, seed=23)
+    inp = W.make_inputs(w)
+    a, b = W.upload(inp, w, DEV), W.upload(inp, w, DEV)
+    ws = B.workspace(w.M, 8, 2, 128, w.max_len, 64, device=DEV)
+    out_a = torch.empty_like(a["q"])
+    out_b = torch.empty_like(b["q"])
+    B.kvs_decode_step(a["q"], a["k_rows"], a["v_rows"], a["positions"], a["k_cache"],
+                      a["v_cache"], out_a, chunk_size=64, workspace=ws)
+    B.kvs_decode_step_slots(b["q"], b["k_rows"], b["v_rows"], b["positions"], None, None,
+                            b["k_cache"], b["v_cache"], out_b, chunk_size=64, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a.view(torch.int32), out_b.view(torch.int32))
+    assert torch.equal(a["k_cache"].view(torch.int32), b["k_cache"].view(torch.int32))
+    assert torch.equal(a["v_cache"].view(torch.int32), b["v_cache"].view(torch.int32))
+
+
+def test_pool_bad_slot_flags_and_skips(schedule):
+    w = W.custom(M=4, num_heads=8, num_kv_heads=2, head_dim=64, max_len=200, seed=29)
+    S = 6
+    slots = np.array([3, 6, 0, -2], np.int32)   # 6 and -2 are outside the pool
+    done = np.array([0, 0, 0, 1], np.uint8)     # the last is finished as well
+    inp, t, slots, done, pk, pv = _pool_case(w, S, seed=1, slots=slots, done=done)
+    before = np.full((w.M, 8, 64), 7.0, np.float32)
+    ref, kp_ref, vp_ref, bad = _oracle_pool_step(inp, slots, done, pk, pv, before)
+    assert bad == [1, 3]
+    out = torch.from_numpy(before).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = B.workspace(w.M, 8, 2, 64, w.max_len, 16, device=DEV)
+    B.kvs_decode_step_slots(t["q"], t["k_rows"], t["v_rows"], t["positions"],
+                            torch.from_numpy(slots).to(DEV), torch.from_numpy(done).to(DEV),
+                            pk, pv, out, chunk_size=16, workspace=ws, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == B.KVS_ERR_SLOT
+    got = out.cpu().numpy()
+    assert np.all(np.isnan(got[1]))
+    assert np.array_equal(got[3], before[3])     # finished: left as it was
+    gate(got[[0, 2]], ref[[0, 2]], where="valid slots beside bad ones")
+    assert np.array_equal(pk.cpu().numpy().view(np.int32), kp_ref.view(np.int32))
+    assert np.array_equal(pv.cpu().numpy().view(np.int32), vp_ref.view(np.int32))
