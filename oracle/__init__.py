@@ -241,3 +241,26 @@ def decode_step_slots(q, k_rows, v_rows, positions, slots, done, k_pool, v_pool,
             continue
         out[i] = attend_seq(q[i], k_pool[slots[i]], v_pool[slots[i]], int(positions[i]) + 1)
     return bad
+
+
+def argmax_rows(logits):
+    """Greedy token of each row of logits [M][V]: the index of the largest
+    value, the smallest such index on ties, NaN entries never chosen (a row
+    with no value above -inf gives index 0).
+
+    Follows realizar 0.8.5, src/cuda/executor/reduces.rs, PAR-062 /
+    PMAT-045 (batched GPU argmax: for each of M logit vectors, the token ID
+    with the maximum logit value).  The pages state no rule for ties or NaN;
+    this is the plain reading (first maximum, NaN is no value).
+    """
+    x = np.asarray(logits, dtype=np.float64)
+    M, V = x.shape
+    out = np.zeros(M, np.int32)
+    for i in range(M):
+        best, arg = -np.inf, 0
+        for j in range(V):
+            v = x[i, j]
+            if v == v and v > best:  # NaN fails both comparisons
+                best, arg = v, j
+        out[i] = arg
+    return out

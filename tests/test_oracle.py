@@ -421,3 +421,33 @@ def test_bad_slot_or_position_is_skipped_and_nan():
             same = np.array_equal(kp[s, :, r], kp0[s, :, r]) and \
                 np.array_equal(vp[s, :, r], vp0[s, :, r])
             assert same == ((s, r) not in touched)
+
+
+# ---------------------------------------------------------------- batched argmax
+def test_argmax_first_maximum_on_ties():
+    x = np.array([[1.0, 3.0, 3.0, 2.0], [5.0, 5.0, 5.0, 5.0], [-1.0, -2.0, -1.0, -3.0]],
+                 np.float32)
+    assert oracle.argmax_rows(x).tolist() == [1, 0, 0]
+
+
+def test_argmax_ignores_nan_and_handles_infinities():
+    nan, inf = np.nan, np.inf
+    x = np.array([[nan, 1.0, nan, 0.5],
+                  [nan, nan, nan, nan],
+                  [-inf, -inf, -inf, -inf],
+                  [0.0, inf, 7.0, inf],
+                  [nan, -inf, -1e30, nan]], np.float32)
+    assert oracle.argmax_rows(x).tolist() == [1, 0, 0, 1, 2]
+
+
+def test_argmax_matches_a_sort_on_random_rows():
+    """Against an independent rule: stable sort by (-value, index)."""
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((6, 3001)).astype(np.float32)
+    x[2, 100] = x[2, 2000] = 50.0          # a tie far apart: the first wins
+    x[4, :] = np.round(x[4, :])            # many ties
+    got = oracle.argmax_rows(x)
+    for i in range(x.shape[0]):
+        order = sorted(range(x.shape[1]), key=lambda j: (-float(x[i, j]), j))
+        assert got[i] == order[0]
+    assert got[2] == 100
