@@ -115,6 +115,38 @@ def ncu_traffic(kernel, workload, chunk):
     return int(e["dram_bytes_per_launch"])
 
 
+VOCAB = 152064  # vocabulary of the pages' batched argmax (PAR-062)
+
+
+def time_argmax(B, torch, M, dev, stream, iters=200):
+    """The batched argmax of the serving step after attention (kvs_argmax):
+    M rows of VOCAB logits, one launch; L2 scrubbed between launches
+    (outside the events).  HBM-bound: M*VOCAB*4 bytes read per launch."""
+    g = torch.Generator(device=dev).manual_seed(1234)
+    logits = torch.randn((M, VOCAB), device=dev, generator=g)
+    ids = torch.empty(M, dtype=torch.int32, device=dev)
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(5):
+        B.kvs_argmax(logits, ids)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for a, b in ev:
+        scrub.zero_()
+        a.record(stream)
+        B.kvs_argmax(logits, ids)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    ok = torch.equal(ids.long(), torch.argmax(logits, dim=1))  # finite data: same first-max rule
+    nbytes = M * VOCAB * 4 + M * 4
+    peak, _ = hbm_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "argmax_cluster_kernel (kvs_argmax)", "M": M, "vocab": VOCAB,
+            "us_per_call": 1e3 * ms, "bytes_per_call": nbytes, "gbs": gbs, "frac": gbs / peak,
+            "l2": "scrubbed between launches", "matches_torch_argmax": bool(ok)}
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled in the background."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -270,6 +302,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--graph", action="store_true",
                     help="launch the whole (multi-layer) step as one captured CUDA graph")
+    ap.add_argument("--no-argmax", action="store_true",
+                    help="skip the batched argmax measurement")
     ap.add_argument("--schedule", default="auto", choices=["auto", "persistent", "cluster"],
                     help="attention kernel (kvs_set_schedule)")
     args = ap.parse_args()
@@ -456,6 +490,7 @@ def main():
         s1.record(stream)
         torch.cuda.synchronize()
         e2e_ms -= s0.elapsed_time(s1) / Ke
+    argmax = time_argmax(B, torch, w.M, dev, stream) if not args.no_argmax else None
     sampler.stop()
     clocks = sampler.summary(wall0, wall1)
 
@@ -521,6 +556,7 @@ def main():
         "gpu_launches": K * nl,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "argmax": argmax,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

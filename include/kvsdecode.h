@@ -299,6 +299,25 @@ int kvs_flash_decode_static(const float *q, const float *k_cache,
                             int *d_status, kvs_stream_t stream);
 
 /*
+ * kvs_argmax -- batched greedy token selection (realizar 0.8.5, reduces.rs,
+ * gpu_argmax PAR-062 / batched_gpu_argmax PMAT-045: the token ID with the
+ * largest logit for each of M logit vectors, computed on the GPU so that
+ * only the IDs need to leave it), in ONE launch for all rows.
+ *
+ *   logits     in   [M][vocab_size] float32, device, 4-byte aligned
+ *                   (16-byte aligned rows are read with 16-byte loads)
+ *   token_ids  out  [M] int32, device
+ * token_ids[m] is the smallest index j with logits[m][j] equal to the row's
+ * largest value; NaN entries are never chosen; a row with no value above
+ * -inf gives 0.  The result is enqueued on `stream`; copy it to the host
+ * with one cudaMemcpyAsync and one synchronisation for the whole batch.
+ * Errors: DIMS (M < 0, vocab_size < 1), NULL, ALIGN, LAUNCH.  M = 0 enqueues
+ * nothing.
+ */
+int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
+               kvs_stream_t stream);
+
+/*
  * Kernel schedule of kvs_flash_decode, kvs_decode_step (and so of the
  * graphs and the static entry point), process-wide:
  *   KVS_SCHEDULE_AUTO        (the default) the cluster kernel for steps

@@ -34,7 +34,7 @@ EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspac
            "kvs_flash_decode", "kvs_decode_step", "kvs_strerror", "kvs_flash_decode_static",
            "kvs_step_graph_create", "kvs_step_graph_launch", "kvs_step_graph_destroy",
            "kvs_set_schedule", "kvs_get_schedule", "kvs_schedule_for", "kvs_prepare",
-           "kvs_decode_step_slots")
+           "kvs_decode_step_slots", "kvs_argmax")
 
 # kvs_schedule values (kernel schedule of the attention entry points)
 KVS_SCHEDULE_AUTO = 0
@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
             L.kvs_decode_step_slots.restype = _I
             L.kvs_decode_step_slots.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I,
                                                 _I, _I, _I, _I, _P, _SZ, _P, _P]
+            L.kvs_argmax.restype = _I
+            L.kvs_argmax.argtypes = [_P, _I, _I, _P, _P]
             L.kvs_set_schedule.restype = _I
             L.kvs_set_schedule.argtypes = [_I]
             L.kvs_get_schedule.restype = _I
@@ -154,6 +156,19 @@ def kvs_kv_scatter(k_rows, v_rows, positions, k_cache, v_cache, d_status=None, s
                               _f32(v_cache, "v_cache", 4), M, Hkv, D, Lmax,
                               _status_ptr(d_status), _stream(stream))
     _check(rc, "kvs_kv_scatter")
+
+
+def kvs_argmax(logits, token_ids=None, stream=None):
+    """Greedy token of each row of logits [M, V] (float32, CUDA): int32 [M] on the device."""
+    if not (logits.is_cuda and logits.dtype == torch.float32 and logits.dim() == 2 and
+            logits.stride(1) == 1 and logits.stride(0) == logits.shape[1]):
+        raise TypeError("logits: need a contiguous float32 CUDA matrix [M, V]")
+    M, V = logits.shape
+    if token_ids is None:
+        token_ids = torch.empty(M, dtype=torch.int32, device=logits.device)
+    _check(lib().kvs_argmax(logits.data_ptr(), M, V, _i32(token_ids, "token_ids"),
+                            _stream(stream)), "kvs_argmax")
+    return token_ids
 
 
 def kvs_set_schedule(schedule: int) -> int:

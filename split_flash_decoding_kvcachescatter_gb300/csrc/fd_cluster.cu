@@ -49,37 +49,6 @@ constexpr int kMaxClusterDevices = 64;
 template <int D, int G>
 using ClusterGeo = Geo<D, G, 4, 2>;
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// Address of the same shared-memory location in cluster block `rank`.
-__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t a) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
 template <int D, int G>
 __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::MINB)
     fd_cluster_kernel(const float *__restrict__ q, float *k_cache, float *v_cache, SeqMap sm,

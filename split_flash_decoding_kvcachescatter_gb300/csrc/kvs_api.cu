@@ -206,6 +206,16 @@ int kvs_decode_step_slots(const float *q, const float *k_rows, const float *v_ro
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
+               kvs_stream_t stream) {
+  if (M < 0 || vocab_size < 1) return KVS_ERR_DIMS;
+  if (M == 0) return KVS_OK;
+  if (!logits || !token_ids) return KVS_ERR_NULL;
+  if (!aligned(logits, 4) || !aligned(token_ids, 4)) return KVS_ERR_ALIGN;
+  return kvs::launch_argmax(logits, M, vocab_size, token_ids,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kvs_set_schedule(int schedule) {
   if (schedule != KVS_SCHEDULE_AUTO && schedule != KVS_SCHEDULE_PERSISTENT &&
       schedule != KVS_SCHEDULE_CLUSTER)

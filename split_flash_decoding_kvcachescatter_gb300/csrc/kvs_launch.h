@@ -109,6 +109,9 @@ int prepare_cluster_kernel(int H, int Hkv, int D);
 // (current device; configures the kernel on first use), else 0.
 int cluster_auto_ok(int M, int H, int Hkv, int D, int max_len);
 
+// One launch of the batched argmax (ids[m] = argmax of logits row m).
+int launch_argmax(const float *logits, int M, int V, int32_t *ids, cudaStream_t stream);
+
 // Sets the step kernel's attributes for (H / Hkv, D) on the current device
 // (done on first use anyway; a stream capture calls it beforehand).
 int prepare_step_kernel(int H, int Hkv, int D);

@@ -234,3 +234,16 @@ def test_decode_step_slots_validation(L, kw, code):
 def test_decode_step_slots_empty_batch_ok(L):
     assert _dss(L, M=0, q=None, kr=None, vr=None, pos=None, slots=None, done=None, k=None,
                 v=None, out=None, ws=None, wsb=0) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((A16, -1, 10, A16), B.KVS_ERR_DIMS),
+    ((A16, 1, 0, A16), B.KVS_ERR_DIMS),
+    ((None, 1, 10, A16), B.KVS_ERR_NULL),
+    ((A16, 1, 10, None), B.KVS_ERR_NULL),
+    ((A16 + 2, 1, 10, A16), B.KVS_ERR_ALIGN),
+    ((A16, 1, 10, A16 + 1), B.KVS_ERR_ALIGN),
+    ((None, 0, 10, None), B.KVS_OK),
+])
+def test_argmax_validation(L, args, code):
+    assert L.kvs_argmax(*args, None) == code
