@@ -264,3 +264,33 @@ def argmax_rows(logits):
                 best, arg = v, j
         out[i] = arg
     return out
+
+
+def prefill_attention(q, k, v, causal, fp16_inputs=True):
+    """Softmax attention of every query row of every head over the keys of
+    the same head: q, k, v [n_heads][seq_len][head_dim] -> out (float64).
+
+    Follows realizar 0.8.5, src/cuda/executor/head_dim.rs,
+    tensor_core_attention (PARITY-001.3): inputs given as FP32 and converted
+    to FP16 on the GPU, softmax(q k^T / sqrt(head_dim)) v per head, FP32
+    output, optional causal masking (query i sees keys 0..i).  With
+    fp16_inputs the inputs are first rounded to IEEE half (that conversion is
+    a step of the method); everything after it is float64.
+    """
+    q = np.asarray(q, np.float32)
+    k = np.asarray(k, np.float32)
+    v = np.asarray(v, np.float32)
+    if fp16_inputs:
+        q, k, v = (a.astype(np.float16) for a in (q, k, v))
+    q, k, v = (a.astype(np.float64) for a in (q, k, v))
+    H, S, D = q.shape
+    out = np.empty((H, S, D), np.float64)
+    scale = 1.0 / np.sqrt(D)
+    for h in range(H):
+        s = (q[h] @ k[h].T) * scale                  # [S][S] scores
+        if causal:
+            s = np.where(np.tril(np.ones((S, S), bool)), s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        w = np.exp(s - m)
+        out[h] = (w @ v[h]) / w.sum(axis=1, keepdims=True)
+    return out

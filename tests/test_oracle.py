@@ -451,3 +451,53 @@ def test_argmax_matches_a_sort_on_random_rows():
         order = sorted(range(x.shape[1]), key=lambda j: (-float(x[i, j]), j))
         assert got[i] == order[0]
     assert got[2] == 100
+
+
+# ---------------------------------------------------------------- prefill attention
+def test_prefill_causal_first_row_is_first_value_row():
+    rng = np.random.default_rng(2)
+    q, k, v = (rng.standard_normal((2, 16, 16)).astype(np.float32) for _ in range(3))
+    out = oracle.prefill_attention(q, k, v, causal=True, fp16_inputs=False)
+    assert np.array_equal(out[:, 0, :], v[:, 0, :].astype(np.float64))
+
+
+def test_prefill_equals_per_row_decode_attention():
+    """Row i of causal prefill is the decode attention of query i over keys
+    0..i (the pinned decode oracle); non-causal rows attend all keys."""
+    rng = np.random.default_rng(3)
+    H, S, D = 2, 32, 64
+    q, k, v = (rng.standard_normal((H, S, D)).astype(np.float32) for _ in range(3))
+    c = oracle.prefill_attention(q, k, v, causal=True, fp16_inputs=False)
+    n = oracle.prefill_attention(q, k, v, causal=False, fp16_inputs=False)
+    for h in range(H):
+        for i in (0, 1, 17, S - 1):
+            want = oracle.attend_row(q[h, i], k[h, :i + 1], v[h, :i + 1], f64=True)
+            assert np.allclose(c[h, i], want, rtol=1e-12, atol=1e-13)
+            want = oracle.attend_row(q[h, i], k[h], v[h], f64=True)
+            assert np.allclose(n[h, i], want, rtol=1e-12, atol=1e-13)
+    assert np.allclose(c[:, S - 1], n[:, S - 1], rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_identical_keys_give_running_mean():
+    rng = np.random.default_rng(4)
+    H, S, D = 1, 16, 16
+    q = rng.standard_normal((H, S, D)).astype(np.float32)
+    k = np.tile(rng.standard_normal((1, 1, D)).astype(np.float32), (H, S, 1))
+    v = rng.standard_normal((H, S, D)).astype(np.float32)
+    out = oracle.prefill_attention(q, k, v, causal=True, fp16_inputs=False)
+    for i in range(S):
+        want = [math.fsum(float(v[0, j, d]) for j in range(i + 1)) / (i + 1) for d in range(D)]
+        assert np.allclose(out[0, i], want, rtol=1e-13, atol=1e-14)
+
+
+def test_prefill_fp16_inputs_are_rounded_first():
+    """The FP16 mode equals the exact mode applied to half-rounded inputs,
+    and differs from the unrounded result."""
+    rng = np.random.default_rng(5)
+    q, k, v = (rng.standard_normal((2, 32, 64)).astype(np.float32) for _ in range(3))
+    r = [a.astype(np.float16).astype(np.float32) for a in (q, k, v)]
+    a = oracle.prefill_attention(q, k, v, causal=True, fp16_inputs=True)
+    b = oracle.prefill_attention(*r, causal=True, fp16_inputs=False)
+    assert np.array_equal(a, b)
+    c = oracle.prefill_attention(q, k, v, causal=True, fp16_inputs=False)
+    assert not np.array_equal(a, c) and np.abs(a - c).max() < 1e-2
