@@ -318,6 +318,28 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
                kvs_stream_t stream);
 
 /*
+ * kvs_prefill_attention -- softmax attention over whole sequences on the
+ * tensor cores (realizar 0.8.5, head_dim.rs, tensor_core_attention,
+ * PARITY-001.3: FP32 inputs converted to FP16 on the GPU, Q K^T and P V as
+ * tensor-core products, FP32 output, optional causal mask).
+ *
+ *   q, k, v  in   [num_heads][seq_len][head_dim] float32, device, 16-byte aligned
+ *   out      out  [num_heads][seq_len][head_dim] float32, device, 16-byte aligned
+ * out[h][i] = softmax_j(q[h][i] . k[h][j] / sqrt(head_dim)) v[h][j] over
+ * j = 0..seq_len-1, or j = 0..i when causal != 0.  q, k and v are rounded to
+ * FP16 (round to nearest even); scores, the softmax and the output
+ * accumulate in FP32; the probabilities are rounded to FP16 before the P V
+ * product.  head_dim must be 64 or 128; any seq_len >= 1 (the pages require
+ * a multiple of 16; here the last tile is masked).
+ * Errors: DIMS (negative sizes, num_heads > 65535), UNSUPPORTED, NULL,
+ * ALIGN, LAUNCH on the host; TIMEOUT via d_status.  num_heads = 0 or
+ * seq_len = 0 enqueues nothing.
+ */
+int kvs_prefill_attention(const float *q, const float *k, const float *v,
+                          float *out, int num_heads, int seq_len, int head_dim,
+                          int causal, int *d_status, kvs_stream_t stream);
+
+/*
  * Kernel schedule of kvs_flash_decode, kvs_decode_step (and so of the
  * graphs and the static entry point), process-wide:
  *   KVS_SCHEDULE_AUTO        (the default) the cluster kernel for steps

@@ -216,6 +216,20 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kvs_prefill_attention(const float *q, const float *k, const float *v, float *out,
+                          int num_heads, int seq_len, int head_dim, int causal, int *d_status,
+                          kvs_stream_t stream) {
+  if (num_heads < 0 || seq_len < 0) return KVS_ERR_DIMS;
+  if (!head_dim_supported(head_dim)) return KVS_ERR_UNSUPPORTED;
+  if ((int64_t)num_heads > 65535) return KVS_ERR_DIMS;
+  if (num_heads == 0 || seq_len == 0) return KVS_OK;
+  if (!q || !k || !v || !out) return KVS_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return KVS_ERR_ALIGN;
+  return kvs::launch_prefill(q, k, v, out, num_heads, seq_len, head_dim, causal ? 1 : 0,
+                             d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kvs_set_schedule(int schedule) {
   if (schedule != KVS_SCHEDULE_AUTO && schedule != KVS_SCHEDULE_PERSISTENT &&
       schedule != KVS_SCHEDULE_CLUSTER)

@@ -247,3 +247,19 @@ def test_decode_step_slots_empty_batch_ok(L):
 ])
 def test_argmax_validation(L, args, code):
     assert L.kvs_argmax(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((A16, A16, A16, A16, -1, 16, 64, 1), B.KVS_ERR_DIMS),
+    ((A16, A16, A16, A16, 2, -1, 64, 1), B.KVS_ERR_DIMS),
+    ((A16, A16, A16, A16, 70000, 16, 64, 1), B.KVS_ERR_DIMS),
+    ((A16, A16, A16, A16, 2, 16, 96, 1), B.KVS_ERR_UNSUPPORTED),
+    ((None, A16, A16, A16, 2, 16, 64, 1), B.KVS_ERR_NULL),
+    ((A16, A16, None, A16, 2, 16, 64, 0), B.KVS_ERR_NULL),
+    ((A16, A16 + 4, A16, A16, 2, 16, 64, 1), B.KVS_ERR_ALIGN),
+    ((A16, A16, A16, A16 + 8, 2, 16, 128, 1), B.KVS_ERR_ALIGN),
+    ((None, None, None, None, 0, 16, 64, 1), B.KVS_OK),
+    ((None, None, None, None, 2, 0, 64, 1), B.KVS_OK),
+])
+def test_prefill_validation(L, args, code):
+    assert L.kvs_prefill_attention(*args, None, None) == code

@@ -1,0 +1,106 @@
+"""GPU parity of the tensor-core prefill attention (kvs_prefill_attention,
+through the C ABI) against the oracle.
+
+Tolerance, from the arithmetic: q, k and v are rounded to FP16 on both
+sides (a step of the method), so the only rounding the oracle does not
+share is the kernel's: probabilities rounded to FP16 before the P.V product
+(relative error <= 2^-11 each) and FP32 accumulation.  With the row sum taken
+over the rounded probabilities, output element (h, i, d) then differs from
+the exact attention of the rounded inputs by at most
+2^-11 * max_j |v16[h, j, d] - out[h, i, d]| over the attended keys j; the
+gate adds 5 % and 1e-5 for FP32 accumulation and exp2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from split_flash_decoding_kvcachescatter_gb300 import binding as B
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from split_flash_decoding_kvcachescatter_gb300 import build
+    build.build()
+    B.lib()
+
+
+def inputs(H, S, D, seed):
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal((H, S, D)).astype(np.float32) for _ in range(3)]
+
+
+def bound(v, ref, causal):
+    v16 = v.astype(np.float16).astype(np.float64)
+    H, S, D = v.shape
+    b = np.empty_like(ref)
+    for h in range(H):
+        if causal:
+            # running max / min of v over keys 0..i
+            hi = np.maximum.accumulate(v16[h], axis=0)
+            lo = np.minimum.accumulate(v16[h], axis=0)
+        else:
+            hi = np.broadcast_to(v16[h].max(axis=0), (S, D))
+            lo = np.broadcast_to(v16[h].min(axis=0), (S, D))
+        b[h] = np.maximum(np.abs(hi - ref[h]), np.abs(lo - ref[h]))
+    return 2.0 ** -11 * b * 1.05 + 1e-5
+
+
+def run(q, k, v, causal):
+    H, S, D = q.shape
+    tq, tk, tv = (torch.from_numpy(a).to(DEV) for a in (q, k, v))
+    # the output sits inside a larger buffer: nothing past it may be written
+    buf = torch.full((H * S * D + 64,), 12345.0, device=DEV)
+    out = buf[:H * S * D].view(H, S, D)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.kvs_prefill_attention(tq, tk, tv, out, causal=causal, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, B.strerror(int(status.item()))
+    assert torch.all(buf[H * S * D:] == 12345.0)
+    return out.cpu().numpy()
+
+
+def check(H, S, D, causal, seed):
+    q, k, v = inputs(H, S, D, seed)
+    got = run(q, k, v, causal)
+    ref = oracle.prefill_attention(q, k, v, causal)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref)
+    lim = bound(v, ref, causal)
+    worst = np.unravel_index(np.argmax(err - lim), err.shape)
+    assert np.all(err <= lim), (f"H={H} S={S} D={D} causal={causal}: err {err[worst]:.3e} > "
+                                f"bound {lim[worst]:.3e} at {worst}")
+    return float(err.max())
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_one_tile(D, causal):
+    check(1, 128, D, causal, seed=D + causal)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("S", [1, 16, 100, 129, 384])
+def test_sequence_lengths(S, causal):
+    check(2, S, 64, causal, seed=S * 2 + causal)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_several_heads_head_dim_128(causal):
+    check(3, 300, 128, causal, seed=7 + causal)
+
+
+def test_long_sequence_causal():
+    check(2, 1000, 128, True, seed=11)
+
+
+def test_causal_last_row_equals_full_attention_of_last_query():
+    """The last causal row attends every key: it equals the non-causal row."""
+    q, k, v = inputs(1, 256, 64, seed=13)
+    a = run(q, k, v, True)
+    b = run(q, k, v, False)
+    assert np.allclose(a[0, -1], b[0, -1], rtol=0, atol=1e-6)
