@@ -331,13 +331,22 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
  * accumulate in FP32; the probabilities are rounded to FP16 before the P V
  * product.  head_dim must be 64 or 128; any seq_len >= 1 (the pages require
  * a multiple of 16; here the last tile is masked).
+ *   workspace  device scratch of >= kvs_prefill_workspace_bytes bytes,
+ *              256-byte aligned: q, k and v as FP16 tiles in the tensor-core
+ *              layout (3 * num_heads * ceil(seq_len/128) * 128 * head_dim * 2
+ *              bytes); no initialisation needed; must not be shared by
+ *              calls that can overlap on the GPU.
+ * Two launches: the FP16 pack, then the attention.
  * Errors: DIMS (negative sizes, num_heads > 65535), UNSUPPORTED, NULL,
- * ALIGN, LAUNCH on the host; TIMEOUT via d_status.  num_heads = 0 or
- * seq_len = 0 enqueues nothing.
+ * ALIGN, WORKSPACE, LAUNCH on the host; TIMEOUT via d_status.  num_heads = 0
+ * or seq_len = 0 enqueues nothing.
  */
+size_t kvs_prefill_workspace_bytes(int num_heads, int seq_len, int head_dim);
+
 int kvs_prefill_attention(const float *q, const float *k, const float *v,
                           float *out, int num_heads, int seq_len, int head_dim,
-                          int causal, int *d_status, kvs_stream_t stream);
+                          int causal, void *workspace, size_t workspace_bytes,
+                          int *d_status, kvs_stream_t stream);
 
 /*
  * Kernel schedule of kvs_flash_decode, kvs_decode_step (and so of the

@@ -7,5 +7,5 @@ from .binding import (EXPORTS, kvs_argmax, kvs_prefill_attention, KVS_SCHEDULE_A
                       KVS_SCHEDULE_PERSISTENT, KvsError, StepGraph, kvs_choose_chunk_size,
                       kvs_decode_step, kvs_decode_step_slots, kvs_flash_decode, kvs_flash_decode_static,
                       kvs_flash_decode_workspace_bytes, kvs_get_schedule, kvs_kv_scatter,
-                      kvs_prepare, kvs_schedule_for, kvs_set_schedule, kvs_step_graph_create, lib, strerror,
+                      kvs_prepare, kvs_schedule_for, prefill_workspace, kvs_set_schedule, kvs_step_graph_create, lib, strerror,
                       workspace)

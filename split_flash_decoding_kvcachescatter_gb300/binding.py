@@ -34,7 +34,8 @@ EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspac
            "kvs_flash_decode", "kvs_decode_step", "kvs_strerror", "kvs_flash_decode_static",
            "kvs_step_graph_create", "kvs_step_graph_launch", "kvs_step_graph_destroy",
            "kvs_set_schedule", "kvs_get_schedule", "kvs_schedule_for", "kvs_prepare",
-           "kvs_decode_step_slots", "kvs_argmax", "kvs_prefill_attention")
+           "kvs_decode_step_slots", "kvs_argmax", "kvs_prefill_attention",
+           "kvs_prefill_workspace_bytes")
 
 # kvs_schedule values (kernel schedule of the attention entry points)
 KVS_SCHEDULE_AUTO = 0
@@ -94,7 +95,10 @@ def lib() -> ctypes.CDLL:
             L.kvs_decode_step_slots.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I,
                                                 _I, _I, _I, _I, _P, _SZ, _P, _P]
             L.kvs_prefill_attention.restype = _I
-            L.kvs_prefill_attention.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]
+            L.kvs_prefill_attention.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P,
+                                                _P]
+            L.kvs_prefill_workspace_bytes.restype = _SZ
+            L.kvs_prefill_workspace_bytes.argtypes = [_I, _I, _I]
             L.kvs_argmax.restype = _I
             L.kvs_argmax.argtypes = [_P, _I, _I, _P, _P]
             L.kvs_set_schedule.restype = _I
@@ -160,14 +164,26 @@ def kvs_kv_scatter(k_rows, v_rows, positions, k_cache, v_cache, d_status=None, s
     _check(rc, "kvs_kv_scatter")
 
 
-def kvs_prefill_attention(q, k, v, out, causal=True, d_status=None, stream=None):
+def prefill_workspace(H, S, D, device=None):
+    """A device byte buffer large enough for kvs_prefill_attention (allocated by torch)."""
+    n = int(lib().kvs_prefill_workspace_bytes(H, S, D))
+    if n == 0:
+        raise KvsError(KVS_ERR_DIMS, "kvs_prefill_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def kvs_prefill_attention(q, k, v, out, causal=True, workspace=None, d_status=None, stream=None):
     """Tensor-core attention over whole sequences: q, k, v, out [H, S, D] float32 (CUDA)."""
     H, S, D = q.shape
     for name, t in (("k", k), ("v", v), ("out", out)):
         if tuple(t.shape) != (H, S, D):
             raise ValueError(f"kvs_prefill_attention: {name} must be [H, S, D] like q")
+    if workspace is None:
+        raise ValueError("kvs_prefill_attention: pass a workspace (see binding.prefill_workspace)")
     _check(lib().kvs_prefill_attention(_f32(q, "q", 3), _f32(k, "k", 3), _f32(v, "v", 3),
                                        _f32(out, "out", 3), H, S, D, 1 if causal else 0,
+                                       workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(),
                                        _status_ptr(d_status), _stream(stream)),
            "kvs_prefill_attention")
     return out

@@ -216,9 +216,15 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t kvs_prefill_workspace_bytes(int num_heads, int seq_len, int head_dim) {
+  if (num_heads < 1 || seq_len < 1 || num_heads > 65535 || !head_dim_supported(head_dim))
+    return 0;
+  return kvs::prefill_workspace_bytes(num_heads, seq_len, head_dim);
+}
+
 int kvs_prefill_attention(const float *q, const float *k, const float *v, float *out,
-                          int num_heads, int seq_len, int head_dim, int causal, int *d_status,
-                          kvs_stream_t stream) {
+                          int num_heads, int seq_len, int head_dim, int causal, void *workspace,
+                          size_t workspace_bytes, int *d_status, kvs_stream_t stream) {
   if (num_heads < 0 || seq_len < 0) return KVS_ERR_DIMS;
   if (!head_dim_supported(head_dim)) return KVS_ERR_UNSUPPORTED;
   if ((int64_t)num_heads > 65535) return KVS_ERR_DIMS;
@@ -226,8 +232,12 @@ int kvs_prefill_attention(const float *q, const float *k, const float *v, float 
   if (!q || !k || !v || !out) return KVS_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
     return KVS_ERR_ALIGN;
+  if (!workspace) return KVS_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KVS_ERR_ALIGN;
+  if (workspace_bytes < kvs::prefill_workspace_bytes(num_heads, seq_len, head_dim))
+    return KVS_ERR_WORKSPACE;
   return kvs::launch_prefill(q, k, v, out, num_heads, seq_len, head_dim, causal ? 1 : 0,
-                             d_status, reinterpret_cast<cudaStream_t>(stream));
+                             workspace, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kvs_set_schedule(int schedule) {

@@ -112,9 +112,11 @@ int cluster_auto_ok(int M, int H, int Hkv, int D, int max_len);
 // One launch of the batched argmax (ids[m] = argmax of logits row m).
 int launch_argmax(const float *logits, int M, int V, int32_t *ids, cudaStream_t stream);
 
-// One launch of the tensor-core prefill attention (q, k, v, out [H][S][D]).
+// The tensor-core prefill attention (q, k, v, out [H][S][D]): a pack launch
+// (FP16 tiles into the workspace) and the attention launch.
+size_t prefill_workspace_bytes(int H, int S, int D);
 int launch_prefill(const float *q, const float *k, const float *v, float *out, int H, int S, int D,
-                   int causal, int *d_status, cudaStream_t stream);
+                   int causal, void *workspace, int *d_status, cudaStream_t stream);
 
 // Sets the step kernel's attributes for (H / Hkv, D) on the current device
 // (done on first use anyway; a stream capture calls it beforehand).

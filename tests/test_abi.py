@@ -250,16 +250,28 @@ def test_argmax_validation(L, args, code):
 
 
 @pytest.mark.parametrize("args,code", [
-    ((A16, A16, A16, A16, -1, 16, 64, 1), B.KVS_ERR_DIMS),
-    ((A16, A16, A16, A16, 2, -1, 64, 1), B.KVS_ERR_DIMS),
-    ((A16, A16, A16, A16, 70000, 16, 64, 1), B.KVS_ERR_DIMS),
-    ((A16, A16, A16, A16, 2, 16, 96, 1), B.KVS_ERR_UNSUPPORTED),
-    ((None, A16, A16, A16, 2, 16, 64, 1), B.KVS_ERR_NULL),
-    ((A16, A16, None, A16, 2, 16, 64, 0), B.KVS_ERR_NULL),
-    ((A16, A16 + 4, A16, A16, 2, 16, 64, 1), B.KVS_ERR_ALIGN),
-    ((A16, A16, A16, A16 + 8, 2, 16, 128, 1), B.KVS_ERR_ALIGN),
-    ((None, None, None, None, 0, 16, 64, 1), B.KVS_OK),
-    ((None, None, None, None, 2, 0, 64, 1), B.KVS_OK),
+    ((A16, A16, A16, A16, -1, 16, 64, 1, A16, 1 << 30), B.KVS_ERR_DIMS),
+    ((A16, A16, A16, A16, 2, -1, 64, 1, A16, 1 << 30), B.KVS_ERR_DIMS),
+    ((A16, A16, A16, A16, 70000, 16, 64, 1, A16, 1 << 30), B.KVS_ERR_DIMS),
+    ((A16, A16, A16, A16, 2, 16, 96, 1, A16, 1 << 30), B.KVS_ERR_UNSUPPORTED),
+    ((None, A16, A16, A16, 2, 16, 64, 1, A16, 1 << 30), B.KVS_ERR_NULL),
+    ((A16, A16, None, A16, 2, 16, 64, 0, A16, 1 << 30), B.KVS_ERR_NULL),
+    ((A16, A16 + 4, A16, A16, 2, 16, 64, 1, A16, 1 << 30), B.KVS_ERR_ALIGN),
+    ((A16, A16, A16, A16 + 8, 2, 16, 128, 1, A16, 1 << 30), B.KVS_ERR_ALIGN),
+    ((A16, A16, A16, A16, 2, 16, 64, 1, None, 1 << 30), B.KVS_ERR_WORKSPACE),
+    ((A16, A16, A16, A16, 2, 16, 64, 1, A16 + 16, 1 << 30), B.KVS_ERR_ALIGN),
+    ((A16, A16, A16, A16, 2, 16, 64, 1, A16, 3 * 2 * 128 * 64 * 2 - 1), B.KVS_ERR_WORKSPACE),
+    ((None, None, None, None, 0, 16, 64, 1, None, 0), B.KVS_OK),
+    ((None, None, None, None, 2, 0, 64, 1, None, 0), B.KVS_OK),
 ])
 def test_prefill_validation(L, args, code):
     assert L.kvs_prefill_attention(*args, None, None) == code
+
+
+def test_prefill_workspace_formula(L):
+    # q, k and v as FP16 tiles of 128 rows: 3 * H * ceil(S / 128) * 128 * D * 2
+    for H, S, D in [(1, 1, 64), (2, 128, 64), (3, 129, 128), (32, 4096, 128)]:
+        want = 3 * H * (-(-S // 128)) * 128 * D * 2
+        assert L.kvs_prefill_workspace_bytes(H, S, D) == want
+    assert L.kvs_prefill_workspace_bytes(0, 16, 64) == 0
+    assert L.kvs_prefill_workspace_bytes(2, 16, 96) == 0

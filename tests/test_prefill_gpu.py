@@ -57,7 +57,8 @@ def run(q, k, v, causal):
     buf = torch.full((H * S * D + 64,), 12345.0, device=DEV)
     out = buf[:H * S * D].view(H, S, D)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    B.kvs_prefill_attention(tq, tk, tv, out, causal=causal, d_status=status)
+    ws = B.prefill_workspace(H, S, D, device=DEV).fill_(0xFF)  # stale contents must not matter
+    B.kvs_prefill_attention(tq, tk, tv, out, causal=causal, workspace=ws, d_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, B.strerror(int(status.item()))
     assert torch.all(buf[H * S * D:] == 12345.0)
