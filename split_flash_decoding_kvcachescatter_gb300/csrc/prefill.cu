@@ -47,8 +47,6 @@ namespace {
 
 constexpr int kPM = 128;         // query rows per block (MMA M)
 constexpr int kPN = 128;         // keys per tile
-constexpr int kPThreads = 128;   // thread t <-> query row t <-> TMEM lane t
-constexpr uint32_t kTmemCols = 256;  // S tile [0, 128) + P.V tile [128, 128 + D)
 
 // ---- tensor memory and tcgen05 (inline PTX) ---------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
@@ -159,6 +157,22 @@ __device__ __forceinline__ uint32_t cm_off(int r, int c, int C) {
   return (uint32_t)((((r >> 3) * (C >> 3) + (c >> 3)) << 7) + ((r & 7) << 4) + ((c & 7) << 1));
 }
 
+// 2^x on the special-function unit (inputs far below the FP32 range give 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Keys of a tile that a row does not attend become -inf (no branches).
+__device__ __forceinline__ void mask_keys(float (&r)[32], int key0, int S, bool causal, int i) {
+#pragma unroll
+  for (int u = 0; u < 32; ++u) {
+    const int j = key0 + u;
+    r[u] = (j < S && (!causal || j <= i)) ? r[u] : -__int_as_float(0x7f800000);
+  }
+}
+
 __device__ __forceinline__ uint4 pack8(const float *x) {
   uint4 u;
   __half2 h;
@@ -230,49 +244,70 @@ __global__ void __launch_bounds__(256)
   allow_dependent_launch();
 }
 
+// Block layout: two 128-row query tiles (A = 2b, B = 2b + 1) share every K
+// and V^T tile.  Warpgroup 0 does the softmax of tile A, warpgroup 1 that of
+// tile B (thread t of a warpgroup owns row t, TMEM lane t), and warp 8 moves
+// the tiles and issues the tensor-core work, so one tile's softmax runs
+// while the other tile's products are on the tensor cores.
+// TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D),
+// O_B [256 + D, 256 + 2D).
+constexpr int kPWarpgroups = 2;
+constexpr int kPMmaWarp = 4 * kPWarpgroups;            // warp 8
+constexpr int kPBlockThreads = (kPMmaWarp + 1) * 32;   // 288
+constexpr uint32_t kPTmemCols = 512;
+
 template <int D>
 struct PGeo {
   static constexpr int TILE = kPM * D * 2;  // one FP16 tile of Q, K or V^T
   static constexpr int P_BYTES = kPM * kPN * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_STAGE = OFF_Q + TILE;             // 2 x (K tile, V^T tile)
-  static constexpr int OFF_P = OFF_STAGE + 2 * 2 * TILE;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;            // q, full[2], mma
-  static constexpr int OFF_TMEM = OFF_BAR + 4 * 8;           // TMEM base address
-  static constexpr int OFF_FLAG = OFF_TMEM + 8;              // abort flag
+  static constexpr int OFF_Q = 0;                        // Q_A, Q_B
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;         // K, one stage
+  static constexpr int OFF_V = OFF_K + TILE;             // V^T, two stages
+  static constexpr int OFF_P = OFF_V + 2 * TILE;         // P_A, P_B
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  // barriers: q, kfull, vfull[2], sfull[2], pfull[2], ofree[2], kfree, vfree
+  static constexpr int NBAR = 12;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;    // TMEM base address
+  static constexpr int OFF_FLAG = OFF_TMEM + 8;          // abort, no_abort
   static constexpr int SMEM_BYTES = OFF_FLAG + 16;
   static_assert(SMEM_BYTES <= 227 * 1024, "one block per SM must fit");
 };
 
 template <int D>
-__global__ void __launch_bounds__(kPThreads, 1)
+__global__ void __launch_bounds__(kPBlockThreads, 1)
     prefill_tc_kernel(const unsigned char *__restrict__ ws, float *__restrict__ out, int S,
                       int causal, float sl2, int *d_status) {
   using PG = PGeo<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char *sQ = smem + PG::OFF_Q;
-  unsigned char *sP = smem + PG::OFF_P;
-  uint64_t *bar_q = reinterpret_cast<uint64_t *>(smem + PG::OFF_BAR);
-  uint64_t *full = bar_q + 1;  // [2]: K and V^T tiles of a stage landed
-  uint64_t *bar_mma = bar_q + 3;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PG::OFF_BAR);
+  uint64_t *bar_q = bars + 0;
+  uint64_t *kfull = bars + 1;
+  uint64_t *vfull = bars + 2;  // [2]
+  uint64_t *sfull = bars + 4;  // [2]: S_A, S_B ready (commit)
+  uint64_t *pfull = bars + 6;  // [2]: P_x written, O_x rescaled (128 arrivals)
+  uint64_t *ofree = bars + 8;  // [2]: P V of tile x done (commit)
+  uint64_t *kfree = bars + 10; // the S products of the current key tile done (commit)
+  uint64_t *vfree = bars + 11; // the P V products of the current key tile done (commit)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PG::OFF_TMEM);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + PG::OFF_FLAG);
   volatile int *no_abort = reinterpret_cast<volatile int *>(smem + PG::OFF_FLAG + 4);
 
-  const int t = threadIdx.x;
-  const int warp = t >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int qt = blockIdx.x;
-  const int i = qt * kPM + t;  // this thread's query row
-  const int T = (S + kPN - 1) / kPN;
-  const int n_kt = causal ? min(qt + 1, T) : T;
+  const int T = (S + kPN - 1) / kPN;   // query tiles = key tiles
+  // tile A; tile B = qa + 1 (absent when qa + 1 == T).  Causal blocks with
+  // the most key tiles are launched first.
+  const int qa = 2 * (causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
+  const bool has_b = qa + 1 < T;
+  const int n_a = causal ? qa + 1 : T;            // key tiles tile A attends
+  const int n_b = has_b ? (causal ? qa + 2 : T) : 0;
+  const int n_all = n_a > n_b ? n_a : n_b;
   const size_t tile = (size_t)PG::TILE;
   const size_t per_tensor = (size_t)gridDim.y * T * tile;
-  const unsigned char *gQ = ws + ((size_t)h * T + qt) * tile;
+  const unsigned char *gQh = ws + (size_t)h * T * tile;
   const unsigned char *gKh = ws + per_tensor + (size_t)h * T * tile;
   const unsigned char *gVh = ws + 2 * per_tensor + (size_t)h * T * tile;
-  auto stage_k = [&](int s) { return smem + PG::OFF_STAGE + s * 2 * PG::TILE; };
-  auto stage_v = [&](int s) { return smem + PG::OFF_STAGE + s * 2 * PG::TILE + PG::TILE; };
 
   constexpr uint32_t kIdescS = idesc_f16_f32(kPM, kPN);
   constexpr uint32_t kIdescO = idesc_f16_f32(kPM, D);
@@ -281,177 +316,244 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   grid_dependency_wait();
   if (warp == 0) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, kPTmemCols);
     tmem_relinquish();
   }
-  // Thread 0 moves the tiles and issues the tensor-core work.  Order of its
-  // MMAs: S(0), then per key tile kt: P V(kt), S(kt+1).  One commit after
-  // S(kt+1) (or after the last P V) covers both, since a commit tracks every
-  // MMA the thread issued before it.
-  uint32_t issued = 0;  // key tiles whose copies were issued
-  int t0_ok = 1;        // thread 0: every wait so far succeeded
-  auto issue_tile = [&](int st) {
-    mbar_arrive_expect_tx(&full[st], 2 * PG::TILE);
-    bulk_g2s(stage_k(st), gKh + issued * tile, PG::TILE, &full[st]);
-    bulk_g2s(stage_v(st), gVh + issued * tile, PG::TILE, &full[st]);
-    ++issued;
-  };
-  if (t == 0) {
+  if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(bar_mma, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&vfull[x], 1);
+      mbar_init(&sfull[x], 1);
+      mbar_init(&pfull[x], kPM);
+      mbar_init(&ofree[x], 1);
+    }
+    mbar_init(kfull, 1);
+    mbar_init(kfree, 1);
+    mbar_init(vfree, 1);
     *abort = 0;
     *no_abort = 0;
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar_q, PG::TILE);
-    bulk_g2s(sQ, gQ, PG::TILE, bar_q);
-    while ((int)issued < n_kt && issued < 2) issue_tile(issued & 1);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t tm_s = tmem + lane_base;
-  const uint32_t tm_o = tmem + lane_base + kPN;
-
-  auto issue_s = [&](int kt) {  // thread 0: S(kt) = Q K(kt)^T, once K(kt) has landed
-    if (!mbar_wait(&full[kt & 1], (kt >> 1) & 1, abort)) {
-      t0_ok = 0;
-      return;
-    }
-    tc_fence_after();
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks)
-      mma_f16(tmem, smem_desc(sQ + ks * 256, 128, kSboD),
-              smem_desc(stage_k(kt & 1) + ks * 256, 128, kSboD), kIdescS, ks > 0 ? 1u : 0u);
-  };
-  if (t == 0) {
-    if (!mbar_wait(bar_q, 0, abort)) t0_ok = 0;
-    if (t0_ok) issue_s(0);
-    mma_commit(bar_mma);
-  }
-
-  float m = neg_inf_f();
-  float l = 0.f;
-  uint32_t mma_phase = 0;
   bool failed = false;
-  for (int kt = 0; kt < n_kt; ++kt) {
-    const int key0 = kt * kPN;
-    const int st = kt & 1;
-    // S(kt) and P V(kt-1) are done
-    const bool ok = mbar_wait(bar_mma, mma_phase, abort);
-    mma_phase ^= 1u;
-    if (__syncthreads_or(!ok || (t == 0 && !t0_ok))) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-    // the stage of key tile kt-1 is free: bring key tile kt+1 into it
-    if (t == 0 && kt >= 1 && (int)issued < n_kt) issue_tile(issued & 1);
-    // ---- row maximum of the tile (masked) ----
-    float mt = neg_inf_f();
-#pragma unroll
-    for (int ch = 0; ch < kPN / 32; ++ch) {
-      float r[32];
-      tmem_ld32(tm_s + ch * 32, r);
-      tmem_wait_ld();
-#pragma unroll
-      for (int u = 0; u < 32; ++u) {
-        const int j = key0 + ch * 32 + u;
-        const bool live = j < S && (!causal || j <= i);
-        if (live) mt = fmaxf(mt, r[u] * sl2);
-      }
-    }
-    const float m_new = fmaxf(m, mt);
-    const float alpha = (m_new == neg_inf_f()) ? 1.f : exp2f(m - m_new);
-    // ---- rescale the output accumulator (TMEM) where the maximum moved ----
-    if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        float r[32];
-        tmem_ld32(tm_o + ch * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int u = 0; u < 32; ++u) r[u] *= alpha;
-        tmem_st32(tm_o + ch * 32, r);
-      }
-      tmem_wait_st();
-    }
-    // ---- P (FP16) into shared memory, and its row sum ----
-    float lt = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < kPN / 32; ++ch) {
-      float r[32];
-      tmem_ld32(tm_s + ch * 32, r);
-      tmem_wait_ld();
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        float p8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = key0 + ch * 32 + g8 * 8 + u;
-          const bool live = j < S && (!causal || j <= i) && m_new != neg_inf_f();
-          const float p = live ? exp2f(r[g8 * 8 + u] * sl2 - m_new) : 0.f;
-          p8[u] = __half2float(__float2half_rn(p));
-          lt += p8[u];
-        }
-        *reinterpret_cast<uint4 *>(sP + cm_off(t, ch * 32 + g8 * 8, kPN)) = pack8(p8);
-      }
-    }
-    l = l * alpha + lt;
-    m = m_new;
-    fence_proxy_async_shared();
-    tc_fence_before();
-    __syncthreads();
-    // ---- thread 0: O (+)= P V(kt), then S(kt+1) ----
-    if (t == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < kPN / 16; ++ks)
-        mma_f16(tmem + kPN, smem_desc(sP + ks * 256, 128, kSboN),
-                smem_desc(stage_v(st) + ks * 256, 128, kSboN), kIdescO,
-                (kt > 0 || ks > 0) ? 1u : 0u);
-      if (kt + 1 < n_kt && t0_ok) issue_s(kt + 1);
-      mma_commit(bar_mma);
-    }
-  }
-  if (!failed) {  // the last P V
-    const bool ok = mbar_wait(bar_mma, mma_phase, abort);
-    failed = __syncthreads_or(!ok);
-  }
 
-  if (failed) {
-    if (t == 0) {
+  if (warp == kPMmaWarp) {
+    // ======================= copies and tensor-core work =====================
+    if (lane == 0) {
+      unsigned char *sQ = smem + PG::OFF_Q;
+      unsigned char *sK = smem + PG::OFF_K;
+      unsigned char *sV = smem + PG::OFF_V;
+      unsigned char *sP = smem + PG::OFF_P;
+      uint32_t k_issued = 0, v_issued = 0;
+      auto issue_k = [&]() {  // the single K stage
+        mbar_arrive_expect_tx(kfull, PG::TILE);
+        bulk_g2s(sK, gKh + k_issued * tile, PG::TILE, kfull);
+        ++k_issued;
+      };
+      auto issue_v = [&]() {  // V^T(n) into stage n & 1
+        const int st = v_issued & 1;
+        mbar_arrive_expect_tx(&vfull[st], PG::TILE);
+        bulk_g2s(sV + st * PG::TILE, gVh + v_issued * tile, PG::TILE, &vfull[st]);
+        ++v_issued;
+      };
+      // Order on the tensor cores, per key tile kt: P V_A(kt), S_A(kt+1),
+      // P V_B(kt), S_B(kt+1).  Softmax A(kt+1) then runs while P V_B(kt) and
+      // softmax B(kt) are in progress: the two tiles alternate.
+      auto issue_s = [&](int x) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_f16(tmem + x * kPN, smem_desc(sQ + x * PG::TILE + ks * 256, 128, kSboD),
+                  smem_desc(sK + ks * 256, 128, kSboD), kIdescS, ks > 0 ? 1u : 0u);
+        mma_commit(&sfull[x]);
+      };
+      auto issue_pv = [&](int x, int kt) {
+        const unsigned char *v_st = sV + (kt & 1) * PG::TILE;
+#pragma unroll
+        for (int ks = 0; ks < kPN / 16; ++ks)
+          mma_f16(tmem + 2 * kPN + x * D,
+                  smem_desc(sP + x * PG::P_BYTES + ks * 256, 128, kSboN),
+                  smem_desc(v_st + ks * 256, 128, kSboN), kIdescO, (kt > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&ofree[x]);
+      };
+      mbar_arrive_expect_tx(bar_q, (has_b ? 2 : 1) * PG::TILE);
+      bulk_g2s(sQ, gQh + (size_t)qa * tile, PG::TILE, bar_q);
+      if (has_b) bulk_g2s(sQ + PG::TILE, gQh + (size_t)(qa + 1) * tile, PG::TILE, bar_q);
+      issue_k();
+      while ((int)v_issued < n_all && v_issued < 2) issue_v();
+      bool ok = mbar_wait(bar_q, 0, abort) && mbar_wait(kfull, 0, abort);
+      if (ok) {
+        tc_fence_after();
+        if (n_a > 0) issue_s(0);
+        if (n_b > 0) issue_s(1);
+        mma_commit(kfree);
+      }
+      for (int kt = 0; kt < n_all && ok; ++kt) {
+        const uint32_t ph = (uint32_t)kt & 1u;
+        // the S products of key tile kt are done: bring key tile kt+1 into K
+        ok = mbar_wait(kfree, ph, abort);
+        if (!ok) break;
+        if ((int)k_issued < n_all) issue_k();
+        // the P V products of key tile kt-1 are done: bring V^T(kt+1) into its stage
+        if (kt >= 1) {
+          ok = mbar_wait(vfree, ph ^ 1u, abort);
+          if (!ok) break;
+          if ((int)v_issued < n_all) issue_v();
+        }
+        ok = mbar_wait(&vfull[kt & 1], (kt >> 1) & 1, abort);  // V^T(kt)
+        bool k_next = false;  // key tile kt+1 has landed
+        for (int x = 0; x < 2 && ok; ++x) {
+          const int n_x = x == 0 ? n_a : n_b;
+          if (kt < n_x) {  // P V_x(kt), once softmax x(kt) has written P_x
+            ok = mbar_wait(&pfull[x], ph, abort);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(x, kt);
+          }
+          if (kt + 1 < n_x) {  // S_x(kt+1)
+            if (!k_next) {
+              ok = mbar_wait(kfull, ph ^ 1u, abort);
+              if (!ok) break;
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_s(x);
+          }
+        }
+        if (!ok) break;
+        mma_commit(vfree);  // P V(kt)
+        mma_commit(kfree);  // S(kt+1)
+      }
+      if (!ok) {
+        *abort = 1;
+        record_status(d_status, KVS_ERR_TIMEOUT);
+        // let the copies already issued land before the block exits
+        mbar_wait(bar_q, 0, no_abort);
+        if (k_issued > 0) mbar_wait(kfull, (k_issued - 1) & 1, no_abort);
+        for (uint32_t j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
+          mbar_wait(&vfull[j & 1], (j >> 1) & 1, no_abort);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax of tile x ===============================
+    const int x = warp >> 2;             // warpgroup
+    const int t = threadIdx.x & 127;     // row within the tile
+    const int q_tile = qa + x;
+    const int i = q_tile * kPM + t;      // query row
+    const int n_x = x == 0 ? n_a : n_b;
+    unsigned char *sPx = smem + PG::OFF_P + x * PG::P_BYTES;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tm_s = tmem + lane_base + x * kPN;
+    const uint32_t tm_o = tmem + lane_base + 2 * kPN + x * D;
+    float m = neg_inf_f();
+    float l = 0.f;
+    for (int kt = 0; kt < n_x; ++kt) {
+      const int key0 = kt * kPN;
+      const uint32_t ph = (uint32_t)kt & 1u;
+      if (!mbar_wait(&sfull[x], ph, abort)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      // keys needing a mask: past S, or past the row on the diagonal tile
+      const bool masked = (key0 + kPN > S) || (causal && kt == q_tile);
+      // ---- row maximum of the tile ----
+      float mt = neg_inf_f();
+#pragma unroll 1
+      for (int ch = 0; ch < kPN / 32; ++ch) {
+        float r[32];
+        tmem_ld32(tm_s + ch * 32, r);
+        tmem_wait_ld();
+        if (masked) mask_keys(r, key0 + ch * 32, S, causal, i);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) mt = fmaxf(mt, r[u]);
+      }
+      const float m_new = fmaxf(m, mt * sl2);
+      const float alpha = (m_new == neg_inf_f()) ? 1.f : ex2(m - m_new);
+      // ---- P V of the previous tile must be done before O and P change ----
+      if (kt > 0) {
+        if (!mbar_wait(&ofree[x], ph ^ 1u, abort)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            float r[32];
+            tmem_ld32(tm_o + ch * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) r[u] *= alpha;
+            tmem_st32(tm_o + ch * 32, r);
+          }
+          tmem_wait_st();
+        }
+      }
+      // ---- P (FP16) into shared memory, and its row sum ----
+      // (a row with no key yet has m_new = -inf and every score -inf: p = 0)
+      const float mb = (m_new == neg_inf_f()) ? 0.f : m_new;
+      float lt = 0.f;
+#pragma unroll 1
+      for (int ch = 0; ch < kPN / 32; ++ch) {
+        float r[32];
+        tmem_ld32(tm_s + ch * 32, r);
+        tmem_wait_ld();
+        if (masked) mask_keys(r, key0 + ch * 32, S, causal, i);
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float p0 = ex2(fmaf(r[g8 * 8 + 2 * u], sl2, -mb));
+            const float p1 = ex2(fmaf(r[g8 * 8 + 2 * u + 1], sl2, -mb));
+            const __half2 hp = __floats2half2_rn(p0, p1);
+            const float2 back = __half22float2(hp);
+            lt += back.x + back.y;
+            w[u] = *reinterpret_cast<const uint32_t *>(&hp);
+          }
+          *reinterpret_cast<uint4 *>(sPx + cm_off(t, ch * 32 + g8 * 8, kPN)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      l = l * alpha + lt;
+      m = m_new;
+      fence_proxy_async_shared();  // the tensor cores read P
+      tc_fence_before();
+      mbar_arrive(&pfull[x]);
+    }
+    if (!failed && n_x > 0) {  // the last P V, then the output rows
+      failed = !mbar_wait(&ofree[x], (uint32_t)(n_x - 1) & 1u, abort);
+      if (!failed) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          float r[32];
+          tmem_ld32(tm_o + ch * 32, r);
+          tmem_wait_ld();
+          if (i < S) {
+            float4 *o4 = reinterpret_cast<float4 *>(out + ((size_t)h * S + i) * D + ch * 32);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              o4[u] = make_float4(r[4 * u] * inv, r[4 * u + 1] * inv, r[4 * u + 2] * inv,
+                                  r[4 * u + 3] * inv);
+          }
+        }
+      }
+    }
+    if (failed) {
       *abort = 1;
       record_status(d_status, KVS_ERR_TIMEOUT);
-      // let the copies already issued land before the block exits
-      mbar_wait(bar_q, 0, no_abort);
-      for (uint32_t j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-        mbar_wait(&full[j & 1], (j >> 1) & 1, no_abort);
-    }
-  } else {
-    tc_fence_after();
-    const float inv = 1.f / l;
-#pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      float r[32];
-      tmem_ld32(tm_o + ch * 32, r);
-      tmem_wait_ld();
-      if (i < S) {
-        float4 *o4 = reinterpret_cast<float4 *>(out + ((size_t)h * S + i) * D + ch * 32);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          o4[u] = make_float4(r[4 * u] * inv, r[4 * u + 1] * inv, r[4 * u + 2] * inv,
-                              r[4 * u + 3] * inv);
-      }
     }
   }
   allow_dependent_launch();
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, kPTmemCols);
 }
 
 template <int D>
@@ -476,8 +578,9 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
                              ws, H, S);
   if (e != cudaSuccess) return KVS_ERR_LAUNCH;
   const float sl2 = (float)(1.4426950408889634074 / std::sqrt((double)D));
-  const dim3 grid((S + kPM - 1) / kPM, H, 1);
-  e = launch_pdl(prefill_tc_kernel<D>, grid, dim3(kPThreads), PG::SMEM_BYTES, stream,
+  const int T = (S + kPM - 1) / kPM;
+  const dim3 grid((T + 1) / 2, H, 1);
+  e = launch_pdl(prefill_tc_kernel<D>, grid, dim3(kPBlockThreads), PG::SMEM_BYTES, stream,
                  static_cast<const unsigned char *>(ws), out, S, causal, sl2, d_status);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
