@@ -337,9 +337,9 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
  *              bytes); no initialisation needed; must not be shared by
  *              calls that can overlap on the GPU.
  * Two launches: the FP16 pack, then the attention.
- * Errors: DIMS (negative sizes, num_heads > 65535), UNSUPPORTED, NULL,
- * ALIGN, WORKSPACE, LAUNCH on the host; TIMEOUT via d_status.  num_heads = 0
- * or seq_len = 0 enqueues nothing.
+ * Errors: DIMS (negative sizes, num_heads > 65535, seq_len > 65535 * 128),
+ * UNSUPPORTED, NULL, ALIGN, WORKSPACE, LAUNCH on the host; TIMEOUT via
+ * d_status.  num_heads = 0 or seq_len = 0 enqueues nothing.
  */
 size_t kvs_prefill_workspace_bytes(int num_heads, int seq_len, int head_dim);
 

@@ -217,7 +217,8 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
 }
 
 size_t kvs_prefill_workspace_bytes(int num_heads, int seq_len, int head_dim) {
-  if (num_heads < 1 || seq_len < 1 || num_heads > 65535 || !head_dim_supported(head_dim))
+  if (num_heads < 1 || seq_len < 1 || num_heads > 65535 || (int64_t)seq_len > 65535ll * 128 ||
+      !head_dim_supported(head_dim))
     return 0;
   return kvs::prefill_workspace_bytes(num_heads, seq_len, head_dim);
 }
@@ -227,7 +228,7 @@ int kvs_prefill_attention(const float *q, const float *k, const float *v, float 
                           size_t workspace_bytes, int *d_status, kvs_stream_t stream) {
   if (num_heads < 0 || seq_len < 0) return KVS_ERR_DIMS;
   if (!head_dim_supported(head_dim)) return KVS_ERR_UNSUPPORTED;
-  if ((int64_t)num_heads > 65535) return KVS_ERR_DIMS;
+  if ((int64_t)num_heads > 65535 || (int64_t)seq_len > 65535ll * 128) return KVS_ERR_DIMS;
   if (num_heads == 0 || seq_len == 0) return KVS_OK;
   if (!q || !k || !v || !out) return KVS_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))

@@ -34,6 +34,7 @@
 
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -192,54 +193,70 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
 // ceil(S / 128) and a tile of 128 * D FP16 values (rows past S are zero).
 __host__ __device__ constexpr size_t prefill_tile_bytes(int D) { return (size_t)kPM * D * 2; }
 
+// Grid (2 * D/16 + 1, T, H): blocks [0, D/16) convert tile t of Q, blocks
+// [D/16, 2 * D/16) tile t of K (one 16-byte chunk per thread), the last block
+// tile t of V^T (one 8-key x 8-column block per thread, transposed in
+// registers).  Consecutive threads write consecutive bytes.
 template <int D>
 __global__ void __launch_bounds__(256)
     prefill_pack_kernel(const float *__restrict__ q, const float *__restrict__ k,
-                        const float *__restrict__ v, unsigned char *__restrict__ ws, int H, int S) {
+                        const float *__restrict__ v, unsigned char *__restrict__ ws, int S) {
+  constexpr int NQK = D / 16;  // blocks per Q or K tile (128 * D/8 chunks / 256)
   grid_dependency_wait();
-  const int T = (S + kPM - 1) / kPM;
+  const int T = gridDim.y, H = gridDim.z;
+  const int t = blockIdx.y, h = blockIdx.z;
   const size_t tile = prefill_tile_bytes(D);
-  const long long per_tensor = (long long)H * T * (kPM * D / 8);  // 16-byte chunks
-  unsigned char *wq = ws;
-  unsigned char *wk = ws + (size_t)H * T * tile;
-  unsigned char *wv = wk + (size_t)H * T * tile;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < 3 * per_tensor;
-       e += (long long)gridDim.x * blockDim.x) {
-    const int which = (int)(e / per_tensor);
-    const long long f = e - (long long)which * per_tensor;
-    const long long ht = f / (kPM * D / 8);  // h * T + t
-    const int w = (int)(f - ht * (kPM * D / 8));
-    const int h = (int)(ht / T);
-    const int t = (int)(ht - (long long)h * T);
+  const size_t ht = (size_t)h * T + t;
+  const int bx = blockIdx.x;
+  if (bx < 2 * NQK) {  // Q or K: chunk (row r, 8 columns from c)
+    const int which = bx / NQK;
+    const int w = (bx - which * NQK) * 256 + threadIdx.x;
+    // the 8 rows of a core matrix, then the next core matrix along the row
+    const int r = (w / (8 * (D / 8))) * 8 + (w & 7);
+    const int c = ((w >> 3) % (D / 8)) * 8;
+    const int row = t * kPM + r;
     float x[8];
-    uint32_t off;
-    if (which < 2) {  // Q or K: chunk w = (row r, 8 columns from c)
-      const int r = w / (D / 8);
-      const int c = (w - r * (D / 8)) * 8;
-      const int row = t * kPM + r;
-      const float *src = (which == 0 ? q : k) + ((size_t)h * S + row) * D + c;
-      if (row < S) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(src));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(src) + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-      } else {
+    if (row < S) {
+      const float4 *src =
+          reinterpret_cast<const float4 *>((which == 0 ? q : k) + ((size_t)h * S + row) * D + c);
+      const float4 a = __ldg(src), b = __ldg(src + 1);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = 0.f;
-      }
-      off = cm_off(r, c, D);
-    } else {  // V^T: chunk w = (column d, 8 keys from j); consecutive w, consecutive d
-      const int d = w % D;
-      const int j = (w / D) * 8;
+      for (int u = 0; u < 8; ++u) x[u] = 0.f;
+    }
+    unsigned char *dst = ws + ((size_t)which * H * T + ht) * tile;
+    *reinterpret_cast<uint4 *>(dst + cm_off(r, c, D)) = pack8(x);
+  } else {  // V^T: keys j..j+7 and columns d..d+7
+    const int w = threadIdx.x;
+    if (w < (D / 8) * (kPN / 8)) {
+      const int d = (w % (D / 8)) * 8;
+      const int j = (w / (D / 8)) * 8;
+      float x[8][8];  // [key][column]
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int key = t * kPM + j + u;
-        x[u] = key < S ? __ldg(v + ((size_t)h * S + key) * D + d) : 0.f;
+        const int key = t * kPN + j + u;
+        if (key < S) {
+          const float4 *src =
+              reinterpret_cast<const float4 *>(v + ((size_t)h * S + key) * D + d);
+          const float4 a = __ldg(src), b = __ldg(src + 1);
+          x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
+          x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) x[u][c] = 0.f;
+        }
       }
-      off = cm_off(d, j, kPN);
+      unsigned char *dst = ws + ((size_t)2 * H * T + ht) * tile;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float col[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) col[u] = x[u][c];
+        *reinterpret_cast<uint4 *>(dst + cm_off(d + c, j, kPN)) = pack8(col);
+      }
     }
-    unsigned char *dst = (which == 0 ? wq : which == 1 ? wk : wv) + ht * tile + off;
-    *reinterpret_cast<uint4 *>(dst) = pack8(x);
   }
   allow_dependent_launch();
 }
@@ -252,6 +269,7 @@ __global__ void __launch_bounds__(256)
 // TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D),
 // O_B [256 + D, 256 + 2D).
 constexpr int kPWarpgroups = 2;
+constexpr float kRescaleLog2 = 8.f;
 constexpr int kPMmaWarp = 4 * kPWarpgroups;            // warp 8
 constexpr int kPBlockThreads = (kPMmaWarp + 1) * 32;   // 288
 constexpr uint32_t kPTmemCols = 512;
@@ -471,7 +489,12 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
 #pragma unroll
         for (int u = 0; u < 32; ++u) mt = fmaxf(mt, r[u]);
       }
-      const float m_new = fmaxf(m, mt * sl2);
+      // The reference maximum only moves when the row maximum grows by more
+      // than kRescaleLog2 (log2 units): below that, p = 2^(s - m) stays under
+      // 2^kRescaleLog2 (FP16 holds it), the result is the same, and the
+      // output accumulator needs no rescale.
+      const float m_row = fmaxf(m, mt * sl2);
+      const float m_new = (m_row > m + kRescaleLog2) ? m_row : m;
       const float alpha = (m_new == neg_inf_f()) ? 1.f : ex2(m - m_new);
       // ---- P V of the previous tile must be done before O and P change ----
       if (kt > 0) {
@@ -571,11 +594,10 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
     }
     configured[dev] = true;
   }
-  const int sms = device_sm_count();
-  if (sms <= 0) return KVS_ERR_LAUNCH;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
-  cudaError_t e = launch_pdl(prefill_pack_kernel<D>, dim3(sms * 4), dim3(256), 0, stream, q, k, v,
-                             ws, H, S);
+  const int nt = (S + kPM - 1) / kPM;
+  cudaError_t e = launch_pdl(prefill_pack_kernel<D>, dim3(2 * (D / 16) + 1, nt, H), dim3(256), 0,
+                             stream, q, k, v, ws, S);
   if (e != cudaSuccess) return KVS_ERR_LAUNCH;
   const float sl2 = (float)(1.4426950408889634074 / std::sqrt((double)D));
   const int T = (S + kPM - 1) / kPM;

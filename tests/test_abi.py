@@ -253,6 +253,7 @@ def test_argmax_validation(L, args, code):
     ((A16, A16, A16, A16, -1, 16, 64, 1, A16, 1 << 30), B.KVS_ERR_DIMS),
     ((A16, A16, A16, A16, 2, -1, 64, 1, A16, 1 << 30), B.KVS_ERR_DIMS),
     ((A16, A16, A16, A16, 70000, 16, 64, 1, A16, 1 << 30), B.KVS_ERR_DIMS),
+    ((A16, A16, A16, A16, 1, 65535 * 128 + 1, 64, 1, A16, 1 << 62), B.KVS_ERR_DIMS),
     ((A16, A16, A16, A16, 2, 16, 96, 1, A16, 1 << 30), B.KVS_ERR_UNSUPPORTED),
     ((None, A16, A16, A16, 2, 16, 64, 1, A16, 1 << 30), B.KVS_ERR_NULL),
     ((A16, A16, None, A16, 2, 16, 64, 0, A16, 1 << 30), B.KVS_ERR_NULL),
