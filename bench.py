@@ -147,6 +147,48 @@ def time_argmax(B, torch, M, dev, stream, iters=200):
             "l2": "scrubbed between launches", "matches_torch_argmax": bool(ok)}
 
 
+PREFILL_SHAPE = (32, 4096, 128)  # heads, sequence length, head_dim of an 8B-class prefill
+
+
+def tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16 (burst); fp16 has the same rate"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def time_prefill(B, torch, dev, stream, iters=20):
+    """Tensor-core prefill attention (kvs_prefill_attention, causal): the FP16
+    pack launch and the tcgen05 attention launch, timed together.  Inputs
+    (3 x 67 MB) and the packed workspace exceed L2."""
+    H, S, D = PREFILL_SHAPE
+    g = torch.Generator(device=dev).manual_seed(4321)
+    q, k, v = (torch.randn((H, S, D), device=dev, generator=g) for _ in range(3))
+    out = torch.empty_like(q)
+    ws = B.prefill_workspace(H, S, D, device=dev)
+    for _ in range(3):
+        B.kvs_prefill_attention(q, k, v, out, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for a, b in ev:
+        a.record(stream)
+        B.kvs_prefill_attention(q, k, v, out, causal=True, workspace=ws)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    flops = 4.0 * D * H * S * (S + 1) / 2  # QK^T and PV over the causal triangle
+    tf = flops / (ms * 1e-3) / 1e12
+    peak, kind = tensor_peak()
+    return {"kernel": "prefill_pack_kernel + prefill_tc_kernel (kvs_prefill_attention)",
+            "heads": H, "seq_len": S, "head_dim": D, "causal": True, "dtype": "f16 x f16 -> f32",
+            "us_per_call": 1e3 * ms, "flops_per_call": flops,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "peak_source": kind}}
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled in the background."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -304,6 +346,8 @@ def main():
                     help="launch the whole (multi-layer) step as one captured CUDA graph")
     ap.add_argument("--no-argmax", action="store_true",
                     help="skip the batched argmax measurement")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the tensor-core prefill measurement")
     ap.add_argument("--schedule", default="auto", choices=["auto", "persistent", "cluster"],
                     help="attention kernel (kvs_set_schedule)")
     args = ap.parse_args()
@@ -491,6 +535,7 @@ def main():
         torch.cuda.synchronize()
         e2e_ms -= s0.elapsed_time(s1) / Ke
     argmax = time_argmax(B, torch, w.M, dev, stream) if not args.no_argmax else None
+    prefill = time_prefill(B, torch, dev, stream) if not args.no_prefill else None
     sampler.stop()
     clocks = sampler.summary(wall0, wall1)
 
@@ -557,6 +602,7 @@ def main():
         "clocks": clocks,
         "cpu_baseline": cpu,
         "argmax": argmax,
+        "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
