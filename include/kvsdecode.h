@@ -329,7 +329,7 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
  * j = 0..seq_len-1, or j = 0..i when causal != 0.  q, k and v are rounded to
  * FP16 (round to nearest even); scores, the softmax and the output
  * accumulate in FP32; the probabilities are rounded to FP16 before the P V
- * product.  head_dim must be 64 or 128; any seq_len >= 1 (the pages require
+ * product (the row sum adds them in FP32).  head_dim must be 64 or 128; any seq_len >= 1 (the pages require
  * a multiple of 16; here the last tile is masked).
  *   workspace  device scratch of >= kvs_prefill_workspace_bytes bytes,
  *              256-byte aligned: q, k and v as FP16 tiles in the tensor-core

@@ -14,21 +14,22 @@
 //    K-major layout of the tensor cores (8-row x 16-byte core matrices,
 //    K-adjacent ones 128 B apart); V is stored transposed (head_dim rows of
 //    128 keys), so that P V is again a K-major product.  Every tile is one
-//    contiguous block.
-//  * Attention block = (head, 128 query rows), 4 warps; thread t owns query
-//    row t, which is TMEM lane t of both accumulators.  One thread moves each
-//    tile with a single 1-D bulk asynchronous copy (TMA) into a two-stage
-//    ring (K and V^T of the next key tile land while this one is computed)
-//    and issues the tensor-core work:
-//      S = Q K^T as head_dim/16 tcgen05.mma (M=128, N=128, K=16) into TMEM
-//      columns [0, 128), and P V as 8 tcgen05.mma (M=128, N=head_dim) into
-//      columns [128, 128 + head_dim), each committed to an mbarrier.
-//  * Each thread reads its score row from TMEM (tcgen05.ld 32x32b), takes
-//    the tile maximum, forms p = exp2(s - m) in FP32, rounds it to FP16 into
-//    the P tile (shared memory) and sums the rounded values; after P V it
-//    folds that row into its FP32 output with the online-softmax rescale.
+//    contiguous block, moved later by a single 1-D bulk copy (TMA).
+//  * Attention block = (head, two 128-row query tiles A and B), 9 warps:
+//    warpgroup 0 runs the softmax of tile A, warpgroup 1 that of tile B
+//    (thread t owns query row t, which is TMEM lane t), and warp 8 moves the
+//    tiles and issues the tensor-core work (tcgen05.mma, M = 128, K = 16,
+//    FP32 accumulators in TMEM, completion by tcgen05.commit on mbarriers)
+//    in the order P V_A(kt), S_A(kt+1), P V_B(kt), S_B(kt+1), so one tile's
+//    softmax runs while the other tile's products are on the tensor cores.
+//  * Softmax: each thread reads its score row from TMEM (tcgen05.ld
+//    32x32b) twice -- row maximum, then p = 2^(s - m) on the special-function
+//    unit, rounded to FP16 into the P tile in shared memory, the FP32 values
+//    summed into the row sum.  The reference maximum moves only when the row
+//    maximum grows by more than 2^8, so the output accumulator in TMEM is
+//    rarely rescaled.
 //  * Causal: key tiles after the query tile are skipped; keys j > i and keys
-//    past seq_len get p = 0.
+//    past seq_len get p = 0 (selects, on the diagonal and last tiles only).
 // Every mbarrier wait is bounded; on expiry the block records
 // KVS_ERR_TIMEOUT, lets its copies land, frees its TMEM and returns.
 
@@ -534,8 +535,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
             const float p0 = ex2(fmaf(r[g8 * 8 + 2 * u], sl2, -mb));
             const float p1 = ex2(fmaf(r[g8 * 8 + 2 * u + 1], sl2, -mb));
             const __half2 hp = __floats2half2_rn(p0, p1);
-            const float2 back = __half22float2(hp);
-            lt += back.x + back.y;
+            lt += p0 + p1;
             w[u] = *reinterpret_cast<const uint32_t *>(&hp);
           }
           *reinterpret_cast<uint4 *>(sPx + cm_off(t, ch * 32 + g8 * 8, kPN)) =
