@@ -159,31 +159,33 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
-def time_prefill(B, torch, dev, stream, iters=20):
-    """Tensor-core prefill attention (kvs_prefill_attention, causal): the FP16
-    pack launch and the tcgen05 attention launch, timed together.  Inputs
-    (3 x 67 MB) and the packed workspace exceed L2."""
-    H, S, D = PREFILL_SHAPE
+def time_prefill(B, torch, dev, stream, iters=20, shape=PREFILL_SHAPE, causal=True):
+    """Tensor-core prefill attention (kvs_prefill_attention): the FP16 pack
+    launch and the tcgen05 attention launch, timed together.  At the default
+    shape the inputs (3 x 67 MB) and the packed workspace exceed L2."""
+    H, S, D = shape
     g = torch.Generator(device=dev).manual_seed(4321)
     q, k, v = (torch.randn((H, S, D), device=dev, generator=g) for _ in range(3))
     out = torch.empty_like(q)
     ws = B.prefill_workspace(H, S, D, device=dev)
     for _ in range(3):
-        B.kvs_prefill_attention(q, k, v, out, causal=True, workspace=ws)
+        B.kvs_prefill_attention(q, k, v, out, causal=causal, workspace=ws)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(iters)]
     for a, b in ev:
         a.record(stream)
-        B.kvs_prefill_attention(q, k, v, out, causal=True, workspace=ws)
+        B.kvs_prefill_attention(q, k, v, out, causal=causal, workspace=ws)
         b.record(stream)
     torch.cuda.synchronize()
     ms = statistics.median(a.elapsed_time(b) for a, b in ev)
-    flops = 4.0 * D * H * S * (S + 1) / 2  # QK^T and PV over the causal triangle
+    # QK^T and PV over the causal triangle, or the full square
+    flops = 4.0 * D * H * (S * (S + 1) / 2 if causal else S * S)
     tf = flops / (ms * 1e-3) / 1e12
     peak, kind = tensor_peak()
     return {"kernel": "prefill_pack_kernel + prefill_tc_kernel (kvs_prefill_attention)",
-            "heads": H, "seq_len": S, "head_dim": D, "causal": True, "dtype": "f16 x f16 -> f32",
+            "heads": H, "seq_len": S, "head_dim": D, "causal": causal,
+            "dtype": "f16 x f16 -> f32",
             "us_per_call": 1e3 * ms, "flops_per_call": flops,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / peak, "peak_source": kind}}
@@ -348,6 +350,12 @@ def main():
                     help="skip the batched argmax measurement")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the tensor-core prefill measurement")
+    ap.add_argument("--only", choices=["argmax", "prefill"], default=None,
+                    help="run only that measurement and print its JSON object (profiling)")
+    ap.add_argument("--prefill-shape", default=None,
+                    help="H,S,D of the prefill measurement (default 32,4096,128)")
+    ap.add_argument("--prefill-full", action="store_true",
+                    help="prefill without the causal mask")
     ap.add_argument("--schedule", default="auto", choices=["auto", "persistent", "cluster"],
                     help="attention kernel (kvs_set_schedule)")
     args = ap.parse_args()
@@ -376,6 +384,17 @@ def main():
         tdist.init_process_group("nccl", device_id=dev)
     kbuild.build()
     B.lib()
+    if args.only is not None:  # one measurement alone, for profiling
+        stream = torch.cuda.current_stream()
+        if args.only == "argmax":
+            res = time_argmax(B, torch, w.M, dev, stream, iters=args.steps)
+        else:
+            shape = (tuple(int(v) for v in args.prefill_shape.split(","))
+                     if args.prefill_shape else PREFILL_SHAPE)
+            res = time_prefill(B, torch, dev, stream, iters=args.steps, shape=shape,
+                               causal=not args.prefill_full)
+        print(json.dumps(res), flush=True)
+        return
     B.kvs_set_schedule({"auto": B.KVS_SCHEDULE_AUTO, "persistent": B.KVS_SCHEDULE_PERSISTENT,
                         "cluster": B.KVS_SCHEDULE_CLUSTER}[args.schedule])
     kernel = ("cluster" if B.kvs_schedule_for(w.M, w.num_heads, w.num_kv_heads, w.head_dim,
