@@ -80,6 +80,18 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M rows in TMEM lanes, K FP16 values
+// packed two per 32-bit column, the lower half first), FP16 inputs, FP32
+// accumulate.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // The mbarrier gets one arrival when every tcgen05.mma this thread issued is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
@@ -126,6 +138,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) 
       "r"(__float_as_uint(r[24])), "r"(__float_as_uint(r[25])), "r"(__float_as_uint(r[26])),
       "r"(__float_as_uint(r[27])), "r"(__float_as_uint(r[28])), "r"(__float_as_uint(r[29])),
       "r"(__float_as_uint(r[30])), "r"(__float_as_uint(r[31]))
+      : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane, written.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
+      "r"(w[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
@@ -264,31 +286,38 @@ __global__ void __launch_bounds__(256)
 
 // Block layout: two 128-row query tiles (A = 2b, B = 2b + 1) share every K
 // and V^T tile.  Warpgroup 0 does the softmax of tile A, warpgroup 1 that of
-// tile B (thread t of a warpgroup owns row t, TMEM lane t), and warp 8 moves
-// the tiles and issues the tensor-core work, so one tile's softmax runs
-// while the other tile's products are on the tensor cores.
+// tile B (thread t of a warpgroup owns row t, TMEM lane t), warp 8 issues
+// the tensor-core work and warp 9 moves the tiles, so one tile's softmax
+// runs while the other tile's products are on the tensor cores.
 // TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D),
-// O_B [256 + D, 256 + 2D).
+// O_B [256 + D, 256 + 2D).  The softmax writes P_x in FP16 over the first
+// 64 columns of S_x (two values per column) and P V reads it from there, so
+// no shared memory holds P; K has two stages and V^T three.
 constexpr int kPWarpgroups = 2;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kPMmaWarp = 4 * kPWarpgroups;            // warp 8
-constexpr int kPBlockThreads = (kPMmaWarp + 1) * 32;   // 288
+constexpr int kPCopyWarp = kPMmaWarp + 1;              // warp 9
+constexpr int kPBlockThreads = (kPCopyWarp + 1) * 32;  // 320
 constexpr uint32_t kPTmemCols = 512;
 
 template <int D>
 struct PGeo {
   static constexpr int TILE = kPM * D * 2;  // one FP16 tile of Q, K or V^T
-  static constexpr int P_BYTES = kPM * kPN * 2;
   static constexpr int OFF_Q = 0;                        // Q_A, Q_B
-  static constexpr int OFF_K = OFF_Q + 2 * TILE;         // K, one stage
-  static constexpr int OFF_V = OFF_K + TILE;             // V^T, two stages
-  static constexpr int OFF_P = OFF_V + 2 * TILE;         // P_A, P_B
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  // barriers: q, kfull, vfull[2], sfull[2], pfull[2], ofree[2], kfree, vfree
-  static constexpr int NBAR = 12;
+  static constexpr int KS = 2;                           // K stages
+  static constexpr int VS = 3;                           // V^T stages
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int OFF_V = OFF_K + KS * TILE;
+  static constexpr int OFF_BAR = OFF_V + VS * TILE;
+  // barriers: q, kfull[KS], kfree[KS], vfull[VS], vfree[VS], sfull[2], pfull[2], pvdone
+  static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 5;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;    // TMEM base address
   static constexpr int OFF_FLAG = OFF_TMEM + 8;          // abort, no_abort
-  static constexpr int SMEM_BYTES = OFF_FLAG + 16;
+  // A block holds all 512 TMEM columns, so a second block on the SM would
+  // only wait for them: ask for more than half of the SM's 228 KB of shared
+  // memory (less the 1 KB each block reserves) so that one block fits.
+  static constexpr int ONE_PER_SM = 116 * 1024;
+  static constexpr int SMEM_BYTES = OFF_FLAG + 16 > ONE_PER_SM ? OFF_FLAG + 16 : ONE_PER_SM;
   static_assert(SMEM_BYTES <= 227 * 1024, "one block per SM must fit");
 };
 
@@ -299,14 +328,15 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
   using PG = PGeo<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PG::OFF_BAR);
+  constexpr int KS = PG::KS, VS = PG::VS;
   uint64_t *bar_q = bars + 0;
-  uint64_t *kfull = bars + 1;
-  uint64_t *vfull = bars + 2;  // [2]
-  uint64_t *sfull = bars + 4;  // [2]: S_A, S_B ready (commit)
-  uint64_t *pfull = bars + 6;  // [2]: P_x written, O_x rescaled (128 arrivals)
-  uint64_t *ofree = bars + 8;  // [2]: P V of tile x done (commit)
-  uint64_t *kfree = bars + 10; // the S products of the current key tile done (commit)
-  uint64_t *vfree = bars + 11; // the P V products of the current key tile done (commit)
+  uint64_t *kfull = bar_q + 1;     // [KS] K stage landed
+  uint64_t *kfree = kfull + KS;    // [KS] the S products reading a K stage done (commit)
+  uint64_t *vfull = kfree + KS;    // [VS] V^T stage landed
+  uint64_t *vfree = vfull + VS;    // [VS] the P V products reading a V^T stage done (commit)
+  uint64_t *sfull = vfree + VS;    // [2] S_x ready (commit)
+  uint64_t *pfull = sfull + 2;     // [2] P_x written, O_x rescaled (128 arrivals)
+  uint64_t *pvdone = pfull + 2;    // every product issued so far is done (commit)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PG::OFF_TMEM);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + PG::OFF_FLAG);
   volatile int *no_abort = reinterpret_cast<volatile int *>(smem + PG::OFF_FLAG + 4);
@@ -340,15 +370,19 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
+    for (int j = 0; j < KS; ++j) {
+      mbar_init(&kfull[j], 1);
+      mbar_init(&kfree[j], 1);
+    }
+    for (int j = 0; j < VS; ++j) {
+      mbar_init(&vfull[j], 1);
+      mbar_init(&vfree[j], 1);
+    }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&vfull[x], 1);
       mbar_init(&sfull[x], 1);
       mbar_init(&pfull[x], kPM);
-      mbar_init(&ofree[x], 1);
     }
-    mbar_init(kfull, 1);
-    mbar_init(kfree, 1);
-    mbar_init(vfree, 1);
+    mbar_init(pvdone, 1);
     *abort = 0;
     *no_abort = 0;
     fence_mbar_init();
@@ -358,71 +392,84 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
+  float l = 0.f;  // softmax threads: the row's sum of 2^(s - m)
 
-  if (warp == kPMmaWarp) {
-    // ======================= copies and tensor-core work =====================
+  if (warp == kPCopyWarp) {
+    // ======================= copies ==========================================
+    // K(n) goes to stage n % KS once the S products of K(n - KS) are done,
+    // V^T(n) to stage n % VS once the P V products of V^T(n - VS) are.
     if (lane == 0) {
       unsigned char *sQ = smem + PG::OFF_Q;
       unsigned char *sK = smem + PG::OFF_K;
       unsigned char *sV = smem + PG::OFF_V;
-      unsigned char *sP = smem + PG::OFF_P;
-      uint32_t k_issued = 0, v_issued = 0;
-      auto issue_k = [&]() {  // the single K stage
-        mbar_arrive_expect_tx(kfull, PG::TILE);
-        bulk_g2s(sK, gKh + k_issued * tile, PG::TILE, kfull);
-        ++k_issued;
-      };
-      auto issue_v = [&]() {  // V^T(n) into stage n & 1
-        const int st = v_issued & 1;
-        mbar_arrive_expect_tx(&vfull[st], PG::TILE);
-        bulk_g2s(sV + st * PG::TILE, gVh + v_issued * tile, PG::TILE, &vfull[st]);
-        ++v_issued;
-      };
-      // Order on the tensor cores, per key tile kt: P V_A(kt), S_A(kt+1),
-      // P V_B(kt), S_B(kt+1).  Softmax A(kt+1) then runs while P V_B(kt) and
-      // softmax B(kt) are in progress: the two tiles alternate.
-      auto issue_s = [&](int x) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_f16(tmem + x * kPN, smem_desc(sQ + x * PG::TILE + ks * 256, 128, kSboD),
-                  smem_desc(sK + ks * 256, 128, kSboD), kIdescS, ks > 0 ? 1u : 0u);
-        mma_commit(&sfull[x]);
-      };
-      auto issue_pv = [&](int x, int kt) {
-        const unsigned char *v_st = sV + (kt & 1) * PG::TILE;
-#pragma unroll
-        for (int ks = 0; ks < kPN / 16; ++ks)
-          mma_f16(tmem + 2 * kPN + x * D,
-                  smem_desc(sP + x * PG::P_BYTES + ks * 256, 128, kSboN),
-                  smem_desc(v_st + ks * 256, 128, kSboN), kIdescO, (kt > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(&ofree[x]);
-      };
       mbar_arrive_expect_tx(bar_q, (has_b ? 2 : 1) * PG::TILE);
       bulk_g2s(sQ, gQh + (size_t)qa * tile, PG::TILE, bar_q);
       if (has_b) bulk_g2s(sQ + PG::TILE, gQh + (size_t)(qa + 1) * tile, PG::TILE, bar_q);
-      issue_k();
-      while ((int)v_issued < n_all && v_issued < 2) issue_v();
-      bool ok = mbar_wait(bar_q, 0, abort) && mbar_wait(kfull, 0, abort);
+      int n = 0;
+      bool ok = true;
+      for (; n < n_all; ++n) {
+        const int ks = n % KS, vs = n % VS;
+        if (n >= KS && !(ok = mbar_wait(&kfree[ks], (uint32_t)((n - KS) / KS) & 1u, abort)))
+          break;
+        mbar_arrive_expect_tx(&kfull[ks], PG::TILE);
+        bulk_g2s(sK + ks * PG::TILE, gKh + (size_t)n * tile, PG::TILE, &kfull[ks]);
+        if (n >= VS && !(ok = mbar_wait(&vfree[vs], (uint32_t)((n - VS) / VS) & 1u, abort))) {
+          // K(n) is in flight: let it land
+          mbar_wait(&kfull[ks], (uint32_t)(n / KS) & 1u, no_abort);
+          break;
+        }
+        mbar_arrive_expect_tx(&vfull[vs], PG::TILE);
+        bulk_g2s(sV + vs * PG::TILE, gVh + (size_t)n * tile, PG::TILE, &vfull[vs]);
+      }
+      if (!ok) {
+        *abort = 1;
+        record_status(d_status, KVS_ERR_TIMEOUT);
+        // let the copies already issued land before the block exits
+        mbar_wait(bar_q, 0, no_abort);
+        for (int j = (n > KS ? n - KS : 0); j < n; ++j)
+          mbar_wait(&kfull[j % KS], (uint32_t)(j / KS) & 1u, no_abort);
+        for (int j = (n > VS ? n - VS : 0); j < n; ++j)
+          mbar_wait(&vfull[j % VS], (uint32_t)(j / VS) & 1u, no_abort);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kPMmaWarp) {
+    // ======================= tensor-core work ================================
+    if (lane == 0) {
+      // shared-memory descriptors of the tiles; step ks of a product adds
+      // ks * 256 bytes (16 in the descriptor's address field)
+      const uint64_t dq0 = smem_desc(smem + PG::OFF_Q, 128, kSboD);
+      const uint64_t dk0 = smem_desc(smem + PG::OFF_K, 128, kSboD);
+      const uint64_t dv0 = smem_desc(smem + PG::OFF_V, 128, kSboN);
+      constexpr uint64_t kTileStep = PG::TILE >> 4;  // one tile further on
+      auto issue_s = [&](int x, int n) {  // S_x(n) = Q_x K(n)^T
+        const uint64_t a = dq0 + (x ? kTileStep : 0), b = dk0 + (uint64_t)(n % KS) * kTileStep;
+        const uint32_t d = tmem + x * kPN;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_f16(d, a + 16 * ks, b + 16 * ks, kIdescS, ks > 0 ? 1u : 0u);
+        mma_commit(&sfull[x]);
+      };
+      auto issue_pv = [&](int x, int n) {  // O_x (+)= P_x(n) V^T(n), P_x from TMEM
+        const uint64_t b = dv0 + (uint64_t)(n % VS) * kTileStep;
+        const uint32_t d = tmem + 2 * kPN + x * D;
+        const uint32_t a = tmem + x * kPN;
+#pragma unroll
+        for (int ks = 0; ks < kPN / 16; ++ks)
+          mma_f16_ts(d, a + ks * 8, b + 16 * ks, kIdescO, (n > 0 || ks > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar_q, 0, abort) && mbar_wait(&kfull[0], 0, abort);
       if (ok) {
         tc_fence_after();
-        if (n_a > 0) issue_s(0);
-        if (n_b > 0) issue_s(1);
-        mma_commit(kfree);
+        if (n_a > 0) issue_s(0, 0);
+        if (n_b > 0) issue_s(1, 0);
+        mma_commit(&kfree[0]);
       }
+      uint32_t pv_phase = 0;
       for (int kt = 0; kt < n_all && ok; ++kt) {
         const uint32_t ph = (uint32_t)kt & 1u;
-        // the S products of key tile kt are done: bring key tile kt+1 into K
-        ok = mbar_wait(kfree, ph, abort);
-        if (!ok) break;
-        if ((int)k_issued < n_all) issue_k();
-        // the P V products of key tile kt-1 are done: bring V^T(kt+1) into its stage
-        if (kt >= 1) {
-          ok = mbar_wait(vfree, ph ^ 1u, abort);
-          if (!ok) break;
-          if ((int)v_issued < n_all) issue_v();
-        }
-        ok = mbar_wait(&vfull[kt & 1], (kt >> 1) & 1, abort);  // V^T(kt)
-        bool k_next = false;  // key tile kt+1 has landed
+        ok = mbar_wait(&vfull[kt % VS], (uint32_t)(kt / VS) & 1u, abort);  // V^T(kt)
+        bool k_next = false;  // K(kt+1) has landed
         for (int x = 0; x < 2 && ok; ++x) {
           const int n_x = x == 0 ? n_a : n_b;
           if (kt < n_x) {  // P V_x(kt), once softmax x(kt) has written P_x
@@ -431,28 +478,31 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
             tc_fence_after();
             issue_pv(x, kt);
           }
-          if (kt + 1 < n_x) {  // S_x(kt+1)
+          if (kt + 1 < n_x) {  // S_x(kt+1) overwrites P_x(kt): after P V_x(kt)
+            mma_commit(pvdone);
+            ok = mbar_wait(pvdone, pv_phase, abort);
+            pv_phase ^= 1u;
+            if (!ok) break;
             if (!k_next) {
-              ok = mbar_wait(kfull, ph ^ 1u, abort);
+              ok = mbar_wait(&kfull[(kt + 1) % KS], (uint32_t)((kt + 1) / KS) & 1u, abort);
               if (!ok) break;
               tc_fence_after();
               k_next = true;
             }
-            issue_s(x);
+            issue_s(x, kt + 1);
           }
         }
         if (!ok) break;
-        mma_commit(vfree);  // P V(kt)
-        mma_commit(kfree);  // S(kt+1)
+        mma_commit(&vfree[kt % VS]);        // P V(kt)
+        mma_commit(&kfree[(kt + 1) % KS]);  // S(kt+1)
+      }
+      if (ok) {  // the last P V products
+        mma_commit(pvdone);
+        ok = mbar_wait(pvdone, pv_phase, abort);
       }
       if (!ok) {
         *abort = 1;
         record_status(d_status, KVS_ERR_TIMEOUT);
-        // let the copies already issued land before the block exits
-        mbar_wait(bar_q, 0, no_abort);
-        if (k_issued > 0) mbar_wait(kfull, (k_issued - 1) & 1, no_abort);
-        for (uint32_t j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
-          mbar_wait(&vfull[j & 1], (j >> 1) & 1, no_abort);
       }
     }
     __syncwarp();
@@ -463,15 +513,15 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
     const int q_tile = qa + x;
     const int i = q_tile * kPM + t;      // query row
     const int n_x = x == 0 ? n_a : n_b;
-    unsigned char *sPx = smem + PG::OFF_P + x * PG::P_BYTES;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tm_s = tmem + lane_base + x * kPN;
     const uint32_t tm_o = tmem + lane_base + 2 * kPN + x * D;
     float m = neg_inf_f();
-    float l = 0.f;
     for (int kt = 0; kt < n_x; ++kt) {
       const int key0 = kt * kPN;
       const uint32_t ph = (uint32_t)kt & 1u;
+      // S_x(kt) is ready; it was issued after P V_x(kt-1) completed, so O_x
+      // is quiescent too
       if (!mbar_wait(&sfull[x], ph, abort)) {
         failed = true;
         break;
@@ -497,27 +547,21 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       const float m_row = fmaxf(m, mt * sl2);
       const float m_new = (m_row > m + kRescaleLog2) ? m_row : m;
       const float alpha = (m_new == neg_inf_f()) ? 1.f : ex2(m - m_new);
-      // ---- P V of the previous tile must be done before O and P change ----
-      if (kt > 0) {
-        if (!mbar_wait(&ofree[x], ph ^ 1u, abort)) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // ---- rescale the output accumulator (TMEM) where the maximum moved ----
+      if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            float r[32];
-            tmem_ld32(tm_o + ch * 32, r);
-            tmem_wait_ld();
+        for (int ch = 0; ch < D / 32; ++ch) {
+          float r[32];
+          tmem_ld32(tm_o + ch * 32, r);
+          tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) r[u] *= alpha;
-            tmem_st32(tm_o + ch * 32, r);
-          }
-          tmem_wait_st();
+          for (int u = 0; u < 32; ++u) r[u] *= alpha;
+          tmem_st32(tm_o + ch * 32, r);
         }
       }
-      // ---- P (FP16) into shared memory, and its row sum ----
+      // ---- P (FP16) into TMEM over the consumed scores, and its row sum ----
+      // Chunk c's 32 scores are read before P of keys [32c, 32c + 32) goes to
+      // columns [16c, 16c + 16), whose scores were read already.
       // (a row with no key yet has m_new = -inf and every score -inf: p = 0)
       const float mb = (m_new == neg_inf_f()) ? 0.f : m_new;
       float lt = 0.f;
@@ -527,50 +571,55 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
         tmem_ld32(tm_s + ch * 32, r);
         tmem_wait_ld();
         if (masked) mask_keys(r, key0 + ch * 32, S, causal, i);
+        uint32_t w[16];
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float p0 = ex2(fmaf(r[g8 * 8 + 2 * u], sl2, -mb));
-            const float p1 = ex2(fmaf(r[g8 * 8 + 2 * u + 1], sl2, -mb));
-            const __half2 hp = __floats2half2_rn(p0, p1);
-            lt += p0 + p1;
-            w[u] = *reinterpret_cast<const uint32_t *>(&hp);
-          }
-          *reinterpret_cast<uint4 *>(sPx + cm_off(t, ch * 32 + g8 * 8, kPN)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        for (int u = 0; u < 16; ++u) {
+          const float p0 = ex2(fmaf(r[2 * u], sl2, -mb));
+          const float p1 = ex2(fmaf(r[2 * u + 1], sl2, -mb));
+          const __half2 hp = __floats2half2_rn(p0, p1);
+          lt += p0 + p1;
+          w[u] = *reinterpret_cast<const uint32_t *>(&hp);
         }
+        tmem_st16(tm_s + ch * 16, w);
       }
       l = l * alpha + lt;
       m = m_new;
-      fence_proxy_async_shared();  // the tensor cores read P
+      tmem_wait_st();  // P and the rescaled O are in TMEM before P V reads them
       tc_fence_before();
       mbar_arrive(&pfull[x]);
     }
-    if (!failed && n_x > 0) {  // the last P V, then the output rows
-      failed = !mbar_wait(&ofree[x], (uint32_t)(n_x - 1) & 1u, abort);
-      if (!failed) {
-        tc_fence_after();
-        const float inv = 1.f / l;
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float r[32];
-          tmem_ld32(tm_o + ch * 32, r);
-          tmem_wait_ld();
-          if (i < S) {
-            float4 *o4 = reinterpret_cast<float4 *>(out + ((size_t)h * S + i) * D + ch * 32);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              o4[u] = make_float4(r[4 * u] * inv, r[4 * u + 1] * inv, r[4 * u + 2] * inv,
-                                  r[4 * u + 3] * inv);
-          }
-        }
-      }
-    }
+    // the rows are written after the block-wide barrier below, which the
+    // copy warp reaches once the last P V products are done
     if (failed) {
       *abort = 1;
       record_status(d_status, KVS_ERR_TIMEOUT);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp < kPMmaWarp && !failed && !*abort) {
+    const int x = warp >> 2;
+    const int t = threadIdx.x & 127;
+    const int i = (qa + x) * kPM + t;
+    const int n_x = x == 0 ? n_a : n_b;
+    if (n_x > 0) {
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t tm_o = tmem + lane_base + 2 * kPN + x * D;
+      const float inv = 1.f / l;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        float r[32];
+        tmem_ld32(tm_o + ch * 32, r);
+        tmem_wait_ld();
+        if (i < S) {
+          float4 *o4 = reinterpret_cast<float4 *>(out + ((size_t)h * S + i) * D + ch * 32);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            o4[u] = make_float4(r[4 * u] * inv, r[4 * u + 1] * inv, r[4 * u + 2] * inv,
+                                r[4 * u + 3] * inv);
+        }
+      }
     }
   }
   allow_dependent_launch();
