@@ -13,7 +13,8 @@ value      : algorithmic GB/s of the step (live KV bytes read + Q read + O
              written + positions, plus the scatter's row bytes), inputs resident
              in HBM, device time from CUDA events, max over ranks.
 e2e        : the same metric when every step also copies its inputs (q, new K/V
-             rows, positions) from pinned host memory and reads the output back.
+             rows, positions) from pinned host memory and reads the output back,
+             all through kvs_decode_step_host (one C call per layer).
 roofline   : the step kernel (the step's one launch): its algorithmic bytes /
              its mean event-timed duration, against the measured HBM copy
              bandwidth.
@@ -506,27 +507,23 @@ def main():
         raise SystemExit(f"device status: {B.strerror(int(status.item()))}")
 
     # ---- e2e: host buffers through the public API ----
+    # kvs_decode_step_host: one library call per layer enqueues the copies of
+    # that layer's inputs (pinned host memory) to the device, the fused step,
+    # and the copy of its output back to the host.
     Ke = args.e2e_steps or max(3, min(K, 500))
-    names = ("q", "k_rows", "v_rows")
+    names = ("q", "k_rows", "v_rows", "positions")
     host = [{k: t[k].cpu().pin_memory() for k in names} for t in ts]
-    host_pos = ts[0]["positions"].cpu().pin_memory()
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    dev_in = [{k: torch.empty_like(t[k]) for k in names} for t in ts]
-    dev_pos = torch.empty_like(ts[0]["positions"])
-    h2d = sum(v.numel() * v.element_size() for h in host for v in h.values()) + \
-        host_pos.numel() * host_pos.element_size()
+    io = B.step_io(w.M, w.num_heads, w.num_kv_heads, w.head_dim, device=dev)
+    h2d = sum(v.numel() * v.element_size() for h in host for v in h.values())
     d2h = sum(o.numel() * o.element_size() for o in host_out)
 
     def e2e_step():
-        dev_pos.copy_(host_pos, non_blocking=True)
         for l, t in enumerate(ts):
-            for k in names:
-                dev_in[l][k].copy_(host[l][k], non_blocking=True)
-            B.kvs_decode_step(dev_in[l]["q"], dev_in[l]["k_rows"], dev_in[l]["v_rows"], dev_pos,
-                              t["k_cache"], t["v_cache"], outs[l], chunk_size=resolved_chunk,
-                              workspace=ws, d_status=status)
-        for l in range(nl):
-            host_out[l].copy_(outs[l], non_blocking=True)
+            B.kvs_decode_step_host(host[l]["q"], host[l]["k_rows"], host[l]["v_rows"],
+                                   host[l]["positions"], t["k_cache"], t["v_cache"], host_out[l],
+                                   chunk_size=resolved_chunk, workspace=ws, io=io,
+                                   d_status=status, stream=stream)
 
     for _ in range(args.warmup):
         e2e_step()

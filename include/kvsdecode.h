@@ -182,6 +182,40 @@ int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
                     size_t workspace_bytes, int *d_status, kvs_stream_t stream);
 
 /*
+ * kvs_decode_step_host -- kvs_decode_step with the step's inputs and its
+ * result in HOST memory: the caller's whole step (host -> device copies of
+ * q, k_rows, v_rows and positions, the fused scatter + attention launch, the
+ * device -> host copy of out) in one call, all enqueued on `stream` in that
+ * order.  The pages' step starts from device tensors; this entry point adds
+ * the transfers a host-side caller makes around it.
+ *
+ *   q          in   [M][H][D] float32, host
+ *   k_rows, v_rows  in  [M][Hkv][D] float32, host
+ *   positions  in   [M] int32, host
+ *   out        out  [M][H][D] float32, host: valid once `stream` has
+ *                   reached the end of the call (synchronise it first)
+ *   io         device scratch of >= kvs_step_io_bytes(M, H, Hkv, D) bytes,
+ *              256-byte aligned, owned by the caller: the device copies of
+ *              the inputs and of out; must not be shared by calls that can
+ *              overlap on the GPU
+ *   k_cache, v_cache, workspace, d_status: device, as kvs_decode_step.
+ * Host buffers in pinned memory (cudaHostAlloc / cudaHostRegister) give
+ * asynchronous copies, and must then stay untouched until the stream has
+ * passed them; pageable host memory works, with copies that block the host.
+ * Errors: as kvs_decode_step, plus NULL (a host pointer or io), ALIGN (io),
+ * WORKSPACE (io_bytes too small), LAUNCH (a copy could not be enqueued).
+ */
+size_t kvs_step_io_bytes(int M, int num_heads, int num_kv_heads, int head_dim);
+
+int kvs_decode_step_host(const float *q, const float *k_rows,
+                         const float *v_rows, const int32_t *positions,
+                         float *k_cache, float *v_cache, float *out, int M,
+                         int num_heads, int num_kv_heads, int head_dim,
+                         int max_len, int chunk_size, void *io, size_t io_bytes,
+                         void *workspace, size_t workspace_bytes,
+                         int *d_status, kvs_stream_t stream);
+
+/*
  * kvs_decode_step_slots -- kvs_decode_step for a serving batch whose
  * sequences live in arbitrary slots of a cache pool, some of them finished
  * (the pages' "Step 2: Build pointer arrays": a per-sequence cache pointer

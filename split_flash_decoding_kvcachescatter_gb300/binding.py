@@ -35,7 +35,7 @@ EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspac
            "kvs_step_graph_create", "kvs_step_graph_launch", "kvs_step_graph_destroy",
            "kvs_set_schedule", "kvs_get_schedule", "kvs_schedule_for", "kvs_prepare",
            "kvs_decode_step_slots", "kvs_argmax", "kvs_prefill_attention",
-           "kvs_prefill_workspace_bytes")
+           "kvs_prefill_workspace_bytes", "kvs_step_io_bytes", "kvs_decode_step_host")
 
 # kvs_schedule values (kernel schedule of the attention entry points)
 KVS_SCHEDULE_AUTO = 0
@@ -81,6 +81,11 @@ def lib() -> ctypes.CDLL:
             L.kvs_decode_step.restype = _I
             L.kvs_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                           _P, _SZ, _P, _P]
+            L.kvs_step_io_bytes.restype = _SZ
+            L.kvs_step_io_bytes.argtypes = [_I, _I, _I, _I]
+            L.kvs_decode_step_host.restype = _I
+            L.kvs_decode_step_host.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                               _I, _P, _SZ, _P, _SZ, _P, _P]
             L.kvs_flash_decode_static.restype = _I
             L.kvs_flash_decode_static.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                   _P, _P]
@@ -287,6 +292,46 @@ def kvs_decode_step(q, k_rows, v_rows, positions, k_cache, v_cache, out, chunk_s
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                _status_ptr(d_status), _stream(stream))
     _check(rc, "kvs_decode_step")
+
+
+def step_io(M, num_heads, num_kv_heads, head_dim, device=None):
+    """A device byte buffer large enough for kvs_decode_step_host's copies."""
+    n = int(lib().kvs_step_io_bytes(M, num_heads, num_kv_heads, head_dim))
+    if n == 0:
+        raise KvsError(KVS_ERR_DIMS, "kvs_step_io_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _host(t: torch.Tensor, name: str, dtype, shape) -> int:
+    if t.is_cuda or t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise TypeError(f"{name}: need a contiguous {dtype} CPU tensor of shape {tuple(shape)}, "
+                        f"got {tuple(t.shape)} {t.dtype} {t.device}")
+    return t.data_ptr()
+
+
+def kvs_decode_step_host(q, k_rows, v_rows, positions, k_cache, v_cache, out, chunk_size=0,
+                         workspace=None, io=None, d_status=None, stream=None):
+    """kvs_decode_step with q, k_rows, v_rows, positions and out in host memory
+    (CPU tensors, pinned for asynchronous copies): the copies in, the fused
+    step and the copy of out back, enqueued by one library call.  out is valid
+    after the stream is synchronised."""
+    M, Hkv, Lmax, D = k_cache.shape
+    H = q.shape[1] if q.dim() == 3 else -1
+    if workspace is None or io is None:
+        raise ValueError("kvs_decode_step_host: pass a workspace and an io buffer "
+                         "(see binding.workspace, binding.step_io)")
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("kvs_decode_step_host: inconsistent cache shapes")
+    rc = lib().kvs_decode_step_host(
+        _host(q, "q", torch.float32, (M, H, D)), _host(k_rows, "k_rows", torch.float32, (M, Hkv, D)),
+        _host(v_rows, "v_rows", torch.float32, (M, Hkv, D)),
+        _host(positions, "positions", torch.int32, (M,)),
+        _f32(k_cache, "k_cache", 4), _f32(v_cache, "v_cache", 4),
+        _host(out, "out", torch.float32, (M, H, D)), M, H, Hkv, D, Lmax, int(chunk_size),
+        io.data_ptr(), io.numel() * io.element_size(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _status_ptr(d_status), _stream(stream))
+    _check(rc, "kvs_decode_step_host")
 
 
 def kvs_decode_step_slots(q, k_rows, v_rows, positions, slots, done, k_pool, v_pool, out,

@@ -182,6 +182,81 @@ int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Offsets of the device copies in the io buffer of kvs_decode_step_host:
+// q, k_rows, v_rows, positions, out, each 256-byte aligned.
+struct IoLayout {
+  size_t q, k, v, pos, out, total;
+};
+
+IoLayout io_layout(int M, int num_heads, int num_kv_heads, int head_dim) {
+  const size_t qo = (size_t)M * num_heads * head_dim * sizeof(float);
+  const size_t kv = (size_t)M * num_kv_heads * head_dim * sizeof(float);
+  IoLayout L;
+  L.q = 0;
+  L.k = L.q + round256(qo);
+  L.v = L.k + round256(kv);
+  L.pos = L.v + round256(kv);
+  L.out = L.pos + round256((size_t)M * sizeof(int32_t));
+  L.total = L.out + round256(qo);
+  return L;
+}
+
+}  // namespace
+
+size_t kvs_step_io_bytes(int M, int num_heads, int num_kv_heads, int head_dim) {
+  if (M < 1 || num_heads < 1 || num_kv_heads < 1 || head_dim < 1) return 0;
+  return io_layout(M, num_heads, num_kv_heads, head_dim).total;
+}
+
+int kvs_decode_step_host(const float *q, const float *k_rows, const float *v_rows,
+                         const int32_t *positions, float *k_cache, float *v_cache, float *out,
+                         int M, int num_heads, int num_kv_heads, int head_dim, int max_len,
+                         int chunk_size, void *io, size_t io_bytes, void *workspace,
+                         size_t workspace_bytes, int *d_status, kvs_stream_t stream) {
+  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
+  if (rc != KVS_OK) return rc;
+  if (M == 0) return KVS_OK;
+  if (!q || !k_rows || !v_rows || !positions || !out || !io) return KVS_ERR_NULL;
+  if (!aligned(io, 256)) return KVS_ERR_ALIGN;
+  const IoLayout L = io_layout(M, num_heads, num_kv_heads, head_dim);
+  if (io_bytes < L.total) return KVS_ERR_WORKSPACE;
+  unsigned char *base = static_cast<unsigned char *>(io);
+  float *dq = reinterpret_cast<float *>(base + L.q);
+  float *dk = reinterpret_cast<float *>(base + L.k);
+  float *dv = reinterpret_cast<float *>(base + L.v);
+  int32_t *dpos = reinterpret_cast<int32_t *>(base + L.pos);
+  float *dout = reinterpret_cast<float *>(base + L.out);
+  rc = check_attention_buffers(dq, k_cache, v_cache, dpos, dout, M, num_heads, num_kv_heads,
+                               head_dim, workspace, workspace_bytes);
+  if (rc != KVS_OK) return rc;
+  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
+  if (chunk <= 0) return -chunk;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t qo = (size_t)M * num_heads * head_dim * sizeof(float);
+  const size_t kv = (size_t)M * num_kv_heads * head_dim * sizeof(float);
+  if (cudaMemcpyAsync(dpos, positions, (size_t)M * sizeof(int32_t), cudaMemcpyHostToDevice,
+                      st) != cudaSuccess ||
+      cudaMemcpyAsync(dq, q, qo, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k_rows, kv, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v_rows, kv, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  const kvs::SeqArgs seqs{dpos, nullptr, nullptr, max_len, M};
+  rc = launch_attention(dq, k_cache, v_cache, seqs, dk, dv, dout, M, num_heads, num_kv_heads,
+                        head_dim, chunk, workspace, d_status, st);
+  if (rc != KVS_OK) return rc;
+  if (cudaMemcpyAsync(out, dout, qo, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  return KVS_OK;
+}
+
 int kvs_decode_step_slots(const float *q, const float *k_rows, const float *v_rows,
                           const int32_t *positions, const int32_t *slots, const uint8_t *done,
                           float *k_pool, float *v_pool, int num_slots, float *out, int M,

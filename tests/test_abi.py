@@ -276,3 +276,47 @@ def test_prefill_workspace_formula(L):
         assert L.kvs_prefill_workspace_bytes(H, S, D) == want
     assert L.kvs_prefill_workspace_bytes(0, 16, 64) == 0
     assert L.kvs_prefill_workspace_bytes(2, 16, 96) == 0
+
+
+def _dsh(L, q=A16, kr=A16, vr=A16, pos=A16, k=A16, v=A16, out=A16, M=1, H=4, Hkv=2, D=64,
+         Lmax=256, C=64, io=A16, iob=1 << 30, ws=A16, wsb=1 << 30):
+    return L.kvs_decode_step_host(q, kr, vr, pos, k, v, out, M, H, Hkv, D, Lmax, C, io, iob, ws,
+                                  wsb, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), B.KVS_ERR_DIMS),
+    (dict(H=6, Hkv=4), B.KVS_ERR_DIMS),
+    (dict(D=96), B.KVS_ERR_UNSUPPORTED),
+    (dict(q=None), B.KVS_ERR_NULL),
+    (dict(kr=None), B.KVS_ERR_NULL),
+    (dict(pos=None), B.KVS_ERR_NULL),
+    (dict(out=None), B.KVS_ERR_NULL),
+    (dict(io=None), B.KVS_ERR_NULL),
+    (dict(k=None), B.KVS_ERR_NULL),
+    (dict(io=A16 + 16), B.KVS_ERR_ALIGN),
+    (dict(k=A16 + 8), B.KVS_ERR_ALIGN),
+    (dict(iob=64), B.KVS_ERR_WORKSPACE),
+    (dict(ws=None), B.KVS_ERR_WORKSPACE),
+    (dict(wsb=64), B.KVS_ERR_WORKSPACE),
+    # host buffers need no alignment: they are only copied from and to
+    (dict(q=A16 + 4, kr=A16 + 4, vr=A16 + 4, pos=A16 + 2, out=A16 + 4, iob=64), B.KVS_ERR_WORKSPACE),
+])
+def test_decode_step_host_validation(L, kw, code):
+    assert _dsh(L, **kw) == code
+
+
+def test_decode_step_host_empty_batch_ok(L):
+    assert _dsh(L, M=0, q=None, kr=None, vr=None, pos=None, k=None, v=None, out=None, io=None,
+                iob=0, ws=None, wsb=0) == 0
+
+
+def test_step_io_bytes_formula(L):
+    # q, k_rows, v_rows, positions, out, each rounded up to 256 bytes
+    def r(x):
+        return -(-x // 256) * 256
+    for M, H, Hkv, D in [(1, 4, 2, 64), (3, 14, 2, 64), (32, 32, 8, 128), (5, 40, 8, 128)]:
+        qo, kv = M * H * D * 4, M * Hkv * D * 4
+        assert L.kvs_step_io_bytes(M, H, Hkv, D) == 2 * r(qo) + 2 * r(kv) + r(4 * M)
+    assert L.kvs_step_io_bytes(0, 4, 2, 64) == 0
+    assert L.kvs_step_io_bytes(1, 4, 0, 64) == 0

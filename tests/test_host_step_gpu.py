@@ -1,0 +1,147 @@
+"""GPU parity of kvs_decode_step_host: the decode step called with its inputs
+and result in host memory (the library enqueues the copies in and out).
+
+Bar as for the device entry points: bit-identical caches, outputs within
+max-abs 2e-5 / max-rel 1e-4 of the f64 oracle, and bit-identical to
+kvs_decode_step on the same inputs (the same kernel runs on the copies).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import gate
+from split_flash_decoding_kvcachescatter_gb300 import binding as B
+from split_flash_decoding_kvcachescatter_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from split_flash_decoding_kvcachescatter_gb300 import build
+    build.build()
+    B.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.fixture(autouse=True, params=[B.KVS_SCHEDULE_PERSISTENT, B.KVS_SCHEDULE_CLUSTER],
+                ids=["persistent", "cluster"])
+def schedule(request, _built):
+    prev = B.kvs_set_schedule(request.param)
+    yield request.param
+    B.kvs_set_schedule(prev)
+
+
+def host_inputs(inp, pinned=True):
+    h = {"q": torch.from_numpy(np.ascontiguousarray(inp.q, np.float32)),
+         "k_rows": torch.from_numpy(np.ascontiguousarray(inp.k_rows, np.float32)),
+         "v_rows": torch.from_numpy(np.ascontiguousarray(inp.v_rows, np.float32)),
+         "positions": torch.from_numpy(np.ascontiguousarray(inp.positions, np.int32))}
+    return {k: v.pin_memory() for k, v in h.items()} if pinned else h
+
+
+def host_step(w, inp, t, pinned=True, io=None, ws=None, status=None):
+    M, H, D = inp.q.shape
+    h = host_inputs(inp, pinned)
+    out = torch.full((M, H, D), float("nan"))
+    if pinned:
+        out = out.pin_memory()
+    io = io if io is not None else B.step_io(M, H, w.num_kv_heads, D, device=DEV)
+    ws = ws if ws is not None else B.workspace(M, H, w.num_kv_heads, D, w.max_len, w.chunk_size,
+                                               device=DEV)
+    B.kvs_decode_step_host(h["q"], h["k_rows"], h["v_rows"], h["positions"], t["k_cache"],
+                           t["v_cache"], out, chunk_size=w.chunk_size, workspace=ws, io=io,
+                           d_status=status)
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny", "small_model"])
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_step_matches_oracle(name, pinned):
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    exp = W.upload(inp, w, DEV, include_new_row=True)
+    t = W.upload(inp, w, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = host_step(w, inp, t, pinned=pinned, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, B.strerror(int(status.item()))
+    gate(out.numpy(), oracle.decode_sequences(inp.q, inp.k_seq, inp.v_seq, inp.positions),
+         where=f"{name} host step")
+    for c in ("k_cache", "v_cache"):
+        assert torch.equal(t[c].view(torch.int32), exp[c].view(torch.int32)), c
+
+
+def test_host_step_equals_device_step_bitwise():
+    w = W.custom(M=5, num_heads=40, num_kv_heads=8, head_dim=128, max_len=1300, seed=23)
+    inp = W.make_inputs(w)
+    t1 = W.upload(inp, w, DEV)
+    t2 = W.upload(inp, w, DEV)
+    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, w.chunk_size,
+                     device=DEV)
+    out_dev = torch.empty_like(t1["q"])
+    B.kvs_decode_step(t1["q"], t1["k_rows"], t1["v_rows"], t1["positions"], t1["k_cache"],
+                      t1["v_cache"], out_dev, chunk_size=w.chunk_size, workspace=ws)
+    torch.cuda.synchronize()
+    out_host = host_step(w, inp, t2)
+    torch.cuda.synchronize()
+    assert torch.equal(out_dev.cpu().view(torch.int32), out_host.view(torch.int32))
+    for c in ("k_cache", "v_cache"):
+        assert torch.equal(t1[c].view(torch.int32), t2[c].view(torch.int32)), c
+
+
+def test_host_steps_in_a_row_share_one_io_buffer():
+    """Three steps of one batch enqueued back to back with one io buffer and
+    no synchronisation between them: the stream orders each step's copies
+    after the previous step's read of out, so each result is its own."""
+    w = W.custom(M=3, num_heads=8, num_kv_heads=2, head_dim=64, max_len=600, seed=29)
+    inp = W.make_inputs(w, positions=np.array([5, 250, 596], np.int32))  # room for 2 more rows
+    t = W.upload(inp, w, DEV)
+    io = B.step_io(w.M, w.num_heads, w.num_kv_heads, w.head_dim, device=DEV)
+    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, w.chunk_size,
+                     device=DEV)
+    rng = np.random.default_rng(31)
+    k_seq = [np.asarray(s, np.float32) for s in inp.k_seq]
+    v_seq = [np.asarray(s, np.float32) for s in inp.v_seq]
+    outs, refs, keep = [], [], []
+    pos = np.asarray(inp.positions, np.int32).copy()
+    for step in range(3):
+        q = rng.standard_normal(inp.q.shape).astype(np.float32)
+        kr = rng.standard_normal(inp.k_rows.shape).astype(np.float32)
+        vr = rng.standard_normal(inp.v_rows.shape).astype(np.float32)
+        if step > 0:
+            pos = pos + 1
+            for i in range(w.M):
+                k_seq[i] = np.concatenate([k_seq[i], kr[i][:, None, :]], axis=1)
+                v_seq[i] = np.concatenate([v_seq[i], vr[i][:, None, :]], axis=1)
+        else:
+            kr, vr = np.asarray(inp.k_rows, np.float32), np.asarray(inp.v_rows, np.float32)
+        h = {n: torch.from_numpy(a).pin_memory() for n, a in
+             (("q", q), ("k_rows", kr), ("v_rows", vr), ("positions", pos.copy()))}
+        out = torch.full(inp.q.shape, float("nan")).pin_memory()
+        B.kvs_decode_step_host(h["q"], h["k_rows"], h["v_rows"], h["positions"], t["k_cache"],
+                               t["v_cache"], out, chunk_size=w.chunk_size, workspace=ws, io=io)
+        keep.append(h)  # the pinned inputs stay alive until the stream is done
+        outs.append(out)
+        refs.append(oracle.decode_sequences(q, k_seq, v_seq, pos))
+    torch.cuda.synchronize()
+    for step, (o, r) in enumerate(zip(outs, refs)):
+        gate(o.numpy(), r, where=f"step {step}")
+
+
+def test_host_step_rejects_device_tensors_in_the_binding():
+    w = W.WORKLOADS["tiny"]
+    inp = W.make_inputs(w)
+    t = W.upload(inp, w, DEV)
+    io = B.step_io(w.M, w.num_heads, w.num_kv_heads, w.head_dim, device=DEV)
+    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, w.chunk_size,
+                     device=DEV)
+    with pytest.raises(TypeError):
+        B.kvs_decode_step_host(t["q"], t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
+                               t["v_cache"], torch.empty(inp.q.shape), chunk_size=w.chunk_size,
+                               workspace=ws, io=io)
