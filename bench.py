@@ -15,6 +15,9 @@ value      : algorithmic GB/s of the step (live KV bytes read + Q read + O
 e2e        : the same metric when every step also copies its inputs (q, new K/V
              rows, positions) from pinned host memory and reads the output back,
              all through kvs_decode_step_host (one C call per layer).
+us_per_call: the step's mean, median, p10 and p90 over the timed steps
+             (L2 scrubbed between steps when the working set fits in it), the
+             hot mean of back-to-back steps, and the two-launch breakdown.
 roofline   : the step kernel (the step's one launch): its algorithmic bytes /
              its mean event-timed duration, against the measured HBM copy
              bandwidth.
@@ -68,6 +71,13 @@ def rank_seed(w, rank):
     return w.seed + 7919 * rank
 
 
+def percentile(xs, q):
+    """Nearest-rank percentile of a list (q in 0..100)."""
+    ys = sorted(xs)
+    k = max(0, min(len(ys) - 1, int(round(q / 100.0 * (len(ys) - 1)))))
+    return ys[k]
+
+
 def reduce_over_ranks(step_ms, e2e_ms, bytes_timed, bytes_e2e, world, device):
     """Max of the timings and sum of the bytes over all ranks (the only
     communication of a multi-rank run; nothing on the data path)."""
@@ -117,6 +127,29 @@ def ncu_traffic(kernel, workload, chunk):
 
 
 VOCAB = 152064  # vocabulary of the pages' batched argmax (PAR-062)
+
+
+def time_stream_read(torch, dev, stream, nbytes=2 << 30, iters=10):
+    """A read-only streaming pass measured in the same run, beside the copy
+    peak of MEASURED_PEAKS.json: torch's sum over a 2 GiB float32 buffer
+    (a library kernel, not one of ours), median of CUDA-event times."""
+    x = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        x.sum()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(iters):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x.sum()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    del x
+    ms = statistics.median(ts)
+    return {"read_gbs": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes,
+            "kernel": "torch.sum over a 2 GiB float32 buffer (read-only)"}
 
 
 def time_argmax(B, torch, M, dev, stream, iters=200):
@@ -506,6 +539,42 @@ def main():
     if int(status.item()) != 0:
         raise SystemExit(f"device status: {B.strerror(int(status.item()))}")
 
+    # ---- hot: the same step back to back, nothing between steps (L2 warm) ----
+    # The eager steps are captured into one CUDA graph of HOT_CHUNK steps and
+    # replayed, so that the host's launch rate does not set the time (the
+    # step graph of --graph is launched back to back as it is).
+    HOT_CHUNK = 20
+    hot_reps = max(1, min(K, 200) // HOT_CHUNK)
+    torch.cuda.synchronize()
+    hot_mode = "step graph launched back to back"
+    if graph is not None:
+        hot_run, KH = step, hot_reps * HOT_CHUNK
+        hot_calls = KH
+    else:
+        try:
+            hot_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(hot_graph):
+                for _ in range(HOT_CHUNK):
+                    eager_step()
+            torch.cuda.synchronize()
+            hot_run, hot_calls, KH = hot_graph.replay, hot_reps, hot_reps * HOT_CHUNK
+            hot_mode = f"graph of {HOT_CHUNK} eager steps, replayed"
+        except RuntimeError as e:  # capture refused: eager steps back to back
+            torch.cuda.synchronize()
+            hot_run, KH = step, hot_reps * HOT_CHUNK
+            hot_calls = KH
+            hot_mode = f"eager steps back to back (capture failed: {str(e)[:80]})"
+    hot_run()
+    torch.cuda.synchronize()
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    for _ in range(hot_calls):
+        hot_run()
+    h1.record(stream)
+    torch.cuda.synchronize()
+    hot_ms = h0.elapsed_time(h1) / KH
+
     # ---- e2e: host buffers through the public API ----
     # kvs_decode_step_host: one library call per layer enqueues the copies of
     # that layer's inputs (pinned host memory) to the device, the fused step,
@@ -550,6 +619,7 @@ def main():
         s1.record(stream)
         torch.cuda.synchronize()
         e2e_ms -= s0.elapsed_time(s1) / Ke
+    live_read = time_stream_read(torch, dev, stream)
     argmax = time_argmax(B, torch, w.M, dev, stream) if not args.no_argmax else None
     prefill = time_prefill(B, torch, dev, stream) if not args.no_prefill else None
     sampler.stop()
@@ -603,6 +673,10 @@ def main():
         },
         "us_per_call": {"decode_step": 1e3 * step_mean_ms,
                         "decode_step_median": 1e3 * statistics.median(step_ms),
+                        "decode_step_p10": 1e3 * percentile(step_ms, 10),
+                        "decode_step_p90": 1e3 * percentile(step_ms, 90),
+                        "decode_step_hot": 1e3 * hot_ms,
+                        "hot_steps": KH, "hot_mode": hot_mode,
                         "kv_scatter": 1e3 * statistics.mean(scatter_ms),
                         "flash_decode": 1e3 * statistics.mean(decode_ms),
                         "breakdown_steps": KB},
@@ -611,7 +685,8 @@ def main():
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": f"{KERNEL_NAMES[kernel]} (kvs_decode_step)",
                      "peak_source": peak_kind,
-                     "bytes_per_launch": ab1["step"]},
+                     "bytes_per_launch": ab1["step"],
+                     "live_stream_read": live_read},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
         "gpu_launches": K * nl,
