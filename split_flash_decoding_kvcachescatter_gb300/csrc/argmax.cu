@@ -205,7 +205,11 @@ int launch_argmax(const float *logits, int M, int V, int32_t *ids, cudaStream_t 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, argmax_cluster_kernel, logits, M, V, ids);
-  return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // leave no stale error for the caller's next check
+    return KVS_ERR_LAUNCH;
+  }
+  return KVS_OK;
 }
 
 }  // namespace kvs

@@ -368,7 +368,11 @@ int launch_cluster_impl(const float *q, float *k_cache, float *v_cache, const Se
   const SeqMap sm{seqs.positions, seqs.slots, seqs.done, max_len, seqs.num_slots, Hkv};
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fd_cluster_kernel<D, G>, q, k_cache, v_cache, sm,
                                            k_rows, v_rows, out, Hkv, qscale, d_status);
-  return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // leave no stale error for the caller's next check
+    return KVS_ERR_LAUNCH;
+  }
+  return KVS_OK;
 }
 
 template <int D>

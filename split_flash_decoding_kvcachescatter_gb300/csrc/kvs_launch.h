@@ -70,7 +70,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  // a refused launch also sets the runtime's last error: clear it, so that
+  // the caller's next CUDA error check does not report it a second time
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
 }
 
 // The sequences of one call: positions, and optionally a cache slot per
