@@ -17,10 +17,11 @@
 //    with the same warp-specialised pipeline and consumer tile as the
 //    persistent kernel (bulk async copies into a ring of stages);
 //  * each block leaves its partial (m, l, acc for the G heads) in its own
-//    shared memory, the cluster synchronises once, and block 0 reads the
-//    CS partials over distributed shared memory, merges them and writes the
+//    shared memory, the cluster synchronises once, and each block reads
+//    the CS partials of an equal share of the output elements over
+//    distributed shared memory, merges them and writes that share of the
 //    output; a second cluster barrier keeps every block's shared memory
-//    alive until block 0 has read it.
+//    alive until all of them have read it.
 // No workspace, no atomics, no global round trip between the partials and
 // the merge.  The fused scatter works as in the persistent kernel: the last
 // block of the cluster writes the new rows and reads row p from them.
@@ -42,6 +43,20 @@ namespace kvs {
 namespace {
 
 constexpr int kMaxClusterDevices = 64;
+constexpr int kMaxClusterSize = 16;  // the largest cluster launched
+
+// Stores into cluster block memory (an address from dsmem_addr); they are
+// visible to that block after the next cluster barrier.
+__device__ __forceinline__ void st_dsmem_f4(uint32_t a, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_f2(uint32_t a, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y)
+               : "memory");
+}
 
 // Block geometry: that of the persistent kernel (4 consumer warps, two
 // blocks per SM).  Measured on GB300, 8 consumer warps at one block per SM
@@ -61,10 +76,21 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   uint64_t *empty = full + C::S;
   volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
   volatile int *no_abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG + 4);
-  // this block's partial, published to the cluster: acc aliases warp 0's
-  // accumulator slot, (m, l) the lane-sum area (both free after publish())
-  float4 *part_acc = reinterpret_cast<float4 *>(smem + C::OFF_MACC);  // [G][D/4]
-  float2 *part_ml = reinterpret_cast<float2 *>(smem + C::OFF_MLL);    // [G]
+  // The partials this block merges, written here by every block of the
+  // cluster (itself included) before the cluster barrier: element j of this
+  // block's share (chunk = E / CS elements) from block r at
+  // recv_acc[r * chunk + j], the (m, l) of head h from block r at
+  // recv_ml[r * G + h].  They use the q slots of ring stages 1 and 2: a
+  // block of this kernel has one run, whose q rows come with its first
+  // stage (stage 0), so no copy ever lands in those slots and nothing else
+  // reads them.
+  constexpr int E = G * C::LPR;  // output float4s of one (i, g)
+  static_assert(C::S >= 3, "the receive areas need ring stages 1 and 2");
+  static_assert(E % kMaxClusterSize == 0, "every cluster size divides the output");
+  static_assert(E * 16 <= C::Q_BYTES && kMaxClusterSize * G * 8 <= C::Q_BYTES,
+                "the receive areas fit the q slots");
+  float4 *recv_acc = reinterpret_cast<float4 *>(smem + C::STAGE_BYTES + 2 * C::KV_BYTES);
+  float2 *recv_ml = reinterpret_cast<float2 *>(smem + 2 * C::STAGE_BYTES + 2 * C::KV_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -77,6 +103,18 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   const int H = Hkv * G;
   const bool scatter = (k_rows != nullptr);
 
+  // The ring's barriers live in shared memory only: set them up while the
+  // previous kernel in the stream may still be finishing.
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::NW);
+    }
+    *abort = 0;
+    *no_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
   grid_dependency_wait();
   const int err = sm.error(i);
   const bool finished = sm.finished(i);
@@ -111,17 +149,6 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   const int L = p + 1;
   const int r0 = (int)((long long)L * rank / ncl);
   const int r1 = (int)((long long)L * (rank + 1) / ncl);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::NW);
-    }
-    *abort = 0;
-    *no_abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
   allow_dependent_launch();
 
   if (warp == C::NW) {
@@ -212,49 +239,53 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
     // A block with no rows publishes m = -inf, l = 0, acc = 0.
     tile_publish<C>(tl, acc, m_run, l_lane);
     consumer_sync(C::NW * 32);
-    for (int e = threadIdx.x; e < G * C::LPR; e += C::NW * 32) {
+    // The block's partial, element by element, into the shared memory of
+    // the block that merges it (remote stores: nothing waits for them here).
+    const int chunk = E / ncl;
+    for (int e = threadIdx.x; e < E; e += C::NW * 32) {
       float4 a;
       float mx, lsum;
       merged_warp_states<C>(smem, e, a, mx, lsum);
-      part_acc[e] = a;  // only this thread reads or writes element e here
-      if (e % C::LPR == 0) part_ml[e / C::LPR] = make_float2(mx, lsum);
+      const int dst = e / chunk;
+      st_dsmem_f4(dsmem_addr(&recv_acc[rank * chunk + (e - dst * chunk)], dst), a);
+      if (e % C::LPR == 0) {  // (m, l) of head h to every block merging part of it
+        const int h = e / C::LPR;
+        const int d_last = (e + C::LPR - 1) / chunk;
+        for (int d = dst; d <= d_last; ++d)
+          st_dsmem_f2(dsmem_addr(&recv_ml[rank * G + h], d), make_float2(mx, lsum));
+      }
     }
   }
 
-  cluster_sync_all();  // every block's partial is in its shared memory
-  if (rank == 0 && warp < C::NW) {
-    constexpr int kMaxCS = 16;
-    for (int e = threadIdx.x; e < G * C::LPR; e += C::NW * 32) {
+  cluster_sync_all();  // every partial is in the shared memory of the block merging it
+  if (warp < C::NW) {
+    // Block r merges elements [r * chunk, (r + 1) * chunk) from its own
+    // shared memory and writes that share of the output.
+    const int chunk = E / ncl;
+    for (int j = threadIdx.x; j < chunk; j += C::NW * 32) {
+      const int e = (int)rank * chunk + j;
       const int h = e / C::LPR;
-      float2 ml[kMaxCS];
       float mx = neg_inf();
-#pragma unroll
-      for (int rr = 0; rr < kMaxCS; ++rr) {
-        if (rr < ncl) {
-          ml[rr] = ld_dsmem_f2(dsmem_addr(part_ml + h, rr));
-          mx = fmaxf(mx, ml[rr].x);
-        }
-      }
+      for (int rr = 0; rr < ncl; ++rr) mx = fmaxf(mx, recv_ml[rr * G + h].x);
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
       float l = 0.f;
-#pragma unroll
-      for (int rr = 0; rr < kMaxCS; ++rr) {
-        if (rr < ncl) {
-          const float w = (ml[rr].x == neg_inf()) ? 0.f : exp2f(ml[rr].x - mx);
-          const float4 b = ld_dsmem_f4(dsmem_addr(part_acc + e, rr));
-          a.x = fmaf(w, b.x, a.x);
-          a.y = fmaf(w, b.y, a.y);
-          a.z = fmaf(w, b.z, a.z);
-          a.w = fmaf(w, b.w, a.w);
-          l = fmaf(w, ml[rr].y, l);
-        }
+      for (int rr = 0; rr < ncl; ++rr) {
+        const float2 ml = recv_ml[rr * G + h];
+        const float w = (ml.x == neg_inf()) ? 0.f : exp2f(ml.x - mx);
+        const float4 b = recv_acc[rr * chunk + j];
+        a.x = fmaf(w, b.x, a.x);
+        a.y = fmaf(w, b.y, a.y);
+        a.z = fmaf(w, b.z, a.z);
+        a.w = fmaf(w, b.w, a.w);
+        l = fmaf(w, ml.y, l);
       }
       const float inv = 1.f / l;
       reinterpret_cast<float4 *>(out)[((size_t)i * H + (size_t)g * G) * C::LPR + e] =
           make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
     }
   }
-  cluster_sync_all();  // block 0 has read every partial: shared memory may go
+  // No block reads another's shared memory after the barrier, and every
+  // remote store came before it: the blocks may exit now.
 }
 
 // ---------------------------------------------------------------------------
