@@ -54,7 +54,7 @@ CSRC = os.path.join(ROOT, "split_flash_decoding_kvcachescatter_gb300", "csrc")
 # while these are unchanged).
 KERNEL_SOURCES = {
     "persistent": ("flash_decode.cu", "fd_tile.cuh", "kvs_device.cuh"),
-    "cluster": ("fd_cluster.cu", "fd_tile.cuh", "kvs_device.cuh"),
+    "cluster": ("fd_cluster.cu", "fd_tile.cuh", "kvs_device.cuh", "kvs_cluster.cuh"),
 }
 KERNEL_NAMES = {"persistent": "fd_step_kernel", "cluster": "fd_cluster_kernel"}
 

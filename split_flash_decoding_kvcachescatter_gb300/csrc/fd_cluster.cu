@@ -35,6 +35,7 @@
 #include <mutex>
 
 #include "fd_tile.cuh"
+#include "kvs_cluster.cuh"
 #include "kvs_device.cuh"
 #include "kvs_launch.h"
 
@@ -44,19 +45,6 @@ namespace {
 
 constexpr int kMaxClusterDevices = 64;
 constexpr int kMaxClusterSize = 16;  // the largest cluster launched
-
-// Stores into cluster block memory (an address from dsmem_addr); they are
-// visible to that block after the next cluster barrier.
-__device__ __forceinline__ void st_dsmem_f4(uint32_t a, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w)
-               : "memory");
-}
-
-__device__ __forceinline__ void st_dsmem_f2(uint32_t a, float2 v) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y)
-               : "memory");
-}
 
 // Block geometry: that of the persistent kernel (4 consumer warps, two
 // blocks per SM).  Measured on GB300, 8 consumer warps at one block per SM
@@ -103,6 +91,9 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   const int H = Hkv * G;
   const bool scatter = (k_rows != nullptr);
 
+  // Every block of the cluster has started once this barrier completes;
+  // it is waited on before the first store into another block's memory.
+  cluster_arrive_relaxed();
   // The ring's barriers live in shared memory only: set them up while the
   // previous kernel in the stream may still be finishing.
   if (threadIdx.x == 0) {
@@ -210,6 +201,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       }
     }
     __syncwarp();
+    cluster_wait();  // the split barrier of the kernel entry
   } else {
     // ===================== consumer warps ===================================
     const TileLane<C> tl = tile_lane<C>(smem, warp, lane);
@@ -240,7 +232,9 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
     tile_publish<C>(tl, acc, m_run, l_lane);
     consumer_sync(C::NW * 32);
     // The block's partial, element by element, into the shared memory of
-    // the block that merges it (remote stores: nothing waits for them here).
+    // the block that merges it (remote stores: nothing waits for them here),
+    // once every block of the cluster has started.
+    cluster_wait();
     const int chunk = E / ncl;
     for (int e = threadIdx.x; e < E; e += C::NW * 32) {
       float4 a;
