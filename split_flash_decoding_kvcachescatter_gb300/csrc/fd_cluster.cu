@@ -26,10 +26,11 @@
 // the merge.  The fused scatter works as in the persistent kernel: the last
 // block of the cluster writes the new rows and reads row p from them.
 //
-// Every thread of every block reaches both cluster barriers on every path
-// (the only early exit, an invalid position, is taken by the whole cluster
-// before the first barrier), and every mbarrier wait is bounded in time, so
-// a lost copy ends in KVS_ERR_TIMEOUT, never in a hang.
+// Every thread of every block arrives at the entry barrier, waits on it,
+// and passes the merge barrier on every path (the only early exit, a bad
+// position or a finished sequence, is taken by the whole cluster before any
+// wait), and every mbarrier wait is bounded in time, so a lost copy ends in
+// KVS_ERR_TIMEOUT, never in a hang.
 
 #include <cmath>
 #include <mutex>
@@ -125,7 +126,10 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
             __ldg(reinterpret_cast<const float4 *>(v_rows) + src + e - D4);
     }
   }
-  if (err != KVS_OK || finished) {  // the whole cluster leaves here, before any cluster barrier
+  // The whole cluster leaves here (its blocks share i) before any wait on a
+  // cluster barrier and before any remote store; it has only arrived at the
+  // entry barrier, which no thread then waits on.
+  if (err != KVS_OK || finished) {
     if (err != KVS_OK && rank == 0) {
       if (!finished) {  // a finished sequence's output is left as it is
         const float nan = __int_as_float(0x7fc00000);
