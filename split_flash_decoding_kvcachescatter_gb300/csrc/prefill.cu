@@ -15,19 +15,21 @@
 //    K-adjacent ones 128 B apart); V is stored transposed (head_dim rows of
 //    128 keys), so that P V is again a K-major product.  Every tile is one
 //    contiguous block, moved later by a single 1-D bulk copy (TMA).
-//  * Attention block = (head, two 128-row query tiles A and B), 9 warps:
+//  * Attention block = (head, two 128-row query tiles A and B), 10 warps:
 //    warpgroup 0 runs the softmax of tile A, warpgroup 1 that of tile B
-//    (thread t owns query row t, which is TMEM lane t), and warp 8 moves the
-//    tiles and issues the tensor-core work (tcgen05.mma, M = 128, K = 16,
-//    FP32 accumulators in TMEM, completion by tcgen05.commit on mbarriers)
-//    in the order P V_A(kt), S_A(kt+1), P V_B(kt), S_B(kt+1), so one tile's
-//    softmax runs while the other tile's products are on the tensor cores.
+//    (thread t owns query row t, which is TMEM lane t), warp 8 issues the
+//    tensor-core work (tcgen05.mma, M = 128, K = 16, FP32 accumulators in
+//    TMEM, completion by tcgen05.commit on mbarriers) in the order
+//    P V_A(kt), S_A(kt+1), P V_B(kt), S_B(kt+1), and warp 9 moves the tiles
+//    (K through two stages, V^T through three), so one tile's softmax runs
+//    while the other tile's products are on the tensor cores.
 //  * Softmax: each thread reads its score row from TMEM (tcgen05.ld
 //    32x32b) twice -- row maximum, then p = 2^(s - m) on the special-function
-//    unit, rounded to FP16 into the P tile in shared memory, the FP32 values
+//    unit, rounded to FP16 and written back over the scores already read
+//    (tcgen05.st), where P V takes it as its A operand; the FP32 values are
 //    summed into the row sum.  The reference maximum moves only when the row
-//    maximum grows by more than 2^8, so the output accumulator in TMEM is
-//    rarely rescaled.
+//    maximum grows by more than 2^8 (log2 units), so the output accumulator
+//    in TMEM is rarely rescaled.
 //  * Causal: key tiles after the query tile are skipped; keys j > i and keys
 //    past seq_len get p = 0 (selects, on the diagonal and last tiles only).
 // Every mbarrier wait is bounded; on expiry the block records
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       mbar_arrive(&pfull[x]);
     }
     // the rows are written after the block-wide barrier below, which the
-    // copy warp reaches once the last P V products are done
+    // tensor-core warp reaches once the last P V products are done
     if (failed) {
       *abort = 1;
       record_status(d_status, KVS_ERR_TIMEOUT);
