@@ -15,9 +15,10 @@
  *
  * Conventions shared by every entry point
  *   - All tensors are float32, C-contiguous, in DEVICE memory owned by the
- *     caller; positions are int32 in device memory.  The library never
- *     allocates, frees or synchronises; it does not keep pointers after a
- *     call returns.
+ *     caller; positions are int32 in device memory.  (kvs_decode_step_host
+ *     is the exception: its inputs and result are in host memory.)  The
+ *     library never allocates, frees or synchronises; it does not keep
+ *     pointers after a call returns.
  *   - Layouts (M sequences, H = num_heads query heads, Hkv = num_kv_heads,
  *     G = H / Hkv, D = head_dim, Lmax = max_len):
  *         q, out              [M][H][D]
