@@ -41,9 +41,15 @@
  *     is skipped; the scatter writes nothing for it and its attention
  *     output rows are NaN), KVS_ERR_TIMEOUT if an internal pipeline wait
  *     exceeded its bound (the kernel returns instead of hanging; outputs
- *     of that call are undefined).
- *   - Entry points are stateless and may be called from several host
- *     threads on different streams.
+ *     of that call are undefined, nothing outside them is written, and the
+ *     context stays usable).
+ *   - State: a call keeps nothing of its arguments.  Two process-wide
+ *     settings do apply to every call: the kernel schedule
+ *     (kvs_set_schedule; which attention kernel a call runs) and, per
+ *     device, the wait bound (kvs_set_wait_limit_ns).  A change made on
+ *     one host thread applies to the calls that other threads make from
+ *     then on.  Otherwise the entry points may be called from several host
+ *     threads on different streams (with separate workspaces).
  */
 #ifndef KVSDECODE_H
 #define KVSDECODE_H
@@ -65,7 +71,9 @@ typedef enum kvs_status {
   KVS_ERR_LAUNCH = 6,      /* CUDA reported a launch or device-query error */
   KVS_ERR_POSITION = 7,    /* device: a position outside [0, max_len) */
   KVS_ERR_TIMEOUT = 8,     /* device: a bounded pipeline wait expired */
-  KVS_ERR_SLOT = 9         /* device: a cache slot outside [0, num_slots) */
+  KVS_ERR_SLOT = 9,        /* device: a cache slot outside [0, num_slots) */
+  KVS_ERR_MEMORY = 10      /* the device could not provide memory the library
+                              itself holds (kvs_flash_decode_static) */
 } kvs_status;
 
 /* A cudaStream_t, passed as an opaque pointer so this header needs no CUDA
@@ -97,10 +105,20 @@ int kvs_kv_scatter(const float *k_rows, const float *v_rows,
 /*
  * kvs_choose_chunk_size -- the chunk size used when a caller passes
  * chunk_size = 0 (the pages fix one compile-time FLASH_DECODE_CHUNK_SIZE).
- * Chunks are the scheduling atoms of the persistent chunk kernel, so the
- * chunk size sets how evenly the live rows are shared among the SMs; the
- * rule returns a power of two in [16, 64] that grows with the cache size
- * per SM.  Returns a chunk size in rows (>= 1), or a negative kvs_status.
+ *
+ * On the pages the chunk size also fixes the split count: a sequence of L
+ * rows gets ceil(L / chunk) chunks, each one block of the chunk kernel.
+ * Here the split is made separately: the persistent kernel cuts the live
+ * rows of the whole batch, read from the device positions at run time,
+ * into equal columns, one per resident block (2 per SM), so the number of
+ * pieces a sequence is split into follows from its length and the batch,
+ * whatever the chunk size.  Chunks are only the granule of that cut: a
+ * block's range starts and ends on chunk boundaries, and partials are kept
+ * per run of chunks, not per chunk.  So the rule depends on the SM count
+ * and the cache size (not on positions, which the host does not read).
+ * With r = M * num_kv_heads * max_len / (2 * SMs) cache rows per block
+ * (integer division) it returns 16 for r < 4096, 32 for r < 8192, else 64.
+ * Returns a chunk size in rows (>= 1), or a negative kvs_status.
  *   num_sms > 0: use that SM count; num_sms <= 0: query the current device.
  */
 int kvs_choose_chunk_size(int M, int num_kv_heads, int head_dim, int max_len,
@@ -151,7 +169,14 @@ size_t kvs_flash_decode_workspace_bytes(int M, int num_heads, int num_kv_heads,
  *   workspace       device scratch of >= kvs_flash_decode_workspace_bytes
  *                   bytes, 256-byte aligned; contents need no initialisation
  *                   and are overwritten; it must not be shared by calls
- *                   that can overlap on the GPU.
+ *                   that can overlap on the GPU.  Its first 4 bytes are an
+ *                   epoch that the completion counters' tags include; a
+ *                   call that gives up on a wait (KVS_ERR_TIMEOUT) changes
+ *                   it.  A CUDA graph that the caller captures around these
+ *                   calls replays the same tags: after a replay that
+ *                   reported KVS_ERR_TIMEOUT, zero the workspace before the
+ *                   next replay (kvs_step_graph needs nothing: it writes a
+ *                   fresh epoch at every replay).
  * Errors: NULL, DIMS, UNSUPPORTED, ALIGN, WORKSPACE, LAUNCH on the host;
  * POSITION, TIMEOUT via d_status.
  */
@@ -217,6 +242,41 @@ int kvs_decode_step_host(const float *q, const float *k_rows,
                          int *d_status, kvs_stream_t stream);
 
 /*
+ * kvs_step_io_layout -- where each array sits in a buffer of
+ * kvs_step_io_bytes(M, H, Hkv, D) bytes: offsets[0..4] receive the byte
+ * offsets of q, k_rows, v_rows, positions and out (each 256-byte aligned,
+ * in that order), offsets[5] the total size.  The device io buffer of
+ * kvs_decode_step_host and kvs_decode_step_host_io has this layout, and so
+ * has the host buffer of kvs_decode_step_host_io.
+ *   offsets  out  size_t[6], host
+ * Errors: DIMS (a size < 1), NULL.
+ */
+int kvs_step_io_layout(int M, int num_heads, int num_kv_heads, int head_dim, size_t *offsets);
+
+/*
+ * kvs_decode_step_host_io -- kvs_decode_step_host for a caller that keeps
+ * the step's inputs and result in ONE host buffer laid out like the device
+ * io buffer (kvs_step_io_layout): q, k_rows, v_rows and positions at their
+ * offsets go to the device in one host -> device copy (the padding between
+ * them included), and out comes back to its offset in one device -> host
+ * copy; in between, the fused scatter + attention launch.  All three are
+ * enqueued on `stream` in that order.  Two copies per step instead of five:
+ * at these sizes each copy costs mostly its fixed latency.
+ *
+ *   host_io  in/out  host buffer of >= kvs_step_io_bytes bytes with that
+ *                    layout, pinned (cudaHostAlloc / cudaHostRegister) for
+ *                    asynchronous copies; the inputs must stay untouched,
+ *                    and out is valid, once `stream` has passed the call
+ *   io, k_cache, v_cache, workspace, d_status, other arguments: as
+ *   kvs_decode_step_host.
+ * Errors: as kvs_decode_step_host.
+ */
+int kvs_decode_step_host_io(void *host_io, float *k_cache, float *v_cache, int M,
+                            int num_heads, int num_kv_heads, int head_dim, int max_len,
+                            int chunk_size, void *io, size_t io_bytes, void *workspace,
+                            size_t workspace_bytes, int *d_status, kvs_stream_t stream);
+
+/*
  * kvs_decode_step_slots -- kvs_decode_step for a serving batch whose
  * sequences live in arbitrary slots of a cache pool, some of them finished
  * (the pages' "Step 2: Build pointer arrays": a per-sequence cache pointer
@@ -272,7 +332,11 @@ int kvs_decode_step_slots(const float *q, const float *k_rows,
  * launches.  The graph and its executable are CUDA objects owned by the
  * handle; the library allocates no device memory.
  *
- * kvs_step_graph_launch enqueues the whole step on `stream`.
+ * kvs_step_graph_launch enqueues the whole step on `stream`.  The graph
+ * starts with a 4-byte write of a fresh value to the workspace epoch (see
+ * kvs_flash_decode), so a replay after one that timed out is clean.  One
+ * handle is launched by one host thread at a time (a lock inside orders
+ * concurrent launches).
  * kvs_step_graph_destroy releases the handle (NULL is a no-op).
  */
 typedef struct kvs_step_graph kvs_step_graph;
@@ -309,12 +373,21 @@ int kvs_step_graph_destroy(kvs_step_graph *graph);
  * library's device code is loaded holds that buffer until the process
  * exits.  Problems whose partials need more
  * (kvs_flash_decode_workspace_bytes(...) > KVS_STATIC_WORKSPACE_BYTES)
- * are rejected with KVS_ERR_WORKSPACE before anything is enqueued; use
+ * are rejected with KVS_ERR_WORKSPACE before anything is enqueued, whatever
+ * kernel the schedule would pick for them (the cluster kernel needs no
+ * scratch, but the size rule does not look at the schedule); use
  * kvs_flash_decode with your own workspace for those.
  *
  * Set-up: the first call on each device (with that device current) looks up
- * the buffer's device address; make that first call before any stream
- * capture on that device.
+ * the buffer's device address.  CUDA loads device code lazily, so that
+ * first call is also when the device commits the 32 MiB: a caller under a
+ * fixed memory budget should make one call at start-up, while it may still
+ * allocate.  If the device cannot provide the buffer then, the call returns
+ * KVS_ERR_MEMORY (other set-up failures: KVS_ERR_LAUNCH).  Make that first
+ * call before any stream capture on that device.  The address is kept for
+ * the life of the process: after cudaDeviceReset (or anything else that
+ * destroys the device's primary context) do not call this entry point
+ * again on that device.
  *
  * Sharing: all calls on a device use the same buffer, which keeps whatever
  * the last call left in it.  Nothing in it has to start at zero (each call
@@ -416,6 +489,30 @@ int kvs_get_schedule(void);
  * automatic schedule answers KVS_SCHEDULE_PERSISTENT. */
 int kvs_schedule_for(int M, int num_heads, int num_kv_heads, int head_dim,
                      int max_len);
+
+/*
+ * kvs_set_wait_limit_ns -- the bound on each pipeline wait of this
+ * library's kernels on the current device (default
+ * KVS_WAIT_LIMIT_DEFAULT_NS = 2 s).  A wait that runs past it makes its
+ * kernel record KVS_ERR_TIMEOUT in d_status and return instead of waiting
+ * on; at the default only a fault could take that long.  Lowering the bound
+ * makes waits run out on purpose, so that a caller can test its handling of
+ * KVS_ERR_TIMEOUT; under a bound below the default the waits poll without
+ * sleeping, and 0 ends the first wait that does not find its data ready.
+ * Whatever the bound, a block that gives up still lets every copy and
+ * tensor-core product it issued finish before it exits (those waits keep
+ * 2 s), and leaves the context usable.  Takes effect for kernels that start
+ * after the call returns (a replayed CUDA graph included).  The value
+ * applies to every host thread's calls on that device; set it back when
+ * done.  The call synchronises with the device like cudaMemcpyToSymbol; it
+ * must not be made during a stream capture.
+ *   ns        0 .. KVS_WAIT_LIMIT_DEFAULT_NS, else KVS_ERR_DIMS
+ *   previous  nullable: receives the bound in force before the call
+ * Errors: DIMS, LAUNCH.
+ */
+#define KVS_WAIT_LIMIT_DEFAULT_NS 2000000000ull
+
+int kvs_set_wait_limit_ns(uint64_t ns, uint64_t *previous);
 
 /*
  * kvs_prepare -- sets up, on the current device, both attention kernels

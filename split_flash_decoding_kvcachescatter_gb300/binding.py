@@ -28,6 +28,7 @@ KVS_ERR_LAUNCH = 6
 KVS_ERR_POSITION = 7
 KVS_ERR_TIMEOUT = 8
 KVS_ERR_SLOT = 9
+KVS_ERR_MEMORY = 10
 
 # Every symbol include/kvsdecode.h declares.
 EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspace_bytes",
@@ -35,7 +36,11 @@ EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspac
            "kvs_step_graph_create", "kvs_step_graph_launch", "kvs_step_graph_destroy",
            "kvs_set_schedule", "kvs_get_schedule", "kvs_schedule_for", "kvs_prepare",
            "kvs_decode_step_slots", "kvs_argmax", "kvs_prefill_attention",
-           "kvs_prefill_workspace_bytes", "kvs_step_io_bytes", "kvs_decode_step_host")
+           "kvs_prefill_workspace_bytes", "kvs_step_io_bytes", "kvs_decode_step_host",
+           "kvs_set_wait_limit_ns", "kvs_step_io_layout", "kvs_decode_step_host_io")
+
+# Default bound on each pipeline wait of the kernels (kvs_set_wait_limit_ns).
+KVS_WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
 
 # kvs_schedule values (kernel schedule of the attention entry points)
 KVS_SCHEDULE_AUTO = 0
@@ -114,6 +119,13 @@ def lib() -> ctypes.CDLL:
             L.kvs_schedule_for.argtypes = [_I, _I, _I, _I, _I]
             L.kvs_prepare.restype = _I
             L.kvs_prepare.argtypes = [_I, _I, _I]
+            L.kvs_step_io_layout.restype = _I
+            L.kvs_step_io_layout.argtypes = [_I, _I, _I, _I, ctypes.POINTER(_SZ)]
+            L.kvs_decode_step_host_io.restype = _I
+            L.kvs_decode_step_host_io.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
+                                                  _P, _SZ, _P, _P]
+            L.kvs_set_wait_limit_ns.restype = _I
+            L.kvs_set_wait_limit_ns.argtypes = [ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)]
             L.kvs_strerror.restype = ctypes.c_char_p
             L.kvs_strerror.argtypes = [_I]
             _lib = L
@@ -227,6 +239,14 @@ def kvs_schedule_for(M, num_heads, num_kv_heads, head_dim, max_len) -> int:
     return r
 
 
+def kvs_set_wait_limit_ns(ns: int) -> int:
+    """Set the bound on each pipeline wait of the kernels on the current
+    device (0 .. KVS_WAIT_LIMIT_DEFAULT_NS); returns the previous bound."""
+    prev = ctypes.c_uint64(0)
+    _check(lib().kvs_set_wait_limit_ns(int(ns), ctypes.byref(prev)), "kvs_set_wait_limit_ns")
+    return int(prev.value)
+
+
 def kvs_prepare(num_heads, num_kv_heads, head_dim) -> None:
     """Set up both attention kernels for this shape on the current device."""
     _check(lib().kvs_prepare(num_heads, num_kv_heads, head_dim), "kvs_prepare")
@@ -332,6 +352,56 @@ def kvs_decode_step_host(q, k_rows, v_rows, positions, k_cache, v_cache, out, ch
         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _status_ptr(d_status), _stream(stream))
     _check(rc, "kvs_decode_step_host")
+
+
+def kvs_step_io_layout(M, num_heads, num_kv_heads, head_dim):
+    """Byte offsets of q, k_rows, v_rows, positions, out and the total size
+    of an io buffer (device, or the host buffer of kvs_decode_step_host_io)."""
+    off = (_SZ * 6)()
+    _check(lib().kvs_step_io_layout(M, num_heads, num_kv_heads, head_dim, off),
+           "kvs_step_io_layout")
+    return tuple(int(x) for x in off)
+
+
+class HostIo:
+    """A pinned host buffer with the io layout, and views of its arrays:
+    fill q, k_rows, v_rows and positions, call kvs_decode_step_host_io, and
+    read out once the stream has passed the call."""
+
+    def __init__(self, M, num_heads, num_kv_heads, head_dim):
+        oq, ok, ov, op, oo, total = kvs_step_io_layout(M, num_heads, num_kv_heads, head_dim)
+        self.shape = (M, num_heads, num_kv_heads, head_dim)
+        self.buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+        f = lambda off, n, dt: self.buf[off:off + n * 4].view(dt)
+        self.q = f(oq, M * num_heads * head_dim, torch.float32).view(M, num_heads, head_dim)
+        self.k_rows = f(ok, M * num_kv_heads * head_dim, torch.float32).view(
+            M, num_kv_heads, head_dim)
+        self.v_rows = f(ov, M * num_kv_heads * head_dim, torch.float32).view(
+            M, num_kv_heads, head_dim)
+        self.positions = f(op, M, torch.int32)
+        self.out = f(oo, M * num_heads * head_dim, torch.float32).view(M, num_heads, head_dim)
+        self.in_bytes = op + 4 * M          # what one step copies to the device
+        self.out_bytes = M * num_heads * head_dim * 4  # and back
+
+
+def kvs_decode_step_host_io(host_io, k_cache, v_cache, chunk_size=0, workspace=None, io=None,
+                            d_status=None, stream=None):
+    """kvs_decode_step with the step's inputs and result in one pinned host
+    buffer (a HostIo): one copy in, the fused step, one copy out."""
+    M, Hkv, Lmax, D = k_cache.shape
+    if not isinstance(host_io, HostIo):
+        raise TypeError("host_io: need a binding.HostIo")
+    Mh, H, Hkvh, Dh = host_io.shape
+    if (Mh, Hkvh, Dh) != (M, Hkv, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("kvs_decode_step_host_io: inconsistent shapes")
+    if workspace is None or io is None:
+        raise ValueError("kvs_decode_step_host_io: pass a workspace and an io buffer")
+    rc = lib().kvs_decode_step_host_io(
+        host_io.buf.data_ptr(), _f32(k_cache, "k_cache", 4), _f32(v_cache, "v_cache", 4), M, H,
+        Hkv, D, Lmax, int(chunk_size), io.data_ptr(), io.numel() * io.element_size(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _status_ptr(d_status), _stream(stream))
+    _check(rc, "kvs_decode_step_host_io")
 
 
 def kvs_decode_step_slots(q, k_rows, v_rows, positions, slots, done, k_pool, v_pool, out,

@@ -64,7 +64,6 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *empty = full + C::S;
   volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
-  volatile int *no_abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG + 4);
   // The partials this block merges, written here by every block of the
   // cluster (itself included) before the cluster barrier: element j of this
   // block's share (chunk = E / CS elements) from block r at
@@ -103,7 +102,6 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       mbar_init(&empty[s], C::NW);
     }
     *abort = 0;
-    *no_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -185,6 +183,9 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
           bulk_g2s(stage + 2 * C::KV_BYTES, q + ((size_t)i * H + (size_t)g * G) * D, C::Q_BYTES,
                    &full[s]);
       }
+      // Copies of uses below `first_live` have landed: the consumers
+      // released those stages before the producer's last successful wait.
+      uint32_t first_live = k > (uint32_t)C::S ? k - C::S : 0u;
       if (ok) {  // tell the consumers there is nothing more
         const uint32_t s = k % C::S;
         const uint32_t use = k / C::S;
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
           desc[s].flags = kNoMore;
           desc[s].nrows = 0;
           mbar_arrive(&full[s]);
+          first_live = k + 1 > (uint32_t)C::S ? k + 1 - C::S : 0u;
         } else {
           ok = 0;
         }
@@ -199,10 +201,12 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       if (!ok) {
         *abort = 1;
         record_status(d_status, KVS_ERR_TIMEOUT);
-        // let every copy already issued land before the block goes on
-        for (uint32_t j = (k > (uint32_t)C::S ? k - C::S : 0u); j < k; ++j)
-          mbar_wait(&full[j % C::S], (j / C::S) & 1u, no_abort);
       }
+      // Every copy this block issued lands before the block goes on, also
+      // when a consumer warp gave up and no longer waits for it.  (The
+      // latest use of each ring slot is in [first_live, k), so each wait is
+      // for that use's phase.)
+      for (uint32_t j = first_live; j < k; ++j) mbar_wait_drain(&full[j % C::S], (j / C::S) & 1u);
     }
     __syncwarp();
     cluster_wait();  // the split barrier of the kernel entry
@@ -219,9 +223,12 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
     for (uint32_t k = 0;; ++k) {
       const uint32_t s = k % C::S;
       const uint32_t use = k / C::S;
-      if (!mbar_wait(&full[s], use & 1u, abort)) {
-        *abort = 1;
-        record_status(d_status, KVS_ERR_TIMEOUT);
+      // all lanes of the warp leave together (shuffles follow)
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], use & 1u, abort))) {
+        if (lane == 0) {
+          *abort = 1;
+          record_status(d_status, KVS_ERR_TIMEOUT);
+        }
         break;
       }
       const StageDesc dsc = desc[s];
@@ -428,6 +435,14 @@ int cluster_dispatch(int G, const float *q, float *k_cache, float *v_cache,
 }
 
 }  // namespace
+
+int set_wait_limit_cluster(uint64_t ns) {
+  if (set_unit_wait_limit(ns) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  return KVS_OK;
+}
 
 int prepare_cluster_kernel(int H, int Hkv, int D) {
   const int dev = current_device();

@@ -96,8 +96,8 @@ struct Geo {
   static constexpr int OFF_MLL = OFF_ML + round_up(NW * G * 4, 16);
   static constexpr int OFF_DESC = round_up(OFF_MLL + NW * 32 * 4, 16);
   static constexpr int OFF_BAR = OFF_DESC + S * (int)sizeof(StageDesc);
-  static constexpr int OFF_INFO = OFF_BAR + (2 * S + 1) * 8;  // R, U (int64)
-  static constexpr int OFF_FLAG = OFF_INFO + 32;              // abort, no_abort, last
+  static constexpr int OFF_INFO = OFF_BAR + (2 * S + 1) * 8;  // R, U, tag (int64)
+  static constexpr int OFF_FLAG = OFF_INFO + 32;              // abort, -, last
   static constexpr int SMEM_BYTES = round_up(OFF_FLAG + 16, 128);
   static_assert(G >= 1 && G <= LPR, "group larger than lanes per row");
   static_assert(RP * G <= LPR, "slots exceed lanes");

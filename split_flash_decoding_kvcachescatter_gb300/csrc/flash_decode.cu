@@ -214,7 +214,8 @@ __device__ __forceinline__ int column_of_row(long long r, long long R, int P) {
 // Bounded: after 2^20 failed attempts they record KVS_ERR_TIMEOUT and return
 // 0xffffffff.  `v` is what an atomicAdd(ctr, amount) returned.
 __device__ unsigned resolve_tagged_add(unsigned long long *ctr, unsigned long long v,
-                                       unsigned amount, unsigned tag, int *d_status) {
+                                       unsigned amount, unsigned tag, int *d_status,
+                                       unsigned *epoch) {
   for (int attempt = 0; attempt < (1 << 20); ++attempt) {
     if ((unsigned)(v >> 32) == tag) return (unsigned)v;
     const unsigned long long cur = v + amount;
@@ -227,13 +228,34 @@ __device__ unsigned resolve_tagged_add(unsigned long long *ctr, unsigned long lo
       v = prev - amount;
   }
   record_status(d_status, KVS_ERR_TIMEOUT);
+  atomicAdd(epoch, 1u);
   return 0xffffffffu;
 }
 
 __device__ __forceinline__ unsigned tagged_add(unsigned long long *ctr, unsigned amount,
-                                               unsigned tag, int *d_status) {
+                                               unsigned tag, int *d_status, unsigned *epoch) {
   return resolve_tagged_add(ctr, atomicAdd(ctr, (unsigned long long)amount), amount, tag,
-                            d_status);
+                            d_status, epoch);
+}
+
+// The tag this launch's counters carry: the host's per-launch tag combined
+// with the workspace epoch.  Every block of a launch reads the same epoch
+// (nothing changes it unless a block gives up), so every block computes the
+// same tag.  A launch that gives up changes the epoch, so the counts it
+// leaves can never be taken for a later launch's own, not even by a replayed
+// graph, whose host tag is frozen at capture.  Never 0: a reset counter
+// holds tag 0.
+__device__ __forceinline__ unsigned launch_tag(unsigned host_tag, unsigned epoch) {
+  const unsigned t = host_tag ^ (epoch * 0x9E3779B1u);
+  return t != 0u ? t : 0x5BD1E995u;
+}
+
+// A block gives up the call: stop every role of the block, report it, and
+// move the workspace epoch on (see launch_tag).
+__device__ __forceinline__ void give_up(volatile int *abort, int *d_status, unsigned *epoch) {
+  *abort = 1;
+  record_status(d_status, KVS_ERR_TIMEOUT);
+  atomicAdd(epoch, 1u);
 }
 
 
@@ -402,7 +424,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     fd_step_kernel(const float *__restrict__ q, float *k_cache, float *v_cache, SeqMap sm,
                    const float *__restrict__ k_rows, const float *__restrict__ v_rows,
                    float *__restrict__ out, WsView ws, int M, int Hkv, int chunk, float qscale,
-                   unsigned tag, int *d_status) {
+                   unsigned host_tag, int *d_status) {
   using C = Geo<D, G>;
   constexpr int kCost = kRunCostBytes / (8 * D);  // cost rows per (i, g)
   extern __shared__ __align__(128) unsigned char smem[];
@@ -410,9 +432,8 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *empty = full + C::S;
   uint64_t *mbar = empty + C::S;  // consumer warps: end-of-run steps
-  long long *info = reinterpret_cast<long long *>(smem + C::OFF_INFO);  // R, U
+  long long *info = reinterpret_cast<long long *>(smem + C::OFF_INFO);  // R, U, tag
   volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
-  volatile int *no_abort = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG + 4);
   volatile int *s_last = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG + 8);
 
   const int warp = threadIdx.x >> 5;
@@ -461,17 +482,18 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   }
 
   if (warp == 0) {
+    const unsigned epoch = (lane == 0) ? __ldcg(ws.epoch) : 0u;
     const SplitTotals tot = warp_split_totals(sm, M, Hkv, chunk, kCost, lane);
     if (lane == 0) {
       info[0] = tot.rows;
       info[1] = tot.units;
+      info[2] = launch_tag(host_tag, epoch);
       for (int s = 0; s < C::S; ++s) {
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], C::NW);
       }
       mbar_init(mbar, C::NW);
       *abort = 0;
-      *no_abort = 0;
       *s_last = 0;
       fence_mbar_init();
     }
@@ -479,6 +501,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   __syncthreads();
   allow_dependent_launch();
   const long long R = info[0], U = info[1];
+  const unsigned tag = (unsigned)info[2];
   if (R == 0) return;
 
   if (warp == C::NW) {
@@ -514,7 +537,9 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
         const int r1 = (int)min((long long)(run.c + run.units) * chunk, (long long)run.L);
         const size_t head_base = sm.row_index(run.i, run.g, 0);
         const size_t row_src = ((size_t)run.i * Hkv + run.g) * D;  // new row of (i, g)
-        for (int rs = r0, st = 0; rs < r1 && ok; rs += C::T, ++st, ++k) {
+        // k counts the uses issued: a failed wait leaves the loop before
+        // the increment, so the drain below sees exactly the issued copies.
+        for (int rs = r0, st = 0; rs < r1; rs += C::T, ++st, ++k) {
           if (lane == 0) {
             const uint32_t s = k % C::S;
             const uint32_t use = k / C::S;
@@ -552,6 +577,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
         }
         remaining -= run.units;
         if (ok && remaining > 0)
@@ -559,6 +585,9 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       }
     }
     if (lane == 0) {
+      // Copies of uses below `first_live` have landed: the consumers
+      // released those stages before the producer's last successful wait.
+      uint32_t first_live = k > (uint32_t)C::S ? k - C::S : 0u;
       if (ok) {  // tell the consumers there is nothing more
         const uint32_t s = k % C::S;
         const uint32_t use = k / C::S;
@@ -566,17 +595,17 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
           desc[s].flags = kNoMore;
           desc[s].nrows = 0;
           mbar_arrive(&full[s]);
+          first_live = k + 1 > (uint32_t)C::S ? k + 1 - C::S : 0u;
         } else {
           ok = 0;
         }
       }
-      if (!ok) {
-        *abort = 1;
-        record_status(d_status, KVS_ERR_TIMEOUT);
-        // let every copy already issued land before the block can exit
-        for (uint32_t j = (k > (uint32_t)C::S ? k - C::S : 0u); j < k; ++j)
-          mbar_wait(&full[j % C::S], (j / C::S) & 1u, no_abort);
-      }
+      if (!ok) give_up(abort, d_status, ws.epoch);
+      // Every copy this block issued lands before the block can exit, also
+      // when a consumer warp gave up and no longer waits for it.  (The
+      // latest use of each ring slot is in [first_live, k), so each wait is
+      // for that use's phase.)
+      for (uint32_t j = first_live; j < k; ++j) mbar_wait_drain(&full[j % C::S], (j / C::S) & 1u);
     }
     return;
   }
@@ -592,12 +621,13 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   tile_reset<G>(acc, m_run, l_lane);
 
   uint32_t mphase = 0;
+  // Every wait of a consumer warp ends the same way for all its lanes (the
+  // lanes go on to full-warp shuffles together, or leave together).
   auto consumers_barrier = [&]() -> bool {  // bounded; every consumer warp arrives once
     __syncwarp();
     if (lane == 0) mbar_arrive(mbar);
-    if (!mbar_wait(mbar, mphase, abort)) {
-      *abort = 1;
-      record_status(d_status, KVS_ERR_TIMEOUT);
+    if (!__all_sync(0xffffffffu, mbar_wait(mbar, mphase, abort))) {
+      if (lane == 0) give_up(abort, d_status, ws.epoch);
       return false;
     }
     mphase ^= 1u;
@@ -607,9 +637,8 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   for (uint32_t k = 0;; ++k) {
     const uint32_t s = k % C::S;
     const uint32_t use = k / C::S;
-    if (!mbar_wait(&full[s], use & 1u, abort)) {
-      *abort = 1;
-      record_status(d_status, KVS_ERR_TIMEOUT);
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], use & 1u, abort))) {
+      if (lane == 0) give_up(abort, d_status, ws.epoch);
       return;
     }
     const StageDesc dsc = desc[s];
@@ -649,7 +678,8 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     if (!consumers_barrier()) return;
     if (!whole) {
       if (threadIdx.x == 0) {
-        const unsigned before = tagged_add(ws.done + dsc.ig, (unsigned)dsc.run_rows, tag, d_status);
+        const unsigned before = tagged_add(ws.done + dsc.ig, (unsigned)dsc.run_rows, tag, d_status,
+                                           ws.epoch);
         const bool last = (before != 0xffffffffu && before + (unsigned)dsc.run_rows == (unsigned)dsc.L);
         // Every run of (i, g) has counted: reset the counter (tag 0 is never
         // a call's tag), so a later launch with the same tag -- a replayed
@@ -707,19 +737,6 @@ int step_blocks_per_sm(int dev) {
 // stream for the launch and pipeline fill to pay off.
 constexpr long long kMinRowsPerBlock = 32;
 
-// Tag of one launch for the workspace counters: distinct for consecutive
-// launches of this process (a 32-bit counter started at a time-derived
-// value, never 0), so a counter left by an earlier call, or whatever a fresh
-// workspace holds, is recognised as stale.
-unsigned next_call_tag() {
-  static std::atomic<unsigned> counter{
-      (unsigned)(std::chrono::steady_clock::now().time_since_epoch().count() * 2654435761ull)};
-  unsigned t;
-  do {
-    t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
-  } while (t == 0u);
-  return t;
-}
 
 template <int D, int G>
 int launch_step_impl(const float *q, float *k_cache, float *v_cache, const SeqArgs &seqs,
@@ -742,7 +759,7 @@ int launch_step_impl(const float *q, float *k_cache, float *v_cache, const SeqAr
                                    C::SMEM_BYTES, stream, q, k_cache, v_cache,
                                    SeqMap{seqs.positions, seqs.slots, seqs.done, max_len,
                                           seqs.num_slots, Hkv},
-                                   k_rows, v_rows, out, ws, M, Hkv, chunk, qscale, next_call_tag(),
+                                   k_rows, v_rows, out, ws, M, Hkv, chunk, qscale, fresh_tag(),
                                    d_status);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
@@ -772,6 +789,27 @@ int dispatch_group(int G, const float *q, float *k_cache, float *v_cache,
 }
 
 }  // namespace
+
+// Distinct for consecutive calls of this process (a 32-bit counter started
+// at a time-derived value, never 0), so a counter left by an earlier call, or
+// whatever a fresh workspace holds, is recognised as stale.
+unsigned fresh_tag() {
+  static std::atomic<unsigned> counter{
+      (unsigned)(std::chrono::steady_clock::now().time_since_epoch().count() * 2654435761ull)};
+  unsigned t;
+  do {
+    t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  } while (t == 0u);
+  return t;
+}
+
+int set_wait_limit_step(uint64_t ns) {
+  if (set_unit_wait_limit(ns) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  return KVS_OK;
+}
 
 int device_sm_count() {
   static int cache[kMaxDevices] = {0};

@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "kvs_launch.h"
 #include "kvsdecode.h"
@@ -78,6 +79,7 @@ const char *kvs_strerror(int status) {
     case KVS_ERR_POSITION: return "a position is outside [0, max_len)";
     case KVS_ERR_TIMEOUT: return "a bounded device pipeline wait expired";
     case KVS_ERR_SLOT: return "a cache slot is outside [0, num_slots)";
+    case KVS_ERR_MEMORY: return "the device could not provide the library's own buffer";
     default: return "unknown kvs status";
   }
 }
@@ -257,6 +259,62 @@ int kvs_decode_step_host(const float *q, const float *k_rows, const float *v_row
   return KVS_OK;
 }
 
+int kvs_step_io_layout(int M, int num_heads, int num_kv_heads, int head_dim, size_t *offsets) {
+  if (M < 1 || num_heads < 1 || num_kv_heads < 1 || head_dim < 1) return KVS_ERR_DIMS;
+  if (!offsets) return KVS_ERR_NULL;
+  const IoLayout L = io_layout(M, num_heads, num_kv_heads, head_dim);
+  offsets[0] = L.q;
+  offsets[1] = L.k;
+  offsets[2] = L.v;
+  offsets[3] = L.pos;
+  offsets[4] = L.out;
+  offsets[5] = L.total;
+  return KVS_OK;
+}
+
+int kvs_decode_step_host_io(void *host_io, float *k_cache, float *v_cache, int M, int num_heads,
+                            int num_kv_heads, int head_dim, int max_len, int chunk_size, void *io,
+                            size_t io_bytes, void *workspace, size_t workspace_bytes,
+                            int *d_status, kvs_stream_t stream) {
+  int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
+  if (rc != KVS_OK) return rc;
+  if (M == 0) return KVS_OK;
+  if (!host_io || !io) return KVS_ERR_NULL;
+  if (!aligned(io, 256)) return KVS_ERR_ALIGN;
+  const IoLayout L = io_layout(M, num_heads, num_kv_heads, head_dim);
+  if (io_bytes < L.total) return KVS_ERR_WORKSPACE;
+  unsigned char *base = static_cast<unsigned char *>(io);
+  float *dq = reinterpret_cast<float *>(base + L.q);
+  float *dk = reinterpret_cast<float *>(base + L.k);
+  float *dv = reinterpret_cast<float *>(base + L.v);
+  int32_t *dpos = reinterpret_cast<int32_t *>(base + L.pos);
+  float *dout = reinterpret_cast<float *>(base + L.out);
+  rc = check_attention_buffers(dq, k_cache, v_cache, dpos, dout, M, num_heads, num_kv_heads,
+                               head_dim, workspace, workspace_bytes);
+  if (rc != KVS_OK) return rc;
+  const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
+  if (chunk <= 0) return -chunk;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t qo = (size_t)M * num_heads * head_dim * sizeof(float);
+  unsigned char *host = static_cast<unsigned char *>(host_io);
+  // the inputs (q, k_rows, v_rows, positions and the padding between them)
+  // in one copy
+  const size_t in_bytes = L.pos + (size_t)M * sizeof(int32_t);
+  if (cudaMemcpyAsync(base, host, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  const kvs::SeqArgs seqs{dpos, nullptr, nullptr, max_len, M};
+  rc = launch_attention(dq, k_cache, v_cache, seqs, dk, dv, dout, M, num_heads, num_kv_heads,
+                        head_dim, chunk, workspace, d_status, st);
+  if (rc != KVS_OK) return rc;
+  if (cudaMemcpyAsync(host + L.out, dout, qo, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  return KVS_OK;
+}
+
 int kvs_decode_step_slots(const float *q, const float *k_rows, const float *v_rows,
                           const int32_t *positions, const int32_t *slots, const uint8_t *done,
                           float *k_pool, float *v_pool, int num_slots, float *out, int M,
@@ -324,6 +382,27 @@ int kvs_set_schedule(int schedule) {
 }
 
 int kvs_get_schedule(void) { return g_schedule.load(); }
+
+int kvs_set_wait_limit_ns(uint64_t ns, uint64_t *previous) {
+  static std::mutex mu;
+  static uint64_t current[64];
+  static bool known[64] = {false};
+  if (ns > KVS_WAIT_LIMIT_DEFAULT_NS) return KVS_ERR_DIMS;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  int rc = kvs::set_wait_limit_step(ns);
+  if (rc == KVS_OK) rc = kvs::set_wait_limit_cluster(ns);
+  if (rc == KVS_OK) rc = kvs::set_wait_limit_prefill(ns);
+  if (rc != KVS_OK) return rc;
+  if (previous) *previous = known[dev] ? current[dev] : KVS_WAIT_LIMIT_DEFAULT_NS;
+  current[dev] = ns;
+  known[dev] = true;
+  return KVS_OK;
+}
 
 int kvs_schedule_for(int M, int num_heads, int num_kv_heads, int head_dim, int max_len) {
   const int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, 0);

@@ -13,7 +13,21 @@ namespace kvs {
 // Upper bound on any single pipeline wait.  A wait that runs past it means a
 // bug (a copy that never lands, a role that died); the kernel then records
 // KVS_ERR_TIMEOUT and returns instead of spinning forever.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kWaitLimitNs = KVS_WAIT_LIMIT_DEFAULT_NS;  // 2 s
+
+// The bound the pipeline waits of this translation unit's kernels use on this
+// device (kvs_set_wait_limit_ns lowers it so that a test can make the waits
+// run out).  Read at run time, so a replayed CUDA graph sees the current
+// value; it lives in constant memory, so the waits read it from the SM's
+// constant cache.  Drain waits -- those that let already issued copies or
+// tensor-core products finish before a block exits -- always use kWaitLimitNs.
+static __constant__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
+// Host: sets this translation unit's copy of the bound on the current device.
+static inline cudaError_t set_unit_wait_limit(uint64_t ns) {
+  const unsigned long long v = ns;
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
+}
 
 __device__ __forceinline__ void record_status(int *d_status, int code) {
   if (d_status != nullptr) atomicCAS(d_status, 0, code);
@@ -72,6 +86,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar,
       : "memory");
 }
 
+// Potentially blocking test: the thread may be suspended for a while (until
+// the phase completes or a hardware time limit passes).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -84,18 +100,55 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with the given parity has completed.  Returns false
-// if *abort became non-zero or the wait exceeded kWaitLimitNs.
+// if *abort became non-zero or the wait exceeded the bound g_wait_limit_ns.
+// Under the default bound the thread sleeps in mbarrier.try_wait and looks at
+// the clock and the abort flag every 64 tries.  Under a lowered bound (a
+// test of the timeout path) it polls without sleeping and looks every time,
+// so a bound of 0 ends the first wait that does not find its phase complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int *abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = global_timer_ns();
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t limit = g_wait_limit_ns;
+  const uint64_t t0 = global_timer_ns();
+  if (limit < kWaitLimitNs) {
+    for (;;) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (*abort) return false;
+      if (global_timer_ns() - t0 >= limit) return false;
+    }
+  }
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit) return false;
     }
+  }
+}
+
+// A drain wait: for work this block already issued (a bulk copy into its
+// shared memory, tensor-core products) to finish before the block moves on
+// or exits.  No abort flag, and always the full kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 

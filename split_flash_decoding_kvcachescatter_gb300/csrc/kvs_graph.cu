@@ -10,10 +10,17 @@
 //
 // Here the graph holds one kvs_decode_step per layer -- scatter + split-K
 // attention, one kernel each, chained with programmatic dependent launch --
-// over caller-owned, fixed device buffers.
+// over caller-owned, fixed device buffers.  A memset node ahead of the first
+// layer writes a fresh value into the workspace epoch at every replay
+// (kvs_step_graph_launch sets it): the epoch is part of the tag the step
+// kernel's completion counters carry, so no replay can take counts left by
+// an earlier replay that gave up on a wait for its own, although the tag
+// arguments of the captured launches are frozen.
 
 #include <cstdint>
+#include <mutex>
 #include <new>
+#include <vector>
 
 #include "kvs_launch.h"
 #include "kvsdecode.h"
@@ -21,8 +28,37 @@
 struct kvs_step_graph {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t epoch_node = nullptr;  // memset of the workspace epoch
+  cudaMemsetParams epoch = {};
+  std::mutex mu;  // one launch at a time updates the node and launches
   int layers = 0;
 };
+
+namespace {
+
+// Puts a memset of the workspace epoch word (4 bytes at the workspace base)
+// ahead of every root node of the captured graph.
+bool add_epoch_node(cudaGraph_t g, void *workspace, cudaGraphNode_t *node,
+                    cudaMemsetParams *params) {
+  size_t n = 0;
+  if (cudaGraphGetRootNodes(g, nullptr, &n) != cudaSuccess || n == 0) return false;
+  std::vector<cudaGraphNode_t> roots(n);
+  if (cudaGraphGetRootNodes(g, roots.data(), &n) != cudaSuccess) return false;
+  cudaMemsetParams p = {};
+  p.dst = workspace;
+  p.pitch = 0;
+  p.value = kvs::fresh_tag();
+  p.elementSize = 4;
+  p.width = 1;
+  p.height = 1;
+  if (cudaGraphAddMemsetNode(node, g, nullptr, 0, &p) != cudaSuccess) return false;
+  for (size_t i = 0; i < n; ++i)
+    if (cudaGraphAddDependencies(g, node, &roots[i], nullptr, 1) != cudaSuccess) return false;
+  *params = p;
+  return true;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -64,6 +100,13 @@ int kvs_step_graph_create(int layers, const float *const *q, const float *const 
     cudaGetLastError();
     return rc != KVS_OK ? rc : KVS_ERR_LAUNCH;
   }
+  cudaGraphNode_t epoch_node = nullptr;
+  cudaMemsetParams epoch = {};
+  if (!add_epoch_node(g, workspace, &epoch_node, &epoch)) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
   cudaGraphExec_t exec = nullptr;
   if (cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
     cudaGraphDestroy(g);
@@ -78,6 +121,8 @@ int kvs_step_graph_create(int layers, const float *const *q, const float *const 
   }
   h->graph = g;
   h->exec = exec;
+  h->epoch_node = epoch_node;
+  h->epoch = epoch;
   h->layers = layers;
   *graph = h;
   return KVS_OK;
@@ -85,9 +130,15 @@ int kvs_step_graph_create(int layers, const float *const *q, const float *const 
 
 int kvs_step_graph_launch(kvs_step_graph *graph, kvs_stream_t stream) {
   if (!graph || !graph->exec) return KVS_ERR_NULL;
-  return cudaGraphLaunch(graph->exec, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? KVS_OK
-             : KVS_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lk(graph->mu);
+  cudaMemsetParams p = graph->epoch;
+  p.value = kvs::fresh_tag();  // this replay's epoch
+  if (cudaGraphExecMemsetNodeSetParams(graph->exec, graph->epoch_node, &p) != cudaSuccess ||
+      cudaGraphLaunch(graph->exec, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  return KVS_OK;
 }
 
 int kvs_step_graph_destroy(kvs_step_graph *graph) {

@@ -15,7 +15,11 @@ constexpr int kMaxChunkBlocks = 1024;
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace of kvs_flash_decode / kvs_decode_step.
-//   header  256 bytes, reserved
+//   header  256 bytes: a u32 epoch at offset 0 (changed by any call that
+//           gives up on a bounded wait; part of the counters' tag, so that
+//           counts such a call left behind never match a later call, even a
+//           replayed CUDA graph whose tag argument is frozen), the rest
+//           reserved
 //   done    u64 [M*Hkv]: rows of (i, g) whose partial is written (counters
 //           carry the tag of the call that last used them, so the buffer
 //           needs no initialisation)
@@ -41,6 +45,7 @@ inline WsLayout ws_layout(int M, int Hkv, int G, int D) {
 }
 
 struct WsView {
+  unsigned *epoch;
   unsigned long long *done;
   float2 *ml;
   float *acc;
@@ -49,7 +54,7 @@ struct WsView {
 inline WsView workspace_view(void *base, int M, int Hkv, int G, int D) {
   const WsLayout l = ws_layout(M, Hkv, G, D);
   unsigned char *p = static_cast<unsigned char *>(base);
-  return WsView{reinterpret_cast<unsigned long long *>(p + l.off_done),
+  return WsView{reinterpret_cast<unsigned *>(p), reinterpret_cast<unsigned long long *>(p + l.off_done),
                 reinterpret_cast<float2 *>(p + l.off_ml), reinterpret_cast<float *>(p + l.off_acc)};
 }
 
@@ -128,5 +133,16 @@ int prepare_step_kernel(int H, int Hkv, int D);
 
 // Number of SMs of the current device (cached per device); <= 0 on error.
 int device_sm_count();
+
+// A fresh nonzero 32-bit value for every call (a process-wide counter): the
+// per-launch tag of the step kernel's workspace counters, and the workspace
+// epoch a step graph writes at each replay.
+unsigned fresh_tag();
+
+// Each translation unit that has pipeline waits keeps its own copy of the
+// wait bound (kvs_device.cuh); these set it on the current device.
+int set_wait_limit_step(uint64_t ns);
+int set_wait_limit_cluster(uint64_t ns);
+int set_wait_limit_prefill(uint64_t ns);
 
 }  // namespace kvs

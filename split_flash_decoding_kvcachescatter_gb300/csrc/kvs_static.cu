@@ -15,7 +15,11 @@
 // the process exits.  Host code cannot use the array's name as a device
 // address (on the host it names a stand-in object), so the first call on each
 // device looks up the real address with cudaGetSymbolAddress while that
-// device is current, and caches it.
+// device is current, and caches it.  CUDA loads device code lazily, so that
+// lookup is also when the device commits the buffer; a device that cannot
+// provide it makes the call return KVS_ERR_MEMORY.  The cached address
+// belongs to the device's primary context: it is not valid after that
+// context is destroyed (cudaDeviceReset).
 
 #include <cstdint>
 #include <mutex>
@@ -32,20 +36,26 @@ std::mutex g_mu;
 void *g_addr[kMaxDevices] = {nullptr};
 
 // Device address of g_static_workspace on the current device (looked up once
-// per device).  Returns nullptr on failure.
-void *static_workspace_address() {
+// per device) in *addr.  Returns KVS_OK, KVS_ERR_MEMORY when the device could
+// not provide the buffer, or KVS_ERR_LAUNCH for any other failure.
+int static_workspace_address(void **addr) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_addr[dev] == nullptr) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) {
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+    if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();  // reset the error state so later CUDA calls do not see it
-      return nullptr;
+      return e == cudaErrorMemoryAllocation ? KVS_ERR_MEMORY : KVS_ERR_LAUNCH;
     }
     g_addr[dev] = p;
   }
-  return g_addr[dev];
+  *addr = g_addr[dev];
+  return KVS_OK;
 }
 
 }  // namespace
@@ -65,8 +75,9 @@ extern "C" int kvs_flash_decode_static(const float *q, const float *k_cache,
     return kvs_flash_decode(q, k_cache, v_cache, positions, out, M, num_heads, num_kv_heads,
                             head_dim, max_len, chunk_size, nullptr, 0, d_status, stream);
   if (need > (size_t)KVS_STATIC_WORKSPACE_BYTES) return KVS_ERR_WORKSPACE;
-  void *ws = static_workspace_address();
-  if (ws == nullptr) return KVS_ERR_LAUNCH;
+  void *ws = nullptr;
+  const int rc = static_workspace_address(&ws);
+  if (rc != KVS_OK) return rc;
   // The partials need no initial value: every slot the reduce reads is
   // written by the chunk kernel of the same call.
   return kvs_flash_decode(q, k_cache, v_cache, positions, out, M, num_heads, num_kv_heads,

@@ -33,7 +33,8 @@
 //  * Causal: key tiles after the query tile are skipped; keys j > i and keys
 //    past seq_len get p = 0 (selects, on the diagonal and last tiles only).
 // Every mbarrier wait is bounded; on expiry the block records
-// KVS_ERR_TIMEOUT, lets its copies land, frees its TMEM and returns.
+// KVS_ERR_TIMEOUT, lets its copies and tensor-core products finish, frees its
+// TMEM and returns.
 
 #include <cuda_fp16.h>
 
@@ -314,7 +315,7 @@ struct PGeo {
   // barriers: q, kfull[KS], kfree[KS], vfull[VS], vfree[VS], sfull[2], pfull[2], pvdone
   static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 5;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;    // TMEM base address
-  static constexpr int OFF_FLAG = OFF_TMEM + 8;          // abort, no_abort
+  static constexpr int OFF_FLAG = OFF_TMEM + 8;          // abort
   // A block holds all 512 TMEM columns, so a second block on the SM would
   // only wait for them: ask for more than half of the SM's 228 KB of shared
   // memory (less the 1 KB each block reserves) so that one block fits.
@@ -341,7 +342,6 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
   uint64_t *pvdone = pfull + 2;    // every product issued so far is done (commit)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PG::OFF_TMEM);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + PG::OFF_FLAG);
-  volatile int *no_abort = reinterpret_cast<volatile int *>(smem + PG::OFF_FLAG + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -386,7 +386,6 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
     }
     mbar_init(pvdone, 1);
     *abort = 0;
-    *no_abort = 0;
     fence_mbar_init();
   }
   tc_fence_before();
@@ -407,32 +406,34 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       mbar_arrive_expect_tx(bar_q, (has_b ? 2 : 1) * PG::TILE);
       bulk_g2s(sQ, gQh + (size_t)qa * tile, PG::TILE, bar_q);
       if (has_b) bulk_g2s(sQ + PG::TILE, gQh + (size_t)(qa + 1) * tile, PG::TILE, bar_q);
-      int n = 0;
+      int nk = 0, nv = 0;  // K and V^T tiles issued
       bool ok = true;
-      for (; n < n_all; ++n) {
+      for (int n = 0; n < n_all; ++n) {
         const int ks = n % KS, vs = n % VS;
         if (n >= KS && !(ok = mbar_wait(&kfree[ks], (uint32_t)((n - KS) / KS) & 1u, abort)))
           break;
         mbar_arrive_expect_tx(&kfull[ks], PG::TILE);
         bulk_g2s(sK + ks * PG::TILE, gKh + (size_t)n * tile, PG::TILE, &kfull[ks]);
-        if (n >= VS && !(ok = mbar_wait(&vfree[vs], (uint32_t)((n - VS) / VS) & 1u, abort))) {
-          // K(n) is in flight: let it land
-          mbar_wait(&kfull[ks], (uint32_t)(n / KS) & 1u, no_abort);
+        nk = n + 1;
+        if (n >= VS && !(ok = mbar_wait(&vfree[vs], (uint32_t)((n - VS) / VS) & 1u, abort)))
           break;
-        }
         mbar_arrive_expect_tx(&vfull[vs], PG::TILE);
         bulk_g2s(sV + vs * PG::TILE, gVh + (size_t)n * tile, PG::TILE, &vfull[vs]);
+        nv = n + 1;
       }
       if (!ok) {
         *abort = 1;
         record_status(d_status, KVS_ERR_TIMEOUT);
-        // let the copies already issued land before the block exits
-        mbar_wait(bar_q, 0, no_abort);
-        for (int j = (n > KS ? n - KS : 0); j < n; ++j)
-          mbar_wait(&kfull[j % KS], (uint32_t)(j / KS) & 1u, no_abort);
-        for (int j = (n > VS ? n - VS : 0); j < n; ++j)
-          mbar_wait(&vfull[j % VS], (uint32_t)(j / VS) & 1u, no_abort);
       }
+      // Every copy issued lands before the block can exit, also when another
+      // role gave up and no longer waits for it.  The last KS K tiles and VS
+      // V^T tiles are the latest use of each stage (earlier ones landed
+      // before their stage was refilled), so each wait is for its own phase.
+      mbar_wait_drain(bar_q, 0);
+      for (int j = (nk > KS ? nk - KS : 0); j < nk; ++j)
+        mbar_wait_drain(&kfull[j % KS], (uint32_t)(j / KS) & 1u);
+      for (int j = (nv > VS ? nv - VS : 0); j < nv; ++j)
+        mbar_wait_drain(&vfull[j % VS], (uint32_t)(j / VS) & 1u);
     }
     __syncwarp();
   } else if (warp == kPMmaWarp) {
@@ -461,11 +462,14 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
           mma_f16_ts(d, a + ks * 8, b + 16 * ks, kIdescO, (n > 0 || ks > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar_q, 0, abort) && mbar_wait(&kfull[0], 0, abort);
+      bool issued = false;   // products issued since the last completed pvdone wait
+      bool pending = false;  // a commit on pvdone whose wait did not complete
       if (ok) {
         tc_fence_after();
         if (n_a > 0) issue_s(0, 0);
         if (n_b > 0) issue_s(1, 0);
         mma_commit(&kfree[0]);
+        issued = true;
       }
       uint32_t pv_phase = 0;
       for (int kt = 0; kt < n_all && ok; ++kt) {
@@ -479,12 +483,17 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
             if (!ok) break;
             tc_fence_after();
             issue_pv(x, kt);
+            issued = true;
           }
           if (kt + 1 < n_x) {  // S_x(kt+1) overwrites P_x(kt): after P V_x(kt)
             mma_commit(pvdone);
             ok = mbar_wait(pvdone, pv_phase, abort);
+            if (!ok) {
+              pending = true;
+              break;
+            }
             pv_phase ^= 1u;
-            if (!ok) break;
+            issued = false;
             if (!k_next) {
               ok = mbar_wait(&kfull[(kt + 1) % KS], (uint32_t)((kt + 1) / KS) & 1u, abort);
               if (!ok) break;
@@ -492,6 +501,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
               k_next = true;
             }
             issue_s(x, kt + 1);
+            issued = true;
           }
         }
         if (!ok) break;
@@ -501,10 +511,20 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       if (ok) {  // the last P V products
         mma_commit(pvdone);
         ok = mbar_wait(pvdone, pv_phase, abort);
+        if (!ok) pending = true;
       }
       if (!ok) {
         *abort = 1;
         record_status(d_status, KVS_ERR_TIMEOUT);
+        // Every product issued finishes before the block frees the tensor
+        // memory and exits.  A pending commit covers them all (nothing was
+        // issued after it); otherwise commit once more.  At most one commit
+        // is outstanding, so the parity wait is for that commit's phase.
+        if (!pending && issued) {
+          mma_commit(pvdone);
+          pending = true;
+        }
+        if (pending) mbar_wait_drain(pvdone, pv_phase);
       }
     }
     __syncwarp();
@@ -524,7 +544,9 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       const uint32_t ph = (uint32_t)kt & 1u;
       // S_x(kt) is ready; it was issued after P V_x(kt-1) completed, so O_x
       // is quiescent too
-      if (!mbar_wait(&sfull[x], ph, abort)) {
+      // all lanes of the warp leave together: the TMEM loads and stores
+      // below are .sync.aligned (the whole warp executes them)
+      if (!__all_sync(0xffffffffu, mbar_wait(&sfull[x], ph, abort))) {
         failed = true;
         break;
       }
@@ -659,6 +681,14 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
 }
 
 }  // namespace
+
+int set_wait_limit_prefill(uint64_t ns) {
+  if (set_unit_wait_limit(ns) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
+  return KVS_OK;
+}
 
 size_t prefill_workspace_bytes(int H, int S, int D) {
   const size_t T = ((size_t)S + kPM - 1) / kPM;

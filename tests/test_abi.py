@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_strerror_covers_all_codes(L):
-    for code in range(0, 10):
+    for code in range(0, 11):
         s = B.strerror(code)
         assert s and "unknown" not in s
     assert "unknown" in B.strerror(99)
@@ -150,6 +150,26 @@ def test_chunk_rule_is_pow2_in_range(L):
         B.kvs_choose_chunk_size(32, 8, 128, 8192, 76)
     with pytest.raises(B.KvsError):
         B.kvs_choose_chunk_size(0, 8, 128, 8192, 152)
+
+
+def test_chunk_rule_matches_its_documented_thresholds(L):
+    # r = M * Hkv * max_len // (2 * SMs) cache rows per block: 16 below 4096,
+    # 32 below 8192, else 64 (the header's rule); positions play no part
+    for sms in (1, 76, 152):
+        for (M, Hkv, Lmax) in [(1, 2, 256), (4, 2, 2048), (32, 8, 8192), (8, 8, 32768),
+                               (32, 8, 131072), (1, 1, 4096 * 304), (1, 1, 4096 * 304 - 1),
+                               (1, 1, 8192 * 304), (1, 1, 8192 * 304 - 1)]:
+            r = M * Hkv * Lmax // (2 * sms)
+            want = 16 if r < 4096 else (32 if r < 8192 else 64)
+            assert B.kvs_choose_chunk_size(M, Hkv, 128, Lmax, sms) == want, (M, Hkv, Lmax, sms)
+
+
+def test_wait_limit_rejects_values_above_the_default_before_touching_cuda(L):
+    prev = ctypes.c_uint64(7)
+    assert L.kvs_set_wait_limit_ns(B.KVS_WAIT_LIMIT_DEFAULT_NS + 1, ctypes.byref(prev)) == \
+        B.KVS_ERR_DIMS
+    assert prev.value == 7  # untouched
+    assert L.kvs_set_wait_limit_ns((1 << 64) - 1, None) == B.KVS_ERR_DIMS
 
 
 def test_step_graph_host_checks(L):
@@ -320,3 +340,47 @@ def test_step_io_bytes_formula(L):
         assert L.kvs_step_io_bytes(M, H, Hkv, D) == 2 * r(qo) + 2 * r(kv) + r(4 * M)
     assert L.kvs_step_io_bytes(0, 4, 2, 64) == 0
     assert L.kvs_step_io_bytes(1, 4, 0, 64) == 0
+
+
+def test_step_io_layout_matches_io_bytes(L):
+    def r(x):
+        return -(-x // 256) * 256
+    for M, H, Hkv, D in [(1, 4, 2, 64), (3, 14, 2, 64), (32, 32, 8, 128), (5, 40, 8, 128)]:
+        oq, ok, ov, op, oo, total = B.kvs_step_io_layout(M, H, Hkv, D)
+        qo, kv = M * H * D * 4, M * Hkv * D * 4
+        assert (oq, ok, ov, op, oo) == (0, r(qo), r(qo) + r(kv), r(qo) + 2 * r(kv),
+                                        r(qo) + 2 * r(kv) + r(4 * M))
+        assert total == L.kvs_step_io_bytes(M, H, Hkv, D)
+    off = (ctypes.c_size_t * 6)()
+    assert L.kvs_step_io_layout(0, 4, 2, 64, off) == B.KVS_ERR_DIMS
+    assert L.kvs_step_io_layout(1, 4, 2, 64, None) == B.KVS_ERR_NULL
+
+
+def _dshio(L, hio=A16, k=A16, v=A16, M=1, H=4, Hkv=2, D=64, Lmax=256, C=64, io=A16,
+           iob=1 << 30, ws=A16, wsb=1 << 30):
+    return L.kvs_decode_step_host_io(hio, k, v, M, H, Hkv, D, Lmax, C, io, iob, ws, wsb, None,
+                                     None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), B.KVS_ERR_DIMS),
+    (dict(H=6, Hkv=4), B.KVS_ERR_DIMS),
+    (dict(C=-1), B.KVS_ERR_DIMS),
+    (dict(D=96), B.KVS_ERR_UNSUPPORTED),
+    (dict(hio=None), B.KVS_ERR_NULL),
+    (dict(io=None), B.KVS_ERR_NULL),
+    (dict(k=None), B.KVS_ERR_NULL),
+    (dict(io=A16 + 16), B.KVS_ERR_ALIGN),
+    (dict(v=A16 + 8), B.KVS_ERR_ALIGN),
+    (dict(iob=64), B.KVS_ERR_WORKSPACE),
+    (dict(ws=None), B.KVS_ERR_WORKSPACE),
+    (dict(wsb=64), B.KVS_ERR_WORKSPACE),
+    # the host buffer needs no alignment: it is only copied from and to
+    (dict(hio=A16 + 4, iob=64), B.KVS_ERR_WORKSPACE),
+])
+def test_decode_step_host_io_validation(L, kw, code):
+    assert _dshio(L, **kw) == code
+
+
+def test_decode_step_host_io_empty_batch_ok(L):
+    assert _dshio(L, M=0, hio=None, k=None, v=None, io=None, iob=0, ws=None, wsb=0) == 0

@@ -145,3 +145,96 @@ def test_host_step_rejects_device_tensors_in_the_binding():
         B.kvs_decode_step_host(t["q"], t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
                                t["v_cache"], torch.empty(inp.q.shape), chunk_size=w.chunk_size,
                                workspace=ws, io=io)
+
+
+def fill_host_io(hio, inp):
+    hio.q.copy_(torch.from_numpy(np.ascontiguousarray(inp.q, np.float32)))
+    hio.k_rows.copy_(torch.from_numpy(np.ascontiguousarray(inp.k_rows, np.float32)))
+    hio.v_rows.copy_(torch.from_numpy(np.ascontiguousarray(inp.v_rows, np.float32)))
+    hio.positions.copy_(torch.from_numpy(np.ascontiguousarray(inp.positions, np.int32)))
+    hio.out.fill_(float("nan"))
+
+
+@pytest.mark.parametrize("name", ["tiny", "small_model"])
+def test_host_io_step_matches_oracle_and_device_step(name):
+    """kvs_decode_step_host_io: one pinned buffer in the io layout, one copy
+    in, one copy out; the same kernel as kvs_decode_step, so the output is
+    bit-identical to it, and within the gate of the oracle."""
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    exp = W.upload(inp, w, DEV, include_new_row=True)
+    t = W.upload(inp, w, DEV)
+    t_dev = W.upload(inp, w, DEV)
+    M, H, D = inp.q.shape
+    hio = B.HostIo(M, H, w.num_kv_heads, D)
+    fill_host_io(hio, inp)
+    io = B.step_io(M, H, w.num_kv_heads, D, device=DEV)
+    ws = B.workspace(M, H, w.num_kv_heads, D, w.max_len, w.chunk_size, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.kvs_decode_step_host_io(hio, t["k_cache"], t["v_cache"], chunk_size=w.chunk_size,
+                              workspace=ws, io=io, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, B.strerror(int(status.item()))
+    gate(hio.out.numpy(), oracle.decode_sequences(inp.q, inp.k_seq, inp.v_seq, inp.positions),
+         where=f"{name} host io step")
+    out_dev = torch.empty_like(t_dev["q"])
+    B.kvs_decode_step(t_dev["q"], t_dev["k_rows"], t_dev["v_rows"], t_dev["positions"],
+                      t_dev["k_cache"], t_dev["v_cache"], out_dev, chunk_size=w.chunk_size,
+                      workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_dev.cpu().view(torch.int32), hio.out.view(torch.int32))
+    for c in ("k_cache", "v_cache"):
+        assert torch.equal(t[c].view(torch.int32), exp[c].view(torch.int32)), c
+
+
+def test_host_io_steps_double_buffered_without_synchronisation():
+    """Two host buffers and two io buffers used in alternation, six steps of
+    one batch enqueued with no host synchronisation between them (each
+    buffer's previous step is waited for with an event before it is
+    rewritten): every step's result is its own."""
+    w = W.custom(M=3, num_heads=8, num_kv_heads=2, head_dim=64, max_len=600, seed=37)
+    inp = W.make_inputs(w, positions=np.array([5, 250, 590], np.int32))  # room for 5 more rows
+    t = W.upload(inp, w, DEV)
+    M, H, D = inp.q.shape
+    hios = [B.HostIo(M, H, w.num_kv_heads, D) for _ in range(2)]
+    ios = [B.step_io(M, H, w.num_kv_heads, D, device=DEV) for _ in range(2)]
+    ws = B.workspace(M, H, w.num_kv_heads, D, w.max_len, w.chunk_size, device=DEV)
+    done = [None, None]      # event after each buffer's latest step
+    pending = [None, None]   # the oracle's result for that step
+    rng = np.random.default_rng(41)
+    k_seq = [np.asarray(s, np.float32) for s in inp.k_seq]
+    v_seq = [np.asarray(s, np.float32) for s in inp.v_seq]
+    pos = np.asarray(inp.positions, np.int32).copy()
+    results = []
+    for step in range(6):
+        b = step % 2
+        if done[b] is not None:  # the buffer's previous step: result copied out, inputs read
+            done[b].synchronize()
+            results.append((hios[b].out.clone(), pending[b]))
+        q = rng.standard_normal(inp.q.shape).astype(np.float32)
+        if step == 0:
+            kr, vr = np.asarray(inp.k_rows, np.float32), np.asarray(inp.v_rows, np.float32)
+        else:
+            kr = rng.standard_normal(inp.k_rows.shape).astype(np.float32)
+            vr = rng.standard_normal(inp.v_rows.shape).astype(np.float32)
+            pos = pos + 1
+            for i in range(M):
+                k_seq[i] = np.concatenate([k_seq[i], kr[i][:, None, :]], axis=1)
+                v_seq[i] = np.concatenate([v_seq[i], vr[i][:, None, :]], axis=1)
+        h = hios[b]
+        h.q.copy_(torch.from_numpy(q))
+        h.k_rows.copy_(torch.from_numpy(kr))
+        h.v_rows.copy_(torch.from_numpy(vr))
+        h.positions.copy_(torch.from_numpy(pos.copy()))
+        B.kvs_decode_step_host_io(h, t["k_cache"], t["v_cache"], chunk_size=w.chunk_size,
+                                  workspace=ws, io=ios[b])
+        ev = torch.cuda.Event()
+        ev.record()
+        done[b] = ev
+        pending[b] = oracle.decode_sequences(q, k_seq, v_seq, pos)
+    torch.cuda.synchronize()
+    for b in (0, 1):
+        results.append((hios[b].out.clone(), pending[b]))
+    assert len(results) == 6
+    for n, (o, r) in enumerate(results):
+        gate(o.numpy(), r, where=f"double-buffered step {n}")

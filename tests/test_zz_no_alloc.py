@@ -1,17 +1,21 @@
 """kvs_flash_decode_static: the entry point for callers that cannot allocate
 device memory (it keeps its scratch in a buffer built into the library).
 
-Its output must match kvs_flash_decode (which uses a caller workspace) on the
-same inputs, on two calls in a row -- the second call runs on different inputs
-over whatever the first left in the shared buffer.  This file is collected
-last; it builds the library itself so it also passes alone in a fresh process.
+The persistent kernel is forced, so every call below really keeps its
+partials and completion counters in that one built-in buffer (the cluster
+kernel needs no scratch).  A first call on NaN-filled queries and caches
+leaves NaN partials there; then three calls in a row -- shape A, shape B,
+shape A again -- each run over whatever the previous call left (stale
+partials and counters at other offsets of the workspace layout) and are
+each checked against the f64 oracle with the parity gate used for every
+decode output.  This file is collected last and builds the library itself,
+so it also passes alone in a fresh process.
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from helpers import gate
 from split_flash_decoding_kvcachescatter_gb300 import binding as B
 from split_flash_decoding_kvcachescatter_gb300 import build as kbuild
@@ -20,14 +24,21 @@ from split_flash_decoding_kvcachescatter_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
+CASE_A = dict(seed=41, M=8, H=32, Hkv=8, D=128, Lmax=3000, chunk=0)
+CASE_B = dict(seed=42, M=5, H=14, Hkv=2, D=64, Lmax=777, chunk=100)
 
-def _case(seed, M, H, Hkv, D, Lmax, chunk):
-    w = W.custom(M=M, num_heads=H, num_kv_heads=Hkv, head_dim=D, max_len=Lmax,
-                 chunk_size=chunk, positions="uniform", seed=seed)
+
+def _workload(seed, M, H, Hkv, D, Lmax, chunk):
+    return W.custom(M=M, num_heads=H, num_kv_heads=Hkv, head_dim=D, max_len=Lmax,
+                    chunk_size=chunk, positions="uniform", seed=seed)
+
+
+def _case(c):
+    w = _workload(**c)
     inp = W.make_inputs(w)
-    t = W.upload(inp, w, DEV)
-    B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"], t["v_cache"])
-    return w, t
+    t = W.upload(inp, w, DEV, include_new_row=True)  # caches as the scatter leaves them
+    ref = oracle.decode_sequences(inp.q, inp.k_seq, inp.v_seq, inp.positions)
+    return w, t, ref
 
 
 def _static_call(L, t, w, out, status):
@@ -39,25 +50,45 @@ def _static_call(L, t, w, out, status):
         w.chunk_size, status.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
 
-def test_static_workspace_entry_matches_workspace_entry():
+def test_static_workspace_entry_matches_the_oracle_on_calls_in_a_row():
     assert torch.cuda.is_available(), "GPU test needs a CUDA device"
     kbuild.build()
     L = B.lib()
-    status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    cases = [dict(seed=41, M=8, H=32, Hkv=8, D=128, Lmax=3000, chunk=0),
-             dict(seed=42, M=5, H=14, Hkv=2, D=64, Lmax=777, chunk=100)]
-    for c in cases:  # two calls in a row, different inputs and shapes
-        w, t = _case(**c)
-        ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len,
-                         w.chunk_size, device=DEV)
-        ref = torch.empty_like(t["q"])
-        B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], ref,
-                           chunk_size=w.chunk_size, workspace=ws)
-        out = torch.full_like(t["q"], float("nan"))
-        assert _static_call(L, t, w, out, status) == B.KVS_OK
+    prev = B.kvs_set_schedule(B.KVS_SCHEDULE_PERSISTENT)
+    try:
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        for c in (CASE_A, CASE_B):
+            assert B.kvs_schedule_for(c["M"], c["H"], c["Hkv"], c["D"], c["Lmax"]) == \
+                B.KVS_SCHEDULE_PERSISTENT
+        # a call on garbage: NaN queries and caches fill the buffer with NaN partials
+        w, t, _ = _case(CASE_A)
+        junk = {k: v.clone() for k, v in t.items()}
+        for name in ("q", "k_cache", "v_cache"):
+            junk[name].fill_(float("nan"))
+        out = torch.empty_like(junk["q"])
+        assert _static_call(L, junk, w, out, status) == B.KVS_OK
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        gate(out.cpu().numpy(), ref.cpu().numpy(), where=f"static vs workspace entry {c}")
+        del junk
+        # A, B, A: each over what the previous call left in the shared buffer
+        for c in (CASE_A, CASE_B, CASE_A):
+            w, t, ref = _case(c)
+            out = torch.full_like(t["q"], float("nan"))
+            assert _static_call(L, t, w, out, status) == B.KVS_OK
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            gate(out.cpu().numpy(), ref, where=f"static entry {c}")
+            # and the same as the entry point with a caller workspace
+            ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len,
+                             w.chunk_size, device=DEV)
+            ref_gpu = torch.empty_like(t["q"])
+            B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], ref_gpu,
+                               chunk_size=w.chunk_size, workspace=ws)
+            torch.cuda.synchronize()
+            gate(out.cpu().numpy(), ref_gpu.cpu().numpy().astype(np.float64),
+                 where=f"static vs workspace entry {c}")
+    finally:
+        B.kvs_set_schedule(prev)
 
 
 def test_static_workspace_entry_rejects_problems_beyond_its_buffer():
