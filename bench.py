@@ -1,27 +1,38 @@
-"""Benchmark of one decode step of the attention hot path on GB300.
+"""Benchmark of the decode-step attention hot path on GB300.
 
-A step = one layer's decode step of a seeded synthetic workload through the C
-ABI: kvs_decode_step, i.e. the KV-cache scatter of the new rows, the split
-plan, the chunk partials and the rescaled merge, all in one kernel launch.
-The same step as kvs_kv_scatter + kvs_flash_decode (two launches) is timed
-beside it for the per-call breakdown.  Prints ONE JSON line (rank 0).
+A step = one decode step of a seeded synthetic workload through the C ABI:
+kvs_decode_step per layer, i.e. the KV-cache scatter of the new rows, the
+split plan, the chunk partials and the rescaled merge, all in one kernel
+launch.  One run measures every workload of the decode path and prints ONE
+JSON line (rank 0):
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
                     [--chunk C] [--impl kvs|reference]
 
-value      : algorithmic GB/s of the step (live KV bytes read + Q read + O
-             written + positions, plus the scatter's row bytes), inputs resident
-             in HBM, device time from CUDA events, max over ranks.
-e2e        : the same metric when every step also copies its inputs (q, new K/V
-             rows, positions) from pinned host memory and reads the output back,
-             all through kvs_decode_step_host (one C call per layer).
-us_per_call: the step's mean, median, p10 and p90 over the timed steps
-             (L2 scrubbed between steps when the working set fits in it), the
-             hot mean of back-to-back steps, and the two-launch breakdown.
-roofline   : the step kernel (the step's one launch): its algorithmic bytes /
-             its mean event-timed duration, against the measured HBM copy
-             bandwidth.
-cpu_baseline: the f64 CPU oracle on the host cores (rank 0, N=1 only).
+The headline (`value`, `config`, `roofline`, `e2e`, `cpu_baseline`) is the
+--config workload, by default `ragged`, the largest: 32 sequences of up to
+131,072 positions, 34 GB of caches.  `per_config` holds the same
+measurements for all five workloads (tiny, small_model as one CUDA graph of
+24 layers, 8b_batch, long_context with its chunk sweep, ragged).
+
+value       : algorithmic GB/s of the step (live KV bytes read + Q read + O
+              written + positions, plus the scatter's row bytes), inputs
+              resident in HBM, device time from CUDA events, max over ranks.
+e2e         : the same metric when every step also copies its inputs (q, new
+              K/V rows, positions) from pinned host memory and its output
+              back, through kvs_decode_step_host_io (one C call per layer:
+              one copy in, the step, one copy out); two host buffers in
+              alternation, each reused once its previous step's output has
+              reached the host.
+us_per_call : the step's mean, median, p10 and p90 over the timed steps
+              (L2 scrubbed between steps when the working set fits in it),
+              the hot mean of back-to-back steps, and for the headline the
+              two-launch breakdown.
+roofline    : the step kernel (the step's one launch per layer): its
+              algorithmic bytes / its mean event-timed duration, against the
+              measured HBM copy bandwidth.
+cpu_baseline: the f64 CPU oracle on the host cores, all threads and one
+              (rank 0, N=1 only), on the headline workload.
 --impl reference times that oracle as the reference arm.
 Under torchrun every rank runs its own batch (weak scaling, no collective on
 the data path; a barrier and a max-reduction of the timings only).
@@ -48,7 +59,14 @@ from split_flash_decoding_kvcachescatter_gb300 import workloads as W  # noqa: E4
 
 METRIC = "split-K decode attention: KV-cache HBM GB/s (% of GB300 peak) and µs/call"
 L2_BYTES = 129 * 1024 * 1024
+NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s the targets are stated against
 FALLBACK_HBM_GBS = 6800.0
+HEADLINE = "ragged"  # the largest workload that fits one GPU
+# Every workload of the decode path, in the order they are measured.
+PER_CONFIG = ("tiny", "small_model", "8b_batch", "long_context", "ragged")
+# Timed steps of a per-config leg: at least these, at least --steps.
+MIN_STEPS = {"tiny": 200, "small_model": 200, "8b_batch": 100, "long_context": 100,
+             "ragged": 20}
 CSRC = os.path.join(ROOT, "split_flash_decoding_kvcachescatter_gb300", "csrc")
 # Sources of each attention kernel (a recorded ncu capture is used only
 # while these are unchanged).
@@ -126,6 +144,29 @@ def ncu_traffic(kernel, workload, chunk):
     return int(e["dram_bytes_per_launch"])
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo) and core count."""
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not name:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu model")):
+                        name = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"cpu_model": name or "unknown", "nproc": os.cpu_count() or 1}
+
+
 VOCAB = 152064  # vocabulary of the pages' batched argmax (PAR-062)
 
 
@@ -194,9 +235,9 @@ def tensor_peak():
 
 
 def time_prefill(B, torch, dev, stream, iters=20, shape=PREFILL_SHAPE, causal=True):
-    """Tensor-core prefill attention (kvs_prefill_attention): the FP16 pack
-    launch and the tcgen05 attention launch, timed together.  At the default
-    shape the inputs (3 x 67 MB) and the packed workspace exceed L2."""
+    """Tensor-core prefill attention (kvs_prefill_attention), timed as one
+    call (all its launches).  At the default shape the inputs (3 x 67 MB)
+    and the packed workspace exceed L2."""
     H, S, D = shape
     g = torch.Generator(device=dev).manual_seed(4321)
     q, k, v = (torch.randn((H, S, D), device=dev, generator=g) for _ in range(3))
@@ -217,7 +258,7 @@ def time_prefill(B, torch, dev, stream, iters=20, shape=PREFILL_SHAPE, causal=Tr
     flops = 4.0 * D * H * (S * (S + 1) / 2 if causal else S * S)
     tf = flops / (ms * 1e-3) / 1e12
     peak, kind = tensor_peak()
-    return {"kernel": "prefill_pack_kernel + prefill_tc_kernel (kvs_prefill_attention)",
+    return {"kernel": "prefill kernels (kvs_prefill_attention)",
             "heads": H, "seq_len": S, "head_dim": D, "causal": causal,
             "dtype": "f16 x f16 -> f32",
             "us_per_call": 1e3 * ms, "flops_per_call": flops,
@@ -260,7 +301,9 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, windows):
+        """Median SM clock, max clock and throttle reasons over the samples
+        taken inside the given (t0, t1) windows (the timed regions)."""
         rows = []
         for ts, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -272,11 +315,13 @@ class ClockSampler:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        inside = [r for r in rows if t0 <= r[0] <= t1]
-        window = "timed region"
-        if not inside:  # timed region shorter than the sampling interval
-            inside = rows
-            window = "warmup + timed region"
+        inside = [r for r in rows if any(t0 <= r[0] <= t1 for t0, t1 in windows)]
+        window = "timed regions"
+        if not inside:  # timed regions shorter than the sampling interval
+            t0 = min(w[0] for w in windows) - 1.0
+            t1 = max(w[1] for w in windows) + 1.0
+            inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+            window = "around the timed regions"
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in inside for n, v in zip(names, r[3][5:9])
                           if v.lower().startswith("active")})
@@ -295,17 +340,18 @@ def _unit_bytes(inp, w, i):
 
 class CpuOracleRunner:
     """Runs the f64 CPU oracle over (sequence, query head) units of the
-    workload, in rotation, on all host cores (the C call releases the GIL).
-    A sample is time-bounded: batches of units run until the budget is spent."""
+    workload, in rotation, on `threads` host threads (the C call releases the
+    GIL).  A sample is time-bounded: batches of units run until the budget is
+    spent."""
 
-    def __init__(self, inp, w):
+    def __init__(self, inp, w, threads=None):
         from concurrent.futures import ThreadPoolExecutor
         import oracle
         oracle.build()
         self.oracle = oracle
         self.inp, self.w = inp, w
-        self.threads = os.cpu_count() or 1
-        self.pool = ThreadPoolExecutor(max_workers=self.threads)
+        self.threads = threads or os.cpu_count() or 1
+        self.pool = ThreadPoolExecutor(max_workers=self.threads) if self.threads > 1 else None
         self.units = [(i, h) for i in range(w.M) for h in range(w.num_heads)]
         self.next = 0
         self.G = w.group
@@ -325,16 +371,19 @@ class CpuOracleRunner:
         while True:
             us = [self.units[(self.next + k) % len(self.units)] for k in range(batch)]
             self.next = (self.next + batch) % len(self.units)
-            done_bytes += sum(self.pool.map(self._one, us))
+            if self.pool is not None:
+                done_bytes += sum(self.pool.map(self._one, us))
+            else:
+                done_bytes += sum(self._one(u) for u in us)
             n += batch
             if time.perf_counter() - t0 >= budget_s:
                 break
         return time.perf_counter() - t0, done_bytes, n
 
-    def describe(self, n_units, passes=None):
+    def describe(self, n_units):
         return (f"{n_units} (sequence, query head) units of the {self.w.name} workload in "
                 f"rotation ({len(self.units)} units = the whole batch), f64 C oracle on "
-                f"{self.threads} host threads")
+                f"{self.threads} host thread{'s' if self.threads > 1 else ''}")
 
 
 def run_reference(args, w, inp, rank, world):
@@ -361,25 +410,315 @@ def run_reference(args, w, inp, rank, world):
                    "max_len": w.max_len, "algorithmic_bytes_per_step": ab["step"],
                    "step": f"a time-bounded sample of about {budget:.2f} s of oracle work"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": runner.threads,
-                         "kind": "oracle", "sample": runner.describe(tot_n)},
+                         "kind": "oracle", "sample": runner.describe(tot_n), **cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+class Ctx:
+    """What every leg of a run shares: the torch modules, the device, the
+    stream, the binding, the rank layout and the timed-region clock."""
+
+    def __init__(self, torch, tdist, B, dev, rank, world):
+        self.torch, self.tdist, self.B = torch, tdist, B
+        self.dev, self.rank, self.world = dev, rank, world
+        self.stream = torch.cuda.current_stream()
+        self.windows = []  # wall-clock (t0, t1) of every timed region
+
+    def barrier(self):
+        if self.world > 1:
+            self.tdist.barrier()
+
+
+def measure_workload(ctx, w, seed, steps, warmup, chunks, graph=False, full=False,
+                     e2e_steps=None, keep_inputs=False):
+    """Times one workload's decode step for each chunk size in `chunks` (0 =
+    the library rule), on the same inputs.  Returns a list of result dicts,
+    one per chunk; the first also carries the e2e leg, and with `full` the
+    two-launch breakdown.  Multi-layer workloads (small_model) time all
+    layers as one step, eagerly or, with `graph`, as one captured graph."""
+    torch, B, dev, stream = ctx.torch, ctx.B, ctx.dev, ctx.stream
+    nl = w.layers
+    inp = W.make_inputs(w, seed=seed)
+    inps = [inp] + [W.make_inputs(w, layer=l, seed=seed, positions=inp.positions)
+                    for l in range(1, nl)]
+    ts = [W.upload(x, w, dev) for x in inps]
+    outs = [torch.empty_like(t["q"]) for t in ts]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ab1 = W.algorithmic_bytes(inp, w)  # one layer; every layer has the same positions
+    ab = {k: v * nl for k, v in ab1.items()}
+    flush = ab["step"] < 4 * L2_BYTES  # small working sets: scrub L2 between steps
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    kernel = ("cluster" if B.kvs_schedule_for(w.M, w.num_heads, w.num_kv_heads, w.head_dim,
+                                               w.max_len) == B.KVS_SCHEDULE_CLUSTER
+              else "persistent")
+    peak, peak_kind = hbm_peak()
+    results = []
+    for ci, chunk in enumerate(chunks):
+        resolved = chunk if chunk > 0 else B.kvs_choose_chunk_size(
+            w.M, w.num_kv_heads, w.head_dim, w.max_len)
+        ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, resolved,
+                         device=dev)
+
+        def eager_step():
+            for t, out in zip(ts, outs):
+                B.kvs_decode_step(t["q"], t["k_rows"], t["v_rows"], t["positions"],
+                                  t["k_cache"], t["v_cache"], out, chunk_size=resolved,
+                                  workspace=ws, d_status=status)
+
+        sg = None
+        if graph:
+            eager_step()  # configure the kernels outside the capture
+            torch.cuda.synchronize()
+            sg = B.kvs_step_graph_create(
+                [t["q"] for t in ts], [t["k_rows"] for t in ts], [t["v_rows"] for t in ts],
+                ts[0]["positions"], [t["k_cache"] for t in ts], [t["v_cache"] for t in ts],
+                outs, chunk_size=resolved, workspace=ws, d_status=status)
+
+        def step():
+            if sg is not None:
+                sg.launch(stream)
+            else:
+                eager_step()
+
+        for _ in range(warmup):
+            if flush:
+                scrub.zero_()
+            step()
+        torch.cuda.synchronize()
+        # events only at step boundaries, so the programmatic launch overlap
+        # between the step's kernels is untouched
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ctx.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        for k in range(steps):
+            if flush:
+                scrub.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+        ctx.barrier()
+        ctx.windows.append((wall0, time.time()))
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        if int(status.item()) != 0:
+            raise SystemExit(f"{w.name}: device status {B.strerror(int(status.item()))}")
+
+        # hot: the same step back to back, nothing between steps (L2 warm);
+        # eager steps are captured into one CUDA graph of HOT_CHUNK steps and
+        # replayed, so that the host's launch rate does not set the time
+        HOT_CHUNK = 20
+        hot_reps = max(1, min(steps, 200) // HOT_CHUNK)
+        hot_mode = "step graph launched back to back"
+        if sg is not None:
+            hot_run, hot_calls, KH = step, hot_reps * HOT_CHUNK, hot_reps * HOT_CHUNK
+        else:
+            try:
+                hot_graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(hot_graph):
+                    for _ in range(HOT_CHUNK):
+                        eager_step()
+                torch.cuda.synchronize()
+                hot_run, hot_calls, KH = hot_graph.replay, hot_reps, hot_reps * HOT_CHUNK
+                hot_mode = f"graph of {HOT_CHUNK} eager steps, replayed"
+            except RuntimeError as e:  # capture refused: eager steps back to back
+                torch.cuda.synchronize()
+                hot_run, hot_calls, KH = step, hot_reps * HOT_CHUNK, hot_reps * HOT_CHUNK
+                hot_mode = f"eager steps back to back (capture failed: {str(e)[:80]})"
+        hot_run()
+        torch.cuda.synchronize()
+        h0 = torch.cuda.Event(enable_timing=True)
+        h1 = torch.cuda.Event(enable_timing=True)
+        h0.record(stream)
+        for _ in range(hot_calls):
+            hot_run()
+        h1.record(stream)
+        torch.cuda.synchronize()
+        hot_ms = h0.elapsed_time(h1) / KH
+
+        total_ms = sum(step_ms)
+        total_ms_max, _, bytes_all, _ = reduce_over_ranks(total_ms, 0.0, ab["step"] * steps, 0.0,
+                                                          ctx.world, dev)
+        mean_ms = total_ms / steps
+        achieved = ab["step"] / (mean_ms * 1e-3) / 1e9
+        traffic1 = ncu_traffic(kernel, w.name, resolved)
+        res = {
+            "workload": w.name, "kernel": KERNEL_NAMES[kernel], "chunk_size": resolved,
+            "chunk_rule": "given" if chunk > 0 else "library rule (chunk_size=0)",
+            "layers": nl,
+            "launch": ("one CUDA graph for all layers" if sg is not None
+                       else f"{nl} kvs_decode_step launch(es)"),
+            "steps": steps,
+            "value": bytes_all / (total_ms_max * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": total_ms_max / steps,
+            "us_per_call": {"decode_step": 1e3 * mean_ms,
+                            "decode_step_median": 1e3 * statistics.median(step_ms),
+                            "decode_step_p10": 1e3 * percentile(step_ms, 10),
+                            "decode_step_p90": 1e3 * percentile(step_ms, 90),
+                            "decode_step_hot": 1e3 * hot_ms, "hot_steps": KH,
+                            "hot_mode": hot_mode},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                         "traffic": traffic1,
+                         "kernel": f"{KERNEL_NAMES[kernel]} (kvs_decode_step)",
+                         "bytes_per_launch": ab1["step"]},
+            "live_kv_bytes": W.kv_bytes(inp, w) * nl,
+            "algorithmic_bytes_per_step": ab["step"],
+            "cache_bytes_allocated": 2 * w.cache_elems() * 4 * nl,
+            "l2": ("L2 scrubbed (2x129 MB write) between timed steps, outside the events"
+                   if flush else "inputs larger than L2 (live KV bytes >> 129 MB)"),
+            "seed": seed,
+        }
+        if nl > 1:
+            res["us_per_layer"] = 1e3 * mean_ms / nl
+
+        if full:  # the same step as kvs_kv_scatter + kvs_flash_decode, an event between
+            KB = min(steps, 500)
+            b_start = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
+            b_end = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
+            mids = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
+            torch.cuda.synchronize()
+            for k in range(KB):
+                if flush:
+                    scrub.zero_()
+                b_start[k].record(stream)
+                for t in ts:
+                    B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
+                                     t["v_cache"], d_status=status)
+                mids[k].record(stream)
+                for t, out in zip(ts, outs):
+                    B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
+                                       chunk_size=resolved, workspace=ws, d_status=status)
+                b_end[k].record(stream)
+            torch.cuda.synchronize()
+            scatter_ms = [s.elapsed_time(m) for s, m in zip(b_start, mids)]
+            decode_ms = [m.elapsed_time(e) for m, e in zip(mids, b_end)]
+            res["us_per_call"].update({"kv_scatter": 1e3 * statistics.mean(scatter_ms),
+                                       "flash_decode": 1e3 * statistics.mean(decode_ms),
+                                       "breakdown_steps": KB})
+            res["attention_gbs"] = ab["attention"] / (statistics.mean(decode_ms) * 1e-3) / 1e9
+
+        if ci == 0:
+            res["e2e"] = measure_e2e(ctx, w, ts, inps, ws, resolved, status, scrub, warmup,
+                                     e2e_steps or max(3, min(steps, 500)), ab["step"])
+        if sg is not None:
+            sg.destroy()
+        del ws
+        results.append(res)
+    if keep_inputs:  # the host inputs, for the CPU baseline on the same batch
+        results[0]["_inputs"] = inp
+    del ts, outs, scrub
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return results
+
+
+def measure_e2e(ctx, w, ts, inps, ws, chunk, status, scrub, warmup, Ke, step_bytes):
+    """The step through the public host-buffer entry point: for every layer
+    one kvs_decode_step_host_io call (one copy of q, k_rows, v_rows and
+    positions from pinned host memory, the fused step, one copy of out back).
+    Two sets of host and device io buffers in alternation: a set is reused
+    once the event after its previous step has passed, i.e. its output has
+    reached the host (the host waits for it), so step k+1's calls are
+    enqueued while step k runs."""
+    torch, B, dev, stream = ctx.torch, ctx.B, ctx.dev, ctx.stream
+    M, H, D = ts[0]["q"].shape
+    Hkv = w.num_kv_heads
+    sets = []
+    for _ in range(2):
+        hios = []
+        for x in inps:
+            h = B.HostIo(M, H, Hkv, D)
+            h.q.copy_(torch.from_numpy(np.ascontiguousarray(x.q, np.float32)))
+            h.k_rows.copy_(torch.from_numpy(np.ascontiguousarray(x.k_rows, np.float32)))
+            h.v_rows.copy_(torch.from_numpy(np.ascontiguousarray(x.v_rows, np.float32)))
+            h.positions.copy_(torch.from_numpy(np.ascontiguousarray(x.positions, np.int32)))
+            hios.append(h)
+        sets.append((hios, B.step_io(M, H, Hkv, D, device=dev)))
+    h2d = sum(h.in_bytes for h in sets[0][0])
+    d2h = sum(h.out_bytes for h in sets[0][0])
+    done = [None, None]
+
+    def e2e_step(k):
+        b = k % 2
+        if done[b] is not None:
+            done[b].synchronize()  # that set's previous output is on the host
+        hios, io = sets[b]
+        for l, t in enumerate(ts):
+            B.kvs_decode_step_host_io(hios[l], t["k_cache"], t["v_cache"], chunk_size=chunk,
+                                      workspace=ws, io=io, d_status=status, stream=stream)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        done[b] = ev
+
+    for k in range(warmup):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    done[0] = done[1] = None
+    ctx.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record(stream)
+    for k in range(Ke):
+        if scrub is not None:
+            scrub.zero_()
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ctx.windows.append((wall0, time.time()))
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if scrub is not None:  # take the scrub time back out
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(Ke):
+            scrub.zero_()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms -= s0.elapsed_time(s1) / Ke
+    if int(status.item()) != 0:
+        raise SystemExit(f"{w.name} e2e: device status {B.strerror(int(status.item()))}")
+    _, e2e_ms_max, _, bytes_all = reduce_over_ranks(0.0, e2e_ms, 0.0, step_bytes * Ke,
+                                                    ctx.world, dev)
+    return {"value": bytes_all / (e2e_ms_max * Ke * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": e2e_ms_max, "steps": Ke,
+            "api": "kvs_decode_step_host_io, one call per layer; two buffer sets in alternation"}
+
+
+def brief(res):
+    """The per_config view of one measurement."""
+    keep = ("kernel", "chunk_size", "chunk_rule", "layers", "launch", "steps", "value", "unit",
+            "ms_per_step", "us_per_call", "us_per_layer", "live_kv_bytes",
+            "algorithmic_bytes_per_step", "l2", "e2e")
+    out = {k: res[k] for k in keep if k in res}
+    r = res["roofline"]
+    out["roofline"] = {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                         "frac_of_nominal_8tbs", "traffic")}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b_batch", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--chunk", type=int, default=None, help="override the chunk size")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=HEADLINE, choices=sorted(W.WORKLOADS),
+                    help="the headline workload")
+    ap.add_argument("--chunk", type=int, default=None, help="override the headline chunk size")
     ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--graph", action="store_true",
-                    help="launch the whole (multi-layer) step as one captured CUDA graph")
+                    help="launch the headline's (multi-layer) step as one captured CUDA graph")
+    ap.add_argument("--only-headline", action="store_true",
+                    help="measure the headline workload alone (no per_config legs)")
     ap.add_argument("--no-argmax", action="store_true",
                     help="skip the batched argmax measurement")
     ap.add_argument("--no-prefill", action="store_true",
@@ -399,10 +738,9 @@ def main():
     rank, world, local = dist_env()
     w = W.WORKLOADS[args.config]
     seed = rank_seed(w, rank)
-    inp = W.make_inputs(w, seed=seed)
 
     if args.impl == "reference":
-        return run_reference(args, w, inp, rank, world)
+        return run_reference(args, w, W.make_inputs(w, seed=seed), rank, world)
 
     import torch
     import torch.distributed as tdist
@@ -431,267 +769,90 @@ def main():
         return
     B.kvs_set_schedule({"auto": B.KVS_SCHEDULE_AUTO, "persistent": B.KVS_SCHEDULE_PERSISTENT,
                         "cluster": B.KVS_SCHEDULE_CLUSTER}[args.schedule])
-    kernel = ("cluster" if B.kvs_schedule_for(w.M, w.num_heads, w.num_kv_heads, w.head_dim,
-                                               w.max_len) == B.KVS_SCHEDULE_CLUSTER
-              else "persistent")
-
-    def barrier():
-        if world > 1:
-            tdist.barrier()
-
-    nl = w.layers  # a step covers every layer of the workload (24 for small_model)
-    inps = [inp] + [W.make_inputs(w, layer=l, seed=seed, positions=inp.positions)
-                    for l in range(1, nl)]
-    ts = [W.upload(x, w, dev) for x in inps]
-    chunk = args.chunk if args.chunk is not None else w.chunk_size
-    resolved_chunk = chunk if chunk > 0 else B.kvs_choose_chunk_size(
-        w.M, w.num_kv_heads, w.head_dim, w.max_len)
-    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, resolved_chunk,
-                     device=dev)
-    outs = [torch.empty_like(t["q"]) for t in ts]
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ab1 = W.algorithmic_bytes(inp, w)  # one layer; every layer has the same positions
-    ab = {k: v * nl for k, v in ab1.items()}
-    cache_bytes = 2 * w.cache_elems() * 4 * nl
-    flush = ab["step"] < 4 * L2_BYTES  # small working sets: scrub L2 between steps
-    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-    stream = torch.cuda.current_stream()
-
-    def eager_step():
-        """The whole hot path, one launch per layer: scatter, split plan, chunk
-        partials and the rescaled merge (kvs_decode_step)."""
-        for t, out in zip(ts, outs):
-            B.kvs_decode_step(t["q"], t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
-                              t["v_cache"], out, chunk_size=resolved_chunk, workspace=ws,
-                              d_status=status)
-
-    graph = None
-    if args.graph:
-        eager_step()  # configure the kernels outside the capture
-        torch.cuda.synchronize()
-        graph = B.kvs_step_graph_create(
-            [t["q"] for t in ts], [t["k_rows"] for t in ts], [t["v_rows"] for t in ts],
-            ts[0]["positions"], [t["k_cache"] for t in ts], [t["v_cache"] for t in ts], outs,
-            chunk_size=resolved_chunk, workspace=ws, d_status=status)
-        for t in ts[1:]:  # the graph reads the positions of layer 0 for every layer
-            t["positions"] = ts[0]["positions"]
-
-    def step():
-        if graph is not None:
-            graph.launch(stream)
-        else:
-            eager_step()
-
-    def two_calls(mid):
-        """The same step as the two separate entry points (all layers' scatters,
-        an event, then all layers' attention)."""
-        for t in ts:
-            B.kvs_kv_scatter(t["k_rows"], t["v_rows"], t["positions"], t["k_cache"],
-                             t["v_cache"], d_status=status)
-        mid.record(stream)
-        for t, out in zip(ts, outs):
-            B.kvs_flash_decode(t["q"], t["k_cache"], t["v_cache"], t["positions"], out,
-                               chunk_size=resolved_chunk, workspace=ws, d_status=status)
-
+    ctx = Ctx(torch, tdist, B, dev, rank, world)
     sampler = ClockSampler(local)
     sampler.start()
-    for _ in range(args.warmup):
-        if flush:
-            scrub.zero_()
-        step()
-    torch.cuda.synchronize()
 
-    K = args.steps
-    # Region A (the headline): events only at step boundaries, so the
-    # programmatic launch overlap between the step's kernels is untouched.
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    barrier()
-    torch.cuda.synchronize()
-    wall0 = time.time()
-    for k in range(K):
-        if flush:
-            scrub.zero_()
-        starts[k].record(stream)
-        step()
-        ends[k].record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    wall1 = time.time()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    # Region B (breakdown): the step as kvs_kv_scatter + kvs_flash_decode,
-    # an event between the two launches.
-    KB = min(K, 500)
-    b_start = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
-    b_end = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(KB)]
-    torch.cuda.synchronize()
-    for k in range(KB):
-        if flush:
-            scrub.zero_()
-        b_start[k].record(stream)
-        two_calls(mids[k])
-        b_end[k].record(stream)
-    torch.cuda.synchronize()
-    scatter_ms = [s.elapsed_time(m) for s, m in zip(b_start, mids)]
-    decode_ms = [m.elapsed_time(e) for m, e in zip(mids, b_end)]
-    if int(status.item()) != 0:
-        raise SystemExit(f"device status: {B.strerror(int(status.item()))}")
+    per_config = {}
+    head = None
+    legs = [args.config] if args.only_headline else \
+        [n for n in PER_CONFIG if n != args.config] + [args.config]
+    for name in legs:
+        wl = W.WORKLOADS[name]
+        is_head = name == args.config
+        steps = args.steps if is_head else max(args.steps, MIN_STEPS[name])
+        graph = (args.graph if is_head else wl.layers > 1)
+        if is_head:
+            chunks = [args.chunk if args.chunk is not None else wl.chunk_size]
+        else:
+            chunks = [wl.chunk_size]
+        if wl.chunk_sweep and not (is_head and args.chunk is not None):
+            chunks += [c for c in wl.chunk_sweep if c != chunks[0]] + [0]
+        res = measure_workload(ctx, wl, rank_seed(wl, rank), steps, args.warmup, chunks,
+                               graph=graph, full=is_head, e2e_steps=args.e2e_steps,
+                               keep_inputs=is_head)
+        entry = brief(res[0])
+        if len(res) > 1:
+            entry["chunk_sweep"] = [
+                {"chunk_size": r["chunk_size"], "chunk_rule": r["chunk_rule"],
+                 "us_per_call": r["us_per_call"]["decode_step"],
+                 "us_median": r["us_per_call"]["decode_step_median"],
+                 "value": r["value"], "frac": r["roofline"]["frac"],
+                 "frac_of_nominal_8tbs": r["roofline"]["frac_of_nominal_8tbs"]}
+                for r in res]
+        per_config[name] = entry
+        if is_head:
+            head = res[0]
 
-    # ---- hot: the same step back to back, nothing between steps (L2 warm) ----
-    # The eager steps are captured into one CUDA graph of HOT_CHUNK steps and
-    # replayed, so that the host's launch rate does not set the time (the
-    # step graph of --graph is launched back to back as it is).
-    HOT_CHUNK = 20
-    hot_reps = max(1, min(K, 200) // HOT_CHUNK)
-    torch.cuda.synchronize()
-    hot_mode = "step graph launched back to back"
-    if graph is not None:
-        hot_run, KH = step, hot_reps * HOT_CHUNK
-        hot_calls = KH
-    else:
-        try:
-            hot_graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(hot_graph):
-                for _ in range(HOT_CHUNK):
-                    eager_step()
-            torch.cuda.synchronize()
-            hot_run, hot_calls, KH = hot_graph.replay, hot_reps, hot_reps * HOT_CHUNK
-            hot_mode = f"graph of {HOT_CHUNK} eager steps, replayed"
-        except RuntimeError as e:  # capture refused: eager steps back to back
-            torch.cuda.synchronize()
-            hot_run, KH = step, hot_reps * HOT_CHUNK
-            hot_calls = KH
-            hot_mode = f"eager steps back to back (capture failed: {str(e)[:80]})"
-    hot_run()
-    torch.cuda.synchronize()
-    h0 = torch.cuda.Event(enable_timing=True)
-    h1 = torch.cuda.Event(enable_timing=True)
-    h0.record(stream)
-    for _ in range(hot_calls):
-        hot_run()
-    h1.record(stream)
-    torch.cuda.synchronize()
-    hot_ms = h0.elapsed_time(h1) / KH
-
-    # ---- e2e: host buffers through the public API ----
-    # kvs_decode_step_host: one library call per layer enqueues the copies of
-    # that layer's inputs (pinned host memory) to the device, the fused step,
-    # and the copy of its output back to the host.
-    Ke = args.e2e_steps or max(3, min(K, 500))
-    names = ("q", "k_rows", "v_rows", "positions")
-    host = [{k: t[k].cpu().pin_memory() for k in names} for t in ts]
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    io = B.step_io(w.M, w.num_heads, w.num_kv_heads, w.head_dim, device=dev)
-    h2d = sum(v.numel() * v.element_size() for h in host for v in h.values())
-    d2h = sum(o.numel() * o.element_size() for o in host_out)
-
-    def e2e_step():
-        for l, t in enumerate(ts):
-            B.kvs_decode_step_host(host[l]["q"], host[l]["k_rows"], host[l]["v_rows"],
-                                   host[l]["positions"], t["k_cache"], t["v_cache"], host_out[l],
-                                   chunk_size=resolved_chunk, workspace=ws, io=io,
-                                   d_status=status, stream=stream)
-
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(Ke):
-        if flush:
-            scrub.zero_()
-        e2e_step()
-        # the result must be on the host before the step counts as done
-        stream.synchronize()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / Ke
-    if flush:  # take the scrub time back out
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(Ke):
-            scrub.zero_()
-        s1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms -= s0.elapsed_time(s1) / Ke
-    live_read = time_stream_read(torch, dev, stream)
-    argmax = time_argmax(B, torch, w.M, dev, stream) if not args.no_argmax else None
-    prefill = time_prefill(B, torch, dev, stream) if not args.no_prefill else None
+    live_read = time_stream_read(torch, dev, ctx.stream)
+    argmax = time_argmax(B, torch, w.M, dev, ctx.stream) if not args.no_argmax else None
+    prefill = time_prefill(B, torch, dev, ctx.stream) if not args.no_prefill else None
     sampler.stop()
-    clocks = sampler.summary(wall0, wall1)
-
-    # ---- reduce over ranks ----
-    total_ms_max, e2e_ms_max, bytes_all, bytes_e2e_all = reduce_over_ranks(
-        total_ms, e2e_ms, ab["step"] * K, ab["step"] * Ke, world, dev)
+    clocks = sampler.summary(ctx.windows)
 
     if rank != 0:
         if world > 1:
             tdist.destroy_process_group()
         return
 
-    value = bytes_all / (total_ms_max * 1e-3) / 1e9
-    e2e_value = bytes_e2e_all / (e2e_ms_max * Ke * 1e-3) / 1e9
-    # A step is one launch of the step kernel per layer and nothing else, so
-    # the headline events time exactly those launches: bytes per launch over
-    # the mean launch time is the step's bytes over the step's time.
-    step_mean_ms = total_ms / K
-    achieved = ab["step"] / (step_mean_ms * 1e-3) / 1e9
-    peak, peak_kind = hbm_peak()
-    traffic = ncu_traffic(kernel, w.name, resolved_chunk)
-
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
+        inp = head.pop("_inputs")
         runner = CpuOracleRunner(inp, w)
         runner.sample(0.5)  # warm the pool and the page cache
-        dt, b, n = runner.sample(10.0)
+        dt, b, n = runner.sample(8.0)
+        one = CpuOracleRunner(inp, w, threads=1)
+        dt1, b1, n1 = one.sample(8.0)
         cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": runner.threads, "kind": "oracle",
-               "sample": runner.describe(n)}
+               "sample": runner.describe(n), **cpu_model(),
+               "single_core": {"value": b1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                               "sample": one.describe(n1)}}
 
+    roof = dict(head["roofline"])
+    roof["live_stream_read"] = live_read
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": total_ms_max / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world,
+        "steps": head["steps"], "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
         "config": {
             "workload": w.name, "M": w.M, "num_heads": w.num_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "max_len": w.max_len,
-            "chunk_size": resolved_chunk,
-            "chunk_rule": "given" if chunk > 0 else "library rule (chunk_size=0)",
-            "schedule": args.schedule, "kernel": KERNEL_NAMES[kernel],
-            "layers": nl, "launch": ("one CUDA graph for all layers" if graph is not None
-                                     else f"{nl} kvs_decode_step launch(es)"),
-            "live_kv_bytes": W.kv_bytes(inp, w) * nl,
-            "algorithmic_bytes_per_step": ab["step"],
-            "cache_bytes_allocated": cache_bytes,
-            "l2": ("L2 scrubbed (2x129 MB write) between timed steps, outside the events"
-                   if flush else "inputs larger than L2 (live KV bytes >> 129 MB)"),
-            "seed": seed, "parallelism": f"replicas x{world} (independent batches)",
+            "chunk_size": head["chunk_size"], "chunk_rule": head["chunk_rule"],
+            "schedule": args.schedule, "kernel": head["kernel"], "layers": head["layers"],
+            "launch": head["launch"], "live_kv_bytes": head["live_kv_bytes"],
+            "algorithmic_bytes_per_step": head["algorithmic_bytes_per_step"],
+            "cache_bytes_allocated": head["cache_bytes_allocated"], "l2": head["l2"],
+            "seed": head["seed"], "parallelism": f"replicas x{world} (independent batches)",
         },
-        "us_per_call": {"decode_step": 1e3 * step_mean_ms,
-                        "decode_step_median": 1e3 * statistics.median(step_ms),
-                        "decode_step_p10": 1e3 * percentile(step_ms, 10),
-                        "decode_step_p90": 1e3 * percentile(step_ms, 90),
-                        "decode_step_hot": 1e3 * hot_ms,
-                        "hot_steps": KH, "hot_mode": hot_mode,
-                        "kv_scatter": 1e3 * statistics.mean(scatter_ms),
-                        "flash_decode": 1e3 * statistics.mean(decode_ms),
-                        "breakdown_steps": KB},
-        "attention_gbs": ab["attention"] / (statistics.mean(decode_ms) * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": f"{KERNEL_NAMES[kernel]} (kvs_decode_step)",
-                     "peak_source": peak_kind,
-                     "bytes_per_launch": ab1["step"],
-                     "live_stream_read": live_read},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
-        "gpu_launches": K * nl,
+        "us_per_call": head["us_per_call"],
+        "attention_gbs": head.get("attention_gbs"),
+        "roofline": roof,
+        "e2e": head["e2e"],
+        "gpu_launches": head["steps"] * head["layers"],
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "per_config": per_config,
         "argmax": argmax,
         "prefill": prefill,
     }

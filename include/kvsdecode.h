@@ -497,15 +497,18 @@ int kvs_schedule_for(int M, int num_heads, int num_kv_heads, int head_dim,
  * kernel record KVS_ERR_TIMEOUT in d_status and return instead of waiting
  * on; at the default only a fault could take that long.  Lowering the bound
  * makes waits run out on purpose, so that a caller can test its handling of
- * KVS_ERR_TIMEOUT; under a bound below the default the waits poll without
- * sleeping, and 0 ends the first wait that does not find its data ready.
- * Whatever the bound, a block that gives up still lets every copy and
- * tensor-core product it issued finish before it exits (those waits keep
- * 2 s), and leaves the context usable.  Takes effect for kernels that start
- * after the call returns (a replayed CUDA graph included).  The value
- * applies to every host thread's calls on that device; set it back when
- * done.  The call synchronises with the device like cudaMemcpyToSymbol; it
- * must not be made during a stream capture.
+ * KVS_ERR_TIMEOUT.  Calls made while the bound is below the default launch
+ * a variant of each kernel whose waits poll without sleeping and compare
+ * against the bound at every poll (0 ends the first wait that does not find
+ * its data ready); calls at the default launch the kernels whose waits
+ * sleep in the hardware wait and carry no such test.  A CUDA graph keeps
+ * the variant its capture launched: one captured under a lowered bound
+ * reads the bound in force at each replay.  Whatever the bound, a block
+ * that gives up still lets every copy and tensor-core product it issued
+ * finish before it exits (those waits keep 2 s), and leaves the context
+ * usable.  The value applies to every host thread's calls on that device;
+ * set it back when done.  The call synchronises with the device like
+ * cudaMemcpyToSymbol; it must not be made during a stream capture.
  *   ns        0 .. KVS_WAIT_LIMIT_DEFAULT_NS, else KVS_ERR_DIMS
  *   previous  nullable: receives the bound in force before the call
  * Errors: DIMS, LAUNCH.

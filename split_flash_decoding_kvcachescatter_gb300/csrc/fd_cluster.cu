@@ -53,7 +53,7 @@ constexpr int kMaxClusterSize = 16;  // the largest cluster launched
 template <int D, int G>
 using ClusterGeo = Geo<D, G, 4, 2>;
 
-template <int D, int G>
+template <int D, int G, bool kPoll>
 __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::MINB)
     fd_cluster_kernel(const float *__restrict__ q, float *k_cache, float *v_cache, SeqMap sm,
                       const float *__restrict__ k_rows, const float *__restrict__ v_rows,
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       for (int rs = r0; rs < r1 && ok; rs += C::T, ++k) {
         const uint32_t s = k % C::S;
         const uint32_t use = k / C::S;
-        if (!mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
+        if (!mbar_wait<kPoll>(&empty[s], (use & 1u) ^ 1u, abort)) {
           ok = 0;
           break;
         }
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       if (ok) {  // tell the consumers there is nothing more
         const uint32_t s = k % C::S;
         const uint32_t use = k / C::S;
-        if (mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
+        if (mbar_wait<kPoll>(&empty[s], (use & 1u) ^ 1u, abort)) {
           desc[s].flags = kNoMore;
           desc[s].nrows = 0;
           mbar_arrive(&full[s]);
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       const uint32_t s = k % C::S;
       const uint32_t use = k / C::S;
       // all lanes of the warp leave together (shuffles follow)
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], use & 1u, abort))) {
+      if (!__all_sync(0xffffffffu, mbar_wait<kPoll>(&full[s], use & 1u, abort))) {
         if (lane == 0) {
           *abort = 1;
           record_status(d_status, KVS_ERR_TIMEOUT);
@@ -325,18 +325,21 @@ const ClusterInfo *cluster_info(int dev) {
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   if (!info[dev].configured) {
-    auto kern = fd_cluster_kernel<D, G>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    auto kern = fd_cluster_kernel<D, G, false>;
     int top = 16;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      top = 8;
+    // both wait variants have the same shared memory and launch bounds
+    for (auto k : {fd_cluster_kernel<D, G, false>, fd_cluster_kernel<D, G, true>}) {
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+      }
+      cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        top = 8;
+      }
     }
     ClusterInfo rec;
     for (int k = 0, cs = 1; cs <= top; ++k, cs <<= 1) {
@@ -402,8 +405,9 @@ int launch_cluster_impl(const float *q, float *k_cache, float *v_cache, const Se
   cfg.numAttrs = 2;
   const float qscale = (float)(1.4426950408889634074 / std::sqrt((double)D));
   const SeqMap sm{seqs.positions, seqs.slots, seqs.done, max_len, seqs.num_slots, Hkv};
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fd_cluster_kernel<D, G>, q, k_cache, v_cache, sm,
-                                           k_rows, v_rows, out, Hkv, qscale, d_status);
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, poll_waits() ? fd_cluster_kernel<D, G, true> : fd_cluster_kernel<D, G, false>, q,
+      k_cache, v_cache, sm, k_rows, v_rows, out, Hkv, qscale, d_status);
   if (e != cudaSuccess) {
     cudaGetLastError();  // leave no stale error for the caller's next check
     return KVS_ERR_LAUNCH;

@@ -419,7 +419,7 @@ __device__ __noinline__ void merge_runs(const WsView &ws, float *out, int i, int
 // ---------------------------------------------------------------------------
 // The step kernel (k_rows == nullptr: attention only; else scatter + attention)
 // ---------------------------------------------------------------------------
-template <int D, int G>
+template <int D, int G, bool kPoll>
 __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     fd_step_kernel(const float *__restrict__ q, float *k_cache, float *v_cache, SeqMap sm,
                    const float *__restrict__ k_rows, const float *__restrict__ v_rows,
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
           if (lane == 0) {
             const uint32_t s = k % C::S;
             const uint32_t use = k / C::S;
-            if (!mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
+            if (!mbar_wait<kPoll>(&empty[s], (use & 1u) ^ 1u, abort)) {
               ok = 0;
             } else {
               const int nrows = min(C::T, r1 - rs);
@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       if (ok) {  // tell the consumers there is nothing more
         const uint32_t s = k % C::S;
         const uint32_t use = k / C::S;
-        if (mbar_wait(&empty[s], (use & 1u) ^ 1u, abort)) {
+        if (mbar_wait<kPoll>(&empty[s], (use & 1u) ^ 1u, abort)) {
           desc[s].flags = kNoMore;
           desc[s].nrows = 0;
           mbar_arrive(&full[s]);
@@ -622,11 +622,16 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
 
   uint32_t mphase = 0;
   // Every wait of a consumer warp ends the same way for all its lanes (the
-  // lanes go on to full-warp shuffles together, or leave together).
+  // lanes go on to full-warp shuffles together, or leave together).  The
+  // warp enters this barrier's wait converged (__syncwarp) and every test in
+  // the wait is warp-uniform; the polling variant, whose waits are made to
+  // run out, also takes the outcome by vote.
   auto consumers_barrier = [&]() -> bool {  // bounded; every consumer warp arrives once
     __syncwarp();
     if (lane == 0) mbar_arrive(mbar);
-    if (!__all_sync(0xffffffffu, mbar_wait(mbar, mphase, abort))) {
+    bool got = mbar_wait<kPoll>(mbar, mphase, abort);
+    if (kPoll) got = __all_sync(0xffffffffu, got);
+    if (!got) {
       if (lane == 0) give_up(abort, d_status, ws.epoch);
       return false;
     }
@@ -637,7 +642,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
   for (uint32_t k = 0;; ++k) {
     const uint32_t s = k % C::S;
     const uint32_t use = k / C::S;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], use & 1u, abort))) {
+    if (!__all_sync(0xffffffffu, mbar_wait<kPoll>(&full[s], use & 1u, abort))) {
       if (lane == 0) give_up(abort, d_status, ws.epoch);
       return;
     }
@@ -717,14 +722,18 @@ int step_blocks_per_sm(int dev) {
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   if (!info[dev].configured) {
-    auto kern = fd_step_kernel<D, G>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
-      return -1;
-    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    // both wait variants have the same shared memory and launch bounds
+    for (auto kern : {fd_step_kernel<D, G, false>, fd_step_kernel<D, G, true>}) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+      }
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    }
     int bps = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, C::THREADS, C::SMEM_BYTES) !=
-            cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fd_step_kernel<D, G, false>,
+                                                      C::THREADS, C::SMEM_BYTES) != cudaSuccess ||
         bps < 1)
       return -1;
     info[dev].blocks_per_sm = bps;
@@ -755,8 +764,10 @@ int launch_step_impl(const float *q, float *k_cache, float *v_cache, const SeqAr
       (int)std::min<long long>({(long long)sms * bps, (long long)kMaxChunkBlocks, by_rows});
   const WsView ws = workspace_view(workspace, M, Hkv, G, D);
   const float qscale = (float)(1.4426950408889634074 / std::sqrt((double)D));
-  const cudaError_t e = launch_pdl(fd_step_kernel<D, G>, dim3(grid), dim3(C::THREADS),
-                                   C::SMEM_BYTES, stream, q, k_cache, v_cache,
+  const cudaError_t e = launch_pdl(poll_waits() ? fd_step_kernel<D, G, true>
+                                                : fd_step_kernel<D, G, false>,
+                                   dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, q,
+                                   k_cache, v_cache,
                                    SeqMap{seqs.positions, seqs.slots, seqs.done, max_len,
                                           seqs.num_slots, Hkv},
                                    k_rows, v_rows, out, ws, M, Hkv, chunk, qscale, fresh_tag(),

@@ -28,6 +28,16 @@ int check_attention_shape(int M, int H, int Hkv, int D, int max_len, int chunk) 
 // Kernel schedule (kvs_set_schedule); process-wide.
 std::atomic<int> g_schedule{KVS_SCHEDULE_AUTO};
 
+// Wait bound of each device (kvs_set_wait_limit_ns), as last set.
+constexpr int kMaxLimitDevices = 64;
+std::mutex g_limit_mu;
+std::atomic<uint64_t> g_limit[kMaxLimitDevices] = {};
+struct LimitInit {
+  LimitInit() {
+    for (auto &x : g_limit) x.store(KVS_WAIT_LIMIT_DEFAULT_NS);
+  }
+} g_limit_init;
+
 // Upper bound of the K/V bytes of one step above which the automatic
 // schedule never considers the cluster kernel (checked before any device
 // query).
@@ -64,6 +74,15 @@ int resolve_chunk(int M, int Hkv, int D, int max_len, int chunk) {
 }
 
 }  // namespace
+
+bool kvs::poll_waits() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxLimitDevices) {
+    cudaGetLastError();
+    return false;
+  }
+  return g_limit[dev].load(std::memory_order_relaxed) < KVS_WAIT_LIMIT_DEFAULT_NS;
+}
 
 extern "C" {
 
@@ -384,23 +403,19 @@ int kvs_set_schedule(int schedule) {
 int kvs_get_schedule(void) { return g_schedule.load(); }
 
 int kvs_set_wait_limit_ns(uint64_t ns, uint64_t *previous) {
-  static std::mutex mu;
-  static uint64_t current[64];
-  static bool known[64] = {false};
   if (ns > KVS_WAIT_LIMIT_DEFAULT_NS) return KVS_ERR_DIMS;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxLimitDevices) {
     cudaGetLastError();
     return KVS_ERR_LAUNCH;
   }
-  std::lock_guard<std::mutex> lk(mu);
+  std::lock_guard<std::mutex> lk(g_limit_mu);
   int rc = kvs::set_wait_limit_step(ns);
   if (rc == KVS_OK) rc = kvs::set_wait_limit_cluster(ns);
   if (rc == KVS_OK) rc = kvs::set_wait_limit_prefill(ns);
   if (rc != KVS_OK) return rc;
-  if (previous) *previous = known[dev] ? current[dev] : KVS_WAIT_LIMIT_DEFAULT_NS;
-  current[dev] = ns;
-  known[dev] = true;
+  if (previous) *previous = g_limit[dev].load();
+  g_limit[dev].store(ns);
   return KVS_OK;
 }
 

@@ -15,12 +15,9 @@ namespace kvs {
 // KVS_ERR_TIMEOUT and returns instead of spinning forever.
 constexpr uint64_t kWaitLimitNs = KVS_WAIT_LIMIT_DEFAULT_NS;  // 2 s
 
-// The bound the pipeline waits of this translation unit's kernels use on this
-// device (kvs_set_wait_limit_ns lowers it so that a test can make the waits
-// run out).  Read at run time, so a replayed CUDA graph sees the current
-// value; it lives in constant memory, so the waits read it from the SM's
-// constant cache.  Drain waits -- those that let already issued copies or
-// tensor-core products finish before a block exits -- always use kWaitLimitNs.
+// The bound of the polling variant's waits (below): each translation unit
+// with waits has its own copy, set on the current device by
+// kvs_set_wait_limit_ns and read at run time.
 static __constant__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
 
 // Host: sets this translation unit's copy of the bound on the current device.
@@ -114,29 +111,38 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Returns false
-// if *abort became non-zero or the wait exceeded the bound g_wait_limit_ns.
-// Under the default bound the thread sleeps in mbarrier.try_wait and looks at
-// the clock and the abort flag every 64 tries.  Under a lowered bound (a
-// test of the timeout path) it polls without sleeping and looks every time,
-// so a bound of 0 ends the first wait that does not find its phase complete.
+// if *abort became non-zero or the wait ran past its bound.
+//   kPoll = false (kernels launched at the default bound): the thread sleeps
+//     in mbarrier.try_wait (the hardware wakes it when the phase completes,
+//     or after about 4 us) and looks at the abort flag and the clock every
+//     64 tries, against the fixed kWaitLimitNs.  Nothing is added to a wait
+//     that finds its phase complete.
+//   kPoll = true (kernels launched while kvs_set_wait_limit_ns has lowered
+//     the bound, to test the timeout path): the thread polls with the
+//     non-blocking test_wait and looks at the abort flag and the clock at
+//     every poll, against g_wait_limit_ns, so a bound of 0 ends the first
+//     wait that does not find its phase complete.
+template <bool kPoll>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int *abort) {
+  if (!kPoll) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((it & 63u) == 0) {
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      }
+    }
+  }
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t limit = g_wait_limit_ns;
   const uint64_t t0 = global_timer_ns();
-  if (limit < kWaitLimitNs) {
-    for (;;) {
-      if (mbar_test_wait(bar, parity)) return true;
-      if (*abort) return false;
-      if (global_timer_ns() - t0 >= limit) return false;
-    }
-  }
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > limit) return false;
-    }
+  for (;;) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 >= limit) return false;
   }
 }
 
@@ -144,7 +150,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
 // shared memory, tensor-core products) to finish before the block moves on
 // or exits.  No abort flag, and always the full kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
-  if (mbar_test_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;

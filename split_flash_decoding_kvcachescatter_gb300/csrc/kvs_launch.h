@@ -139,6 +139,11 @@ int device_sm_count();
 // epoch a step graph writes at each replay.
 unsigned fresh_tag();
 
+// True while kvs_set_wait_limit_ns has lowered the wait bound of the current
+// device: launches then take the kernels' polling wait variant, which reads
+// the bound at run time (kvs_device.cuh).
+bool poll_waits();
+
 // Each translation unit that has pipeline waits keeps its own copy of the
 // wait bound (kvs_device.cuh); these set it on the current device.
 int set_wait_limit_step(uint64_t ns);

@@ -324,7 +324,7 @@ struct PGeo {
   static_assert(SMEM_BYTES <= 227 * 1024, "one block per SM must fit");
 };
 
-template <int D>
+template <int D, bool kPoll>
 __global__ void __launch_bounds__(kPBlockThreads, 1)
     prefill_tc_kernel(const unsigned char *__restrict__ ws, float *__restrict__ out, int S,
                       int causal, float sl2, int *d_status) {
@@ -410,12 +410,12 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       bool ok = true;
       for (int n = 0; n < n_all; ++n) {
         const int ks = n % KS, vs = n % VS;
-        if (n >= KS && !(ok = mbar_wait(&kfree[ks], (uint32_t)((n - KS) / KS) & 1u, abort)))
+        if (n >= KS && !(ok = mbar_wait<kPoll>(&kfree[ks], (uint32_t)((n - KS) / KS) & 1u, abort)))
           break;
         mbar_arrive_expect_tx(&kfull[ks], PG::TILE);
         bulk_g2s(sK + ks * PG::TILE, gKh + (size_t)n * tile, PG::TILE, &kfull[ks]);
         nk = n + 1;
-        if (n >= VS && !(ok = mbar_wait(&vfree[vs], (uint32_t)((n - VS) / VS) & 1u, abort)))
+        if (n >= VS && !(ok = mbar_wait<kPoll>(&vfree[vs], (uint32_t)((n - VS) / VS) & 1u, abort)))
           break;
         mbar_arrive_expect_tx(&vfull[vs], PG::TILE);
         bulk_g2s(sV + vs * PG::TILE, gVh + (size_t)n * tile, PG::TILE, &vfull[vs]);
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
         for (int ks = 0; ks < kPN / 16; ++ks)
           mma_f16_ts(d, a + ks * 8, b + 16 * ks, kIdescO, (n > 0 || ks > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(bar_q, 0, abort) && mbar_wait(&kfull[0], 0, abort);
+      bool ok = mbar_wait<kPoll>(bar_q, 0, abort) && mbar_wait<kPoll>(&kfull[0], 0, abort);
       bool issued = false;   // products issued since the last completed pvdone wait
       bool pending = false;  // a commit on pvdone whose wait did not complete
       if (ok) {
@@ -474,12 +474,12 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       uint32_t pv_phase = 0;
       for (int kt = 0; kt < n_all && ok; ++kt) {
         const uint32_t ph = (uint32_t)kt & 1u;
-        ok = mbar_wait(&vfull[kt % VS], (uint32_t)(kt / VS) & 1u, abort);  // V^T(kt)
+        ok = mbar_wait<kPoll>(&vfull[kt % VS], (uint32_t)(kt / VS) & 1u, abort);  // V^T(kt)
         bool k_next = false;  // K(kt+1) has landed
         for (int x = 0; x < 2 && ok; ++x) {
           const int n_x = x == 0 ? n_a : n_b;
           if (kt < n_x) {  // P V_x(kt), once softmax x(kt) has written P_x
-            ok = mbar_wait(&pfull[x], ph, abort);
+            ok = mbar_wait<kPoll>(&pfull[x], ph, abort);
             if (!ok) break;
             tc_fence_after();
             issue_pv(x, kt);
@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
           }
           if (kt + 1 < n_x) {  // S_x(kt+1) overwrites P_x(kt): after P V_x(kt)
             mma_commit(pvdone);
-            ok = mbar_wait(pvdone, pv_phase, abort);
+            ok = mbar_wait<kPoll>(pvdone, pv_phase, abort);
             if (!ok) {
               pending = true;
               break;
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
             pv_phase ^= 1u;
             issued = false;
             if (!k_next) {
-              ok = mbar_wait(&kfull[(kt + 1) % KS], (uint32_t)((kt + 1) / KS) & 1u, abort);
+              ok = mbar_wait<kPoll>(&kfull[(kt + 1) % KS], (uint32_t)((kt + 1) / KS) & 1u, abort);
               if (!ok) break;
               tc_fence_after();
               k_next = true;
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       }
       if (ok) {  // the last P V products
         mma_commit(pvdone);
-        ok = mbar_wait(pvdone, pv_phase, abort);
+        ok = mbar_wait<kPoll>(pvdone, pv_phase, abort);
         if (!ok) pending = true;
       }
       if (!ok) {
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       // is quiescent too
       // all lanes of the warp leave together: the TMEM loads and stores
       // below are .sync.aligned (the whole warp executes them)
-      if (!__all_sync(0xffffffffu, mbar_wait(&sfull[x], ph, abort))) {
+      if (!__all_sync(0xffffffffu, mbar_wait<kPoll>(&sfull[x], ph, abort))) {
         failed = true;
         break;
       }
@@ -660,10 +660,12 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVS_ERR_LAUNCH;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PG::SMEM_BYTES) != cudaSuccess) {
-      cudaGetLastError();
-      return KVS_ERR_LAUNCH;
+    for (auto kern : {prefill_tc_kernel<D, false>, prefill_tc_kernel<D, true>}) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PG::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return KVS_ERR_LAUNCH;
+      }
     }
     configured[dev] = true;
   }
@@ -675,7 +677,8 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
   const float sl2 = (float)(1.4426950408889634074 / std::sqrt((double)D));
   const int T = (S + kPM - 1) / kPM;
   const dim3 grid((T + 1) / 2, H, 1);
-  e = launch_pdl(prefill_tc_kernel<D>, grid, dim3(kPBlockThreads), PG::SMEM_BYTES, stream,
+  e = launch_pdl(poll_waits() ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>, grid,
+                 dim3(kPBlockThreads), PG::SMEM_BYTES, stream,
                  static_cast<const unsigned char *>(ws), out, S, causal, sl2, d_status);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }

@@ -5,7 +5,8 @@ For each kernel with waits -- the persistent decode kernel, the cluster
 decode kernel and the tensor-core prefill kernel -- and for a replayed step
 graph, a call under a lowered bound must
   * return KVS_OK from the host call (the kernel gives up, it does not fault),
-  * record KVS_ERR_TIMEOUT in d_status when the bound is 0 (the first wait
+  * record KVS_ERR_TIMEOUT in d_status when the bound is 0 (calls made under
+    a lowered bound run the kernels' polling wait variant, whose first wait
     that does not find its data ready ends at once), or nothing else but
     KVS_ERR_TIMEOUT under a bound of a few microseconds (then waits run out
     at random points of the pipeline, with copies and tensor-core products
@@ -150,7 +151,10 @@ def test_cluster_kernel_small_model_layer_times_out_and_recovers():
 def test_step_graph_replay_after_a_timed_out_replay():
     """A captured step replays frozen kernel arguments, the counters' host tag
     included.  A replay that gives up part-way can leave completion counts
-    behind; the graph's epoch write makes the next replay start clean."""
+    behind; the graph's epoch write makes the next replay start clean.  The
+    graph is captured under a lowered bound, so it holds the kernels' polling
+    wait variant, which reads the bound at run time: each replay then runs
+    under the bound set just before it."""
     B.kvs_set_schedule(B.KVS_SCHEDULE_PERSISTENT)
     w = W.custom(positions="uniform", seed=65, M=8, num_heads=32, num_kv_heads=8, head_dim=128,
                  max_len=2048, chunk_size=0)
@@ -166,6 +170,7 @@ def test_step_graph_replay_after_a_timed_out_replay():
     # configure the kernels outside the capture
     _step(w, ts[0], ws, outs[0], status)
     torch.cuda.synchronize()
+    B.kvs_set_wait_limit_ns(0)
     g = B.kvs_step_graph_create([t["q"] for t in ts], [t["k_rows"] for t in ts],
                                 [t["v_rows"] for t in ts], ts[0]["positions"],
                                 [t["k_cache"] for t in ts], [t["v_cache"] for t in ts], outs,
