@@ -23,13 +23,14 @@
 //    P V_A(kt), S_A(kt+1), P V_B(kt), S_B(kt+1), and warp 9 moves the tiles
 //    (K through two stages, V^T through three), so one tile's softmax runs
 //    while the other tile's products are on the tensor cores.
-//  * Softmax: each thread reads its score row from TMEM (tcgen05.ld
-//    32x32b) twice -- row maximum, then p = 2^(s - m) on the special-function
-//    unit, rounded to FP16 and written back over the scores already read
-//    (tcgen05.st), where P V takes it as its A operand; the FP32 values are
-//    summed into the row sum.  The reference maximum moves only when the row
-//    maximum grows by more than 2^8 (log2 units), so the output accumulator
-//    in TMEM is rarely rescaled.
+//  * Softmax: each thread reads its score row from TMEM (tcgen05.ld 32x32b,
+//    64 columns at a time) once: p = 2^(s - m) on the special-function unit
+//    against a reference maximum, rounded to FP16 and written back over
+//    scores already read (tcgen05.st), where P V takes it as its A operand;
+//    the FP32 values are summed into the row sum.  The reference maximum
+//    moves only when the row maximum grows by more than 2^8 (log2 units), so
+//    P written earlier and the output accumulator in TMEM are rarely
+//    rescaled.
 //  * Causal: key tiles after the query tile are skipped; keys j > i and keys
 //    past seq_len get p = 0 (selects, on the diagonal and last tiles only).
 // Every mbarrier wait is bounded; on expiry the block records
@@ -143,14 +144,31 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) 
       "r"(__float_as_uint(r[30])), "r"(__float_as_uint(r[31]))
       : "memory");
 }
-// 16 consecutive 32-bit columns of this thread's TMEM lane, written.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16]) {
+// 64 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
+  uint32_t u[64];
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
-      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
-      "r"(w[15])
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31]), "=r"(u[32]), "=r"(u[33]), "=r"(u[34]), "=r"(u[35]), "=r"(u[36]), "=r"(u[37]), "=r"(u[38]), "=r"(u[39]), "=r"(u[40]), "=r"(u[41]), "=r"(u[42]), "=r"(u[43]), "=r"(u[44]), "=r"(u[45]), "=r"(u[46]), "=r"(u[47]), "=r"(u[48]), "=r"(u[49]), "=r"(u[50]), "=r"(u[51]), "=r"(u[52]), "=r"(u[53]), "=r"(u[54]), "=r"(u[55]), "=r"(u[56]), "=r"(u[57]), "=r"(u[58]), "=r"(u[59]), "=r"(u[60]), "=r"(u[61]), "=r"(u[62]), "=r"(u[63])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 64; ++i) r[i] = __uint_as_float(u[i]);
+}
+// 32 consecutive 32-bit columns of this thread's TMEM lane, as raw words.
+__device__ __forceinline__ void tmem_ld32u(uint32_t taddr, uint32_t (&w)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]), "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15]), "=r"(w[16]), "=r"(w[17]), "=r"(w[18]), "=r"(w[19]), "=r"(w[20]), "=r"(w[21]), "=r"(w[22]), "=r"(w[23]), "=r"(w[24]), "=r"(w[25]), "=r"(w[26]), "=r"(w[27]), "=r"(w[28]), "=r"(w[29]), "=r"(w[30]), "=r"(w[31])
+      : "r"(taddr));
+}
+// 32 consecutive 32-bit columns of this thread's TMEM lane, written.
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&w)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]), "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
@@ -345,17 +363,19 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  // grid (H, pairs): blocks launch in linear order, head fastest, so every
+  // head's heaviest query-tile pair goes first (longest first across heads)
+  const int h = blockIdx.x;
   const int T = (S + kPN - 1) / kPN;   // query tiles = key tiles
   // tile A; tile B = qa + 1 (absent when qa + 1 == T).  Causal blocks with
   // the most key tiles are launched first.
-  const int qa = 2 * (causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
+  const int qa = 2 * (causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y);
   const bool has_b = qa + 1 < T;
   const int n_a = causal ? qa + 1 : T;            // key tiles tile A attends
   const int n_b = has_b ? (causal ? qa + 2 : T) : 0;
   const int n_all = n_a > n_b ? n_a : n_b;
   const size_t tile = (size_t)PG::TILE;
-  const size_t per_tensor = (size_t)gridDim.y * T * tile;
+  const size_t per_tensor = (size_t)gridDim.x * T * tile;
   const unsigned char *gQh = ws + (size_t)h * T * tile;
   const unsigned char *gKh = ws + per_tensor + (size_t)h * T * tile;
   const unsigned char *gVh = ws + 2 * per_tensor + (size_t)h * T * tile;
@@ -553,58 +573,74 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       tc_fence_after();
       // keys needing a mask: past S, or past the row on the diagonal tile
       const bool masked = (key0 + kPN > S) || (causal && kt == q_tile);
-      // ---- row maximum of the tile ----
-      float mt = neg_inf_f();
-#pragma unroll 1
-      for (int ch = 0; ch < kPN / 32; ++ch) {
-        float r[32];
-        tmem_ld32(tm_s + ch * 32, r);
-        tmem_wait_ld();
-        if (masked) mask_keys(r, key0 + ch * 32, S, causal, i);
-#pragma unroll
-        for (int u = 0; u < 32; ++u) mt = fmaxf(mt, r[u]);
-      }
-      // The reference maximum only moves when the row maximum grows by more
-      // than kRescaleLog2 (log2 units): below that, p = 2^(s - m) stays under
-      // 2^kRescaleLog2 (FP16 holds it), the result is the same, and the
-      // output accumulator needs no rescale.
-      const float m_row = fmaxf(m, mt * sl2);
-      const float m_new = (m_row > m + kRescaleLog2) ? m_row : m;
-      const float alpha = (m_new == neg_inf_f()) ? 1.f : ex2(m - m_new);
-      // ---- rescale the output accumulator (TMEM) where the maximum moved ----
-      if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float r[32];
-          tmem_ld32(tm_o + ch * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 32; ++u) r[u] *= alpha;
-          tmem_st32(tm_o + ch * 32, r);
-        }
-      }
-      // ---- P (FP16) into TMEM over the consumed scores, and its row sum ----
-      // Chunk c's 32 scores are read before P of keys [32c, 32c + 32) goes to
-      // columns [16c, 16c + 16), whose scores were read already.
-      // (a row with no key yet has m_new = -inf and every score -inf: p = 0)
-      const float mb = (m_new == neg_inf_f()) ? 0.f : m_new;
+      // ---- one pass over the scores, in two chunks of 64 keys ----
+      // The reference maximum m_ref only moves when a chunk's maximum exceeds
+      // it by more than kRescaleLog2 (log2 units): below that, p = 2^(s - m_ref)
+      // stays under 2^kRescaleLog2 (FP16 holds it), the result is the same,
+      // and nothing needs rescaling.  P of chunk c (FP16, two keys per
+      // column) goes to columns [32c, 32c + 32), whose scores were read with
+      // chunk 0.  When chunk 1 moves m_ref, chunk 0's P (already in TMEM) is
+      // scaled by the power of two 2^(old - new): exact in FP16 down to the
+      // subnormals, where it rounds like a direct evaluation would.
+      // (Every row attends a key in chunk 0: key0 <= row on the diagonal
+      // tile, and key0 < S.)
+      float m_ref = m;
       float lt = 0.f;
 #pragma unroll 1
-      for (int ch = 0; ch < kPN / 32; ++ch) {
-        float r[32];
-        tmem_ld32(tm_s + ch * 32, r);
+      for (int ch = 0; ch < kPN / 64; ++ch) {
+        float r[64];
+        tmem_ld64(tm_s + ch * 64, r);
         tmem_wait_ld();
-        if (masked) mask_keys(r, key0 + ch * 32, S, causal, i);
-        uint32_t w[16];
+        if (masked) {
+          mask_keys(*reinterpret_cast<float(*)[32]>(&r[0]), key0 + ch * 64, S, causal, i);
+          mask_keys(*reinterpret_cast<float(*)[32]>(&r[32]), key0 + ch * 64 + 32, S, causal, i);
+        }
+        float cm = neg_inf_f();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 64; ++u) cm = fmaxf(cm, r[u]);
+        cm *= sl2;
+        const float m_prev = m_ref;
+        if (cm > m_ref + kRescaleLog2) m_ref = cm;
+        if (ch > 0 && __any_sync(0xffffffffu, m_ref != m_prev)) {  // rare
+          const float f = (m_ref != m_prev) ? ex2(m_prev - m_ref) : 1.f;
+          lt *= f;
+          const __half2 f2 = __float2half2_rn(f);
+          uint32_t w0[32];
+          tmem_wait_st();  // chunk 0's P has landed
+          tmem_ld32u(tm_s, w0);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&w0[u]), f2);
+            w0[u] = *reinterpret_cast<const uint32_t *>(&v);
+          }
+          tmem_st32u(tm_s, w0);
+        }
+        const float mb = (m_ref == neg_inf_f()) ? 0.f : m_ref;
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
           const float p0 = ex2(fmaf(r[2 * u], sl2, -mb));
           const float p1 = ex2(fmaf(r[2 * u + 1], sl2, -mb));
           const __half2 hp = __floats2half2_rn(p0, p1);
           lt += p0 + p1;
           w[u] = *reinterpret_cast<const uint32_t *>(&hp);
         }
-        tmem_st16(tm_s + ch * 16, w);
+        tmem_st32u(tm_s + ch * 32, w);
+      }
+      const float m_new = m_ref;
+      const float alpha = (m == neg_inf_f()) ? 1.f : ex2(m - m_new);
+      // ---- rescale the output accumulator (TMEM) where the maximum moved ----
+      if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float r[32];
+          tmem_ld32(tm_o + c * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) r[u] *= alpha;
+          tmem_st32(tm_o + c * 32, r);
+        }
       }
       l = l * alpha + lt;
       m = m_new;
@@ -676,7 +712,7 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
   if (e != cudaSuccess) return KVS_ERR_LAUNCH;
   const float sl2 = (float)(1.4426950408889634074 / std::sqrt((double)D));
   const int T = (S + kPM - 1) / kPM;
-  const dim3 grid((T + 1) / 2, H, 1);
+  const dim3 grid(H, (T + 1) / 2, 1);
   e = launch_pdl(poll_waits() ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>, grid,
                  dim3(kPBlockThreads), PG::SMEM_BYTES, stream,
                  static_cast<const unsigned char *>(ws), out, S, causal, sl2, d_status);

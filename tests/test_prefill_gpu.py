@@ -102,3 +102,43 @@ def test_causal_last_row_equals_full_attention_of_last_query():
     a = run(q, k, v, True)
     b = run(q, k, v, False)
     assert np.allclose(a[0, -1], b[0, -1], rtol=0, atol=1e-6)
+
+
+def planted(H, S, D, seed, keys, scale):
+    """N(0,1) inputs whose k rows at the given key positions are scaled, so
+    that those keys' scores jump far above the rest."""
+    q, k, v = inputs(H, S, D, seed)
+    for j in keys:
+        if j < S:
+            k[:, j, :] *= scale
+    return q, k, v
+
+
+def check_inputs(q, k, v, causal, where):
+    got = run(q, k, v, causal)
+    ref = oracle.prefill_attention(q, k, v, causal)
+    assert np.all(np.isfinite(got)), where
+    err = np.abs(got - ref)
+    lim = bound(v, ref, causal)
+    worst = np.unravel_index(np.argmax(err - lim), err.shape)
+    assert np.all(err <= lim), f"{where}: err {err[worst]:.3e} > bound {lim[worst]:.3e} at {worst}"
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_score_jump_inside_a_key_tile(D, causal):
+    """Keys in the second half of a 128-key tile (64..127) score far above the
+    first half: the running maximum moves in the middle of the tile, and the
+    FP16 P already written for the first half is rescaled in place."""
+    S = 512
+    q, k, v = planted(2, S, D, seed=17 + D, keys=[70, 200, 330, 460], scale=6.0)
+    check_inputs(q, k, v, causal, f"jump inside a tile D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_score_jump_across_key_tiles(D):
+    """A key far above all earlier ones in a later key tile: the output
+    accumulator of the rows that attend it is rescaled."""
+    S = 640
+    q, k, v = planted(2, S, D, seed=29 + D, keys=[300, 610], scale=8.0)
+    check_inputs(q, k, v, True, f"jump across tiles D={D}")
