@@ -237,15 +237,21 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
 // ceil(S / 128) and a tile of 128 * D FP16 values (rows past S are zero).
 __host__ __device__ constexpr size_t prefill_tile_bytes(int D) { return (size_t)kPM * D * 2; }
 
-// Grid (2 * D/16 + 1, T, H): blocks [0, D/16) convert tile t of Q, blocks
-// [D/16, 2 * D/16) tile t of K (one 16-byte chunk per thread), the last block
-// tile t of V^T (one 8-key x 8-column block per thread, transposed in
-// registers).  Consecutive threads write consecutive bytes.
+// Grid (3 * D/16, T, H): blocks [0, D/16) convert tile t of Q, blocks
+// [D/16, 2 * D/16) tile t of K (one 16-byte chunk per thread), blocks
+// [2 * D/16, 3 * D/16) tile t of V^T, 16 of its D rows each (so every block
+// moves the same bytes).  A V^T block reads its 128 keys x 16 columns of v
+// with float4 loads into shared memory (rows padded so the transposed reads
+// are free of bank conflicts), then each thread writes one 16-byte chunk:
+// 8 keys of one column, and eight consecutive threads fill one 128-byte
+// line of a core matrix.  Consecutive threads write consecutive bytes.
 template <int D>
 __global__ void __launch_bounds__(256)
     prefill_pack_kernel(const float *__restrict__ q, const float *__restrict__ k,
                         const float *__restrict__ v, unsigned char *__restrict__ ws, int S) {
-  constexpr int NQK = D / 16;  // blocks per Q or K tile (128 * D/8 chunks / 256)
+  constexpr int NQK = D / 16;  // blocks per Q, K or V^T tile (128 * D/8 chunks / 256)
+  constexpr int kVPad = kPN + 4;  // row stride (floats) of the V slab in shared memory
+  __shared__ __align__(16) float sv[16 * kVPad];
   grid_dependency_wait();
   const int T = gridDim.y, H = gridDim.z;
   const int t = blockIdx.y, h = blockIdx.z;
@@ -272,35 +278,31 @@ __global__ void __launch_bounds__(256)
     }
     unsigned char *dst = ws + ((size_t)which * H * T + ht) * tile;
     *reinterpret_cast<uint4 *>(dst + cm_off(r, c, D)) = pack8(x);
-  } else {  // V^T: keys j..j+7 and columns d..d+7
-    const int w = threadIdx.x;
-    if (w < (D / 8) * (kPN / 8)) {
-      const int d = (w % (D / 8)) * 8;
-      const int j = (w / (D / 8)) * 8;
-      float x[8][8];  // [key][column]
+  } else {  // V^T rows [d0, d0 + 16): keys of tile t, columns d0.. of v
+    const int d0 = (bx - 2 * NQK) * 16;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int key = t * kPN + j + u;
-        if (key < S) {
-          const float4 *src =
-              reinterpret_cast<const float4 *>(v + ((size_t)h * S + key) * D + d);
-          const float4 a = __ldg(src), b = __ldg(src + 1);
-          x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
-          x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) x[u][c] = 0.f;
-        }
-      }
-      unsigned char *dst = ws + ((size_t)2 * H * T + ht) * tile;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float col[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) col[u] = x[u][c];
-        *reinterpret_cast<uint4 *>(dst + cm_off(d + c, j, kPN)) = pack8(col);
-      }
+    for (int u = 0; u < 2; ++u) {  // 128 keys x 4 float4 = 512 loads, 2 per thread
+      const int e = threadIdx.x + 256 * u;
+      const int key = e >> 2, f4 = e & 3;
+      const int gkey = t * kPN + key;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (gkey < S)
+        a = __ldg(reinterpret_cast<const float4 *>(v + ((size_t)h * S + gkey) * D + d0) + f4);
+      sv[(4 * f4 + 0) * kVPad + key] = a.x;
+      sv[(4 * f4 + 1) * kVPad + key] = a.y;
+      sv[(4 * f4 + 2) * kVPad + key] = a.z;
+      sv[(4 * f4 + 3) * kVPad + key] = a.w;
     }
+    __syncthreads();
+    // thread: row d0 + dr of V^T (dr = 8 * (w >> 7) + (w & 7)), keys 8g..8g+7
+    const int w = threadIdx.x;
+    const int dr = 8 * (w >> 7) + (w & 7);
+    const int g = (w >> 3) & 15;
+    const float4 *row4 = reinterpret_cast<const float4 *>(sv + dr * kVPad + 8 * g);
+    const float4 a = row4[0], b = row4[1];
+    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    unsigned char *dst = ws + ((size_t)2 * H * T + ht) * tile;
+    *reinterpret_cast<uint4 *>(dst + cm_off(d0 + dr, 8 * g, kPN)) = pack8(x);
   }
   allow_dependent_launch();
 }
@@ -707,7 +709,7 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
   }
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   const int nt = (S + kPM - 1) / kPM;
-  cudaError_t e = launch_pdl(prefill_pack_kernel<D>, dim3(2 * (D / 16) + 1, nt, H), dim3(256), 0,
+  cudaError_t e = launch_pdl(prefill_pack_kernel<D>, dim3(3 * (D / 16), nt, H), dim3(256), 0,
                              stream, q, k, v, ws, S);
   if (e != cudaSuccess) return KVS_ERR_LAUNCH;
   const float sl2 = (float)(1.4426950408889634074 / std::sqrt((double)D));
