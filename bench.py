@@ -539,6 +539,8 @@ def measure_workload(ctx, w, seed, steps, warmup, chunks, graph=False, full=Fals
         h1.record(stream)
         torch.cuda.synchronize()
         hot_ms = h0.elapsed_time(h1) / KH
+        if int(status.item()) != 0:
+            raise SystemExit(f"{w.name} hot: device status {B.strerror(int(status.item()))}")
 
         total_ms = sum(step_ms)
         total_ms_max, _, bytes_all, _ = reduce_over_ranks(total_ms, 0.0, ab["step"] * steps, 0.0,
@@ -602,6 +604,9 @@ def measure_workload(ctx, w, seed, steps, warmup, chunks, graph=False, full=Fals
                                        "flash_decode": 1e3 * statistics.mean(decode_ms),
                                        "breakdown_steps": KB})
             res["attention_gbs"] = ab["attention"] / (statistics.mean(decode_ms) * 1e-3) / 1e9
+            if int(status.item()) != 0:
+                raise SystemExit(f"{w.name} breakdown: device status "
+                                 f"{B.strerror(int(status.item()))}")
 
         if ci == 0:
             res["e2e"] = measure_e2e(ctx, w, ts, inps, ws, resolved, status, scrub, warmup,

@@ -260,13 +260,15 @@ int kvs_step_io_layout(int M, int num_heads, int num_kv_heads, int head_dim, siz
  * offsets go to the device in one host -> device copy (the padding between
  * them included), and out comes back to its offset in one device -> host
  * copy; in between, the fused scatter + attention launch.  All three are
- * enqueued on `stream` in that order.  Two copies per step instead of five:
- * at these sizes each copy costs mostly its fixed latency.
+ * enqueued on `stream` in that order.  When host_io is pinned memory the GPU
+ * can address (cudaHostAlloc / cudaHostRegister), the two copies are
+ * kernels of this library (every SM moves a share over the host link, far
+ * faster than one copy engine at these sizes); otherwise they are
+ * cudaMemcpyAsync calls, which for pageable memory block the host.
  *
  *   host_io  in/out  host buffer of >= kvs_step_io_bytes bytes with that
- *                    layout, pinned (cudaHostAlloc / cudaHostRegister) for
- *                    asynchronous copies; the inputs must stay untouched,
- *                    and out is valid, once `stream` has passed the call
+ *                    layout; the inputs must stay untouched, and out is
+ *                    valid, once `stream` has passed the call
  *   io, k_cache, v_cache, workspace, d_status, other arguments: as
  *   kvs_decode_step_host.
  * Errors: as kvs_decode_step_host.

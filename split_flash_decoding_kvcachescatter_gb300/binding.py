@@ -364,14 +364,16 @@ def kvs_step_io_layout(M, num_heads, num_kv_heads, head_dim):
 
 
 class HostIo:
-    """A pinned host buffer with the io layout, and views of its arrays:
-    fill q, k_rows, v_rows and positions, call kvs_decode_step_host_io, and
-    read out once the stream has passed the call."""
+    """A host buffer with the io layout, and views of its arrays: fill q,
+    k_rows, v_rows and positions, call kvs_decode_step_host_io, and read out
+    once the stream has passed the call.  Pinned by default (the library then
+    moves it with its copy kernel); pinned=False gives pageable memory (moved
+    by copy engines, the host waiting for them)."""
 
-    def __init__(self, M, num_heads, num_kv_heads, head_dim):
+    def __init__(self, M, num_heads, num_kv_heads, head_dim, pinned=True):
         oq, ok, ov, op, oo, total = kvs_step_io_layout(M, num_heads, num_kv_heads, head_dim)
         self.shape = (M, num_heads, num_kv_heads, head_dim)
-        self.buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+        self.buf = torch.empty(total, dtype=torch.uint8, pin_memory=pinned)
         f = lambda off, n, dt: self.buf[off:off + n * 4].view(dt)
         self.q = f(oq, M * num_heads * head_dim, torch.float32).view(M, num_heads, head_dim)
         self.k_rows = f(ok, M * num_kv_heads * head_dim, torch.float32).view(

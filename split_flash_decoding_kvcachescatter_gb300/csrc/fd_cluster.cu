@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   grid_dependency_wait();
   const int err = sm.error(i);
   const bool finished = sm.finished(i);
-  const int p = __ldg(sm.pos + i);
+  const int p = __ldca(sm.pos + i);
   // ---- Step 1, scatter: the block holding row p writes the new rows (a
   //      finished sequence too; none for a bad position or slot) ----
   if (scatter && err == KVS_OK && rank == (uint32_t)(ncl - 1)) {
@@ -118,10 +118,10 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
     for (int e = threadIdx.x; e < 2 * D4; e += C::THREADS) {
       if (e < D4)
         reinterpret_cast<float4 *>(k_cache)[dst + e] =
-            __ldg(reinterpret_cast<const float4 *>(k_rows) + src + e);
+            __ldcg(reinterpret_cast<const float4 *>(k_rows) + src + e);
       else
         reinterpret_cast<float4 *>(v_cache)[dst + e - D4] =
-            __ldg(reinterpret_cast<const float4 *>(v_rows) + src + e - D4);
+            __ldcg(reinterpret_cast<const float4 *>(v_rows) + src + e - D4);
     }
   }
   // The whole cluster leaves here (its blocks share i) before any wait on a

@@ -142,6 +142,13 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 //            (null: slot i)
 //   done[i]  nonzero: finished -- scattered, but not attended (null: none)
 // ---------------------------------------------------------------------------
+//
+// Loads here are coherent (ld.global.ca, not the read-only ld.global.nc):
+// these arrays may come from the preceding kernel in the stream, which with
+// programmatic dependent launch can still be writing them while this kernel
+// is already resident; the read-only path is only valid for data that does
+// not change during the kernel's life, and was measured to return stale
+// positions in that case.
 struct SeqMap {
   const int32_t *pos;
   const int32_t *slot;
@@ -150,14 +157,14 @@ struct SeqMap {
   int num_slots;
   int Hkv;
 
-  __device__ __forceinline__ int slot_of(int i) const { return slot ? __ldg(slot + i) : i; }
-  __device__ __forceinline__ bool finished(int i) const { return done && __ldg(done + i) != 0; }
+  __device__ __forceinline__ int slot_of(int i) const { return slot ? __ldca(slot + i) : i; }
+  __device__ __forceinline__ bool finished(int i) const { return done && __ldca(done + i) != 0; }
   // KVS_OK, or why sequence i can be neither scattered nor attended
   __device__ __forceinline__ int error(int i) const {
-    const int p = __ldg(pos + i);
+    const int p = __ldca(pos + i);
     if (p < 0 || p >= max_len) return KVS_ERR_POSITION;
     if (slot) {
-      const int s = __ldg(slot + i);
+      const int s = __ldca(slot + i);
       if (s < 0 || s >= num_slots) return KVS_ERR_SLOT;
     }
     return KVS_OK;
@@ -165,10 +172,10 @@ struct SeqMap {
   // rows attended by sequence i (0: finished, or a bad position or slot)
   __device__ __forceinline__ int len(int i) const {
     if (finished(i)) return 0;
-    const int p = __ldg(pos + i);
+    const int p = __ldca(pos + i);
     if (p < 0 || p >= max_len) return 0;
     if (slot) {
-      const int s = __ldg(slot + i);
+      const int s = __ldca(slot + i);
       if (s < 0 || s >= num_slots) return 0;
     }
     return p + 1;

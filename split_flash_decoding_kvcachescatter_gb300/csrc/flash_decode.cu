@@ -472,12 +472,12 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
       const long long ig = f / D4;
       const int i = (int)(ig / Hkv);
       if (sm.error(i) != KVS_OK) continue;
-      const int p = __ldg(sm.pos + i);
+      const int p = __ldca(sm.pos + i);
       const size_t dst = sm.row_index(i, (int)(ig - (long long)i * Hkv), p) * D4 + (f - ig * D4);
       if (is_v)
-        reinterpret_cast<float4 *>(v_cache)[dst] = __ldg(reinterpret_cast<const float4 *>(v_rows) + f);
+        reinterpret_cast<float4 *>(v_cache)[dst] = __ldcg(reinterpret_cast<const float4 *>(v_rows) + f);
       else
-        reinterpret_cast<float4 *>(k_cache)[dst] = __ldg(reinterpret_cast<const float4 *>(k_rows) + f);
+        reinterpret_cast<float4 *>(k_cache)[dst] = __ldcg(reinterpret_cast<const float4 *>(k_rows) + f);
     }
   }
 

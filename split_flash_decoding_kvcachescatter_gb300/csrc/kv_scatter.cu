@@ -37,16 +37,16 @@ __global__ void __launch_bounds__(256)
   const int d4 = (int)(e % D4);
   const int64_t ig = e / D4;  // i * Hkv + g
   const int i = (int)(ig / Hkv);
-  const int p = __ldg(positions + i);
+  const int p = __ldca(positions + i);
   if (p < 0 || p >= max_len) {
     if (!is_v && d4 == 0 && ig % Hkv == 0) record_status(d_status, KVS_ERR_POSITION);
     return;
   }
   const int64_t dst = (ig * max_len + p) * D4 + d4;
   if (is_v)
-    v_cache[dst] = __ldg(v_rows + e);
+    v_cache[dst] = __ldcg(v_rows + e);
   else
-    k_cache[dst] = __ldg(k_rows + e);
+    k_cache[dst] = __ldcg(k_rows + e);
 }
 
 int launch_kv_scatter(const float *k_rows, const float *v_rows,

@@ -319,7 +319,19 @@ int kvs_decode_step_host_io(void *host_io, float *k_cache, float *v_cache, int M
   // the inputs (q, k_rows, v_rows, positions and the padding between them)
   // in one copy
   const size_t in_bytes = L.pos + (size_t)M * sizeof(int32_t);
-  if (cudaMemcpyAsync(base, host, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+  // Pinned host memory the GPU can address is moved by the library's copy
+  // kernel; any other host memory by a copy engine.
+  cudaPointerAttributes pa;
+  unsigned char *mapped = nullptr;
+  if (cudaPointerGetAttributes(&pa, host_io) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+      pa.devicePointer != nullptr && aligned(pa.devicePointer, 16))
+    mapped = static_cast<unsigned char *>(pa.devicePointer);
+  else
+    cudaGetLastError();
+  if (mapped) {
+    rc = kvs::launch_io_copy(mapped, base, in_bytes, st);
+    if (rc != KVS_OK) return rc;
+  } else if (cudaMemcpyAsync(base, host, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
     cudaGetLastError();
     return KVS_ERR_LAUNCH;
   }
@@ -327,6 +339,7 @@ int kvs_decode_step_host_io(void *host_io, float *k_cache, float *v_cache, int M
   rc = launch_attention(dq, k_cache, v_cache, seqs, dk, dv, dout, M, num_heads, num_kv_heads,
                         head_dim, chunk, workspace, d_status, st);
   if (rc != KVS_OK) return rc;
+  if (mapped) return kvs::launch_io_copy(dout, mapped + L.out, qo, st);
   if (cudaMemcpyAsync(host + L.out, dout, qo, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
     cudaGetLastError();
     return KVS_ERR_LAUNCH;

@@ -61,7 +61,10 @@ inline WsView workspace_view(void *base, int M, int Hkv, int G, int D) {
 // Launch with programmatic stream serialisation: the kernel may start while
 // its predecessor in the stream finishes; every kernel of this library
 // executes griddepcontrol.wait before it touches global memory, so results
-// are those of plain stream order.
+// are those of plain stream order.  Because the kernel is resident while its
+// predecessor may still be writing, it never reads through the read-only
+// (ld.global.nc) path data that a preceding kernel can write: those loads are
+// coherent (.ca or .cg), or bulk copies through L2.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args... args) {
@@ -133,6 +136,10 @@ int prepare_step_kernel(int H, int Hkv, int D);
 
 // Number of SMs of the current device (cached per device); <= 0 on error.
 int device_sm_count();
+
+// dst[0, bytes) = src[0, bytes) by a kernel (the SMs' loads and stores), for
+// a host buffer the GPU can address; src and dst 16-byte aligned.
+int launch_io_copy(const void *src, void *dst, size_t bytes, cudaStream_t stream);
 
 // A fresh nonzero 32-bit value for every call (a process-wide counter): the
 // per-launch tag of the step kernel's workspace counters, and the workspace

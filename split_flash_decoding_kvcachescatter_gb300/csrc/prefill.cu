@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(256)
     if (row < S) {
       const float4 *src =
           reinterpret_cast<const float4 *>((which == 0 ? q : k) + ((size_t)h * S + row) * D + c);
-      const float4 a = __ldg(src), b = __ldg(src + 1);
+      const float4 a = __ldcg(src), b = __ldcg(src + 1);
       x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
       x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     } else {
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(256)
       const int gkey = t * kPN + key;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
       if (gkey < S)
-        a = __ldg(reinterpret_cast<const float4 *>(v + ((size_t)h * S + gkey) * D + d0) + f4);
+        a = __ldcg(reinterpret_cast<const float4 *>(v + ((size_t)h * S + gkey) * D + d0) + f4);
       sv[(4 * f4 + 0) * kVPad + key] = a.x;
       sv[(4 * f4 + 1) * kVPad + key] = a.y;
       sv[(4 * f4 + 2) * kVPad + key] = a.z;

@@ -155,18 +155,20 @@ def fill_host_io(hio, inp):
     hio.out.fill_(float("nan"))
 
 
-@pytest.mark.parametrize("name", ["tiny", "small_model"])
-def test_host_io_step_matches_oracle_and_device_step(name):
-    """kvs_decode_step_host_io: one pinned buffer in the io layout, one copy
-    in, one copy out; the same kernel as kvs_decode_step, so the output is
-    bit-identical to it, and within the gate of the oracle."""
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("name", ["tiny", "small_model", "8b_batch"])
+def test_host_io_step_matches_oracle_and_device_step(name, pinned):
+    """kvs_decode_step_host_io: one host buffer in the io layout, moved in
+    and out by the library's copy kernel (pinned) or by copy engines
+    (pageable); the same attention kernel as kvs_decode_step, so the output
+    is bit-identical to it, and within the gate of the oracle."""
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w)
     exp = W.upload(inp, w, DEV, include_new_row=True)
     t = W.upload(inp, w, DEV)
     t_dev = W.upload(inp, w, DEV)
     M, H, D = inp.q.shape
-    hio = B.HostIo(M, H, w.num_kv_heads, D)
+    hio = B.HostIo(M, H, w.num_kv_heads, D, pinned=pinned)
     fill_host_io(hio, inp)
     io = B.step_io(M, H, w.num_kv_heads, D, device=DEV)
     ws = B.workspace(M, H, w.num_kv_heads, D, w.max_len, w.chunk_size, device=DEV)
