@@ -47,11 +47,23 @@ namespace {
 constexpr int kMaxClusterDevices = 64;
 constexpr int kMaxClusterSize = 16;  // the largest cluster launched
 
-// Block geometry: that of the persistent kernel (4 consumer warps, two
-// blocks per SM).  Measured on GB300, 8 consumer warps at one block per SM
-// made small steps slower (fewer clusters resident at once).
+// Block geometry: four consumer warps, two blocks per SM, as in the
+// persistent kernel, but each warp folds up to four sub-tiles per stage, the
+// most whose ring still fits two blocks per SM.  A block's slice is a few
+// dozen to a few hundred rows, so the stages it walks one after another,
+// each a chain of shared-memory, shuffle and exponential latencies, set its
+// time, not the bytes: more rows per stage means fewer chains.  Measured on
+// GB300 (small model layer: M=4, 14 heads over 2 kv heads, head_dim 64):
+// 9.6 us a layer with one sub-tile, 8.2 with four; eight consumer warps at
+// one block per SM were slower (fewer clusters resident at once), and seven
+// consumer warps with two sub-tiles each (two blocks per SM at 128
+// registers) no faster than four with four.
 template <int D, int G>
-using ClusterGeo = Geo<D, G, 4, 2>;
+constexpr int cluster_nsub() {
+  return Geo<D, G, 4, 2, 4>::FITS ? 4 : Geo<D, G, 4, 2, 2>::FITS ? 2 : 1;
+}
+template <int D, int G>
+using ClusterGeo = Geo<D, G, 4, 2, cluster_nsub<D, G>()>;
 
 template <int D, int G, bool kPoll>
 __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::MINB)
@@ -73,6 +85,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   // stage (stage 0), so no copy ever lands in those slots and nothing else
   // reads them.
   constexpr int E = G * C::LPR;  // output float4s of one (i, g)
+  static_assert(C::FITS, "two blocks per SM must fit");
   static_assert(C::S >= 3, "the receive areas need ring stages 1 and 2");
   static_assert(E % kMaxClusterSize == 0, "every cluster size divides the output");
   static_assert(E * 16 <= C::Q_BYTES && kMaxClusterSize * G * 8 <= C::Q_BYTES,

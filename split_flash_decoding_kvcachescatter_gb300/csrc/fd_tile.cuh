@@ -61,12 +61,19 @@ constexpr int kMergeScratchBytes = kMergeWindow * 4 + 16;
 constexpr int kRingBytes = 96 * 1024;
 
 // Compile-time geometry of one (head_dim, group) instantiation.
-template <int D_, int G_, int NW_ = 4, int MINB_ = 2>
+//
+// A consumer warp folds NSUB sub-tiles of RW1 rows per stage.  Sub-tile u of
+// warp w holds stage rows [(u * NW + w) * RW1, +RW1), so a partial stage is
+// spread over the warps.  The sub-tiles' butterflies are independent, so a
+// warp overlaps their shuffle chains: more rows per stage for little more
+// latency, which is what a latency-bound step (few rows per block) needs.
+template <int D_, int G_, int NW_ = 4, int MINB_ = 2, int NSUB_ = 1>
 struct Geo {
   static constexpr int D = D_;
   static constexpr int G = G_;
   static constexpr int NW = NW_;                  // consumer warps
   static constexpr int MINB = MINB_;              // blocks per SM the budget is for
+  static constexpr int NSUB = NSUB_;              // sub-tiles per warp and stage
   static constexpr int THREADS = (NW + 1) * 32;   // + one producer warp
   static constexpr int LPR = D / 4;               // lanes per row (float4 each)
   static constexpr int RPI = 32 / LPR;            // rows per warp instruction
@@ -74,7 +81,8 @@ struct Geo {
   static constexpr int NSLOT = pow2ceil(RP * G);  // butterfly slots (<= LPR)
   static constexpr int LOG2NS = ilog2(NSLOT);
   static constexpr int SPAN = LPR / NSLOT;        // lanes sharing one slot
-  static constexpr int RW = RPI * RP;             // rows per warp tile
+  static constexpr int RW1 = RPI * RP;            // rows per sub-tile
+  static constexpr int RW = RW1 * NSUB;           // rows per warp and stage
   static constexpr int T = NW * RW;               // rows per stage
   static constexpr int RWP = round_up(RW, 4);     // padded score row length
   static constexpr int GP = round_up(G, 4);       // padded p row length
@@ -101,9 +109,12 @@ struct Geo {
   static constexpr int SMEM_BYTES = round_up(OFF_FLAG + 16, 128);
   static_assert(G >= 1 && G <= LPR, "group larger than lanes per row");
   static_assert(RP * G <= LPR, "slots exceed lanes");
-  static_assert(RW * G <= 32 * RPI, "tile too large");
+  static_assert(RW1 * G <= 32 * RPI, "tile too large");
+  static_assert(NSUB >= 1, "at least one sub-tile");
   // MINB blocks per SM: 228 KB of shared memory less 1 KB reserved per block
-  static_assert(SMEM_BYTES <= (228 * 1024) / MINB - 1024, "MINB blocks per SM must fit");
+  // (checked by each kernel; a geometry that does not fit may still be named
+  // here, so that a kernel can pick the largest NSUB that does)
+  static constexpr bool FITS = SMEM_BYTES <= (228 * 1024) / MINB - 1024;
 };
 
 // ---------------------------------------------------------------------------
@@ -193,10 +204,12 @@ struct SeqMap {
 // of the running sum and the lane's float4 column of the unnormalised
 // accumulator.
 //
-// Warp tile: RW rows x G heads per stage.  Lane (gi, li): gi = row group
-// within a warp instruction, li = float4 column of head_dim.  Each lane
-// forms RP*G partial dot products; the transposing butterfly leaves lane
-// li with the full score of slot li / SPAN (row slot_row, head slot_h).
+// Warp tile: NSUB sub-tiles of RW1 rows x G heads per stage.  Lane (gi, li):
+// gi = row group within a warp instruction, li = float4 column of head_dim.
+// In each sub-tile a lane forms RP*G partial dot products; the transposing
+// butterfly leaves lane li with the full score of slot li / SPAN (row
+// slot_row of the sub-tile, head slot_h).  Scores and probabilities are kept
+// per warp row u * RW1 + (row in sub-tile u).
 // ---------------------------------------------------------------------------
 template <class C>
 struct TileLane {
@@ -272,30 +285,44 @@ __device__ __forceinline__ void tile_consume(const TileLane<C> &t, const unsigne
   constexpr int G = C::G;
   const float4 *sK = reinterpret_cast<const float4 *>(stage);
   const float4 *sV = reinterpret_cast<const float4 *>(stage + C::KV_BYTES);
-  const int my_valid = min(max(nrows - t.w * C::RW, 0), C::RW);
-  if (my_valid <= 0) return;
-  const int tile0 = t.w * C::RW;
-  // ---- scores: partial dot products, then the butterfly ----
-  float part[C::NSLOT];
+  constexpr int NSUB = C::NSUB;
+  // rows of sub-tile u in this stage; sub-tile 0 has the warp's lowest rows
+  int valid_u[NSUB];
 #pragma unroll
-  for (int j = 0; j < C::NSLOT; ++j) part[j] = 0.f;
+  for (int u = 0; u < NSUB; ++u)
+    valid_u[u] = min(max(nrows - (u * C::NW + t.w) * C::RW1, 0), C::RW1);
+  if (valid_u[0] <= 0) return;
+  // ---- scores: partial dot products, then the butterflies (the rows past
+  //      nrows hold stale data, which the valid masks below discard) ----
+  float s_val[NSUB];
+  bool valid[NSUB];
 #pragma unroll
-  for (int r = 0; r < C::RP; ++r) {
-    const int row = tile0 + r * C::RPI + t.gi;
-    const float4 kv = sK[row * C::LPR + t.li];
+  for (int u = 0; u < NSUB; ++u) {
+    const int base = (u * C::NW + t.w) * C::RW1;
+    float part[C::NSLOT];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float d = qv[h].x * kv.x;
-      d = fmaf(qv[h].y, kv.y, d);
-      d = fmaf(qv[h].z, kv.z, d);
-      d = fmaf(qv[h].w, kv.w, d);
-      part[r * G + h] = d;
+    for (int j = 0; j < C::NSLOT; ++j) part[j] = 0.f;
+#pragma unroll
+    for (int r = 0; r < C::RP; ++r) {
+      const int row = base + r * C::RPI + t.gi;
+      const float4 kv = sK[row * C::LPR + t.li];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float d = qv[h].x * kv.x;
+        d = fmaf(qv[h].y, kv.y, d);
+        d = fmaf(qv[h].z, kv.z, d);
+        d = fmaf(qv[h].w, kv.w, d);
+        part[r * G + h] = d;
+      }
     }
+    const float sc = butterfly_sum<C::NSLOT, C::LOG2NS, C::LPR>(part, t.li);
+    valid[u] = t.slot_used && t.slot_row < valid_u[u];
+    s_val[u] = valid[u] ? sc : neg_inf();
   }
-  const float sc = butterfly_sum<C::NSLOT, C::LOG2NS, C::LPR>(part, t.li);
-  const bool valid = t.slot_used && t.slot_row < my_valid;
-  const float s_val = valid ? sc : neg_inf();
-  if (t.owner) t.sS[t.slot_h * C::RWP + t.slot_row] = s_val;
+  if (t.owner) {
+#pragma unroll
+    for (int u = 0; u < NSUB; ++u) t.sS[t.slot_h * C::RWP + u * C::RW1 + t.slot_row] = s_val[u];
+  }
   __syncwarp();
   // ---- running max and rescale factors (all lanes, all heads) ----
   float alpha[G];
@@ -319,11 +346,14 @@ __device__ __forceinline__ void tile_consume(const TileLane<C> &t, const unsigne
   float ah = alpha[0];
 #pragma unroll
   for (int h = 1; h < G; ++h) ah = (t.slot_h == h) ? alpha[h] : ah;
-  const float p = valid ? exp2f(s_val - mh) : 0.f;
-  if (t.owner) {
-    t.sP[t.slot_row * C::GP + t.slot_h] = p;
-    l_lane = l_lane * ah + p;
+  float psum = 0.f;
+#pragma unroll
+  for (int u = 0; u < NSUB; ++u) {
+    const float p = valid[u] ? exp2f(s_val[u] - mh) : 0.f;
+    if (t.owner) t.sP[(u * C::RW1 + t.slot_row) * C::GP + t.slot_h] = p;
+    psum += p;
   }
+  if (t.owner) l_lane = l_lane * ah + psum;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     m_run[h] = m_new[h];
@@ -335,25 +365,30 @@ __device__ __forceinline__ void tile_consume(const TileLane<C> &t, const unsigne
   __syncwarp();
   // ---- P.V ----
 #pragma unroll
-  for (int r = 0; r < C::RP; ++r) {
-    const int trow = r * C::RPI + t.gi;
-    if (trow < my_valid) {
-      const float4 vv = sV[(tile0 + trow) * C::LPR + t.li];
-      float pr[C::GP];
+  for (int u = 0; u < NSUB; ++u) {
+    const int base = (u * C::NW + t.w) * C::RW1;
 #pragma unroll
-      for (int j = 0; j < C::GP / 4; ++j) {
-        const float4 v = reinterpret_cast<const float4 *>(t.sP + trow * C::GP)[j];
-        pr[4 * j + 0] = v.x;
-        pr[4 * j + 1] = v.y;
-        pr[4 * j + 2] = v.z;
-        pr[4 * j + 3] = v.w;
-      }
+    for (int r = 0; r < C::RP; ++r) {
+      const int trow = r * C::RPI + t.gi;
+      if (trow < valid_u[u]) {
+        const float4 vv = sV[(base + trow) * C::LPR + t.li];
+        float pr[C::GP];
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        acc[h].x = fmaf(pr[h], vv.x, acc[h].x);
-        acc[h].y = fmaf(pr[h], vv.y, acc[h].y);
-        acc[h].z = fmaf(pr[h], vv.z, acc[h].z);
-        acc[h].w = fmaf(pr[h], vv.w, acc[h].w);
+        for (int j = 0; j < C::GP / 4; ++j) {
+          const float4 v =
+              reinterpret_cast<const float4 *>(t.sP + (u * C::RW1 + trow) * C::GP)[j];
+          pr[4 * j + 0] = v.x;
+          pr[4 * j + 1] = v.y;
+          pr[4 * j + 2] = v.z;
+          pr[4 * j + 3] = v.w;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          acc[h].x = fmaf(pr[h], vv.x, acc[h].x);
+          acc[h].y = fmaf(pr[h], vv.y, acc[h].y);
+          acc[h].z = fmaf(pr[h], vv.z, acc[h].z);
+          acc[h].w = fmaf(pr[h], vv.w, acc[h].w);
+        }
       }
     }
   }

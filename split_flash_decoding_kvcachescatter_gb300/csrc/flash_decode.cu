@@ -426,6 +426,7 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
                    float *__restrict__ out, WsView ws, int M, int Hkv, int chunk, float qscale,
                    unsigned host_tag, int *d_status) {
   using C = Geo<D, G>;
+  static_assert(C::FITS, "two blocks per SM must fit");
   constexpr int kCost = kRunCostBytes / (8 * D);  // cost rows per (i, g)
   extern __shared__ __align__(128) unsigned char smem[];
   StageDesc *desc = reinterpret_cast<StageDesc *>(smem + C::OFF_DESC);
