@@ -333,6 +333,12 @@ int kvs_decode_step_slots(const float *q, const float *k_rows,
  * graph: update the buffers' contents, never their addresses, between
  * launches.  The graph and its executable are CUDA objects owned by the
  * handle; the library allocates no device memory.
+ * Inside the graph, each layer after the first starts before the layer
+ * ahead of it has finished: it reads `positions` and streams its cache rows
+ * below the positions while that layer runs, and reads q, the new rows and
+ * row p only after it.  So no layer's out may overlap `positions` or any
+ * layer's caches (the library's own writes, row p of each cache, never
+ * overlap what a later layer reads early).
  *
  * kvs_step_graph_launch enqueues the whole step on `stream`.  The graph
  * starts with a 4-byte write of a fresh value to the workspace epoch (see

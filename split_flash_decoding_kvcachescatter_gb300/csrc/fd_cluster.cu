@@ -69,7 +69,8 @@ template <int D, int G, bool kPoll>
 __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::MINB)
     fd_cluster_kernel(const float *__restrict__ q, float *k_cache, float *v_cache, SeqMap sm,
                       const float *__restrict__ k_rows, const float *__restrict__ v_rows,
-                      float *__restrict__ out, int Hkv, float qscale, int *d_status) {
+                      float *__restrict__ out, int Hkv, float qscale, int *d_status,
+                      int early) {
   using C = ClusterGeo<D, G>;
   extern __shared__ __align__(128) unsigned char smem[];
   StageDesc *desc = reinterpret_cast<StageDesc *>(smem + C::OFF_DESC);
@@ -118,17 +119,33 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
     fence_mbar_init();
   }
   __syncthreads();
-  grid_dependency_wait();
-  const int err = sm.error(i);
-  const bool finished = sm.finished(i);
-  const int p = __ldca(sm.pos + i);
-  // ---- Step 1, scatter: the block holding row p writes the new rows (a
-  //      finished sequence too; none for a bad position or slot) ----
-  if (scatter && err == KVS_OK && rank == (uint32_t)(ncl - 1)) {
+  // Without `early`, everything below may read what the preceding kernel in
+  // the stream writes: wait for it first.  With `early` (a layer of a step
+  // graph after the first), positions, slots, finished flags and the cache
+  // rows below each position are not written by the preceding kernel, so
+  // they are read, and the first stages' cache rows streamed, before the
+  // wait; q, the new rows, the caches' row p, the output and the status
+  // come after it.
+  if (!early) grid_dependency_wait();
+  // sequence i (coherent loads: with `early` the preceding kernel may still
+  // be resident, and nothing it wrote may be served from a stale L1 line)
+  const int p = __ldcg(sm.pos + i);
+  const int slot = sm.slot ? __ldcg(sm.slot + i) : i;
+  const bool finished = sm.done && __ldcg(sm.done + i) != 0;
+  const int err = (p < 0 || p >= sm.max_len)                           ? KVS_ERR_POSITION
+                  : (sm.slot && (slot < 0 || slot >= sm.num_slots)) ? KVS_ERR_SLOT
+                                                                     : KVS_OK;
+  // rows of (i, g): the first row of its cache, and its new row
+  const size_t head_base = ((size_t)slot * Hkv + g) * (size_t)sm.max_len;
+  const size_t row_src = ((size_t)i * Hkv + g) * D;
+  // Step 1, scatter: the block holding row p writes the new rows (a finished
+  // sequence too; none for a bad position or slot).  Threads [t0, t0 + nt).
+  auto scatter_rows = [&](int t0, int nt) {
+    if (!scatter || err != KVS_OK || rank != (uint32_t)(ncl - 1)) return;
     constexpr int D4 = D / 4;
-    const size_t dst = sm.row_index(i, g, p) * D4;
-    const size_t src = ((size_t)i * Hkv + g) * D4;
-    for (int e = threadIdx.x; e < 2 * D4; e += C::THREADS) {
+    const size_t dst = (head_base + p) * D4;
+    const size_t src = row_src / 4;
+    for (int e = (int)threadIdx.x - t0; e < 2 * D4; e += nt) {
       if (e < D4)
         reinterpret_cast<float4 *>(k_cache)[dst + e] =
             __ldcg(reinterpret_cast<const float4 *>(k_rows) + src + e);
@@ -136,11 +153,13 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
         reinterpret_cast<float4 *>(v_cache)[dst + e - D4] =
             __ldcg(reinterpret_cast<const float4 *>(v_rows) + src + e - D4);
     }
-  }
+  };
   // The whole cluster leaves here (its blocks share i) before any wait on a
   // cluster barrier and before any remote store; it has only arrived at the
   // entry barrier, which no thread then waits on.
   if (err != KVS_OK || finished) {
+    grid_dependency_wait();
+    scatter_rows(0, C::THREADS);
     if (err != KVS_OK && rank == 0) {
       if (!finished) {  // a finished sequence's output is left as it is
         const float nan = __int_as_float(0x7fc00000);
@@ -155,46 +174,71 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   const int L = p + 1;
   const int r0 = (int)((long long)L * rank / ncl);
   const int r1 = (int)((long long)L * (rank + 1) / ncl);
-  allow_dependent_launch();
 
   if (warp == C::NW) {
     // ===================== producer warp (lane 0 issues) ====================
-    if (lane == 0) {
+    if (lane != 0) {
+      grid_dependency_wait();
+      allow_dependent_launch();
+    } else {
       const uint64_t pol_stream = policy_evict_first();
-      uint32_t k = 0;
       int ok = 1;
-      const size_t head_base = sm.row_index(i, g, 0);
-      const size_t row_src = ((size_t)i * Hkv + g) * D;  // new row of (i, g)
-      for (int rs = r0; rs < r1 && ok; rs += C::T, ++k) {
+      const int nst = (r1 - r0 + C::T - 1) / C::T;  // stages of the block's rows
+      // Stage k in two parts: its cache rows (with the descriptor and the
+      // barrier's byte count for the whole stage), and what the preceding
+      // kernel may write -- q with the first stage, the new rows with the
+      // stage holding row p.  The byte count keeps the stage incomplete
+      // until both parts have landed.
+      auto issue_cache_part = [&](uint32_t k) {
+        const uint32_t s = k % C::S;
+        const int rs = r0 + (int)k * C::T;
+        const int nrows = min(C::T, r1 - rs);
+        StageDesc &dd = desc[s];
+        dd.flags = (k == 0 ? kRunStart : 0) | (rs + C::T >= r1 ? kRunEnd : 0);
+        dd.nrows = nrows;
+        const uint32_t kv_bytes = (uint32_t)nrows * D * 4;
+        mbar_arrive_expect_tx(&full[s], 2 * kv_bytes + (k == 0 ? (uint32_t)C::Q_BYTES : 0u));
+        // with the scatter folded in, row L-1 (position p) comes from the new rows
+        const bool tail = scatter && (rs + nrows == L);
+        const uint32_t cache_bytes = tail ? kv_bytes - D * 4 : kv_bytes;
+        if (cache_bytes > 0) {
+          unsigned char *stage = smem + s * C::STAGE_BYTES;
+          const size_t row0 = (head_base + rs) * D;
+          bulk_g2s_hint(stage, k_cache + row0, cache_bytes, &full[s], pol_stream);
+          bulk_g2s_hint(stage + C::KV_BYTES, v_cache + row0, cache_bytes, &full[s], pol_stream);
+        }
+      };
+      auto issue_input_part = [&](uint32_t k) {
+        const uint32_t s = k % C::S;
+        const int rs = r0 + (int)k * C::T;
+        const int nrows = min(C::T, r1 - rs);
+        unsigned char *stage = smem + s * C::STAGE_BYTES;
+        if (scatter && rs + nrows == L) {
+          const uint32_t cache_bytes = (uint32_t)(nrows - 1) * D * 4;
+          bulk_g2s(stage + cache_bytes, k_rows + row_src, D * 4, &full[s]);
+          bulk_g2s(stage + C::KV_BYTES + cache_bytes, v_rows + row_src, D * 4, &full[s]);
+        }
+        if (k == 0)
+          bulk_g2s(stage + 2 * C::KV_BYTES, q + ((size_t)i * H + (size_t)g * G) * D, C::Q_BYTES,
+                   &full[s]);
+      };
+      // Every ring slot is fresh for its first use: the first S stages need
+      // no wait for a free slot.
+      const uint32_t npre = early ? (uint32_t)min(nst, C::S) : 0u;
+      for (uint32_t k = 0; k < npre; ++k) issue_cache_part(k);
+      grid_dependency_wait();
+      allow_dependent_launch();
+      for (uint32_t k = 0; k < npre; ++k) issue_input_part(k);
+      uint32_t k = npre;
+      for (; k < (uint32_t)nst; ++k) {
         const uint32_t s = k % C::S;
         const uint32_t use = k / C::S;
         if (!mbar_wait<kPoll>(&empty[s], (use & 1u) ^ 1u, abort)) {
           ok = 0;
           break;
         }
-        const int nrows = min(C::T, r1 - rs);
-        StageDesc &dd = desc[s];
-        dd.flags = (rs == r0 ? kRunStart : 0) | (rs + C::T >= r1 ? kRunEnd : 0);
-        dd.nrows = nrows;
-        const uint32_t kv_bytes = (uint32_t)nrows * D * 4;
-        const uint32_t bytes = 2 * kv_bytes + (rs == r0 ? (uint32_t)C::Q_BYTES : 0u);
-        unsigned char *stage = smem + s * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        const size_t row0 = (head_base + rs) * D;
-        // with the scatter folded in, row L-1 (position p) comes from the new rows
-        const bool tail = scatter && (rs + nrows == L);
-        const uint32_t cache_bytes = tail ? kv_bytes - D * 4 : kv_bytes;
-        if (cache_bytes > 0) {
-          bulk_g2s_hint(stage, k_cache + row0, cache_bytes, &full[s], pol_stream);
-          bulk_g2s_hint(stage + C::KV_BYTES, v_cache + row0, cache_bytes, &full[s], pol_stream);
-        }
-        if (tail) {
-          bulk_g2s(stage + cache_bytes, k_rows + row_src, D * 4, &full[s]);
-          bulk_g2s(stage + C::KV_BYTES + cache_bytes, v_rows + row_src, D * 4, &full[s]);
-        }
-        if (rs == r0)
-          bulk_g2s(stage + 2 * C::KV_BYTES, q + ((size_t)i * H + (size_t)g * G) * D, C::Q_BYTES,
-                   &full[s]);
+        issue_cache_part(k);
+        issue_input_part(k);
       }
       // Copies of uses below `first_live` have landed: the consumers
       // released those stages before the producer's last successful wait.
@@ -225,6 +269,9 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
     cluster_wait();  // the split barrier of the kernel entry
   } else {
     // ===================== consumer warps ===================================
+    grid_dependency_wait();
+    allow_dependent_launch();
+    scatter_rows(0, C::NW * 32);
     const TileLane<C> tl = tile_lane<C>(smem, warp, lane);
     float4 qv[G];
     float4 acc[G];
@@ -420,7 +467,7 @@ int launch_cluster_impl(const float *q, float *k_cache, float *v_cache, const Se
   const SeqMap sm{seqs.positions, seqs.slots, seqs.done, max_len, seqs.num_slots, Hkv};
   const cudaError_t e = cudaLaunchKernelEx(
       &cfg, poll_waits() ? fd_cluster_kernel<D, G, true> : fd_cluster_kernel<D, G, false>, q,
-      k_cache, v_cache, sm, k_rows, v_rows, out, Hkv, qscale, d_status);
+      k_cache, v_cache, sm, k_rows, v_rows, out, Hkv, qscale, d_status, seqs.early ? 1 : 0);
   if (e != cudaSuccess) {
     cudaGetLastError();  // leave no stale error for the caller's next check
     return KVS_ERR_LAUNCH;

@@ -187,6 +187,18 @@ int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
                     int num_heads, int num_kv_heads, int head_dim, int max_len, int chunk_size,
                     void *workspace, size_t workspace_bytes, int *d_status,
                     kvs_stream_t stream) {
+  return kvs::decode_step(q, k_rows, v_rows, positions, k_cache, v_cache, out, M, num_heads,
+                          num_kv_heads, head_dim, max_len, chunk_size, workspace,
+                          workspace_bytes, d_status, stream, false);
+}
+
+}  // extern "C"
+
+int kvs::decode_step(const float *q, const float *k_rows, const float *v_rows,
+                     const int32_t *positions, float *k_cache, float *v_cache, float *out, int M,
+                     int num_heads, int num_kv_heads, int head_dim, int max_len, int chunk_size,
+                     void *workspace, size_t workspace_bytes, int *d_status,
+                     kvs_stream_t stream, bool early) {
   int rc = check_attention_shape(M, num_heads, num_kv_heads, head_dim, max_len, chunk_size);
   if (rc != KVS_OK) return rc;
   if (M == 0) return KVS_OK;
@@ -197,11 +209,14 @@ int kvs_decode_step(const float *q, const float *k_rows, const float *v_rows,
   if (rc != KVS_OK) return rc;
   const int chunk = resolve_chunk(M, num_kv_heads, head_dim, max_len, chunk_size);
   if (chunk <= 0) return -chunk;
-  const kvs::SeqArgs seqs{positions, nullptr, nullptr, max_len, M};
+  kvs::SeqArgs seqs{positions, nullptr, nullptr, max_len, M};
+  seqs.early = early;
   return launch_attention(q, k_cache, v_cache, seqs, k_rows, v_rows, out, M, num_heads,
                           num_kv_heads, head_dim, chunk, workspace, d_status,
                           reinterpret_cast<cudaStream_t>(stream));
 }
+
+extern "C" {
 
 namespace {
 

@@ -89,10 +89,13 @@ int kvs_step_graph_create(int layers, const float *const *q, const float *const 
     cudaGetLastError();
     return KVS_ERR_LAUNCH;
   }
+  // A layer after the first follows another layer of the step, which writes
+  // neither the positions nor a cache row below a position: its kernel may
+  // read those before its dependency wait (SeqArgs::early).
   for (int l = 0; l < layers && rc == KVS_OK; ++l)
-    rc = kvs_decode_step(q[l], k_rows[l], v_rows[l], positions, k_cache[l], v_cache[l], out[l], M,
-                         num_heads, num_kv_heads, head_dim, max_len, chunk, workspace,
-                         workspace_bytes, d_status, stream);
+    rc = kvs::decode_step(q[l], k_rows[l], v_rows[l], positions, k_cache[l], v_cache[l], out[l],
+                          M, num_heads, num_kv_heads, head_dim, max_len, chunk, workspace,
+                          workspace_bytes, d_status, stream, l > 0);
   cudaGraph_t g = nullptr;
   const cudaError_t end = cudaStreamEndCapture(s, &g);  // always end the capture
   if (rc != KVS_OK || end != cudaSuccess || g == nullptr) {

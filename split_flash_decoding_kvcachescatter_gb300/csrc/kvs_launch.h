@@ -7,6 +7,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "kvsdecode.h"
+
 namespace kvs {
 
 // Upper bound on the step kernel's persistent grid (GB300: 152 SMs x 2).
@@ -94,7 +96,21 @@ struct SeqArgs {
   const uint8_t *done;
   int max_len;
   int num_slots;
+  // The kernel preceding this launch in the stream writes neither the
+  // positions, slots and finished flags nor any cache row below a sequence's
+  // position (a layer of a step graph after the first): the cluster kernel
+  // then reads them, and starts streaming those rows, before its dependency
+  // wait.  The persistent kernel ignores it.
+  bool early = false;
 };
+
+// kvs_decode_step with SeqArgs::early set as given (the step graph's
+// layers after the first); validation and dispatch are the same.
+int decode_step(const float *q, const float *k_rows, const float *v_rows,
+                const int32_t *positions, float *k_cache, float *v_cache, float *out, int M,
+                int num_heads, int num_kv_heads, int head_dim, int max_len, int chunk_size,
+                void *workspace, size_t workspace_bytes, int *d_status, kvs_stream_t stream,
+                bool early);
 
 int launch_kv_scatter(const float *k_rows, const float *v_rows, const int32_t *positions,
                       float *k_cache, float *v_cache, int M, int Hkv, int D, int max_len,
