@@ -67,13 +67,21 @@ constexpr int kRingBytes = 96 * 1024;
 // spread over the warps.  The sub-tiles' butterflies are independent, so a
 // warp overlaps their shuffle chains: more rows per stage for little more
 // latency, which is what a latency-bound step (few rows per block) needs.
-template <int D_, int G_, int NW_ = 4, int MINB_ = 2, int NSUB_ = 1>
+//
+// SHFL_MAX takes each head's running max over the warp's scores with
+// shuffles, straight from the lanes that hold them after the butterfly,
+// instead of through a shared-memory score tile (fewer instructions and no
+// store-load round trip: faster for a latency-bound block; measured on
+// GB300, the score tile is slightly faster where blocks are many and the
+// stream bandwidth-bound).
+template <int D_, int G_, int NW_ = 4, int MINB_ = 2, int NSUB_ = 1, bool SHFL_MAX_ = false>
 struct Geo {
   static constexpr int D = D_;
   static constexpr int G = G_;
   static constexpr int NW = NW_;                  // consumer warps
   static constexpr int MINB = MINB_;              // blocks per SM the budget is for
   static constexpr int NSUB = NSUB_;              // sub-tiles per warp and stage
+  static constexpr bool SHFL_MAX = SHFL_MAX_;
   static constexpr int THREADS = (NW + 1) * 32;   // + one producer warp
   static constexpr int LPR = D / 4;               // lanes per row (float4 each)
   static constexpr int RPI = 32 / LPR;            // rows per warp instruction
@@ -94,7 +102,7 @@ struct Geo {
   // that one block alone still keeps tens of KB of K/V in flight)
   static constexpr int S = cmin(8, cmax(3, kRingBytes / STAGE_BYTES));
   static constexpr int OFF_SCORE = S * STAGE_BYTES;
-  static constexpr int SCORE_BYTES = NW * G * RWP * 4;
+  static constexpr int SCORE_BYTES = SHFL_MAX ? 0 : NW * G * RWP * 4;
   static constexpr int OFF_P = OFF_SCORE + SCORE_BYTES;
   static constexpr int P_BYTES = NW * RW * GP * 4;
   static constexpr int OFF_MACC = round_up(OFF_P + P_BYTES, 128);
@@ -216,7 +224,7 @@ struct TileLane {
   int w, lane, gi, li;
   int slot_h, slot_row;
   bool slot_used, owner;
-  float *sS;     // [G][RWP] this warp's tile scores
+  float *sS;     // [G][RWP] this warp's tile scores (not with SHFL_MAX)
   float *sP;     // [RW][GP] this warp's tile probabilities
   float4 *sAcc;  // [NW][G][D/4] warp accumulators at a run end
   float *sM;     // [NW][G] warp maxima at a run end
@@ -239,7 +247,8 @@ __device__ __forceinline__ TileLane<C> tile_lane(unsigned char *smem, int warp, 
   t.sM = reinterpret_cast<float *>(smem + C::OFF_MM);
   t.sL = reinterpret_cast<float *>(smem + C::OFF_ML);
   t.sLl = reinterpret_cast<float *>(smem + C::OFF_MLL);
-  for (int e = lane; e < G * C::RWP; e += 32) t.sS[e] = neg_inf();
+  if (!C::SHFL_MAX)
+    for (int e = lane; e < G * C::RWP; e += 32) t.sS[e] = neg_inf();
   for (int e = lane; e < C::RW * C::GP; e += 32) t.sP[e] = 0.f;
   __syncwarp();
   const int slot = t.li / C::SPAN;
@@ -319,22 +328,45 @@ __device__ __forceinline__ void tile_consume(const TileLane<C> &t, const unsigne
     valid[u] = t.slot_used && t.slot_row < valid_u[u];
     s_val[u] = valid[u] ? sc : neg_inf();
   }
-  if (t.owner) {
-#pragma unroll
-    for (int u = 0; u < NSUB; ++u) t.sS[t.slot_h * C::RWP + u * C::RW1 + t.slot_row] = s_val[u];
-  }
-  __syncwarp();
   // ---- running max and rescale factors (all lanes, all heads) ----
+  float hmax = 0.f;  // SHFL_MAX: in lane h * SPAN, the max of head h
+  if (C::SHFL_MAX) {
+    hmax = s_val[0];
+#pragma unroll
+    for (int u = 1; u < NSUB; ++u) hmax = fmaxf(hmax, s_val[u]);
+    // Lane (gi, li) holds the score of slot li / SPAN = (r, h), so head h
+    // sits at lanes (r * G + h) * SPAN + s of every row group gi.  First
+    // over the row groups (lanes LPR apart), then over the RP rows of a
+    // group (G * SPAN apart; a shift past the group's LPR lanes keeps the
+    // lane's own value).  Invalid slots hold -inf.
+#pragma unroll
+    for (int o = C::LPR; o < 32; o <<= 1)
+      hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, o));
+#pragma unroll
+    for (int d = G * C::SPAN; d < C::RP * G * C::SPAN; d <<= 1)
+      hmax = fmaxf(hmax, __shfl_down_sync(0xffffffffu, hmax, d, C::LPR));
+  } else {
+    if (t.owner) {
+#pragma unroll
+      for (int u = 0; u < NSUB; ++u)
+        t.sS[t.slot_h * C::RWP + u * C::RW1 + t.slot_row] = s_val[u];
+    }
+    __syncwarp();
+  }
   float alpha[G];
   float m_new[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const float4 *row4 = reinterpret_cast<const float4 *>(t.sS + h * C::RWP);
     float tmax = neg_inf();
+    if (C::SHFL_MAX) {
+      tmax = __shfl_sync(0xffffffffu, hmax, h * C::SPAN);
+    } else {
+      const float4 *row4 = reinterpret_cast<const float4 *>(t.sS + h * C::RWP);
 #pragma unroll
-    for (int j = 0; j < C::RWP / 4; ++j) {
-      const float4 v = row4[j];
-      tmax = fmaxf(tmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+      for (int j = 0; j < C::RWP / 4; ++j) {
+        const float4 v = row4[j];
+        tmax = fmaxf(tmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+      }
     }
     m_new[h] = fmaxf(m_run[h], tmax);
     alpha[h] = (m_new[h] == m_run[h]) ? 1.f : exp2f(m_run[h] - m_new[h]);
