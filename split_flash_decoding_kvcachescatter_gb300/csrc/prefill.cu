@@ -597,10 +597,17 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
           mask_keys(*reinterpret_cast<float(*)[32]>(&r[0]), key0 + ch * 64, S, causal, i);
           mask_keys(*reinterpret_cast<float(*)[32]>(&r[32]), key0 + ch * 64 + 32, S, causal, i);
         }
-        float cm = neg_inf_f();
+        // chunk maximum as a tree (max is exact in any order; a chain of 64
+        // dependent fmaxf would sit on the tile's critical path)
+        float mx[32];
 #pragma unroll
-        for (int u = 0; u < 64; ++u) cm = fmaxf(cm, r[u]);
-        cm *= sl2;
+        for (int u = 0; u < 32; ++u) mx[u] = fmaxf(r[u], r[u + 32]);
+#pragma unroll
+        for (int w2 = 16; w2 >= 1; w2 >>= 1) {
+#pragma unroll
+          for (int u = 0; u < w2; ++u) mx[u] = fmaxf(mx[u], mx[u + w2]);
+        }
+        float cm = mx[0] * sl2;
         const float m_prev = m_ref;
         if (cm > m_ref + kRescaleLog2) m_ref = cm;
         if (ch > 0 && __any_sync(0xffffffffu, m_ref != m_prev)) {  // rare
@@ -620,14 +627,18 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
         }
         const float mb = (m_ref == neg_inf_f()) ? 0.f : m_ref;
         uint32_t w[32];
+        // the chunk's sum in four independent partial sums (one dependent
+        // chain of 64 additions would sit on the critical path)
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const float p0 = ex2(fmaf(r[2 * u], sl2, -mb));
           const float p1 = ex2(fmaf(r[2 * u + 1], sl2, -mb));
           const __half2 hp = __floats2half2_rn(p0, p1);
-          lt += p0 + p1;
+          ls[u & 3] += p0 + p1;
           w[u] = *reinterpret_cast<const uint32_t *>(&hp);
         }
+        lt += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_st32u(tm_s + ch * 32, w);
       }
       const float m_new = m_ref;
