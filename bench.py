@@ -193,6 +193,29 @@ def time_stream_read(torch, dev, stream, nbytes=2 << 30, iters=10):
             "kernel": "torch.sum over a 2 GiB float32 buffer (read-only)"}
 
 
+def launch_floor(torch, dev, stream, iters=200):
+    """What one launch costs with this file's single-launch timing (L2 scrub,
+    then events around the call) when the kernel does nothing: a one-element
+    add.  The event pair and the launch itself take this much of every
+    single-launch figure here (argmax, tiny)."""
+    one = torch.zeros(1, device=dev)
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(5):
+        one.add_(1.0)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for a, b in ev:
+        scrub.zero_()
+        a.record(stream)
+        one.add_(1.0)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ev)
+    return {"us": us, "kernel": "torch add_ on one float32 element",
+            "method": "L2 scrubbed, then CUDA events around the single launch (as argmax and tiny)"}
+
+
 def time_argmax(B, torch, M, dev, stream, iters=200):
     """The batched argmax of the serving step after attention (kvs_argmax):
     M rows of VOCAB logits, one launch; L2 scrubbed between launches
@@ -811,6 +834,7 @@ def main():
 
     live_read = time_stream_read(torch, dev, ctx.stream)
     argmax = time_argmax(B, torch, w.M, dev, ctx.stream) if not args.no_argmax else None
+    floor = launch_floor(torch, dev, ctx.stream)
     prefill = time_prefill(B, torch, dev, ctx.stream) if not args.no_prefill else None
     sampler.stop()
     clocks = sampler.summary(ctx.windows)
@@ -860,6 +884,7 @@ def main():
         "per_config": per_config,
         "argmax": argmax,
         "prefill": prefill,
+        "launch_floor": floor,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
