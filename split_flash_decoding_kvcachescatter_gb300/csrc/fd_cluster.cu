@@ -82,10 +82,9 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   // cluster (itself included) before the cluster barrier: element j of this
   // block's share (chunk = E / CS elements) from block r at
   // recv_acc[r * chunk + j], the (m, l) of head h from block r at
-  // recv_ml[r * G + h].  They use the q slots of ring stages 1 and 2: a
-  // block of this kernel has one run, whose q rows come with its first
-  // stage (stage 0), so no copy ever lands in those slots and nothing else
-  // reads them.
+  // recv_ml[r * G + h].  They use the q slots of ring stages 1 and 2: the
+  // consumer warps of this kernel load q straight into registers, so no
+  // copy ever lands in a q slot and nothing else reads them.
   constexpr int E = G * C::LPR;  // output float4s of one (i, g)
   static_assert(C::FITS, "two blocks per SM must fit");
   static_assert(C::S >= 3, "the receive areas need ring stages 1 and 2");
@@ -187,9 +186,9 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       const int nst = (r1 - r0 + C::T - 1) / C::T;  // stages of the block's rows
       // Stage k in two parts: its cache rows (with the descriptor and the
       // barrier's byte count for the whole stage), and what the preceding
-      // kernel may write -- q with the first stage, the new rows with the
-      // stage holding row p.  The byte count keeps the stage incomplete
-      // until both parts have landed.
+      // kernel may write -- the new rows, with the stage holding row p.
+      // The byte count keeps the stage incomplete until both parts have
+      // landed.  (q goes straight to the consumers' registers.)
       auto issue_cache_part = [&](uint32_t k) {
         const uint32_t s = k % C::S;
         const int rs = r0 + (int)k * C::T;
@@ -198,7 +197,7 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
         dd.flags = (k == 0 ? kRunStart : 0) | (rs + C::T >= r1 ? kRunEnd : 0);
         dd.nrows = nrows;
         const uint32_t kv_bytes = (uint32_t)nrows * D * 4;
-        mbar_arrive_expect_tx(&full[s], 2 * kv_bytes + (k == 0 ? (uint32_t)C::Q_BYTES : 0u));
+        mbar_arrive_expect_tx(&full[s], 2 * kv_bytes);
         // with the scatter folded in, row L-1 (position p) comes from the new rows
         const bool tail = scatter && (rs + nrows == L);
         const uint32_t cache_bytes = tail ? kv_bytes - D * 4 : kv_bytes;
@@ -219,9 +218,6 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
           bulk_g2s(stage + cache_bytes, k_rows + row_src, D * 4, &full[s]);
           bulk_g2s(stage + C::KV_BYTES + cache_bytes, v_rows + row_src, D * 4, &full[s]);
         }
-        if (k == 0)
-          bulk_g2s(stage + 2 * C::KV_BYTES, q + ((size_t)i * H + (size_t)g * G) * D, C::Q_BYTES,
-                   &full[s]);
       };
       // Every ring slot is fresh for its first use: the first S stages need
       // no wait for a free slot.
@@ -271,15 +267,26 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   } else {
     // ===================== consumer warps ===================================
     grid_dependency_wait();
-    allow_dependent_launch();
-    scatter_rows(0, C::NW * 32);
+    // q of the group, the lane's float4 column, straight from global memory
+    // (coherent loads: the preceding kernel may have written it), scaled as
+    // the stage math wants it (log2(e)/sqrt(D), base-2 softmax)
     const TileLane<C> tl = tile_lane<C>(smem, warp, lane);
     float4 qv[G];
+    {
+      const float4 *q4 = reinterpret_cast<const float4 *>(q) +
+                         ((size_t)i * H + (size_t)g * G) * C::LPR + tl.li;
+      float4 v[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) v[h] = __ldcg(q4 + h * C::LPR);
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        qv[h] = make_float4(v[h].x * qscale, v[h].y * qscale, v[h].z * qscale, v[h].w * qscale);
+    }
+    allow_dependent_launch();
+    scatter_rows(0, C::NW * 32);
     float4 acc[G];
     float m_run[G];
     float l_lane;
-#pragma unroll
-    for (int h = 0; h < G; ++h) qv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
     tile_reset<G>(acc, m_run, l_lane);
     for (uint32_t k = 0;; ++k) {
       const uint32_t s = k % C::S;
@@ -295,7 +302,6 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
       const StageDesc dsc = desc[s];
       if (dsc.flags & kNoMore) break;
       const unsigned char *stage = smem + s * C::STAGE_BYTES;
-      if (dsc.flags & kRunStart) tile_load_q<C>(tl, stage, qscale, qv);
       tile_consume<C>(tl, stage, dsc.nrows, qv, acc, m_run, l_lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
