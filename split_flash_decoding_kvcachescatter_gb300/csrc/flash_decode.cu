@@ -108,25 +108,32 @@ __device__ SplitTotals warp_split_totals(const SeqMap &sm, int M, int Hkv, int c
   return {rows, units};
 }
 
-// First cost row of sequence i (warp-cooperative).
-__device__ long long warp_seq_row0(int i, const SeqMap &sm, int Hkv, int cost, int lane) {
-  long long r = 0;
-  for (int j = lane; j < i; j += 32) {
-    const int L = sm.len(j);
-    if (L > 0) r += (long long)Hkv * (L + cost);
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-  return r;
+// a / b for a >= 0, b > 0: a 32-bit division when both fit (the 64-bit one
+// is a long instruction sequence, on the path to a block's first copy)
+__device__ __forceinline__ long long div_nn(long long a, long long b) {
+  if (((a | b) >> 31) == 0) return (long long)((unsigned)a / (unsigned)b);
+  return a / b;
 }
 
-// Global index of the first chunk that starts at or after cost row t;
-// `total_units` if t is past the end.
-__device__ long long warp_first_unit_at_row(long long t, const SeqMap &sm, int M, int Hkv,
-                                            int chunk, int cost, long long total_units,
-                                            int lane) {
+// A block's share of the plan: the chunks it runs, [ub, ue) -- the first
+// chunk that starts at or after cost row t0, and the first at or after t1
+// (total_units past the end) -- and, for ub, the (i, g, c) the cost row t0
+// falls in with the first cost row of sequence i.  c == n (the chunk count
+// of sequence i) means ub is chunk 0 of the (i, g) after (i, g).  One
+// warp-cooperative pass over the sequences; every lane returns the result.
+struct BlockPlan {
+  long long ub, ue;
+  int i, g, c;
+  long long seq_row0;
+};
+
+__device__ BlockPlan warp_block_plan(long long t0, long long t1, const SeqMap &sm, int M,
+                                     int Hkv, int chunk, int cost, long long total_units,
+                                     int lane) {
+  BlockPlan p{total_units, total_units, M, 0, 0, 0};
+  bool have0 = false, have1 = false;
   long long row_base = 0, unit_base = 0;
-  for (int i0 = 0; i0 < M; i0 += 32) {
+  for (int i0 = 0; i0 < M && !(have0 && have1); i0 += 32) {
     const int i = i0 + lane;
     const int L = (i < M) ? sm.len(i) : 0;
     const int n = (L + chunk - 1) / chunk;
@@ -142,56 +149,48 @@ __device__ long long warp_first_unit_at_row(long long t, const SeqMap &sm, int M
         uinc += b;
       }
     }
-    const long long rexcl = row_base + rinc - rows;
+    const long long rexcl = row_base + rinc - rows;  // first cost row of sequence i
     const long long uexcl = unit_base + uinc - units;
-    const bool hit = rows > 0 && t >= rexcl && t < rexcl + rows;
-    long long u = 0;
-    if (hit) {
+    const long long span = (long long)L + cost;  // cost rows of one (i, g)
+    // the first chunk of sequence i's rows starting at or after cost row t
+    auto chunk_at = [&](long long t, int &g, int &c) {
       const long long off = t - rexcl;
-      const long long span = (long long)L + cost;
-      const long long g = off / span;
-      const long long r = off - g * span - cost;  // offset from chunk 0's start
-      u = uexcl + g * n + (r <= 0 ? 0 : (r + chunk - 1) / chunk);  // c == n: next (i, g)
+      g = (int)div_nn(off, span);
+      const long long r = off - (long long)g * span - cost;  // offset from chunk 0's start
+      c = (r <= 0) ? 0 : (int)div_nn(r + chunk - 1, chunk);
+      return uexcl + (long long)g * n + c;
+    };
+    if (!have0) {
+      const bool hit = rows > 0 && t0 >= rexcl && t0 < rexcl + rows;
+      int g = 0, c = 0;
+      long long u = 0;
+      if (hit) u = chunk_at(t0, g, c);
+      const unsigned ballot = __ballot_sync(0xffffffffu, hit);
+      if (ballot) {
+        const int src = __ffs(ballot) - 1;
+        p.ub = __shfl_sync(0xffffffffu, u, src);
+        p.i = i0 + src;
+        p.g = __shfl_sync(0xffffffffu, g, src);
+        p.c = __shfl_sync(0xffffffffu, c, src);
+        p.seq_row0 = __shfl_sync(0xffffffffu, rexcl, src);
+        have0 = true;
+      }
     }
-    const unsigned ballot = __ballot_sync(0xffffffffu, hit);
-    if (ballot) return __shfl_sync(0xffffffffu, u, __ffs(ballot) - 1);
+    if (!have1) {
+      const bool hit = rows > 0 && t1 >= rexcl && t1 < rexcl + rows;
+      int g = 0, c = 0;
+      long long u = 0;
+      if (hit) u = chunk_at(t1, g, c);
+      const unsigned ballot = __ballot_sync(0xffffffffu, hit);
+      if (ballot) {
+        p.ue = __shfl_sync(0xffffffffu, u, __ffs(ballot) - 1);
+        have1 = true;
+      }
+    }
     row_base += __shfl_sync(0xffffffffu, rinc, 31);
     unit_base += __shfl_sync(0xffffffffu, uinc, 31);
   }
-  return total_units;
-}
-
-// (i, g, c) of global chunk index u (< total units).
-__device__ int3 warp_unit_to_igc(long long u, const SeqMap &sm, int M, int Hkv, int chunk,
-                                 int lane) {
-  long long unit_base = 0;
-  for (int i0 = 0; i0 < M; i0 += 32) {
-    const int i = i0 + lane;
-    const int L = (i < M) ? sm.len(i) : 0;
-    const int n = (L + chunk - 1) / chunk;
-    const long long units = (long long)Hkv * n;
-    long long uinc = units;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long b = __shfl_up_sync(0xffffffffu, uinc, o);
-      if (lane >= o) uinc += b;
-    }
-    const long long uexcl = unit_base + uinc - units;
-    const bool hit = units > 0 && u >= uexcl && u < uexcl + units;
-    int3 r = make_int3(0, 0, 0);
-    if (hit) {
-      const long long rem = u - uexcl;
-      r = make_int3(i, (int)(rem / n), (int)(rem % n));
-    }
-    const unsigned ballot = __ballot_sync(0xffffffffu, hit);
-    if (ballot) {
-      const int src = __ffs(ballot) - 1;
-      return make_int3(__shfl_sync(0xffffffffu, r.x, src), __shfl_sync(0xffffffffu, r.y, src),
-                       __shfl_sync(0xffffffffu, r.z, src));
-    }
-    unit_base += __shfl_sync(0xffffffffu, uinc, 31);
-  }
-  return make_int3(M, 0, 0);
+  return p;
 }
 
 // ---------------------------------------------------------------------------
@@ -513,17 +512,32 @@ __global__ void __launch_bounds__(Geo<D, G>::THREADS, 2)
     uint32_t k = 0;
     int ok = 1;
     const int b = blockIdx.x;
-    const long long ub =
-        warp_first_unit_at_row(column_start_row(R, P, b), sm, M, Hkv, chunk, kCost, U, lane);
-    const long long ue = (b + 1 == P) ? U
-                                      : warp_first_unit_at_row(column_start_row(R, P, b + 1),
-                                                               sm, M, Hkv, chunk, kCost, U, lane);
+    // cost rows where columns b and b + 1 start: R * b / P with one 64-bit
+    // division (R = qP + rem, so R * b / P = q * b + rem * b / P exactly)
+    const long long cq = R / P;
+    const long long crem = R - cq * P;
+    const long long t0 = cq * b + (crem * b) / P;
+    const long long t1 = cq * (b + 1) + (crem * (b + 1)) / P;
+    const BlockPlan plan = warp_block_plan(t0, t1, sm, M, Hkv, chunk, kCost, U, lane);
+    const long long ub = plan.ub, ue = plan.ue;
     if (ub < ue) {
-      const int3 igc = warp_unit_to_igc(ub, sm, M, Hkv, chunk, lane);
-      long long seq_row0 = warp_seq_row0(igc.x, sm, Hkv, kCost, lane);
+      // (i, g, c) of chunk ub and the first cost row of sequence i
+      int pi = plan.i, pg = plan.g, pc = plan.c;
+      long long seq_row0 = plan.seq_row0;
+      const int Lp = sm.len(pi);
+      if (pc == (Lp + chunk - 1) / chunk) {  // chunk 0 of the (i, g) after (i, g)
+        pc = 0;
+        if (++pg == Hkv) {  // of the next live sequence, which starts where i ends
+          pg = 0;
+          seq_row0 += (long long)Hkv * (Lp + kCost);
+          do {
+            ++pi;
+          } while (pi < M && sm.len(pi) == 0);
+        }
+      }
       const long long block_slot = (long long)M * Hkv + b;
       long long remaining = ue - ub;
-      Run run = make_run(igc.x, igc.y, igc.z, remaining, sm, chunk);
+      Run run = make_run(pi, pg, pc, remaining, sm, chunk);
       int run_seq = run.i;
       while (ok && remaining > 0 && run.units > 0) {
         if (run.i != run_seq) {  // moved to a later sequence: advance its first row
