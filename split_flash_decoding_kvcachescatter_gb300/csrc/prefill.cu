@@ -627,18 +627,22 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
         }
         const float mb = (m_ref == neg_inf_f()) ? 0.f : m_ref;
         uint32_t w[32];
-        // the chunk's sum in four independent partial sums (one dependent
-        // chain of 64 additions would sit on the critical path)
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // Two keys per paired FP32 instruction for the scaling and the sum
+        // (each key rounds as it would alone): the softmax is bound by
+        // instruction issue, not by the exponentials.  The sum runs in two
+        // independent pairs (one dependent chain would sit on the critical
+        // path).
+        float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 sl2x2 = make_float2(sl2, sl2), nmb2 = make_float2(-mb, -mb);
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-          const float p0 = ex2(fmaf(r[2 * u], sl2, -mb));
-          const float p1 = ex2(fmaf(r[2 * u + 1], sl2, -mb));
+          const float2 x2 = __ffma2_rn(make_float2(r[2 * u], r[2 * u + 1]), sl2x2, nmb2);
+          const float p0 = ex2(x2.x), p1 = ex2(x2.y);
           const __half2 hp = __floats2half2_rn(p0, p1);
-          ls[u & 3] += p0 + p1;
+          ls[u & 1] = __fadd2_rn(ls[u & 1], make_float2(p0, p1));
           w[u] = *reinterpret_cast<const uint32_t *>(&hp);
         }
-        lt += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        lt += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
         tmem_st32u(tm_s + ch * 32, w);
       }
       const float m_new = m_ref;
