@@ -352,6 +352,40 @@ def test_step_graph_multi_layer():
     g.destroy()
 
 
+def test_step_graph_bad_position_and_length_one():
+    """A step graph whose shared positions hold a bad position and a
+    sequence of one row: every layer flags KVS_ERR_POSITION and leaves NaN
+    in the bad sequence's rows, and the others match the oracle (the layers
+    after the first read the positions before their dependency wait)."""
+    layers = 3
+    w = W.custom(M=4, num_heads=14, num_kv_heads=2, head_dim=64, max_len=300, chunk_size=64,
+                 seed=72)
+    pos = np.array([0, 300, 157, 299], np.int32)
+    ins = [W.make_inputs(w, layer=l, positions=pos) for l in range(layers)]
+    ts = [W.upload(x, w, DEV) for x in ins]
+    exps = [W.upload(x, w, DEV, include_new_row=True) for x in ins]
+    outs = [torch.zeros_like(t["q"]) for t in ts]
+    ws = B.workspace(w.M, w.num_heads, w.num_kv_heads, w.head_dim, w.max_len, 64, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.Stream()
+    g = B.kvs_step_graph_create([t["q"] for t in ts], [t["k_rows"] for t in ts],
+                                [t["v_rows"] for t in ts], ts[0]["positions"],
+                                [t["k_cache"] for t in ts], [t["v_cache"] for t in ts], outs,
+                                chunk_size=64, workspace=ws, d_status=status, stream=stream)
+    g.launch(stream)
+    stream.synchronize()
+    assert int(status.item()) == B.KVS_ERR_POSITION
+    good = [0, 2, 3]
+    for l in range(layers):
+        out = outs[l].cpu().numpy()
+        assert np.all(np.isnan(out[1])), f"layer {l}: bad sequence not NaN"
+        ref = oracle.decode_sequences(ins[l].q[good], [ins[l].k_seq[i] for i in good],
+                                      [ins[l].v_seq[i] for i in good], pos[good])
+        gate(out[good], ref, where=f"graph layer {l} beside an invalid position")
+        assert_cache_bit_exact(ts[l], exps[l])
+    g.destroy()
+
+
 # ---------------------------------------------------------------- schedules
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("max_len", [1, 2, 31, 32, 33, 100, 513, 1200])
