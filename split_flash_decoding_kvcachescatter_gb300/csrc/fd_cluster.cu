@@ -332,28 +332,38 @@ __global__ void __launch_bounds__(ClusterGeo<D, G>::THREADS, ClusterGeo<D, G>::M
   cluster_sync_all();  // every partial is in the shared memory of the block merging it
   if (warp < C::NW) {
     // Block r merges elements [r * chunk, (r + 1) * chunk) from its own
-    // shared memory and writes that share of the output.
+    // shared memory and writes that share of the output.  Element j takes
+    // ncl consecutive lanes, lane rr holding block rr's partial; max and
+    // sums go over those lanes by shuffles (ncl is a power of two <= 16 and
+    // divides E, so an element's lanes lie in one warp and are all active
+    // or all idle).
     const int chunk = E / ncl;
-    for (int j = threadIdx.x; j < chunk; j += C::NW * 32) {
+    for (int base = warp * 32; base < E; base += C::NW * 32) {
+      const int t = base + lane;
+      const bool act = t < E;
+      const int j = t / ncl;
+      const int rr = t - j * ncl;
       const int e = (int)rank * chunk + j;
       const int h = e / C::LPR;
-      float mx = neg_inf();
-      for (int rr = 0; rr < ncl; ++rr) mx = fmaxf(mx, recv_ml[rr * G + h].x);
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      float l = 0.f;
-      for (int rr = 0; rr < ncl; ++rr) {
-        const float2 ml = recv_ml[rr * G + h];
-        const float w = (ml.x == neg_inf()) ? 0.f : exp2f(ml.x - mx);
-        const float4 b = recv_acc[rr * chunk + j];
-        a.x = fmaf(w, b.x, a.x);
-        a.y = fmaf(w, b.y, a.y);
-        a.z = fmaf(w, b.z, a.z);
-        a.w = fmaf(w, b.w, a.w);
-        l = fmaf(w, ml.y, l);
+      const float2 ml = act ? recv_ml[rr * G + h] : make_float2(neg_inf(), 0.f);
+      const float4 b = act ? recv_acc[rr * chunk + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+      float mx = ml.x;
+      for (int o = 1; o < ncl; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float w = (ml.x == neg_inf()) ? 0.f : exp2f(ml.x - mx);
+      float4 a = make_float4(w * b.x, w * b.y, w * b.z, w * b.w);
+      float l = w * ml.y;
+      for (int o = 1; o < ncl; o <<= 1) {
+        a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+        a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+        a.z += __shfl_xor_sync(0xffffffffu, a.z, o);
+        a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
+        l += __shfl_xor_sync(0xffffffffu, l, o);
       }
-      const float inv = 1.f / l;
-      reinterpret_cast<float4 *>(out)[((size_t)i * H + (size_t)g * G) * C::LPR + e] =
-          make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+      if (act && rr == 0) {
+        const float inv = 1.f / l;
+        reinterpret_cast<float4 *>(out)[((size_t)i * H + (size_t)g * G) * C::LPR + e] =
+            make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+      }
     }
   }
   // No block reads another's shared memory after the barrier, and every
