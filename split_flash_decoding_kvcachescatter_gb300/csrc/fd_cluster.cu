@@ -16,21 +16,23 @@
 //  * block r of the cluster streams rows [L*r/CS, L*(r+1)/CS) of (i, g)
 //    with the same warp-specialised pipeline and consumer tile as the
 //    persistent kernel (bulk async copies into a ring of stages);
-//  * each block leaves its partial (m, l, acc for the G heads) in its own
-//    shared memory, the cluster synchronises once, and each block reads
-//    the CS partials of an equal share of the output elements over
-//    distributed shared memory, merges them and writes that share of the
-//    output; a second cluster barrier keeps every block's shared memory
-//    alive until all of them have read it.
+//  * each block stores its partial (m, l, acc for the G heads), element by
+//    element, into the shared memory of the block that merges each share of
+//    the output (distributed shared memory); one cluster barrier makes the
+//    stores visible, and each block merges its share from its own shared
+//    memory and writes it.  No block reads another's memory, so the blocks
+//    may exit after that one barrier.
 // No workspace, no atomics, no global round trip between the partials and
 // the merge.  The fused scatter works as in the persistent kernel: the last
-// block of the cluster writes the new rows and reads row p from them.
+// block of the cluster writes the new rows, and the stage holding row p
+// takes it from the new rows.  Inside a step graph, a layer after the first
+// streams its cache rows before its dependency wait (SeqArgs::early).
 //
-// Every thread of every block arrives at the entry barrier, waits on it,
-// and passes the merge barrier on every path (the only early exit, a bad
-// position or a finished sequence, is taken by the whole cluster before any
-// wait), and every mbarrier wait is bounded in time, so a lost copy ends in
-// KVS_ERR_TIMEOUT, never in a hang.
+// Every thread of every block arrives at the entry barrier, waits on it
+// before its first remote store, and passes the merge barrier on every path
+// (the only early exit, a bad position or a finished sequence, is taken by
+// the whole cluster before any wait), and every mbarrier wait is bounded in
+// time, so a lost copy ends in KVS_ERR_TIMEOUT, never in a hang.
 
 #include <cmath>
 #include <mutex>
