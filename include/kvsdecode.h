@@ -359,6 +359,48 @@ int kvs_step_graph_create(int layers, const float *const *q,
                           size_t workspace_bytes, int *d_status,
                           kvs_stream_t stream, kvs_step_graph **graph);
 
+/*
+ * kvs_step_graph_io_layout -- the layout of one buffer holding a whole
+ * step's inputs and results for kvs_step_graph_create_host_io: the inputs
+ * first (q, k_rows, v_rows of layer 0, then of layer 1, ..., then the
+ * positions, shared by the layers), then the results (out of layer 0, 1,
+ * ...), each array 256-byte aligned, with the shapes of kvs_decode_step.
+ *   offsets  out  size_t[4 * layers + 2], host: offsets[3l], [3l + 1],
+ *                 [3l + 2] = q, k_rows, v_rows of layer l; [3 layers] =
+ *                 positions; [3 layers + 1 + l] = out of layer l (the inputs
+ *                 end at [3 layers + 1]); [4 layers + 1] = the total size.
+ * Errors: DIMS (a size < 1), NULL.
+ */
+int kvs_step_graph_io_layout(int layers, int M, int num_heads, int num_kv_heads, int head_dim,
+                             size_t *offsets);
+
+/*
+ * kvs_step_graph_create_host_io -- kvs_step_graph_create for a step whose
+ * per-token inputs and results live in ONE pinned host buffer (the pages'
+ * graphed decode: inputs at fixed addresses that the host rewrites before
+ * each launch).  The graph copies every layer's inputs and the positions to
+ * the device buffer `io` (the same layout) in one copy, runs the layers from
+ * there (fused scatter + attention, as kvs_step_graph_create), and copies
+ * every layer's out back in one copy.  The copies are kernels of this
+ * library moving the bytes over the host link.
+ *   host_io   in/out  host buffer of >= the layout's total size, pinned and
+ *                     addressable by the GPU (cudaHostAlloc /
+ *                     cudaHostRegister; other memory: UNSUPPORTED).  Write
+ *                     the inputs before a launch; the outs are valid once
+ *                     `stream` has passed it.
+ *   io        scratch device buffer of >= the total size, 256-byte aligned
+ *   k_cache, v_cache, M, num_heads, num_kv_heads, head_dim, max_len,
+ *   chunk_size, workspace, d_status, stream, graph: as kvs_step_graph_create
+ *   (k_cache, v_cache: host arrays of `layers` device pointers).
+ * Errors: NULL, DIMS, ALIGN (io), WORKSPACE (io_bytes), UNSUPPORTED (host_io
+ * not pinned), and those of kvs_step_graph_create.
+ */
+int kvs_step_graph_create_host_io(int layers, void *host_io, void *io, size_t io_bytes,
+                                  float *const *k_cache, float *const *v_cache, int M,
+                                  int num_heads, int num_kv_heads, int head_dim, int max_len,
+                                  int chunk_size, void *workspace, size_t workspace_bytes,
+                                  int *d_status, kvs_stream_t stream, kvs_step_graph **graph);
+
 int kvs_step_graph_launch(kvs_step_graph *graph, kvs_stream_t stream);
 
 int kvs_step_graph_destroy(kvs_step_graph *graph);

@@ -37,7 +37,8 @@ EXPORTS = ("kvs_kv_scatter", "kvs_choose_chunk_size", "kvs_flash_decode_workspac
            "kvs_set_schedule", "kvs_get_schedule", "kvs_schedule_for", "kvs_prepare",
            "kvs_decode_step_slots", "kvs_argmax", "kvs_prefill_attention",
            "kvs_prefill_workspace_bytes", "kvs_step_io_bytes", "kvs_decode_step_host",
-           "kvs_set_wait_limit_ns", "kvs_step_io_layout", "kvs_decode_step_host_io")
+           "kvs_set_wait_limit_ns", "kvs_step_io_layout", "kvs_decode_step_host_io",
+           "kvs_step_graph_io_layout", "kvs_step_graph_create_host_io")
 
 # Default bound on each pipeline wait of the kernels (kvs_set_wait_limit_ns).
 KVS_WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
@@ -99,6 +100,11 @@ def lib() -> ctypes.CDLL:
                                                 _I, _I, _P, _SZ, _P, _P, _P]
             L.kvs_step_graph_launch.restype = _I
             L.kvs_step_graph_launch.argtypes = [_P, _P]
+            L.kvs_step_graph_io_layout.restype = _I
+            L.kvs_step_graph_io_layout.argtypes = [_I, _I, _I, _I, _I, _P]
+            L.kvs_step_graph_create_host_io.restype = _I
+            L.kvs_step_graph_create_host_io.argtypes = [_I, _P, _P, _SZ, _P, _P, _I, _I, _I, _I,
+                                                        _I, _I, _P, _SZ, _P, _P, _P]
             L.kvs_step_graph_destroy.restype = _I
             L.kvs_step_graph_destroy.argtypes = [_P]
             L.kvs_decode_step_slots.restype = _I
@@ -404,6 +410,67 @@ def kvs_decode_step_host_io(host_io, k_cache, v_cache, chunk_size=0, workspace=N
         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _status_ptr(d_status), _stream(stream))
     _check(rc, "kvs_decode_step_host_io")
+
+
+def kvs_step_graph_io_layout(layers, M, num_heads, num_kv_heads, head_dim):
+    """Offsets of kvs_step_graph_io_layout: a list of 4 * layers + 2 ints."""
+    off = (ctypes.c_size_t * (4 * layers + 2))()
+    _check(lib().kvs_step_graph_io_layout(layers, M, num_heads, num_kv_heads, head_dim, off),
+           "kvs_step_graph_io_layout")
+    return list(off)
+
+
+class HostStepIo:
+    """A pinned host buffer with the layout of kvs_step_graph_io_layout and
+    views of its arrays: q[l], k_rows[l], v_rows[l], out[l] per layer and the
+    shared positions.  Fill the inputs, launch the host-io step graph, read
+    the outs once the stream has passed the launch."""
+
+    def __init__(self, layers, M, num_heads, num_kv_heads, head_dim):
+        off = kvs_step_graph_io_layout(layers, M, num_heads, num_kv_heads, head_dim)
+        self.layers, self.shape = layers, (M, num_heads, num_kv_heads, head_dim)
+        self.total = off[4 * layers + 1]
+        self.buf = torch.empty(self.total, dtype=torch.uint8, pin_memory=True)
+        f = lambda o, n, dt: self.buf[o:o + n * 4].view(dt)
+        qn, kn = M * num_heads * head_dim, M * num_kv_heads * head_dim
+        self.q = [f(off[3 * l], qn, torch.float32).view(M, num_heads, head_dim)
+                  for l in range(layers)]
+        self.k_rows = [f(off[3 * l + 1], kn, torch.float32).view(M, num_kv_heads, head_dim)
+                       for l in range(layers)]
+        self.v_rows = [f(off[3 * l + 2], kn, torch.float32).view(M, num_kv_heads, head_dim)
+                       for l in range(layers)]
+        self.positions = f(off[3 * layers], M, torch.int32)
+        self.out = [f(off[3 * layers + 1 + l], qn, torch.float32).view(M, num_heads, head_dim)
+                    for l in range(layers)]
+        self.in_bytes = off[3 * layers + 1]          # one copy to the device a step
+        self.out_bytes = self.total - self.in_bytes  # and one back
+
+
+def kvs_step_graph_create_host_io(host_io, k_cache, v_cache, chunk_size=0, workspace=None,
+                                  io=None, d_status=None, stream=None):
+    """A step graph over one pinned host buffer (a HostStepIo): one copy of
+    every layer's inputs in, the layers, one copy of every layer's out back."""
+    if not isinstance(host_io, HostStepIo):
+        raise TypeError("host_io: need a binding.HostStepIo")
+    layers = host_io.layers
+    if not (len(k_cache) == len(v_cache) == layers):
+        raise ValueError("kvs_step_graph_create_host_io: one cache per layer")
+    if workspace is None or io is None:
+        raise ValueError("kvs_step_graph_create_host_io: pass a workspace and an io buffer")
+    M, Hkv, Lmax, D = k_cache[0].shape
+    Mh, H, Hkvh, Dh = host_io.shape
+    if (Mh, Hkvh, Dh) != (M, Hkv, D):
+        raise ValueError("kvs_step_graph_create_host_io: inconsistent shapes")
+    arr = lambda ts, name: (ctypes.c_void_p * layers)(*[_f32(t, name, 4) for t in ts])
+    s = torch.cuda.Stream() if stream is None else stream
+    handle = ctypes.c_void_p()
+    rc = lib().kvs_step_graph_create_host_io(
+        layers, host_io.buf.data_ptr(), io.data_ptr(), io.numel() * io.element_size(),
+        arr(k_cache, "k_cache"), arr(v_cache, "v_cache"), M, H, Hkv, D, Lmax, int(chunk_size),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _status_ptr(d_status), _stream(s), ctypes.byref(handle))
+    _check(rc, "kvs_step_graph_create_host_io")
+    return StepGraph(handle, (host_io, io, k_cache, v_cache, workspace))
 
 
 def kvs_decode_step_slots(q, k_rows, v_rows, positions, slots, done, k_pool, v_pool, out,

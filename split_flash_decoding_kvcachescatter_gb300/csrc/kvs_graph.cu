@@ -58,44 +58,17 @@ bool add_epoch_node(cudaGraph_t g, void *workspace, cudaGraphNode_t *node,
   return true;
 }
 
-}  // namespace
-
-extern "C" {
-
-int kvs_step_graph_create(int layers, const float *const *q, const float *const *k_rows,
-                          const float *const *v_rows, const int32_t *positions,
-                          float *const *k_cache, float *const *v_cache, float *const *out,
-                          int M, int num_heads, int num_kv_heads, int head_dim, int max_len,
-                          int chunk_size, void *workspace, size_t workspace_bytes,
-                          int *d_status, kvs_stream_t stream, kvs_step_graph **graph) {
-  if (!graph) return KVS_ERR_NULL;
-  *graph = nullptr;
-  if (layers < 1 || M < 1 || chunk_size < 0) return KVS_ERR_DIMS;
-  if (!q || !k_rows || !v_rows || !k_cache || !v_cache || !out) return KVS_ERR_NULL;
-  if (!stream) return KVS_ERR_DIMS;  // the legacy default stream cannot be captured
-  // Validate every layer's pointers and configure the kernel before capturing.
-  for (int l = 0; l < layers; ++l) {
-    if (!q[l] || !k_rows[l] || !v_rows[l] || !k_cache[l] || !v_cache[l] || !out[l])
-      return KVS_ERR_NULL;
-  }
-  const int chunk = chunk_size > 0 ? chunk_size
-                                   : kvs_choose_chunk_size(M, num_kv_heads, head_dim, max_len, 0);
-  if (chunk <= 0) return -chunk;
-  int rc = kvs_prepare(num_heads, num_kv_heads, head_dim);
-  if (rc != KVS_OK) return rc;
-
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+// Captures what `body` enqueues on `s` (thread-local mode, the capture
+// always ended), puts the epoch memset ahead of it and instantiates it into
+// a new handle.  On any error nothing is kept and the status is returned.
+template <class Body>
+int capture_step_graph(cudaStream_t s, void *workspace, int layers, Body body,
+                       kvs_step_graph **graph) {
   if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
     cudaGetLastError();
     return KVS_ERR_LAUNCH;
   }
-  // A layer after the first follows another layer of the step, which writes
-  // neither the positions nor a cache row below a position: its kernel may
-  // read those before its dependency wait (SeqArgs::early).
-  for (int l = 0; l < layers && rc == KVS_OK; ++l)
-    rc = kvs::decode_step(q[l], k_rows[l], v_rows[l], positions, k_cache[l], v_cache[l], out[l],
-                          M, num_heads, num_kv_heads, head_dim, max_len, chunk, workspace,
-                          workspace_bytes, d_status, stream, l > 0);
+  const int rc = body();
   cudaGraph_t g = nullptr;
   const cudaError_t end = cudaStreamEndCapture(s, &g);  // always end the capture
   if (rc != KVS_OK || end != cudaSuccess || g == nullptr) {
@@ -129,6 +102,139 @@ int kvs_step_graph_create(int layers, const float *const *q, const float *const 
   h->layers = layers;
   *graph = h;
   return KVS_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Offsets of kvs_step_graph_io_layout (see the header).
+void step_io_offsets(int layers, int M, int H, int Hkv, int D, size_t *off) {
+  const size_t qo = (size_t)M * H * D * sizeof(float);
+  const size_t kv = (size_t)M * Hkv * D * sizeof(float);
+  size_t at = 0;
+  for (int l = 0; l < layers; ++l) {
+    off[3 * l + 0] = at;
+    at += round256(qo);
+    off[3 * l + 1] = at;
+    at += round256(kv);
+    off[3 * l + 2] = at;
+    at += round256(kv);
+  }
+  off[3 * layers] = at;  // positions
+  at += round256((size_t)M * sizeof(int32_t));
+  for (int l = 0; l < layers; ++l) {
+    off[3 * layers + 1 + l] = at;
+    at += round256(qo);
+  }
+  off[4 * layers + 1] = at;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvs_step_graph_create(int layers, const float *const *q, const float *const *k_rows,
+                          const float *const *v_rows, const int32_t *positions,
+                          float *const *k_cache, float *const *v_cache, float *const *out,
+                          int M, int num_heads, int num_kv_heads, int head_dim, int max_len,
+                          int chunk_size, void *workspace, size_t workspace_bytes,
+                          int *d_status, kvs_stream_t stream, kvs_step_graph **graph) {
+  if (!graph) return KVS_ERR_NULL;
+  *graph = nullptr;
+  if (layers < 1 || M < 1 || chunk_size < 0) return KVS_ERR_DIMS;
+  if (!q || !k_rows || !v_rows || !k_cache || !v_cache || !out) return KVS_ERR_NULL;
+  if (!stream) return KVS_ERR_DIMS;  // the legacy default stream cannot be captured
+  // Validate every layer's pointers and configure the kernel before capturing.
+  for (int l = 0; l < layers; ++l) {
+    if (!q[l] || !k_rows[l] || !v_rows[l] || !k_cache[l] || !v_cache[l] || !out[l])
+      return KVS_ERR_NULL;
+  }
+  const int chunk = chunk_size > 0 ? chunk_size
+                                   : kvs_choose_chunk_size(M, num_kv_heads, head_dim, max_len, 0);
+  if (chunk <= 0) return -chunk;
+  int rc = kvs_prepare(num_heads, num_kv_heads, head_dim);
+  if (rc != KVS_OK) return rc;
+  // A layer after the first follows another layer of the step, which writes
+  // neither the positions nor a cache row below a position: its kernel may
+  // read those before its dependency wait (SeqArgs::early).
+  return capture_step_graph(
+      reinterpret_cast<cudaStream_t>(stream), workspace, layers,
+      [&]() {
+        int r = KVS_OK;
+        for (int l = 0; l < layers && r == KVS_OK; ++l)
+          r = kvs::decode_step(q[l], k_rows[l], v_rows[l], positions, k_cache[l], v_cache[l],
+                               out[l], M, num_heads, num_kv_heads, head_dim, max_len, chunk,
+                               workspace, workspace_bytes, d_status, stream, l > 0);
+        return r;
+      },
+      graph);
+}
+
+int kvs_step_graph_io_layout(int layers, int M, int num_heads, int num_kv_heads, int head_dim,
+                             size_t *offsets) {
+  if (layers < 1 || M < 1 || num_heads < 1 || num_kv_heads < 1 || head_dim < 1)
+    return KVS_ERR_DIMS;
+  if (!offsets) return KVS_ERR_NULL;
+  step_io_offsets(layers, M, num_heads, num_kv_heads, head_dim, offsets);
+  return KVS_OK;
+}
+
+int kvs_step_graph_create_host_io(int layers, void *host_io, void *io, size_t io_bytes,
+                                  float *const *k_cache, float *const *v_cache, int M,
+                                  int num_heads, int num_kv_heads, int head_dim, int max_len,
+                                  int chunk_size, void *workspace, size_t workspace_bytes,
+                                  int *d_status, kvs_stream_t stream, kvs_step_graph **graph) {
+  if (!graph) return KVS_ERR_NULL;
+  *graph = nullptr;
+  if (layers < 1 || M < 1 || chunk_size < 0 || num_heads < 1 || num_kv_heads < 1 ||
+      head_dim < 1)
+    return KVS_ERR_DIMS;
+  if (!host_io || !io || !k_cache || !v_cache) return KVS_ERR_NULL;
+  if (!stream) return KVS_ERR_DIMS;  // the legacy default stream cannot be captured
+  if ((reinterpret_cast<uintptr_t>(io) & 255u) != 0) return KVS_ERR_ALIGN;
+  for (int l = 0; l < layers; ++l)
+    if (!k_cache[l] || !v_cache[l]) return KVS_ERR_NULL;
+  std::vector<size_t> off(4 * (size_t)layers + 2);
+  step_io_offsets(layers, M, num_heads, num_kv_heads, head_dim, off.data());
+  const size_t in_end = off[3 * layers + 1], total = off[4 * layers + 1];
+  if (io_bytes < total) return KVS_ERR_WORKSPACE;
+  // The copies are kernels of this library reading and writing the host
+  // buffer over the host link: it must be pinned memory the GPU can address
+  // (a copy engine's copy from pageable memory cannot be part of a graph).
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, host_io) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_UNSUPPORTED;
+  }
+  if (pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr ||
+      (reinterpret_cast<uintptr_t>(pa.devicePointer) & 15u) != 0)
+    return KVS_ERR_UNSUPPORTED;
+  unsigned char *mapped = static_cast<unsigned char *>(pa.devicePointer);
+  unsigned char *base = static_cast<unsigned char *>(io);
+  const int chunk = chunk_size > 0 ? chunk_size
+                                   : kvs_choose_chunk_size(M, num_kv_heads, head_dim, max_len, 0);
+  if (chunk <= 0) return -chunk;
+  int rc = kvs_prepare(num_heads, num_kv_heads, head_dim);
+  if (rc != KVS_OK) return rc;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int32_t *pos = reinterpret_cast<const int32_t *>(base + off[3 * layers]);
+  return capture_step_graph(
+      s, workspace, layers,
+      [&]() {
+        // every layer's inputs and the positions, in one copy
+        int r = kvs::launch_io_copy(mapped, base, in_end, s);
+        for (int l = 0; l < layers && r == KVS_OK; ++l)
+          r = kvs::decode_step(reinterpret_cast<const float *>(base + off[3 * l]),
+                               reinterpret_cast<const float *>(base + off[3 * l + 1]),
+                               reinterpret_cast<const float *>(base + off[3 * l + 2]), pos,
+                               k_cache[l], v_cache[l],
+                               reinterpret_cast<float *>(base + off[3 * layers + 1 + l]), M,
+                               num_heads, num_kv_heads, head_dim, max_len, chunk, workspace,
+                               workspace_bytes, d_status, stream, l > 0);
+        // every layer's out, in one copy
+        if (r == KVS_OK) r = kvs::launch_io_copy(base + in_end, mapped + in_end, total - in_end, s);
+        return r;
+      },
+      graph);
 }
 
 int kvs_step_graph_launch(kvs_step_graph *graph, kvs_stream_t stream) {

@@ -356,6 +356,55 @@ def test_step_io_layout_matches_io_bytes(L):
     assert L.kvs_step_io_layout(1, 4, 2, 64, None) == B.KVS_ERR_NULL
 
 
+def test_step_graph_io_layout(L):
+    """Every layer's q, k_rows, v_rows, then the positions, then every
+    layer's out, each 256-byte aligned and in that order."""
+    def r(x):
+        return -(-x // 256) * 256
+    for layers, M, H, Hkv, D in [(1, 1, 4, 2, 64), (3, 4, 14, 2, 64), (24, 4, 14, 2, 64),
+                                 (2, 32, 32, 8, 128), (2, 5, 40, 8, 128)]:
+        off = B.kvs_step_graph_io_layout(layers, M, H, Hkv, D)
+        assert len(off) == 4 * layers + 2
+        qo, kv = r(M * H * D * 4), r(M * Hkv * D * 4)
+        at = 0
+        for l in range(layers):
+            assert off[3 * l: 3 * l + 3] == [at, at + qo, at + qo + kv]
+            at += qo + 2 * kv
+        assert off[3 * layers] == at
+        at += r(4 * M)
+        for l in range(layers):
+            assert off[3 * layers + 1 + l] == at + l * qo
+        assert off[4 * layers + 1] == at + layers * qo
+    off = (ctypes.c_size_t * 6)()
+    assert L.kvs_step_graph_io_layout(0, 1, 4, 2, 64, off) == B.KVS_ERR_DIMS
+    assert L.kvs_step_graph_io_layout(1, 1, 4, 0, 64, off) == B.KVS_ERR_DIMS
+    assert L.kvs_step_graph_io_layout(1, 1, 4, 2, 64, None) == B.KVS_ERR_NULL
+
+
+def test_step_graph_create_host_io_rejects_before_any_device_work(L):
+    """Argument checks that need no device: a NULL handle pointer, bad sizes,
+    NULL buffers, the legacy default stream, a misaligned or short io buffer."""
+    h = ctypes.c_void_p()
+    caches = (ctypes.c_void_p * 1)(A16)
+    def call(**kw):
+        a = dict(layers=1, hio=A16, io=A16, iob=1 << 30, k=caches, v=caches, M=1, H=4, Hkv=2,
+                 D=64, Lmax=256, C=64, ws=A16, wsb=1 << 30, st=A16, out=ctypes.byref(h))
+        a.update(kw)
+        return L.kvs_step_graph_create_host_io(a["layers"], a["hio"], a["io"], a["iob"], a["k"],
+                                               a["v"], a["M"], a["H"], a["Hkv"], a["D"],
+                                               a["Lmax"], a["C"], a["ws"], a["wsb"], None,
+                                               a["st"], a["out"])
+    assert call(out=None) == B.KVS_ERR_NULL
+    assert call(layers=0) == B.KVS_ERR_DIMS
+    assert call(M=0) == B.KVS_ERR_DIMS
+    assert call(hio=None) == B.KVS_ERR_NULL
+    assert call(io=None) == B.KVS_ERR_NULL
+    assert call(k=None) == B.KVS_ERR_NULL
+    assert call(st=None) == B.KVS_ERR_DIMS
+    assert call(io=A16 + 16) == B.KVS_ERR_ALIGN
+    assert call(iob=1024) == B.KVS_ERR_WORKSPACE
+
+
 def _dshio(L, hio=A16, k=A16, v=A16, M=1, H=4, Hkv=2, D=64, Lmax=256, C=64, io=A16,
            iob=1 << 30, ws=A16, wsb=1 << 30):
     return L.kvs_decode_step_host_io(hio, k, v, M, H, Hkv, D, Lmax, C, io, iob, ws, wsb, None,

@@ -5,6 +5,8 @@ Bar as for the device entry points: bit-identical caches, outputs within
 max-abs 2e-5 / max-rel 1e-4 of the f64 oracle, and bit-identical to
 kvs_decode_step on the same inputs (the same kernel runs on the copies).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -35,6 +37,16 @@ def schedule(request, _built):
     prev = B.kvs_set_schedule(request.param)
     yield request.param
     B.kvs_set_schedule(prev)
+
+
+def oracle_out(inp):
+    return oracle.decode_sequences(inp.q, inp.k_seq, inp.v_seq, inp.positions)
+
+
+def assert_cache_bit_exact(t, expected):
+    torch.cuda.synchronize()
+    for name in ("k_cache", "v_cache"):
+        assert torch.equal(t[name].view(torch.int32), expected[name].view(torch.int32)), name
 
 
 def host_inputs(inp, pinned=True):
@@ -240,3 +252,90 @@ def test_host_io_steps_double_buffered_without_synchronisation():
     assert len(results) == 6
     for n, (o, r) in enumerate(results):
         gate(o.numpy(), r, where=f"double-buffered step {n}")
+
+
+def test_step_graph_host_io_equals_device_step_graph():
+    """kvs_step_graph_create_host_io: every layer's inputs in one pinned host
+    buffer; outputs bit-identical to kvs_step_graph_create on the same inputs
+    (the same kernels run on the copies), within the gate of the oracle, and
+    the caches bit-exact; then a second token through the same graphs."""
+    layers = 3
+    w = W.custom(M=4, num_heads=14, num_kv_heads=2, head_dim=64, max_len=700, chunk_size=64,
+                 seed=81)
+    pos = W.draw_positions(w)
+    ins = [W.make_inputs(w, layer=l, positions=pos) for l in range(layers)]
+    M, H, D = ins[0].q.shape
+    # the device step graph on one set of caches, the host-io graph on another
+    td = [W.upload(x, w, DEV) for x in ins]
+    th = [W.upload(x, w, DEV) for x in ins]
+    exps = [W.upload(x, w, DEV, include_new_row=True) for x in ins]
+    outs = [torch.full_like(t["q"], float("nan")) for t in td]
+    ws_d = B.workspace(M, H, w.num_kv_heads, D, w.max_len, 64, device=DEV)
+    ws_h = B.workspace(M, H, w.num_kv_heads, D, w.max_len, 64, device=DEV)
+    st_d = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st_h = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.Stream()
+    gd = B.kvs_step_graph_create([t["q"] for t in td], [t["k_rows"] for t in td],
+                                 [t["v_rows"] for t in td], td[0]["positions"],
+                                 [t["k_cache"] for t in td], [t["v_cache"] for t in td], outs,
+                                 chunk_size=64, workspace=ws_d, d_status=st_d, stream=stream)
+    hio = B.HostStepIo(layers, M, H, w.num_kv_heads, D)
+    io = torch.empty(hio.total, dtype=torch.uint8, device=DEV)
+    gh = B.kvs_step_graph_create_host_io(hio, [t["k_cache"] for t in th],
+                                         [t["v_cache"] for t in th], chunk_size=64,
+                                         workspace=ws_h, io=io, d_status=st_h, stream=stream)
+
+    def fill(inputs, positions):
+        for l, x in enumerate(inputs):
+            hio.q[l].copy_(torch.from_numpy(np.ascontiguousarray(x.q, np.float32)))
+            hio.k_rows[l].copy_(torch.from_numpy(np.ascontiguousarray(x.k_rows, np.float32)))
+            hio.v_rows[l].copy_(torch.from_numpy(np.ascontiguousarray(x.v_rows, np.float32)))
+            hio.out[l].fill_(float("nan"))
+        hio.positions.copy_(torch.from_numpy(np.ascontiguousarray(positions, np.int32)))
+
+    fill(ins, pos)
+    gd.launch(stream)
+    gh.launch(stream)
+    stream.synchronize()
+    assert int(st_d.item()) == 0 and int(st_h.item()) == 0
+    for l in range(layers):
+        assert torch.equal(outs[l].cpu().view(torch.int32), hio.out[l].view(torch.int32)), l
+        gate(hio.out[l].numpy(), oracle_out(ins[l]), where=f"host-io graph layer {l}")
+        assert_cache_bit_exact(th[l], exps[l])
+    # a second token: new inputs at the same addresses, next positions
+    pos2 = np.minimum(pos + 1, w.max_len - 1).astype(np.int32)
+    ins2 = [W.make_inputs(w, layer=l, positions=pos2, seed=82) for l in range(layers)]
+    for l in range(layers):
+        for tt in (td[l], th[l]):
+            fresh = W.upload(ins2[l], w, DEV)
+            for name in ("q", "k_rows", "v_rows", "k_cache", "v_cache"):
+                tt[name].copy_(fresh[name])
+    td[0]["positions"].copy_(torch.from_numpy(pos2).to(DEV))
+    fill(ins2, pos2)
+    gd.launch(stream)
+    gh.launch(stream)
+    stream.synchronize()
+    for l in range(layers):
+        assert torch.equal(outs[l].cpu().view(torch.int32), hio.out[l].view(torch.int32)), l
+        gate(hio.out[l].numpy(), oracle_out(ins2[l]), where=f"host-io graph relaunch layer {l}")
+    gd.destroy()
+    gh.destroy()
+
+
+def test_step_graph_host_io_rejects_pageable_memory():
+    w = W.custom(M=2, num_heads=4, num_kv_heads=2, head_dim=64, max_len=64, chunk_size=32,
+                 seed=83)
+    t = W.upload(W.make_inputs(w), w, DEV)
+    off = B.kvs_step_graph_io_layout(1, 2, 4, 2, 64)
+    pageable = torch.empty(off[-1], dtype=torch.uint8)  # not pinned
+    io = torch.empty(off[-1], dtype=torch.uint8, device=DEV)
+    ws = B.workspace(2, 4, 2, 64, 64, 32, device=DEV)
+    h = ctypes.c_void_p()
+    caches_k = (ctypes.c_void_p * 1)(t["k_cache"].data_ptr())
+    caches_v = (ctypes.c_void_p * 1)(t["v_cache"].data_ptr())
+    stream = torch.cuda.Stream()
+    rc = B.lib().kvs_step_graph_create_host_io(
+        1, pageable.data_ptr(), io.data_ptr(), off[-1], caches_k, caches_v, 2, 4, 2, 64, 64, 32,
+        ws.data_ptr(), ws.numel(), None, stream.cuda_stream, ctypes.byref(h))
+    assert rc == B.KVS_ERR_UNSUPPORTED
+    assert not h.value
