@@ -633,7 +633,8 @@ def measure_workload(ctx, w, seed, steps, warmup, chunks, graph=False, full=Fals
 
         if ci == 0:
             res["e2e"] = measure_e2e(ctx, w, ts, inps, ws, resolved, status, scrub, warmup,
-                                     e2e_steps or max(3, min(steps, 500)), ab["step"])
+                                     e2e_steps or max(3, min(steps, 500)), ab["step"],
+                                     graph=sg is not None)
         if sg is not None:
             sg.destroy()
         del ws
@@ -646,40 +647,65 @@ def measure_workload(ctx, w, seed, steps, warmup, chunks, graph=False, full=Fals
     return results
 
 
-def measure_e2e(ctx, w, ts, inps, ws, chunk, status, scrub, warmup, Ke, step_bytes):
-    """The step through the public host-buffer entry point: for every layer
-    one kvs_decode_step_host_io call (one copy of q, k_rows, v_rows and
-    positions from pinned host memory, the fused step, one copy of out back).
-    Two sets of host and device io buffers in alternation: a set is reused
-    once the event after its previous step has passed, i.e. its output has
-    reached the host (the host waits for it), so step k+1's calls are
+def measure_e2e(ctx, w, ts, inps, ws, chunk, status, scrub, warmup, Ke, step_bytes,
+                graph=False):
+    """The step through the public host-buffer entry points, all inputs
+    copied in from pinned host memory and every out copied back each step:
+    with `graph` (a multi-layer step launched as one graph), one launch of a
+    kvs_step_graph_create_host_io graph (one copy of every layer's q,
+    k_rows, v_rows and the positions in, the layers, one copy of every out
+    back); otherwise one kvs_decode_step_host_io call per layer (the same for
+    one layer).  Two sets of host and device io buffers in alternation: a
+    set is reused once the event after its previous step has passed, i.e.
+    its output has reached the host (the host waits for it), so step k+1 is
     enqueued while step k runs."""
     torch, B, dev, stream = ctx.torch, ctx.B, ctx.dev, ctx.stream
     M, H, D = ts[0]["q"].shape
     Hkv = w.num_kv_heads
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32))
     sets = []
     for _ in range(2):
-        hios = []
-        for x in inps:
-            h = B.HostIo(M, H, Hkv, D)
-            h.q.copy_(torch.from_numpy(np.ascontiguousarray(x.q, np.float32)))
-            h.k_rows.copy_(torch.from_numpy(np.ascontiguousarray(x.k_rows, np.float32)))
-            h.v_rows.copy_(torch.from_numpy(np.ascontiguousarray(x.v_rows, np.float32)))
-            h.positions.copy_(torch.from_numpy(np.ascontiguousarray(x.positions, np.int32)))
-            hios.append(h)
-        sets.append((hios, B.step_io(M, H, Hkv, D, device=dev)))
-    h2d = sum(h.in_bytes for h in sets[0][0])
-    d2h = sum(h.out_bytes for h in sets[0][0])
+        if graph:
+            h = B.HostStepIo(len(inps), M, H, Hkv, D)
+            for l, x in enumerate(inps):
+                h.q[l].copy_(f32(x.q))
+                h.k_rows[l].copy_(f32(x.k_rows))
+                h.v_rows[l].copy_(f32(x.v_rows))
+            h.positions.copy_(torch.from_numpy(np.ascontiguousarray(inps[0].positions, np.int32)))
+            io = torch.empty(h.total, dtype=torch.uint8, device=dev)
+            # captured on a side stream of the binding's, launched on `stream`
+            g = B.kvs_step_graph_create_host_io(h, [t["k_cache"] for t in ts],
+                                                [t["v_cache"] for t in ts], chunk_size=chunk,
+                                                workspace=ws, io=io, d_status=status)
+            sets.append((h, io, g))
+        else:
+            hios = []
+            for x in inps:
+                h = B.HostIo(M, H, Hkv, D)
+                h.q.copy_(f32(x.q))
+                h.k_rows.copy_(f32(x.k_rows))
+                h.v_rows.copy_(f32(x.v_rows))
+                h.positions.copy_(torch.from_numpy(np.ascontiguousarray(x.positions, np.int32)))
+                hios.append(h)
+            sets.append((hios, B.step_io(M, H, Hkv, D, device=dev), None))
+    if graph:
+        h2d, d2h = sets[0][0].in_bytes, sets[0][0].out_bytes
+    else:
+        h2d = sum(h.in_bytes for h in sets[0][0])
+        d2h = sum(h.out_bytes for h in sets[0][0])
     done = [None, None]
 
     def e2e_step(k):
         b = k % 2
         if done[b] is not None:
             done[b].synchronize()  # that set's previous output is on the host
-        hios, io = sets[b]
-        for l, t in enumerate(ts):
-            B.kvs_decode_step_host_io(hios[l], t["k_cache"], t["v_cache"], chunk_size=chunk,
-                                      workspace=ws, io=io, d_status=status, stream=stream)
+        hios, io, g = sets[b]
+        if g is not None:
+            g.launch(stream)
+        else:
+            for l, t in enumerate(ts):
+                B.kvs_decode_step_host_io(hios[l], t["k_cache"], t["v_cache"], chunk_size=chunk,
+                                          workspace=ws, io=io, d_status=status, stream=stream)
         ev = torch.cuda.Event()
         ev.record(stream)
         done[b] = ev
@@ -717,7 +743,10 @@ def measure_e2e(ctx, w, ts, inps, ws, chunk, status, scrub, warmup, Ke, step_byt
     return {"value": bytes_all / (e2e_ms_max * Ke * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": e2e_ms_max, "steps": Ke,
-            "api": "kvs_decode_step_host_io, one call per layer; two buffer sets in alternation"}
+            "api": ("kvs_step_graph_create_host_io, one graph launch a step (one copy in, the "
+                    "layers, one copy out)" if graph else
+                    "kvs_decode_step_host_io, one call per layer") +
+                   "; two buffer sets in alternation"}
 
 
 def brief(res):
