@@ -15,14 +15,18 @@
 //    K-adjacent ones 128 B apart); V is stored transposed (head_dim rows of
 //    128 keys), so that P V is again a K-major product.  Every tile is one
 //    contiguous block, moved later by a single 1-D bulk copy (TMA).
-//  * Attention block = (head, two 128-row query tiles A and B), 10 warps:
-//    warpgroup 0 runs the softmax of tile A, warpgroup 1 that of tile B
-//    (thread t owns query row t, which is TMEM lane t), warp 8 issues the
-//    tensor-core work (tcgen05.mma, M = 128, K = 16, FP32 accumulators in
-//    TMEM, completion by tcgen05.commit on mbarriers) in the order
-//    P V_A(kt), S_A(kt+1), P V_B(kt), S_B(kt+1), and warp 9 moves the tiles
-//    (K through two stages, V^T through three), so one tile's softmax runs
-//    while the other tile's products are on the tensor cores.
+//  * Attention work item = (head, two 128-row query tiles A and B); a
+//    persistent grid of one 10-warp block per SM walks the items, longest
+//    first, in a snake order across the blocks.  Warpgroup 0 runs the
+//    softmax of tile A, warpgroup 1 that of tile B (thread t owns query row
+//    t, which is TMEM lane t), warp 8 issues the tensor-core work
+//    (tcgen05.mma, M = 128, K = 16, FP32 accumulators in TMEM, completion by
+//    tcgen05.commit on mbarriers) in the order P V_A(kt), S_A(kt+1),
+//    P V_B(kt), S_B(kt+1), and warp 9 moves the tiles (K through two stages,
+//    V^T through three), so one tile's softmax runs while the other tile's
+//    products are on the tensor cores.  The barriers count on across items:
+//    the next item's tiles load and its first products run while the
+//    softmax warps write the current item's output.
 //  * Softmax: each thread reads its score row from TMEM (tcgen05.ld 32x32b,
 //    64 columns at a time) once: p = 2^(s - m) on the special-function unit
 //    against a reference maximum, rounded to FP16 and written back over
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(256)
   allow_dependent_launch();
 }
 
-// Block layout: two 128-row query tiles (A = 2b, B = 2b + 1) share every K
+// Block layout: two 128-row query tiles (A = qa, B = qa + 1) share every K
 // and V^T tile.  Warpgroup 0 does the softmax of tile A, warpgroup 1 that of
 // tile B (thread t of a warpgroup owns row t, TMEM lane t), warp 8 issues
 // the tensor-core work and warp 9 moves the tiles, so one tile's softmax
@@ -316,6 +320,12 @@ __global__ void __launch_bounds__(256)
 // O_B [256 + D, 256 + 2D).  The softmax writes P_x in FP16 over the first
 // 64 columns of S_x (two values per column) and P V reads it from there, so
 // no shared memory holds P; K has two stages and V^T three.
+//
+// The grid is persistent: one block per SM walks a list of items (head,
+// pair of query tiles).  Its barriers keep counting from one item to the
+// next, so the copy warp loads the next item's Q and first K and V^T tiles,
+// and the tensor-core warp starts its S products, while the softmax warps
+// still write the current item's output rows.
 constexpr int kPWarpgroups = 2;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kPMmaWarp = 4 * kPWarpgroups;            // warp 8
@@ -332,8 +342,9 @@ struct PGeo {
   static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + KS * TILE;
   static constexpr int OFF_BAR = OFF_V + VS * TILE;
-  // barriers: q, kfull[KS], kfree[KS], vfull[VS], vfree[VS], sfull[2], pfull[2], pvdone
-  static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 5;
+  // barriers: q, qfree, kfull[KS], kfree[KS], vfull[VS], vfree[VS], sfull[2],
+  // pfull[2], pvdone, odone[2]
+  static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 7;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;    // TMEM base address
   static constexpr int OFF_FLAG = OFF_TMEM + 8;          // abort
   // A block holds all 512 TMEM columns, so a second block on the SM would
@@ -344,43 +355,65 @@ struct PGeo {
   static_assert(SMEM_BYTES <= 227 * 1024, "one block per SM must fit");
 };
 
+// One work item: head h and the query tiles qa (A) and qa + 1 (B, absent
+// when qa + 1 == T), with the key tiles each attends.
+struct PItem {
+  int h, qa, n_a, n_b, n_all;
+  bool has_b;
+};
+
+// Item idx of the list: head fastest; with the causal mask, the pairs with
+// the most key tiles first (longest first across the blocks).
+__device__ __forceinline__ PItem prefill_item(int idx, int H, int T, int causal) {
+  PItem it;
+  const int pr = idx / H;
+  it.h = idx - pr * H;
+  it.qa = 2 * (causal ? (T + 1) / 2 - 1 - pr : pr);
+  it.has_b = it.qa + 1 < T;
+  it.n_a = causal ? it.qa + 1 : T;
+  it.n_b = it.has_b ? (causal ? it.qa + 2 : T) : 0;
+  it.n_all = it.n_a > it.n_b ? it.n_a : it.n_b;
+  return it;
+}
+
+// Item of round r for block b of P: rounds of P consecutive items, the
+// block order reversed every other round (a snake), so that the heavy and
+// the light end of the longest-first list even out across the blocks
+// (within 2 % of a greedy dynamic schedule for the causal case).  Indexes
+// only grow with r, so the first one past the list ends the walk.
+__device__ __forceinline__ int prefill_item_index(int b, int r, int P) {
+  return r * P + ((r & 1) ? P - 1 - b : b);
+}
+
 template <int D, bool kPoll>
 __global__ void __launch_bounds__(kPBlockThreads, 1)
-    prefill_tc_kernel(const unsigned char *__restrict__ ws, float *__restrict__ out, int S,
+    prefill_tc_kernel(const unsigned char *__restrict__ ws, float *__restrict__ out, int H, int S,
                       int causal, float sl2, int *d_status) {
   using PG = PGeo<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PG::OFF_BAR);
   constexpr int KS = PG::KS, VS = PG::VS;
-  uint64_t *bar_q = bars + 0;
-  uint64_t *kfull = bar_q + 1;     // [KS] K stage landed
+  uint64_t *bar_q = bars + 0;      // Q_A, Q_B of the item landed
+  uint64_t *qfree = bar_q + 1;     // the item's S products done (commit): Q may be replaced
+  uint64_t *kfull = qfree + 1;     // [KS] K stage landed
   uint64_t *kfree = kfull + KS;    // [KS] the S products reading a K stage done (commit)
   uint64_t *vfull = kfree + KS;    // [VS] V^T stage landed
   uint64_t *vfree = vfull + VS;    // [VS] the P V products reading a V^T stage done (commit)
   uint64_t *sfull = vfree + VS;    // [2] S_x ready (commit)
   uint64_t *pfull = sfull + 2;     // [2] P_x written, O_x rescaled (128 arrivals)
   uint64_t *pvdone = pfull + 2;    // every product issued so far is done (commit)
+  uint64_t *odone = pvdone + 1;    // [2] the item's last P V_x done: O_x final (commit)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PG::OFF_TMEM);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + PG::OFF_FLAG);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // grid (H, pairs): blocks launch in linear order, head fastest, so every
-  // head's heaviest query-tile pair goes first (longest first across heads)
-  const int h = blockIdx.x;
   const int T = (S + kPN - 1) / kPN;   // query tiles = key tiles
-  // tile A; tile B = qa + 1 (absent when qa + 1 == T).  Causal blocks with
-  // the most key tiles are launched first.
-  const int qa = 2 * (causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y);
-  const bool has_b = qa + 1 < T;
-  const int n_a = causal ? qa + 1 : T;            // key tiles tile A attends
-  const int n_b = has_b ? (causal ? qa + 2 : T) : 0;
-  const int n_all = n_a > n_b ? n_a : n_b;
+  const int NI = H * ((T + 1) / 2);    // items
+  const int P = (int)gridDim.x;
+  const int b = (int)blockIdx.x;
   const size_t tile = (size_t)PG::TILE;
-  const size_t per_tensor = (size_t)gridDim.x * T * tile;
-  const unsigned char *gQh = ws + (size_t)h * T * tile;
-  const unsigned char *gKh = ws + per_tensor + (size_t)h * T * tile;
-  const unsigned char *gVh = ws + 2 * per_tensor + (size_t)h * T * tile;
+  const size_t per_tensor = (size_t)H * T * tile;
 
   constexpr uint32_t kIdescS = idesc_f16_f32(kPM, kPN);
   constexpr uint32_t kIdescO = idesc_f16_f32(kPM, D);
@@ -394,6 +427,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
+    mbar_init(qfree, 1);
     for (int j = 0; j < KS; ++j) {
       mbar_init(&kfull[j], 1);
       mbar_init(&kfree[j], 1);
@@ -407,6 +441,8 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       mbar_init(&pfull[x], kPM);
     }
     mbar_init(pvdone, 1);
+    mbar_init(&odone[0], 1);
+    mbar_init(&odone[1], 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -415,43 +451,58 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
-  float l = 0.f;  // softmax threads: the row's sum of 2^(s - m)
 
   if (warp == kPCopyWarp) {
     // ======================= copies ==========================================
-    // K(n) goes to stage n % KS once the S products of K(n - KS) are done,
-    // V^T(n) to stage n % VS once the P V products of V^T(n - VS) are.
+    // Tiles are counted over all items: K tile number nk goes to stage
+    // nk % KS once the S products of tile nk - KS are done, V^T tile nv to
+    // stage nv % VS once the P V products of tile nv - VS are.  Item j's Q
+    // replaces item j - 1's once the S products of item j - 1 are done.
     if (lane == 0) {
       unsigned char *sQ = smem + PG::OFF_Q;
       unsigned char *sK = smem + PG::OFF_K;
       unsigned char *sV = smem + PG::OFF_V;
-      mbar_arrive_expect_tx(bar_q, (has_b ? 2 : 1) * PG::TILE);
-      bulk_g2s(sQ, gQh + (size_t)qa * tile, PG::TILE, bar_q);
-      if (has_b) bulk_g2s(sQ + PG::TILE, gQh + (size_t)(qa + 1) * tile, PG::TILE, bar_q);
       int nk = 0, nv = 0;  // K and V^T tiles issued
+      int jq = -1;         // the last item whose Q was issued
       bool ok = true;
-      for (int n = 0; n < n_all; ++n) {
-        const int ks = n % KS, vs = n % VS;
-        if (n >= KS && !(ok = mbar_wait<kPoll>(&kfree[ks], (uint32_t)((n - KS) / KS) & 1u, abort)))
-          break;
-        mbar_arrive_expect_tx(&kfull[ks], PG::TILE);
-        bulk_g2s(sK + ks * PG::TILE, gKh + (size_t)n * tile, PG::TILE, &kfull[ks]);
-        nk = n + 1;
-        if (n >= VS && !(ok = mbar_wait<kPoll>(&vfree[vs], (uint32_t)((n - VS) / VS) & 1u, abort)))
-          break;
-        mbar_arrive_expect_tx(&vfull[vs], PG::TILE);
-        bulk_g2s(sV + vs * PG::TILE, gVh + (size_t)n * tile, PG::TILE, &vfull[vs]);
-        nv = n + 1;
+      for (int rd = 0; ok; ++rd) {
+        const int idx = prefill_item_index(b, rd, P);
+        if (idx >= NI) break;
+        const PItem it = prefill_item(idx, H, T, causal);
+        const unsigned char *gQh = ws + (size_t)it.h * T * tile;
+        const unsigned char *gKh = gQh + per_tensor;
+        const unsigned char *gVh = gQh + 2 * per_tensor;
+        if (rd > 0 && !(ok = mbar_wait<kPoll>(qfree, (uint32_t)(rd - 1) & 1u, abort))) break;
+        mbar_arrive_expect_tx(bar_q, (it.has_b ? 2 : 1) * PG::TILE);
+        bulk_g2s(sQ, gQh + (size_t)it.qa * tile, PG::TILE, bar_q);
+        if (it.has_b) bulk_g2s(sQ + PG::TILE, gQh + (size_t)(it.qa + 1) * tile, PG::TILE, bar_q);
+        jq = rd;
+        for (int n = 0; n < it.n_all; ++n) {
+          const int ks = nk % KS, vs = nv % VS;
+          if (nk >= KS &&
+              !(ok = mbar_wait<kPoll>(&kfree[ks], (uint32_t)((nk - KS) / KS) & 1u, abort)))
+            break;
+          mbar_arrive_expect_tx(&kfull[ks], PG::TILE);
+          bulk_g2s(sK + ks * PG::TILE, gKh + (size_t)n * tile, PG::TILE, &kfull[ks]);
+          ++nk;
+          if (nv >= VS &&
+              !(ok = mbar_wait<kPoll>(&vfree[vs], (uint32_t)((nv - VS) / VS) & 1u, abort)))
+            break;
+          mbar_arrive_expect_tx(&vfull[vs], PG::TILE);
+          bulk_g2s(sV + vs * PG::TILE, gVh + (size_t)n * tile, PG::TILE, &vfull[vs]);
+          ++nv;
+        }
       }
       if (!ok) {
         *abort = 1;
         record_status(d_status, KVS_ERR_TIMEOUT);
       }
       // Every copy issued lands before the block can exit, also when another
-      // role gave up and no longer waits for it.  The last KS K tiles and VS
-      // V^T tiles are the latest use of each stage (earlier ones landed
-      // before their stage was refilled), so each wait is for its own phase.
-      mbar_wait_drain(bar_q, 0);
+      // role gave up and no longer waits for it.  Only the latest Q load and
+      // the last KS K tiles and VS V^T tiles can still be in flight (an
+      // earlier one landed before its slot was refilled), so each wait is
+      // for its own phase.
+      if (jq >= 0) mbar_wait_drain(bar_q, (uint32_t)jq & 1u);
       for (int j = (nk > KS ? nk - KS : 0); j < nk; ++j)
         mbar_wait_drain(&kfull[j % KS], (uint32_t)(j / KS) & 1u);
       for (int j = (nv > VS ? nv - VS : 0); j < nv; ++j)
@@ -467,73 +518,99 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
       const uint64_t dk0 = smem_desc(smem + PG::OFF_K, 128, kSboD);
       const uint64_t dv0 = smem_desc(smem + PG::OFF_V, 128, kSboN);
       constexpr uint64_t kTileStep = PG::TILE >> 4;  // one tile further on
-      auto issue_s = [&](int x, int n) {  // S_x(n) = Q_x K(n)^T
-        const uint64_t a = dq0 + (x ? kTileStep : 0), b = dk0 + (uint64_t)(n % KS) * kTileStep;
-        const uint32_t d = tmem + x * kPN;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_f16(d, a + 16 * ks, b + 16 * ks, kIdescS, ks > 0 ? 1u : 0u);
-        mma_commit(&sfull[x]);
-      };
-      auto issue_pv = [&](int x, int n) {  // O_x (+)= P_x(n) V^T(n), P_x from TMEM
-        const uint64_t b = dv0 + (uint64_t)(n % VS) * kTileStep;
-        const uint32_t d = tmem + 2 * kPN + x * D;
-        const uint32_t a = tmem + x * kPN;
-#pragma unroll
-        for (int ks = 0; ks < kPN / 16; ++ks)
-          mma_f16_ts(d, a + ks * 8, b + 16 * ks, kIdescO, (n > 0 || ks > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait<kPoll>(bar_q, 0, abort) && mbar_wait<kPoll>(&kfull[0], 0, abort);
+      int gk = 0, gv = 0;      // K and V^T tile numbers of the item's tile 0
+      int sb[2] = {0, 0};      // S_x products of the earlier items
+      uint32_t pv_phase = 0;
+      bool ok = true;
       bool issued = false;   // products issued since the last completed pvdone wait
       bool pending = false;  // a commit on pvdone whose wait did not complete
-      if (ok) {
+      for (int rd = 0; ok; ++rd) {
+        const int idx = prefill_item_index(b, rd, P);
+        if (idx >= NI) break;
+        const PItem it = prefill_item(idx, H, T, causal);
+        auto issue_s = [&](int x, int n) {  // S_x(n) = Q_x K(n)^T
+          const uint64_t a = dq0 + (x ? kTileStep : 0);
+          const uint64_t bk = dk0 + (uint64_t)((gk + n) % KS) * kTileStep;
+          const uint32_t d = tmem + x * kPN;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_f16(d, a + 16 * ks, bk + 16 * ks, kIdescS, ks > 0 ? 1u : 0u);
+          mma_commit(&sfull[x]);
+        };
+        auto issue_pv = [&](int x, int n) {  // O_x (+)= P_x(n) V^T(n), P_x from TMEM
+          const uint64_t bv = dv0 + (uint64_t)((gv + n) % VS) * kTileStep;
+          const uint32_t d = tmem + 2 * kPN + x * D;
+          const uint32_t a = tmem + x * kPN;
+#pragma unroll
+          for (int ks = 0; ks < kPN / 16; ++ks)
+            mma_f16_ts(d, a + ks * 8, bv + 16 * ks, kIdescO, (n > 0 || ks > 0) ? 1u : 0u);
+        };
+        ok = mbar_wait<kPoll>(bar_q, (uint32_t)rd & 1u, abort) &&
+             mbar_wait<kPoll>(&kfull[gk % KS], (uint32_t)(gk / KS) & 1u, abort);
+        if (!ok) break;
         tc_fence_after();
-        if (n_a > 0) issue_s(0, 0);
-        if (n_b > 0) issue_s(1, 0);
-        mma_commit(&kfree[0]);
+        issue_s(0, 0);
+        if (it.n_b > 0) issue_s(1, 0);
+        mma_commit(&kfree[gk % KS]);
+        if (it.n_all == 1) mma_commit(qfree);
         issued = true;
-      }
-      uint32_t pv_phase = 0;
-      for (int kt = 0; kt < n_all && ok; ++kt) {
-        const uint32_t ph = (uint32_t)kt & 1u;
-        ok = mbar_wait<kPoll>(&vfull[kt % VS], (uint32_t)(kt / VS) & 1u, abort);  // V^T(kt)
-        bool k_next = false;  // K(kt+1) has landed
-        for (int x = 0; x < 2 && ok; ++x) {
-          const int n_x = x == 0 ? n_a : n_b;
-          if (kt < n_x) {  // P V_x(kt), once softmax x(kt) has written P_x
-            ok = mbar_wait<kPoll>(&pfull[x], ph, abort);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(x, kt);
-            issued = true;
-          }
-          if (kt + 1 < n_x) {  // S_x(kt+1) overwrites P_x(kt): after P V_x(kt)
-            mma_commit(pvdone);
-            ok = mbar_wait<kPoll>(pvdone, pv_phase, abort);
-            if (!ok) {
-              pending = true;
-              break;
-            }
-            pv_phase ^= 1u;
-            issued = false;
-            if (!k_next) {
-              ok = mbar_wait<kPoll>(&kfull[(kt + 1) % KS], (uint32_t)((kt + 1) / KS) & 1u, abort);
+        for (int kt = 0; kt < it.n_all && ok; ++kt) {
+          const int gvk = gv + kt;
+          ok = mbar_wait<kPoll>(&vfull[gvk % VS], (uint32_t)(gvk / VS) & 1u, abort);  // V^T(kt)
+          bool k_next = false;  // K(kt+1) has landed
+          for (int x = 0; x < 2 && ok; ++x) {
+            const int n_x = x == 0 ? it.n_a : it.n_b;
+            if (kt < n_x) {  // P V_x(kt), once softmax x(kt) has written P_x
+              ok = mbar_wait<kPoll>(&pfull[x], (uint32_t)(sb[x] + kt) & 1u, abort);
               if (!ok) break;
               tc_fence_after();
-              k_next = true;
+              issue_pv(x, kt);
+              issued = true;
+              // O_x is final once its last product is done.  (A tile without
+              // products gets no commit, and its softmax warps no wait, so
+              // they never fall a phase behind.)
+              if (kt + 1 == n_x) mma_commit(&odone[x]);
             }
-            issue_s(x, kt + 1);
-            issued = true;
+            if (kt + 1 < n_x) {  // S_x(kt+1) overwrites P_x(kt): after P V_x(kt)
+              mma_commit(pvdone);
+              ok = mbar_wait<kPoll>(pvdone, pv_phase, abort);
+              if (!ok) {
+                pending = true;
+                break;
+              }
+              pv_phase ^= 1u;
+              issued = false;
+              if (!k_next) {
+                const int gkn = gk + kt + 1;
+                ok = mbar_wait<kPoll>(&kfull[gkn % KS], (uint32_t)(gkn / KS) & 1u, abort);
+                if (!ok) break;
+                tc_fence_after();
+                k_next = true;
+              }
+              issue_s(x, kt + 1);
+              issued = true;
+            }
           }
+          if (!ok) break;
+          mma_commit(&vfree[gvk % VS]);                                   // P V(kt)
+          if (kt + 1 < it.n_all) mma_commit(&kfree[(gk + kt + 1) % KS]);  // S(kt+1)
+          if (kt + 2 == it.n_all) mma_commit(qfree);  // the item's last S products
         }
         if (!ok) break;
-        mma_commit(&vfree[kt % VS]);        // P V(kt)
-        mma_commit(&kfree[(kt + 1) % KS]);  // S(kt+1)
-      }
-      if (ok) {  // the last P V products
+        // the item's last P V products done: the next item's S_x may
+        // overwrite P_x
         mma_commit(pvdone);
         ok = mbar_wait<kPoll>(pvdone, pv_phase, abort);
-        if (!ok) pending = true;
+        if (!ok) {
+          pending = true;
+          break;
+        }
+        pv_phase ^= 1u;
+        issued = false;
+        gk += it.n_all;
+        gv += it.n_all;
+        sb[0] += it.n_a;
+        sb[1] += it.n_b;
       }
       if (!ok) {
         *abort = 1;
@@ -554,149 +631,153 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
     // ======================= softmax of tile x ===============================
     const int x = warp >> 2;             // warpgroup
     const int t = threadIdx.x & 127;     // row within the tile
-    const int q_tile = qa + x;
-    const int i = q_tile * kPM + t;      // query row
-    const int n_x = x == 0 ? n_a : n_b;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tm_s = tmem + lane_base + x * kPN;
     const uint32_t tm_o = tmem + lane_base + 2 * kPN + x * D;
-    float m = neg_inf_f();
-    for (int kt = 0; kt < n_x; ++kt) {
-      const int key0 = kt * kPN;
-      const uint32_t ph = (uint32_t)kt & 1u;
-      // S_x(kt) is ready; it was issued after P V_x(kt-1) completed, so O_x
-      // is quiescent too
-      // all lanes of the warp leave together: the TMEM loads and stores
-      // below are .sync.aligned (the whole warp executes them)
-      if (!__all_sync(0xffffffffu, mbar_wait<kPoll>(&sfull[x], ph, abort))) {
+    int sb = 0;  // S_x products of the earlier items
+    int ob = 0;  // earlier items with a tile x (odone[x] phases)
+    for (int rd = 0; !failed; ++rd) {
+      const int idx = prefill_item_index(b, rd, P);
+      if (idx >= NI) break;
+      const PItem it = prefill_item(idx, H, T, causal);
+      const int q_tile = it.qa + x;
+      const int i = q_tile * kPM + t;      // query row
+      const int n_x = x == 0 ? it.n_a : it.n_b;
+      float m = neg_inf_f();
+      float l = 0.f;  // the row's sum of 2^(s - m)
+      for (int kt = 0; kt < n_x; ++kt) {
+        const int key0 = kt * kPN;
+        const uint32_t ph = (uint32_t)(sb + kt) & 1u;
+        // S_x(kt) is ready; it was issued after P V_x(kt-1) completed, so O_x
+        // is quiescent too
+        // all lanes of the warp leave together: the TMEM loads and stores
+        // below are .sync.aligned (the whole warp executes them)
+        if (!__all_sync(0xffffffffu, mbar_wait<kPoll>(&sfull[x], ph, abort))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        // keys needing a mask: past S, or past the row on the diagonal tile
+        const bool masked = (key0 + kPN > S) || (causal && kt == q_tile);
+        // ---- one pass over the scores, in two chunks of 64 keys ----
+        // The reference maximum m_ref only moves when a chunk's maximum exceeds
+        // it by more than kRescaleLog2 (log2 units): below that, p = 2^(s - m_ref)
+        // stays under 2^kRescaleLog2 (FP16 holds it), the result is the same,
+        // and nothing needs rescaling.  P of chunk c (FP16, two keys per
+        // column) goes to columns [32c, 32c + 32), whose scores were read with
+        // chunk 0.  When chunk 1 moves m_ref, chunk 0's P (already in TMEM) is
+        // scaled by the power of two 2^(old - new): exact in FP16 down to the
+        // subnormals, where it rounds like a direct evaluation would.
+        // (Every row attends a key in chunk 0: key0 <= row on the diagonal
+        // tile, and key0 < S.)
+        float m_ref = m;
+        float lt = 0.f;
+#pragma unroll 1
+        for (int ch = 0; ch < kPN / 64; ++ch) {
+          float r[64];
+          tmem_ld64(tm_s + ch * 64, r);
+          tmem_wait_ld();
+          if (masked) {
+            mask_keys(*reinterpret_cast<float(*)[32]>(&r[0]), key0 + ch * 64, S, causal, i);
+            mask_keys(*reinterpret_cast<float(*)[32]>(&r[32]), key0 + ch * 64 + 32, S, causal, i);
+          }
+          // chunk maximum as a tree (max is exact in any order; a chain of 64
+          // dependent fmaxf would sit on the tile's critical path)
+          float mx[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) mx[u] = fmaxf(r[u], r[u + 32]);
+#pragma unroll
+          for (int w2 = 16; w2 >= 1; w2 >>= 1) {
+#pragma unroll
+            for (int u = 0; u < w2; ++u) mx[u] = fmaxf(mx[u], mx[u + w2]);
+          }
+          float cm = mx[0] * sl2;
+          const float m_prev = m_ref;
+          if (cm > m_ref + kRescaleLog2) m_ref = cm;
+          if (ch > 0 && __any_sync(0xffffffffu, m_ref != m_prev)) {  // rare
+            const float f = (m_ref != m_prev) ? ex2(m_prev - m_ref) : 1.f;
+            lt *= f;
+            const __half2 f2 = __float2half2_rn(f);
+            uint32_t w0[32];
+            tmem_wait_st();  // chunk 0's P has landed
+            tmem_ld32u(tm_s, w0);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+              const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&w0[u]), f2);
+              w0[u] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+            tmem_st32u(tm_s, w0);
+          }
+          const float mb = (m_ref == neg_inf_f()) ? 0.f : m_ref;
+          uint32_t w[32];
+          // Two keys per paired FP32 instruction for the scaling and the sum
+          // (each key rounds as it would alone): the softmax is bound by
+          // instruction issue, not by the exponentials.  The sum runs in two
+          // independent pairs (one dependent chain would sit on the critical
+          // path).
+          float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          const float2 sl2x2 = make_float2(sl2, sl2), nmb2 = make_float2(-mb, -mb);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float2 x2 = __ffma2_rn(make_float2(r[2 * u], r[2 * u + 1]), sl2x2, nmb2);
+            const float p0 = ex2(x2.x), p1 = ex2(x2.y);
+            const __half2 hp = __floats2half2_rn(p0, p1);
+            ls[u & 1] = __fadd2_rn(ls[u & 1], make_float2(p0, p1));
+            w[u] = *reinterpret_cast<const uint32_t *>(&hp);
+          }
+          lt += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
+          tmem_st32u(tm_s + ch * 32, w);
+        }
+        const float m_new = m_ref;
+        const float alpha = (m == neg_inf_f()) ? 1.f : ex2(m - m_new);
+        // ---- rescale the output accumulator (TMEM) where the maximum moved ----
+        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float r[32];
+            tmem_ld32(tm_o + c * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) r[u] *= alpha;
+            tmem_st32(tm_o + c * 32, r);
+          }
+        }
+        l = l * alpha + lt;
+        m = m_new;
+        tmem_wait_st();  // P and the rescaled O are in TMEM before P V reads them
+        tc_fence_before();
+        mbar_arrive(&pfull[x]);
+      }
+      if (failed) break;
+      sb += n_x;
+      if (n_x == 0) continue;
+      // the tile's last P V product is done: O_x is final.  Its rows go out
+      // while the tensor cores already work on the next item's S products.
+      if (!__all_sync(0xffffffffu, mbar_wait<kPoll>(&odone[x], (uint32_t)ob & 1u, abort))) {
         failed = true;
         break;
       }
+      ++ob;
       tc_fence_after();
-      // keys needing a mask: past S, or past the row on the diagonal tile
-      const bool masked = (key0 + kPN > S) || (causal && kt == q_tile);
-      // ---- one pass over the scores, in two chunks of 64 keys ----
-      // The reference maximum m_ref only moves when a chunk's maximum exceeds
-      // it by more than kRescaleLog2 (log2 units): below that, p = 2^(s - m_ref)
-      // stays under 2^kRescaleLog2 (FP16 holds it), the result is the same,
-      // and nothing needs rescaling.  P of chunk c (FP16, two keys per
-      // column) goes to columns [32c, 32c + 32), whose scores were read with
-      // chunk 0.  When chunk 1 moves m_ref, chunk 0's P (already in TMEM) is
-      // scaled by the power of two 2^(old - new): exact in FP16 down to the
-      // subnormals, where it rounds like a direct evaluation would.
-      // (Every row attends a key in chunk 0: key0 <= row on the diagonal
-      // tile, and key0 < S.)
-      float m_ref = m;
-      float lt = 0.f;
-#pragma unroll 1
-      for (int ch = 0; ch < kPN / 64; ++ch) {
-        float r[64];
-        tmem_ld64(tm_s + ch * 64, r);
-        tmem_wait_ld();
-        if (masked) {
-          mask_keys(*reinterpret_cast<float(*)[32]>(&r[0]), key0 + ch * 64, S, causal, i);
-          mask_keys(*reinterpret_cast<float(*)[32]>(&r[32]), key0 + ch * 64 + 32, S, causal, i);
-        }
-        // chunk maximum as a tree (max is exact in any order; a chain of 64
-        // dependent fmaxf would sit on the tile's critical path)
-        float mx[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) mx[u] = fmaxf(r[u], r[u + 32]);
-#pragma unroll
-        for (int w2 = 16; w2 >= 1; w2 >>= 1) {
-#pragma unroll
-          for (int u = 0; u < w2; ++u) mx[u] = fmaxf(mx[u], mx[u + w2]);
-        }
-        float cm = mx[0] * sl2;
-        const float m_prev = m_ref;
-        if (cm > m_ref + kRescaleLog2) m_ref = cm;
-        if (ch > 0 && __any_sync(0xffffffffu, m_ref != m_prev)) {  // rare
-          const float f = (m_ref != m_prev) ? ex2(m_prev - m_ref) : 1.f;
-          lt *= f;
-          const __half2 f2 = __float2half2_rn(f);
-          uint32_t w0[32];
-          tmem_wait_st();  // chunk 0's P has landed
-          tmem_ld32u(tm_s, w0);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&w0[u]), f2);
-            w0[u] = *reinterpret_cast<const uint32_t *>(&v);
-          }
-          tmem_st32u(tm_s, w0);
-        }
-        const float mb = (m_ref == neg_inf_f()) ? 0.f : m_ref;
-        uint32_t w[32];
-        // Two keys per paired FP32 instruction for the scaling and the sum
-        // (each key rounds as it would alone): the softmax is bound by
-        // instruction issue, not by the exponentials.  The sum runs in two
-        // independent pairs (one dependent chain would sit on the critical
-        // path).
-        float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        const float2 sl2x2 = make_float2(sl2, sl2), nmb2 = make_float2(-mb, -mb);
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float2 x2 = __ffma2_rn(make_float2(r[2 * u], r[2 * u + 1]), sl2x2, nmb2);
-          const float p0 = ex2(x2.x), p1 = ex2(x2.y);
-          const __half2 hp = __floats2half2_rn(p0, p1);
-          ls[u & 1] = __fadd2_rn(ls[u & 1], make_float2(p0, p1));
-          w[u] = *reinterpret_cast<const uint32_t *>(&hp);
-        }
-        lt += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
-        tmem_st32u(tm_s + ch * 32, w);
-      }
-      const float m_new = m_ref;
-      const float alpha = (m == neg_inf_f()) ? 1.f : ex2(m - m_new);
-      // ---- rescale the output accumulator (TMEM) where the maximum moved ----
-      if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float r[32];
-          tmem_ld32(tm_o + c * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 32; ++u) r[u] *= alpha;
-          tmem_st32(tm_o + c * 32, r);
-        }
-      }
-      l = l * alpha + lt;
-      m = m_new;
-      tmem_wait_st();  // P and the rescaled O are in TMEM before P V reads them
-      tc_fence_before();
-      mbar_arrive(&pfull[x]);
-    }
-    // the rows are written after the block-wide barrier below, which the
-    // tensor-core warp reaches once the last P V products are done
-    if (failed) {
-      *abort = 1;
-      record_status(d_status, KVS_ERR_TIMEOUT);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp < kPMmaWarp && !failed && !*abort) {
-    const int x = warp >> 2;
-    const int t = threadIdx.x & 127;
-    const int i = (qa + x) * kPM + t;
-    const int n_x = x == 0 ? n_a : n_b;
-    if (n_x > 0) {
-      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-      const uint32_t tm_o = tmem + lane_base + 2 * kPN + x * D;
       const float inv = 1.f / l;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
-        float r[32];
-        tmem_ld32(tm_o + ch * 32, r);
+        float o[32];
+        tmem_ld32(tm_o + ch * 32, o);
         tmem_wait_ld();
         if (i < S) {
-          float4 *o4 = reinterpret_cast<float4 *>(out + ((size_t)h * S + i) * D + ch * 32);
+          float4 *o4 = reinterpret_cast<float4 *>(out + ((size_t)it.h * S + i) * D + ch * 32);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            o4[u] = make_float4(r[4 * u] * inv, r[4 * u + 1] * inv, r[4 * u + 2] * inv,
-                                r[4 * u + 3] * inv);
+            o4[u] = make_float4(o[4 * u] * inv, o[4 * u + 1] * inv, o[4 * u + 2] * inv,
+                                o[4 * u + 3] * inv);
         }
       }
+    }
+    if (failed) {
+      *abort = 1;
+      record_status(d_status, KVS_ERR_TIMEOUT);
     }
   }
   allow_dependent_launch();
@@ -710,9 +791,16 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
                         int causal, void *workspace, int *d_status, cudaStream_t stream) {
   using PG = PGeo<D>;
   static bool configured[64] = {false};
+  static int num_sms[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVS_ERR_LAUNCH;
   if (!configured[dev]) {
+    if (cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess ||
+        num_sms[dev] < 1) {
+      cudaGetLastError();
+      return KVS_ERR_LAUNCH;
+    }
     for (auto kern : {prefill_tc_kernel<D, false>, prefill_tc_kernel<D, true>}) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                PG::SMEM_BYTES) != cudaSuccess) {
@@ -729,10 +817,14 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
   if (e != cudaSuccess) return KVS_ERR_LAUNCH;
   const float sl2 = (float)(1.4426950408889634074 / std::sqrt((double)D));
   const int T = (S + kPM - 1) / kPM;
-  const dim3 grid(H, (T + 1) / 2, 1);
-  e = launch_pdl(poll_waits() ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>, grid,
-                 dim3(kPBlockThreads), PG::SMEM_BYTES, stream,
-                 static_cast<const unsigned char *>(ws), out, S, causal, sl2, d_status);
+  // one block per SM (the shared memory and the 512 TMEM columns allow no
+  // second), each walking its share of the items; more blocks than SMs
+  // would only run one after another
+  const long long items = (long long)H * ((T + 1) / 2);
+  const int grid = (int)std::min<long long>(items, num_sms[dev]);
+  e = launch_pdl(poll_waits() ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>,
+                 dim3(grid), dim3(kPBlockThreads), PG::SMEM_BYTES, stream,
+                 static_cast<const unsigned char *>(ws), out, H, S, causal, sl2, d_status);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
