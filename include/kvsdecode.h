@@ -490,11 +490,16 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
  * product (the row sum adds them in FP32).  head_dim must be 64 or 128; any seq_len >= 1 (the pages require
  * a multiple of 16; here the last tile is masked).
  *   workspace  device scratch of >= kvs_prefill_workspace_bytes bytes,
- *              256-byte aligned: q, k and v as FP16 tiles in the tensor-core
- *              layout (3 * num_heads * ceil(seq_len/128) * 128 * head_dim * 2
- *              bytes); no initialisation needed; must not be shared by
- *              calls that can overlap on the GPU.
- * Two launches: the FP16 pack, then the attention.
+ *              256-byte aligned: a 4-byte ready flag per tile and a task
+ *              counter (3 * num_heads * T + 1 words, T = ceil(seq_len/128),
+ *              padded to a multiple of 256 bytes), then q, k and v as FP16
+ *              tiles in the tensor-core layout (3 * num_heads * T * 128 *
+ *              head_dim * 2 bytes); no initialisation needed (the call
+ *              zeroes the flags); must not be shared by calls that can
+ *              overlap on the GPU.
+ * Enqueued: a memset of the flags, an FP16 pack launch for the tiles needed
+ * first, then the attention launch, whose pack warps convert the remaining
+ * tiles while it runs.
  * Errors: DIMS (negative sizes, num_heads > 65535, seq_len > 65535 * 128),
  * UNSUPPORTED, NULL, ALIGN, WORKSPACE, LAUNCH on the host; TIMEOUT via
  * d_status.  num_heads = 0 or seq_len = 0 enqueues nothing.

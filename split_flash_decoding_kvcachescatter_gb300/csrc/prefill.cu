@@ -9,24 +9,29 @@
 // WMMA 16x16 tiles, one block of 8 warps per 16 query rows.
 //
 // GB300 design (flash-attention forward, one pass over the keys):
-//  * A pack kernel rounds q, k and v to FP16 once into the caller's
-//    workspace, already cut into 128-row tiles in the canonical no-swizzle
-//    K-major layout of the tensor cores (8-row x 16-byte core matrices,
-//    K-adjacent ones 128 B apart); V is stored transposed (head_dim rows of
-//    128 keys), so that P V is again a K-major product.  Every tile is one
-//    contiguous block, moved later by a single 1-D bulk copy (TMA).
+//  * q, k and v are rounded to FP16 once into the caller's workspace,
+//    already cut into 128-row tiles in the canonical no-swizzle K-major
+//    layout of the tensor cores (8-row x 16-byte core matrices, K-adjacent
+//    ones 128 B apart); V is stored transposed (head_dim rows of 128 keys),
+//    so that P V is again a K-major product.  Every tile is one contiguous
+//    block, moved later by a single 1-D bulk copy (TMA).  The tiles needed
+//    first (the first round's Q tiles, the first 60 % of the key tiles) are
+//    packed by a separate launch at full bandwidth; two warps of the
+//    attention kernel pack the rest while it runs, in the order the items
+//    need them, and publish each tile with a flag that the copy warp waits
+//    for.
 //  * Attention work item = (head, two 128-row query tiles A and B); a
-//    persistent grid of one 10-warp block per SM walks the items, longest
+//    persistent grid of one 12-warp block per SM walks the items, longest
 //    first, in a snake order across the blocks.  Warpgroup 0 runs the
 //    softmax of tile A, warpgroup 1 that of tile B (thread t owns query row
 //    t, which is TMEM lane t), warp 8 issues the tensor-core work
 //    (tcgen05.mma, M = 128, K = 16, FP32 accumulators in TMEM, completion by
 //    tcgen05.commit on mbarriers) in the order P V_A(kt), S_A(kt+1),
-//    P V_B(kt), S_B(kt+1), and warp 9 moves the tiles (K through two stages,
-//    V^T through three), so one tile's softmax runs while the other tile's
-//    products are on the tensor cores.  The barriers count on across items:
-//    the next item's tiles load and its first products run while the
-//    softmax warps write the current item's output.
+//    P V_B(kt), S_B(kt+1), warp 9 moves the tiles (K and V^T through two
+//    stages each), and warps 10-11 pack, so one tile's softmax runs while
+//    the other tile's products are on the tensor cores.  The barriers count
+//    on across items: the next item's tiles load and its first products run
+//    while the softmax warps write the current item's output.
 //  * Softmax: each thread reads its score row from TMEM (tcgen05.ld 32x32b,
 //    64 columns at a time) once: p = 2^(s - m) on the special-function unit
 //    against a reference maximum, rounded to FP16 and written back over
@@ -37,7 +42,7 @@
 //    rescaled.
 //  * Causal: key tiles after the query tile are skipped; keys j > i and keys
 //    past seq_len get p = 0 (selects, on the diagonal and last tiles only).
-// Every mbarrier wait is bounded; on expiry the block records
+// Every wait (mbarriers, tile flags) is bounded; on expiry the block records
 // KVS_ERR_TIMEOUT, lets its copies and tensor-core products finish, frees its
 // TMEM and returns.
 
@@ -236,43 +241,150 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
   return u;
 }
 
-// ---- pack: FP32 [H][S][D] -> FP16 tiles in the tensor-core layout ----------
-// Workspace: Q tiles, K tiles, V^T tiles, each [H][T][tile] with T =
-// ceil(S / 128) and a tile of 128 * D FP16 values (rows past S are zero).
+// ---- packing: FP32 [H][S][D] -> FP16 tiles in the tensor-core layout ------
+// Workspace: a flag per tile and a task counter (zeroed before every launch),
+// padded to 256 bytes, then the Q tiles, K tiles and V^T tiles, each
+// [H][T][tile] with T = ceil(S / 128) and a tile of 128 * D FP16 values
+// (rows past S are zero).
 __host__ __device__ constexpr size_t prefill_tile_bytes(int D) { return (size_t)kPM * D * 2; }
+__host__ __device__ constexpr size_t prefill_flag_bytes(int H, int T) {
+  return ((4 * (3 * (size_t)H * T + 1)) + 255) / 256 * 256;
+}
 
-// Grid (3 * D/16, T, H): blocks [0, D/16) convert tile t of Q, blocks
-// [D/16, 2 * D/16) tile t of K (one 16-byte chunk per thread), blocks
-// [2 * D/16, 3 * D/16) tile t of V^T, 16 of its D rows each (so every block
-// moves the same bytes).  A V^T block reads its 128 keys x 16 columns of v
-// with float4 loads into shared memory (rows padded so the transposed reads
-// are free of bank conflicts), then each thread writes one 16-byte chunk:
-// 8 keys of one column, and eight consecutive threads fill one 128-byte
-// line of a core matrix.  Consecutive threads write consecutive bytes.
+// One tile of the packing work: tensor 0 (Q), 1 (K) or 2 (V^T), head h,
+// tile t.
+struct PTile {
+  int tensor, h, t;
+};
+
+// Query tiles of the pair with rank pr in the item list (see prefill_item).
+__device__ __forceinline__ int prefill_pair_tiles(int pr, int T, int causal, int *qa) {
+  const int np = (T + 1) / 2;
+  *qa = 2 * (causal ? np - 1 - pr : pr);
+  return *qa + 1 < T ? 2 : 1;
+}
+
+// Task `task` of the in-kernel packing list, in the order the attention
+// items need the tiles: K and V^T key tile by key tile from tile s0 (tile s
+// of every head), the Q tiles of one further pair rank (from rq) after every
+// second key tile, and the Q tiles left at the end.  The Q tiles of pair
+// ranks below rq and the K and V^T tiles below s0 are packed before the
+// attention kernel starts.
+__device__ PTile prefill_task(int task, int H, int T, int causal, int rq, int s0) {
+  const int np = (T + 1) / 2;
+  int qa = 0;
+  int next = rq;
+  for (int s = s0; s < T; ++s) {
+    if (task < 2 * H) return PTile{1 + (task & 1), task >> 1, s};
+    task -= 2 * H;
+    if (((s - s0) & 1) && next < np) {
+      const int nq = prefill_pair_tiles(next, T, causal, &qa);
+      if (task < H * nq) return PTile{0, task / nq, qa + task % nq};
+      task -= H * nq;
+      ++next;
+    }
+  }
+  for (; next < np; ++next) {
+    const int nq = prefill_pair_tiles(next, T, causal, &qa);
+    if (task < H * nq) return PTile{0, task / nq, qa + task % nq};
+    task -= H * nq;
+  }
+  return PTile{0, 0, 0};  // not reached for task < the list's length
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy view of global memory with its later
+// bulk (async-proxy) copies.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Warp-collective: waits until the flag of tile n (of f[0, last)) is set.
+// Lane j reads the flag of tile n + j (acquire), so one round trip learns
+// about 32 tiles; `mask` keeps which of [base, base + 32) were seen set, and
+// a tile already seen costs nothing.  Bound and abort as in mbar_wait; the
+// outcome is the same in every lane.
+template <bool kPoll>
+__device__ __forceinline__ bool tile_wait(const unsigned *f, int n, int last, uint32_t &mask,
+                                          int &base, volatile int *abort, int lane) {
+  if (n >= base && n - base < 32 && ((mask >> (n - base)) & 1u)) return true;
+  base = n;
+  auto look = [&]() {
+    const int t = n + lane;
+    return __ballot_sync(0xffffffffu, t < last && ld_acquire_u32(f + t) != 0u);
+  };
+  mask = look();
+  if (mask & 1u) return true;
+  const uint64_t limit = kPoll ? (uint64_t)g_wait_limit_ns : kWaitLimitNs;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (!kPoll) __nanosleep(128);
+    mask = look();
+    if (mask & 1u) return true;
+    int stop = 0;
+    if (lane == 0) stop = (*abort != 0) || (global_timer_ns() - t0 >= limit);
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+  }
+}
+
+// Share of the key tiles (K and V^T) packed before the attention kernel
+// starts, in percent; the attention kernel's pack warps convert the rest
+// while it runs.  Measured on GB300 (H=32, S=4096, D=128, causal): 55 %
+// 172.9 us, 60 % 167.6, 65 % 168.2, 70 % 169.8, 100 % 179.7, 0 % 211.8;
+// the pack warps move about 1.5 TB/s beside the attention, the separate
+// launch the full bandwidth.
+constexpr int kPUpfrontKeyPct = 60;
+
+// The tiles needed first, packed at full bandwidth before the attention
+// starts: grid (pieces * D/16, H); piece z of a head is a Q tile of a pair
+// rank below rq (two per rank), then K and V^T of key tiles 0, 1, ...;
+// block j of a Q or K tile converts 256 16-byte pieces, of a V^T tile 16 of
+// its D rows (staged through shared memory).  Each tile's flag is set for
+// the attention kernel, which reads it only after this kernel completed.
 template <int D>
 __global__ void __launch_bounds__(256)
     prefill_pack_kernel(const float *__restrict__ q, const float *__restrict__ k,
-                        const float *__restrict__ v, unsigned char *__restrict__ ws, int S) {
-  constexpr int NQK = D / 16;  // blocks per Q, K or V^T tile (128 * D/8 chunks / 256)
-  constexpr int kVPad = kPN + 4;  // row stride (floats) of the V slab in shared memory
+                        const float *__restrict__ v, unsigned char *__restrict__ ws, int H, int S,
+                        int causal, int rq) {
+  constexpr int kVPad = kPN + 4;
   __shared__ __align__(16) float sv[16 * kVPad];
   grid_dependency_wait();
-  const int T = gridDim.y, H = gridDim.z;
-  const int t = blockIdx.y, h = blockIdx.z;
+  const int T = (S + kPM - 1) / kPM;
+  PTile p;
+  p.h = blockIdx.y;
+  const int z = (int)blockIdx.x / (D / 16);
+  const int bx = (int)blockIdx.x % (D / 16);
+  if (z < 2 * rq) {
+    int qa = 0;
+    const int nq = prefill_pair_tiles(z >> 1, T, causal, &qa);
+    if ((z & 1) >= nq) return;  // the pair has no tile B
+    p.tensor = 0;
+    p.t = qa + (z & 1);
+  } else {
+    p.tensor = 1 + ((z - 2 * rq) & 1);
+    p.t = (z - 2 * rq) >> 1;
+  }
   const size_t tile = prefill_tile_bytes(D);
-  const size_t ht = (size_t)h * T + t;
-  const int bx = blockIdx.x;
-  if (bx < 2 * NQK) {  // Q or K: chunk (row r, 8 columns from c)
-    const int which = bx / NQK;
-    const int w = (bx - which * NQK) * 256 + threadIdx.x;
-    // the 8 rows of a core matrix, then the next core matrix along the row
+  unsigned *flags = reinterpret_cast<unsigned *>(ws);
+  unsigned char *dst = ws + prefill_flag_bytes(H, T) + (((size_t)p.tensor * H + p.h) * T + p.t) * tile;
+  if (p.tensor < 2) {
+    const int w = bx * 256 + threadIdx.x;
     const int r = (w / (8 * (D / 8))) * 8 + (w & 7);
     const int c = ((w >> 3) % (D / 8)) * 8;
-    const int row = t * kPM + r;
+    const int row = p.t * kPM + r;
     float x[8];
     if (row < S) {
-      const float4 *src =
-          reinterpret_cast<const float4 *>((which == 0 ? q : k) + ((size_t)h * S + row) * D + c);
+      const float4 *src = reinterpret_cast<const float4 *>((p.tensor == 0 ? q : k) +
+                                                           ((size_t)p.h * S + row) * D + c);
       const float4 a = __ldcg(src), b = __ldcg(src + 1);
       x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
       x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
@@ -280,46 +392,47 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int u = 0; u < 8; ++u) x[u] = 0.f;
     }
-    unsigned char *dst = ws + ((size_t)which * H * T + ht) * tile;
     *reinterpret_cast<uint4 *>(dst + cm_off(r, c, D)) = pack8(x);
-  } else {  // V^T rows [d0, d0 + 16): keys of tile t, columns d0.. of v
-    const int d0 = (bx - 2 * NQK) * 16;
+  } else {
+    const int d0 = bx * 16;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {  // 128 keys x 4 float4 = 512 loads, 2 per thread
+    for (int u = 0; u < 2; ++u) {
       const int e = threadIdx.x + 256 * u;
       const int key = e >> 2, f4 = e & 3;
-      const int gkey = t * kPN + key;
+      const int gkey = p.t * kPN + key;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
       if (gkey < S)
-        a = __ldcg(reinterpret_cast<const float4 *>(v + ((size_t)h * S + gkey) * D + d0) + f4);
+        a = __ldcg(reinterpret_cast<const float4 *>(v + ((size_t)p.h * S + gkey) * D + d0) + f4);
       sv[(4 * f4 + 0) * kVPad + key] = a.x;
       sv[(4 * f4 + 1) * kVPad + key] = a.y;
       sv[(4 * f4 + 2) * kVPad + key] = a.z;
       sv[(4 * f4 + 3) * kVPad + key] = a.w;
     }
     __syncthreads();
-    // thread: row d0 + dr of V^T (dr = 8 * (w >> 7) + (w & 7)), keys 8g..8g+7
     const int w = threadIdx.x;
     const int dr = 8 * (w >> 7) + (w & 7);
     const int g = (w >> 3) & 15;
     const float4 *row4 = reinterpret_cast<const float4 *>(sv + dr * kVPad + 8 * g);
     const float4 a = row4[0], b = row4[1];
     const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    unsigned char *dst = ws + ((size_t)2 * H * T + ht) * tile;
     *reinterpret_cast<uint4 *>(dst + cm_off(d0 + dr, 8 * g, kPN)) = pack8(x);
   }
+  // read only after this kernel has completed (the attention's dependency wait)
+  if (bx == 0 && threadIdx.x == 0) flags[((size_t)p.tensor * H + p.h) * T + p.t] = 1u;
   allow_dependent_launch();
 }
 
 // Block layout: two 128-row query tiles (A = qa, B = qa + 1) share every K
 // and V^T tile.  Warpgroup 0 does the softmax of tile A, warpgroup 1 that of
 // tile B (thread t of a warpgroup owns row t, TMEM lane t), warp 8 issues
-// the tensor-core work and warp 9 moves the tiles, so one tile's softmax
-// runs while the other tile's products are on the tensor cores.
-// TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D),
-// O_B [256 + D, 256 + 2D).  The softmax writes P_x in FP16 over the first
-// 64 columns of S_x (two values per column) and P V reads it from there, so
-// no shared memory holds P; K has two stages and V^T three.
+// the tensor-core work, warp 9 moves the tiles and warps 10-11 pack tiles,
+// so one tile's softmax runs while the other tile's products are on the
+// tensor cores.  TMEM columns: S_A [0, 128), S_B [128, 256),
+// O_A [256, 256 + D), O_B [256 + D, 256 + 2D).  The softmax writes P_x in
+// FP16 over the first 64 columns of S_x (two values per column) and P V
+// reads it from there, so no shared memory holds P; K and V^T have two
+// stages each (a third V^T stage measured no faster), and the pack warps'
+// staging takes the room a third stage would.
 //
 // The grid is persistent: one block per SM walks a list of items (head,
 // pair of query tiles).  Its barriers keep counting from one item to the
@@ -330,7 +443,10 @@ constexpr int kPWarpgroups = 2;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kPMmaWarp = 4 * kPWarpgroups;            // warp 8
 constexpr int kPCopyWarp = kPMmaWarp + 1;              // warp 9
-constexpr int kPBlockThreads = (kPCopyWarp + 1) * 32;  // 320
+constexpr int kPPackWarp0 = kPCopyWarp + 1;            // warps 10 and 11
+constexpr int kPPackWarps = 2;
+constexpr int kPBlockThreads = (kPPackWarp0 + kPPackWarps) * 32;  // 384
+constexpr int kPStgRows = 16;                          // rows of one staged chunk
 constexpr uint32_t kPTmemCols = 512;
 
 template <int D>
@@ -338,13 +454,18 @@ struct PGeo {
   static constexpr int TILE = kPM * D * 2;  // one FP16 tile of Q, K or V^T
   static constexpr int OFF_Q = 0;                        // Q_A, Q_B
   static constexpr int KS = 2;                           // K stages
-  static constexpr int VS = 3;                           // V^T stages
+  static constexpr int VS = 2;                           // V^T stages
   static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + KS * TILE;
-  static constexpr int OFF_BAR = OFF_V + VS * TILE;
+  // staging of the pack warps: two buffers each of kPStgRows FP32 rows,
+  // padded by 16 bytes (conflict-free reads along a row and down a column)
+  static constexpr int STG_STRIDE = D + 4;                 // floats per staged row
+  static constexpr int STG_BUF = kPStgRows * STG_STRIDE * 4;
+  static constexpr int OFF_STG = OFF_V + VS * TILE;
+  static constexpr int OFF_BAR = OFF_STG + kPPackWarps * 2 * STG_BUF;
   // barriers: q, qfree, kfull[KS], kfree[KS], vfull[VS], vfree[VS], sfull[2],
-  // pfull[2], pvdone, odone[2]
-  static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 7;
+  // pfull[2], pvdone, odone[2], staging[2 * kPPackWarps]
+  static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 7 + 2 * kPPackWarps;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;    // TMEM base address
   static constexpr int OFF_FLAG = OFF_TMEM + 8;          // abort
   // A block holds all 512 TMEM columns, so a second block on the SM would
@@ -387,8 +508,10 @@ __device__ __forceinline__ int prefill_item_index(int b, int r, int P) {
 
 template <int D, bool kPoll>
 __global__ void __launch_bounds__(kPBlockThreads, 1)
-    prefill_tc_kernel(const unsigned char *__restrict__ ws, float *__restrict__ out, int H, int S,
-                      int causal, float sl2, int *d_status) {
+    prefill_tc_kernel(const float *__restrict__ q, const float *__restrict__ k,
+                      const float *__restrict__ v, unsigned char *__restrict__ ws,
+                      float *__restrict__ out, int H, int S, int causal, float sl2,
+                      int *d_status, int rq, int s0, int nt_in) {
   using PG = PGeo<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PG::OFF_BAR);
@@ -403,6 +526,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
   uint64_t *pfull = sfull + 2;     // [2] P_x written, O_x rescaled (128 arrivals)
   uint64_t *pvdone = pfull + 2;    // every product issued so far is done (commit)
   uint64_t *odone = pvdone + 1;    // [2] the item's last P V_x done: O_x final (commit)
+  uint64_t *stgfull = odone + 2;   // [2 * kPPackWarps] a staged chunk landed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PG::OFF_TMEM);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + PG::OFF_FLAG);
 
@@ -414,6 +538,8 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
   const int b = (int)blockIdx.x;
   const size_t tile = (size_t)PG::TILE;
   const size_t per_tensor = (size_t)H * T * tile;
+  unsigned *flags = reinterpret_cast<unsigned *>(ws);  // [3][H][T] tile packed, then the counter
+  unsigned char *tiles = ws + prefill_flag_bytes(H, T);
 
   constexpr uint32_t kIdescS = idesc_f16_f32(kPM, kPN);
   constexpr uint32_t kIdescO = idesc_f16_f32(kPM, D);
@@ -443,6 +569,7 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
     mbar_init(pvdone, 1);
     mbar_init(&odone[0], 1);
     mbar_init(&odone[1], 1);
+    for (int j = 0; j < 2 * kPPackWarps; ++j) mbar_init(&stgfull[j], 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -458,7 +585,9 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
     // nk % KS once the S products of tile nk - KS are done, V^T tile nv to
     // stage nv % VS once the P V products of tile nv - VS are.  Item j's Q
     // replaces item j - 1's once the S products of item j - 1 are done.
-    if (lane == 0) {
+    // The whole warp runs the loop (it reads the tile flags 32 at a time);
+    // lane 0 issues the copies.
+    {
       unsigned char *sQ = smem + PG::OFF_Q;
       unsigned char *sK = smem + PG::OFF_K;
       unsigned char *sV = smem + PG::OFF_V;
@@ -469,44 +598,72 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
         const int idx = prefill_item_index(b, rd, P);
         if (idx >= NI) break;
         const PItem it = prefill_item(idx, H, T, causal);
-        const unsigned char *gQh = ws + (size_t)it.h * T * tile;
+        const unsigned char *gQh = tiles + (size_t)it.h * T * tile;
         const unsigned char *gKh = gQh + per_tensor;
         const unsigned char *gVh = gQh + 2 * per_tensor;
-        if (rd > 0 && !(ok = mbar_wait<kPoll>(qfree, (uint32_t)(rd - 1) & 1u, abort))) break;
-        mbar_arrive_expect_tx(bar_q, (it.has_b ? 2 : 1) * PG::TILE);
-        bulk_g2s(sQ, gQh + (size_t)it.qa * tile, PG::TILE, bar_q);
-        if (it.has_b) bulk_g2s(sQ + PG::TILE, gQh + (size_t)(it.qa + 1) * tile, PG::TILE, bar_q);
+        if (rd > 0 &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait<kPoll>(qfree, (uint32_t)(rd - 1) & 1u, abort))))
+          break;
+        // a tile is bulk-copied only once a pack warp has published it
+        const unsigned *fq = flags + (size_t)it.h * T;
+        const unsigned *fk = fq + (size_t)H * T;
+        const unsigned *fv = fk + (size_t)H * T;
+        uint32_t mq = 0, mk = 0, mv = 0;
+        int bq = 0, bk = 0, bv = 0;
+        // (tiles packed before this kernel started need no look)
+        if (idx / H >= rq) {
+          if (!(ok = tile_wait<kPoll>(fq, it.qa, T, mq, bq, abort, lane))) break;
+          if (it.has_b && !(ok = tile_wait<kPoll>(fq, it.qa + 1, T, mq, bq, abort, lane))) break;
+        }
+        if (lane == 0) {
+          fence_proxy_async_global();
+          mbar_arrive_expect_tx(bar_q, (it.has_b ? 2 : 1) * PG::TILE);
+          bulk_g2s(sQ, gQh + (size_t)it.qa * tile, PG::TILE, bar_q);
+          if (it.has_b) bulk_g2s(sQ + PG::TILE, gQh + (size_t)(it.qa + 1) * tile, PG::TILE, bar_q);
+        }
         jq = rd;
         for (int n = 0; n < it.n_all; ++n) {
           const int ks = nk % KS, vs = nv % VS;
           if (nk >= KS &&
-              !(ok = mbar_wait<kPoll>(&kfree[ks], (uint32_t)((nk - KS) / KS) & 1u, abort)))
+              !(ok = __all_sync(0xffffffffu, mbar_wait<kPoll>(&kfree[ks],
+                                                               (uint32_t)((nk - KS) / KS) & 1u, abort))))
             break;
-          mbar_arrive_expect_tx(&kfull[ks], PG::TILE);
-          bulk_g2s(sK + ks * PG::TILE, gKh + (size_t)n * tile, PG::TILE, &kfull[ks]);
+          if (n >= s0 && !(ok = tile_wait<kPoll>(fk, n, it.n_all, mk, bk, abort, lane))) break;
+          if (lane == 0) {
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(&kfull[ks], PG::TILE);
+            bulk_g2s(sK + ks * PG::TILE, gKh + (size_t)n * tile, PG::TILE, &kfull[ks]);
+          }
           ++nk;
           if (nv >= VS &&
-              !(ok = mbar_wait<kPoll>(&vfree[vs], (uint32_t)((nv - VS) / VS) & 1u, abort)))
+              !(ok = __all_sync(0xffffffffu, mbar_wait<kPoll>(&vfree[vs],
+                                                               (uint32_t)((nv - VS) / VS) & 1u, abort))))
             break;
-          mbar_arrive_expect_tx(&vfull[vs], PG::TILE);
-          bulk_g2s(sV + vs * PG::TILE, gVh + (size_t)n * tile, PG::TILE, &vfull[vs]);
+          if (n >= s0 && !(ok = tile_wait<kPoll>(fv, n, it.n_all, mv, bv, abort, lane))) break;
+          if (lane == 0) {
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(&vfull[vs], PG::TILE);
+            bulk_g2s(sV + vs * PG::TILE, gVh + (size_t)n * tile, PG::TILE, &vfull[vs]);
+          }
           ++nv;
         }
       }
-      if (!ok) {
-        *abort = 1;
-        record_status(d_status, KVS_ERR_TIMEOUT);
+      if (lane == 0) {
+        if (!ok) {
+          *abort = 1;
+          record_status(d_status, KVS_ERR_TIMEOUT);
+        }
+        // Every copy issued lands before the block can exit, also when
+        // another role gave up and no longer waits for it.  Only the latest
+        // Q load and the last KS K tiles and VS V^T tiles can still be in
+        // flight (an earlier one landed before its slot was refilled), so
+        // each wait is for its own phase.
+        if (jq >= 0) mbar_wait_drain(bar_q, (uint32_t)jq & 1u);
+        for (int j = (nk > KS ? nk - KS : 0); j < nk; ++j)
+          mbar_wait_drain(&kfull[j % KS], (uint32_t)(j / KS) & 1u);
+        for (int j = (nv > VS ? nv - VS : 0); j < nv; ++j)
+          mbar_wait_drain(&vfull[j % VS], (uint32_t)(j / VS) & 1u);
       }
-      // Every copy issued lands before the block can exit, also when another
-      // role gave up and no longer waits for it.  Only the latest Q load and
-      // the last KS K tiles and VS V^T tiles can still be in flight (an
-      // earlier one landed before its slot was refilled), so each wait is
-      // for its own phase.
-      if (jq >= 0) mbar_wait_drain(bar_q, (uint32_t)jq & 1u);
-      for (int j = (nk > KS ? nk - KS : 0); j < nk; ++j)
-        mbar_wait_drain(&kfull[j % KS], (uint32_t)(j / KS) & 1u);
-      for (int j = (nv > VS ? nv - VS : 0); j < nv; ++j)
-        mbar_wait_drain(&vfull[j % VS], (uint32_t)(j / VS) & 1u);
     }
     __syncwarp();
   } else if (warp == kPMmaWarp) {
@@ -626,6 +783,140 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
         if (pending) mbar_wait_drain(pvdone, pv_phase);
       }
     }
+    __syncwarp();
+  } else if (warp >= kPPackWarp0) {
+    // ======================= packing =========================================
+    // Each pack warp takes tiles from the task list (one atomicAdd per tile,
+    // fetched a tile ahead) and moves a tile as 8 chunks of 16 rows: lane 0
+    // bulk-copies the FP32 rows into a staging buffer (rows padded by 16
+    // bytes), the warp rounds them to FP16 and stores 16-byte pieces in the
+    // tensor-core layout, then publishes the tile's flag.  Two buffers: the
+    // next chunk is in flight while this one converts.
+    const int pw = warp - kPPackWarp0;
+    float *stg = reinterpret_cast<float *>(smem + PG::OFF_STG + pw * 2 * PG::STG_BUF);
+    uint64_t *sbar = stgfull + 2 * pw;
+    unsigned *counter = flags + 3 * (size_t)H * T;
+    const int NT = nt_in;
+    constexpr int kChunks = kPM / kPStgRows;
+    constexpr int kBufFloats = PG::STG_BUF / 4;
+    int tl = 0;  // lane 0: the next task number, fetched ahead
+    auto fetch = [&]() {
+      if (lane == 0) tl = (int)atomicAdd(counter, 1u);
+    };
+    auto take = [&]() { return __shfl_sync(0xffffffffu, tl, 0); };
+    // chunk c of tile p into buffer bb (rows past S are not copied)
+    auto issue = [&](const PTile &p, int c, uint32_t bb) {
+      if (lane == 0) {
+        const int row0 = p.t * kPM + c * kPStgRows;
+        const int nvalid = max(0, min(kPStgRows, S - row0));
+        const float *src = (p.tensor == 0 ? q : p.tensor == 1 ? k : v) +
+                           ((size_t)p.h * S + row0) * D;
+        mbar_arrive_expect_tx(&sbar[bb], (uint32_t)nvalid * D * 4);
+        for (int r = 0; r < nvalid; ++r)
+          bulk_g2s(stg + bb * kBufFloats + r * PG::STG_STRIDE, src + (size_t)r * D, D * 4,
+                   &sbar[bb]);
+      }
+    };
+    bool ok = true;
+    uint32_t issued = 0, done = 0;  // chunks issued and converted by this warp
+    fetch();
+    int task = take();
+    PTile cur{0, 0, 0}, nxt{0, 0, 0};
+    if (task < NT) {
+      cur = prefill_task(task, H, T, causal, rq, s0);
+      issue(cur, 0, 0);
+      issued = 1;
+      fetch();
+    }
+    int c = 0;
+    while (task < NT) {
+      // the next chunk goes into the other buffer, converted a chunk ago
+      int ntask = NT;
+      if (c + 1 < kChunks) {
+        issue(cur, c + 1, issued & 1u);
+        ++issued;
+      } else {
+        ntask = take();
+        if (ntask < NT) {
+          nxt = prefill_task(ntask, H, T, causal, rq, s0);
+          issue(nxt, 0, issued & 1u);
+          ++issued;
+        }
+      }
+      const uint32_t bb = done & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait<kPoll>(&sbar[bb], (done >> 1) & 1u, abort))) {
+        ok = false;
+        break;
+      }
+      const float *sb = stg + bb * kBufFloats;
+      const int nvalid = max(0, min(kPStgRows, S - (cur.t * kPM + c * kPStgRows)));
+      unsigned char *dst = tiles + (((size_t)cur.tensor * H + cur.h) * T + cur.t) * PG::TILE;
+      if (cur.tensor < 2) {
+        // Q, K: lane (rr, cg) converts row 8 * half + rr, 8 columns from
+        // 8 * (cg + 4 * cc); eight lanes fill one 128-byte core matrix
+        const int rr = lane & 7, cg = lane >> 3;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int lr = 8 * half + rr;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            const int col = 8 * (cg + 4 * cc);
+            float x[8];
+            if (lr < nvalid) {
+              const float4 a = *reinterpret_cast<const float4 *>(sb + lr * PG::STG_STRIDE + col);
+              const float4 e = *reinterpret_cast<const float4 *>(sb + lr * PG::STG_STRIDE + col + 4);
+              x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+              x[4] = e.x; x[5] = e.y; x[6] = e.z; x[7] = e.w;
+            } else {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) x[u] = 0.f;
+            }
+            *reinterpret_cast<uint4 *>(dst + cm_off(c * kPStgRows + lr, col, D)) = pack8(x);
+          }
+        }
+      } else {
+        // V^T: lane converts column d = lane + 32 j of v over keys 8g..8g+7
+        // of the chunk into one 16-byte piece of V^T row d
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) {
+          const int d = lane + 32 * j;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              x[u] = (8 * g + u < nvalid) ? sb[(8 * g + u) * PG::STG_STRIDE + d] : 0.f;
+            *reinterpret_cast<uint4 *>(dst + cm_off(d, c * kPStgRows + 8 * g, kPN)) = pack8(x);
+          }
+        }
+      }
+      ++done;
+      __syncwarp();
+      if (lane == 0) fence_proxy_async_shared();  // a bulk copy refills the buffer next
+      if (c + 1 == kChunks) {
+        // the tile is complete: every lane's stores are visible at GPU
+        // scope before the flag says so
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          fence_proxy_async_global();
+          st_release_u32(flags + ((size_t)cur.tensor * H + cur.h) * T + cur.t, 1u);
+        }
+        task = ntask;
+        cur = nxt;
+        c = 0;
+        if (task < NT) fetch();
+      } else {
+        ++c;
+      }
+    }
+    if (!ok) {
+      *abort = 1;
+      record_status(d_status, KVS_ERR_TIMEOUT);
+    }
+    // staged copies still in flight land before the block exits
+    if (lane == 0)
+      for (uint32_t j = done; j < issued; ++j) mbar_wait_drain(&sbar[j & 1u], (j >> 1) & 1u);
     __syncwarp();
   } else {
     // ======================= softmax of tile x ===============================
@@ -811,20 +1102,40 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
     configured[dev] = true;
   }
   unsigned char *ws = static_cast<unsigned char *>(workspace);
-  const int nt = (S + kPM - 1) / kPM;
-  cudaError_t e = launch_pdl(prefill_pack_kernel<D>, dim3(3 * (D / 16), nt, H), dim3(256), 0,
-                             stream, q, k, v, ws, S);
-  if (e != cudaSuccess) return KVS_ERR_LAUNCH;
   const float sl2 = (float)(1.4426950408889634074 / std::sqrt((double)D));
   const int T = (S + kPM - 1) / kPM;
+  // tile and task numbers are 32-bit (far beyond any workspace a GPU holds)
+  if (3LL * H * T > (1LL << 30)) return KVS_ERR_UNSUPPORTED;
+  // the tile flags and the task counter start at zero in every call
+  if (cudaMemsetAsync(ws, 0, prefill_flag_bytes(H, T), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
   // one block per SM (the shared memory and the 512 TMEM columns allow no
   // second), each walking its share of the items; more blocks than SMs
   // would only run one after another
   const long long items = (long long)H * ((T + 1) / 2);
   const int grid = (int)std::min<long long>(items, num_sms[dev]);
-  e = launch_pdl(poll_waits() ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>,
-                 dim3(grid), dim3(kPBlockThreads), PG::SMEM_BYTES, stream,
-                 static_cast<const unsigned char *>(ws), out, H, S, causal, sl2, d_status);
+  // packed before the attention starts: the Q tiles of the first round's
+  // pairs and the first s0 key tiles of K and V^T
+  const int np = (T + 1) / 2;
+  const int rq = std::min(np, (grid + H - 1) / H);
+  const int s0 = std::min(T, (T * kPUpfrontKeyPct + 99) / 100);
+  int nq_up = 0;
+  for (int pr = 0; pr < rq; ++pr) {
+    const int qa = 2 * (causal ? np - 1 - pr : pr);
+    nq_up += qa + 1 < T ? 2 : 1;
+  }
+  const int nt_in = 3 * H * T - H * nq_up - 2 * H * s0;
+  if (rq + s0 > 0) {
+    if (launch_pdl(prefill_pack_kernel<D>, dim3((2 * rq + 2 * s0) * (D / 16), H), dim3(256), 0, stream,
+                   q, k, v, ws, H, S, causal, rq) != cudaSuccess)
+      return KVS_ERR_LAUNCH;
+  }
+  const cudaError_t e =
+      launch_pdl(poll_waits() ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>,
+                 dim3(grid), dim3(kPBlockThreads), PG::SMEM_BYTES, stream, q, k, v, ws, out, H,
+                 S, causal, sl2, d_status, rq, s0, nt_in);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_LAUNCH;
 }
 
@@ -840,7 +1151,7 @@ int set_wait_limit_prefill(uint64_t ns) {
 
 size_t prefill_workspace_bytes(int H, int S, int D) {
   const size_t T = ((size_t)S + kPM - 1) / kPM;
-  return 3 * (size_t)H * T * prefill_tile_bytes(D);
+  return prefill_flag_bytes((int)H, (int)T) + 3 * (size_t)H * T * prefill_tile_bytes(D);
 }
 
 int launch_prefill(const float *q, const float *k, const float *v, float *out, int H, int S, int D,

@@ -290,9 +290,12 @@ def test_prefill_validation(L, args, code):
 
 
 def test_prefill_workspace_formula(L):
-    # q, k and v as FP16 tiles of 128 rows: 3 * H * ceil(S / 128) * 128 * D * 2
+    # a 4-byte flag per tile and a task counter, padded to 256 bytes, then q,
+    # k and v as FP16 tiles of 128 rows: 3 * H * ceil(S / 128) * 128 * D * 2
     for H, S, D in [(1, 1, 64), (2, 128, 64), (3, 129, 128), (32, 4096, 128)]:
-        want = 3 * H * (-(-S // 128)) * 128 * D * 2
+        T = -(-S // 128)
+        flags = -(-(4 * (3 * H * T + 1)) // 256) * 256
+        want = flags + 3 * H * T * 128 * D * 2
         assert L.kvs_prefill_workspace_bytes(H, S, D) == want
     assert L.kvs_prefill_workspace_bytes(0, 16, 64) == 0
     assert L.kvs_prefill_workspace_bytes(2, 16, 96) == 0
