@@ -336,14 +336,6 @@ __device__ __forceinline__ bool tile_wait(const unsigned *f, int n, int last, ui
   }
 }
 
-// Share of the key tiles (K and V^T) packed before the attention kernel
-// starts, in percent; the attention kernel's pack warps convert the rest
-// while it runs.  Measured on GB300 (H=32, S=4096, D=128, causal): 55 %
-// 172.9 us, 60 % 167.6, 65 % 168.2, 70 % 169.8, 100 % 179.7, 0 % 211.8;
-// the pack warps move about 1.5 TB/s beside the attention, the separate
-// launch the full bandwidth.
-constexpr int kPUpfrontKeyPct = 60;
-
 // The tiles needed first, packed at full bandwidth before the attention
 // starts: grid (pieces * D/16, H); piece z of a head is a Q tile of a pair
 // rank below rq (two per rank), then K and V^T of key tiles 0, 1, ...;
@@ -796,12 +788,15 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
     float *stg = reinterpret_cast<float *>(smem + PG::OFF_STG + pw * 2 * PG::STG_BUF);
     uint64_t *sbar = stgfull + 2 * pw;
     unsigned *counter = flags + 3 * (size_t)H * T;
-    const int NT = nt_in;
+    const unsigned NT = (unsigned)nt_in;
     constexpr int kChunks = kPM / kPStgRows;
     constexpr int kBufFloats = PG::STG_BUF / 4;
-    int tl = 0;  // lane 0: the next task number, fetched ahead
+    // Task numbers count up from zero (the counter is zeroed before every
+    // launch that has tasks; with none, the counter is not touched), and
+    // compare unsigned, so every warp's walk ends.
+    unsigned tl = 0;  // lane 0: the next task number, fetched ahead
     auto fetch = [&]() {
-      if (lane == 0) tl = (int)atomicAdd(counter, 1u);
+      if (lane == 0) tl = atomicAdd(counter, 1u);
     };
     auto take = [&]() { return __shfl_sync(0xffffffffu, tl, 0); };
     // chunk c of tile p into buffer bb (rows past S are not copied)
@@ -819,11 +814,14 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
     };
     bool ok = true;
     uint32_t issued = 0, done = 0;  // chunks issued and converted by this warp
-    fetch();
-    int task = take();
+    unsigned task = NT;
+    if (NT > 0) {
+      fetch();
+      task = take();
+    }
     PTile cur{0, 0, 0}, nxt{0, 0, 0};
     if (task < NT) {
-      cur = prefill_task(task, H, T, causal, rq, s0);
+      cur = prefill_task((int)task, H, T, causal, rq, s0);
       issue(cur, 0, 0);
       issued = 1;
       fetch();
@@ -831,14 +829,14 @@ __global__ void __launch_bounds__(kPBlockThreads, 1)
     int c = 0;
     while (task < NT) {
       // the next chunk goes into the other buffer, converted a chunk ago
-      int ntask = NT;
+      unsigned ntask = NT;
       if (c + 1 < kChunks) {
         issue(cur, c + 1, issued & 1u);
         ++issued;
       } else {
         ntask = take();
         if (ntask < NT) {
-          nxt = prefill_task(ntask, H, T, causal, rq, s0);
+          nxt = prefill_task((int)ntask, H, T, causal, rq, s0);
           issue(nxt, 0, issued & 1u);
           ++issued;
         }
@@ -1106,11 +1104,6 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
   const int T = (S + kPM - 1) / kPM;
   // tile and task numbers are 32-bit (far beyond any workspace a GPU holds)
   if (3LL * H * T > (1LL << 30)) return KVS_ERR_UNSUPPORTED;
-  // the tile flags and the task counter start at zero in every call
-  if (cudaMemsetAsync(ws, 0, prefill_flag_bytes(H, T), stream) != cudaSuccess) {
-    cudaGetLastError();
-    return KVS_ERR_LAUNCH;
-  }
   // one block per SM (the shared memory and the 512 TMEM columns allow no
   // second), each walking its share of the items; more blocks than SMs
   // would only run one after another
@@ -1119,14 +1112,33 @@ int launch_prefill_impl(const float *q, const float *k, const float *v, float *o
   // packed before the attention starts: the Q tiles of the first round's
   // pairs and the first s0 key tiles of K and V^T
   const int np = (T + 1) / 2;
-  const int rq = std::min(np, (grid + H - 1) / H);
-  const int s0 = std::min(T, (T * kPUpfrontKeyPct + 99) / 100);
+  // key tiles left to the pack warps: 40 % of them, fewer when one key
+  // tile of every head (K and V^T) is more than 4 MiB of FP32, so that the
+  // pack warps (about 1.5 TB/s beside the attention) stay ahead of the
+  // items; none below 16 key tiles, where the in-kernel packing only adds
+  // latency.  Measured on GB300 (H=32, S=4096, D=128, causal), key tiles
+  // packed upfront: 55 % 172.9 us, 60 % 167.6, 65 % 168.2, 70 % 169.8,
+  // 100 % 179.7, 0 % 211.8; with no in-kernel share, 64 and 128 heads at
+  // S=1024 ran 20 % faster than with 40 %.
+  const double step_bytes = 2.0 * H * kPM * D * 4;
+  const int n_in =
+      T < 16 ? 0 : (int)(0.4 * T * std::min(1.0, (double)(4 << 20) / step_bytes));
+  const int s0 = T - n_in;
+  // the Q tiles of the first round's pairs; all of them when the pack warps
+  // get no key tiles (then the later rounds' Q tiles would come too late)
+  const int rq = n_in > 0 ? std::min(np, (grid + H - 1) / H) : np;
   int nq_up = 0;
   for (int pr = 0; pr < rq; ++pr) {
     const int qa = 2 * (causal ? np - 1 - pr : pr);
     nq_up += qa + 1 < T ? 2 : 1;
   }
   const int nt_in = 3 * H * T - H * nq_up - 2 * H * s0;
+  // the tile flags and the task counter start at zero in every call that
+  // packs in the attention kernel (otherwise no flag is read)
+  if (nt_in > 0 && cudaMemsetAsync(ws, 0, prefill_flag_bytes(H, T), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_LAUNCH;
+  }
   if (rq + s0 > 0) {
     if (launch_pdl(prefill_pack_kernel<D>, dim3((2 * rq + 2 * s0) * (D / 16), H), dim3(256), 0, stream,
                    q, k, v, ws, H, S, causal, rq) != cudaSuccess)
