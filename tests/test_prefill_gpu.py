@@ -96,6 +96,32 @@ def test_long_sequence_causal():
     check(2, 1000, 128, True, seed=11)
 
 
+@pytest.mark.parametrize("H,S,D,causal", [(2, 2100, 128, True), (3, 2048, 64, False),
+                                          (1, 4096, 128, True), (5, 2500, 64, True)])
+def test_tiles_packed_beside_the_attention(H, S, D, causal):
+    """From 16 key tiles on, part of the FP16 packing runs in the attention
+    kernel's pack warps and reaches the copy warp tile by tile through ready
+    flags (zeroed by the call, over a workspace full of 0xFF bytes)."""
+    check(H, S, D, causal, seed=H * 31 + S + D + causal)
+
+
+def test_no_in_kernel_tasks_over_any_workspace_contents():
+    """Below 16 key tiles the pack warps get no tasks and the call neither
+    zeroes nor reads the flags and the task counter: a workspace whose
+    counter word reads negative (0x80 bytes) must not matter."""
+    H, S, D = 3, 1000, 128
+    q, k, v = inputs(H, S, D, seed=5)
+    tq, tk, tv = (torch.from_numpy(a).to(DEV) for a in (q, k, v))
+    out = torch.empty((H, S, D), device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = B.prefill_workspace(H, S, D, device=DEV).fill_(0x80)
+    B.kvs_prefill_attention(tq, tk, tv, out, causal=True, workspace=ws, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.prefill_attention(q, k, v, True)
+    assert np.all(np.abs(out.cpu().numpy() - ref) <= bound(v, ref, True))
+
+
 def test_causal_last_row_equals_full_attention_of_last_query():
     """The last causal row attends every key: it equals the non-causal row."""
     q, k, v = inputs(1, 256, 64, seed=13)

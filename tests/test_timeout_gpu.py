@@ -203,10 +203,11 @@ def _prefill_inputs(H, S, D, seed):
     return [rng.standard_normal((H, S, D)).astype(np.float32) for _ in range(3)]
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_prefill_kernel_times_out_and_recovers(D):
-    H, S = 4, 1000
-    q, k, v = _prefill_inputs(H, S, D, seed=66 + D)
+@pytest.mark.parametrize("D,H,S", [(64, 4, 1000), (128, 4, 1000), (128, 2, 2100), (64, 3, 2048)])
+def test_prefill_kernel_times_out_and_recovers(D, H, S):
+    # S >= 2048 adds the waits of the in-kernel packing: the copy warp's tile
+    # flags and the pack warps' staged chunks
+    q, k, v = _prefill_inputs(H, S, D, seed=66 + D + S)
     ref = oracle.prefill_attention(q, k, v, True)
     tq, tk, tv = (torch.from_numpy(a).to(DEV) for a in (q, k, v))
     ws = B.prefill_workspace(H, S, D, device=DEV)
