@@ -501,7 +501,8 @@ int kvs_argmax(const float *logits, int M, int vocab_size, int32_t *token_ids,
  * first, then the attention launch, whose pack warps convert the remaining
  * tiles while it runs.
  * Errors: DIMS (negative sizes, num_heads > 65535, seq_len > 65535 * 128),
- * UNSUPPORTED, NULL, ALIGN, WORKSPACE, LAUNCH on the host; TIMEOUT via
+ * UNSUPPORTED (head_dim not 64 or 128; more than 2^30 tiles), NULL, ALIGN,
+ * WORKSPACE, LAUNCH on the host; TIMEOUT via
  * d_status.  num_heads = 0 or seq_len = 0 enqueues nothing.
  */
 size_t kvs_prefill_workspace_bytes(int num_heads, int seq_len, int head_dim);
